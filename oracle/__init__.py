@@ -1,0 +1,171 @@
+"""CPU oracle for gated fine-grained sparse attention — TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The product path (the C-ABI library and
+its Python binding) never calls it and shares no code with it.
+
+The arithmetic lives in ``esa_oracle.c`` (plain C, int64 / fp64, OpenMP over
+query rows); this file only compiles it with gcc and marshals numpy/torch
+arrays. What each function computes, and which passage of the pages it
+follows, is stated in the C source. Every function is pinned by the CPU tests
+(brute force, closed forms, invariants, numpy/torch library routines); no
+function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "esa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libesa_oracle.so")
+_lib = None
+
+c_long = ctypes.c_long
+c_int = ctypes.c_int
+vp = ctypes.c_void_p
+
+
+def build(src: str = _SRC, out: str = _LIB_PATH, extra_flags=()) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP). Returns the .so path."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", *extra_flags, "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    lib.oracle_indexer_row.restype = c_long
+    lib.oracle_indexer_row.argtypes = [vp, vp, vp, c_long, c_long, c_long, c_long, c_int, c_int, c_long, c_long, vp]
+    lib.oracle_topk_rows.restype = c_int
+    lib.oracle_topk_rows.argtypes = [vp, vp, vp, c_long, c_long, c_long, c_long, c_int, c_int, c_int, vp, c_long,
+                                     vp, vp, c_int]
+    lib.oracle_attention_rows.restype = c_int
+    lib.oracle_attention_rows.argtypes = [vp, vp, vp, vp, vp, c_int, c_long, c_long, c_long, c_long, c_int, c_int,
+                                          c_int, ctypes.c_double, vp, vp, vp, vp, c_long, vp, vp, c_int]
+    lib.oracle_threshold_row.restype = c_int
+    lib.oracle_threshold_row.argtypes = [vp, c_long, c_int, vp, vp]
+    return lib
+
+
+def lib(path: str | None = None):
+    """The compiled oracle (built on first use when missing or stale)."""
+    global _lib
+    if path is not None:
+        return _bind(path)
+    if _lib is None:
+        if (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+            build()
+        _lib = _bind(_LIB_PATH)
+    return _lib
+
+
+def threads() -> int:
+    return int(os.environ.get("ESA_ORACLE_THREADS", os.cpu_count() or 1))
+
+
+def _np(x, dtype):
+    """numpy array of ``dtype``; bf16 tensors become their uint16 bit patterns."""
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().contiguous()
+        if x.dtype == torch.bfloat16:
+            x = x.view(torch.int16)
+        x = x.numpy()
+    a = np.ascontiguousarray(x)
+    if dtype == np.uint16 and a.dtype in (np.int16, np.uint16):
+        return a.view(np.uint16)
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(vp) if a is not None else None
+
+
+def _rows(B, Tq, rows):
+    if rows is None:
+        return np.arange(B * Tq, dtype=np.int64)
+    return np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+
+
+def indexer_row(qI, kI, wI, shape: dict, b: int, t: int, L=None) -> np.ndarray:
+    """int32 scores of row (b,t) against keys 0..q_offset+t."""
+    L = L or lib()
+    qa, ka, wa = _np(qI, np.int8), _np(kI, np.int8), _np(wI, np.int32)
+    n = shape["q_offset"] + t + 1
+    out = np.empty(n, dtype=np.int32)
+    r = L.oracle_indexer_row(_ptr(qa), _ptr(ka), _ptr(wa), shape["B"], shape["Tq"], shape["Tk"], shape["q_offset"],
+                             shape["H_I"], shape["D_I"], b, t, _ptr(out))
+    if r != n:
+        raise ValueError(f"oracle_indexer_row failed ({r}): score outside int32 or row beyond Tk")
+    return out
+
+
+def topk(qI, kI, wI, shape: dict, K: int, rows=None, L=None):
+    """(idx [n_rows,K] int32, cnt [n_rows] int32) for the listed flat rows."""
+    L = L or lib()
+    qa, ka, wa = _np(qI, np.int8), _np(kI, np.int8), _np(wI, np.int32)
+    rr = _rows(shape["B"], shape["Tq"], rows)
+    idx = np.empty((len(rr), K), dtype=np.int32)
+    cnt = np.empty(len(rr), dtype=np.int32)
+    rc = L.oracle_topk_rows(_ptr(qa), _ptr(ka), _ptr(wa), shape["B"], shape["Tq"], shape["Tk"], shape["q_offset"],
+                            shape["H_I"], shape["D_I"], K, _ptr(rr), len(rr), _ptr(idx), _ptr(cnt), threads())
+    if rc != 0:
+        raise ValueError("oracle_topk_rows: a score does not fit in int32")
+    return idx, cnt
+
+
+def attention(q, k, v, idx, cnt, shape: dict, K: int, scale: float | None = None, g=None, lin=None, route=None,
+              rows=None, L=None):
+    """(out [n_rows,Hq,D] fp64, lse [n_rows,Hq] fp64) for the listed rows.
+
+    idx/cnt are given per listed row (as returned by :func:`topk`)."""
+    L = L or lib()
+    B, Tq, Hq, D = shape["B"], shape["Tq"], shape["Hq"], shape["D"]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    qa, ka, va = _np(q, np.uint16), _np(k, np.uint16), _np(v, np.uint16)
+    rr = _rows(B, Tq, rows)
+    ia = np.ascontiguousarray(np.asarray(idx, dtype=np.int32).reshape(len(rr), K))
+    ca = np.ascontiguousarray(np.asarray(cnt, dtype=np.int32).reshape(len(rr)))
+    ga = _np(g, np.float32) if g is not None else None
+    la = _np(lin, np.uint16) if lin is not None else None
+    ra = _np(route, np.uint8) if route is not None else None
+    out = np.empty((len(rr), Hq, D), dtype=np.float64)
+    lse = np.empty((len(rr), Hq), dtype=np.float64)
+    rc = L.oracle_attention_rows(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ia), _ptr(ca), K, B, Tq, shape["Tk"],
+                                 shape["q_offset"], Hq, shape["Hkv"], D, float(scale), _ptr(ga), _ptr(la), _ptr(ra),
+                                 _ptr(rr), len(rr), _ptr(out), _ptr(lse), threads())
+    if rc != 0:
+        raise ValueError("oracle_attention_rows: an index lies outside the causal prefix")
+    return out, lse
+
+
+def gated_sparse_attention(inp: dict, shape: dict, K: int, rows=None, gate=True, L=None):
+    """The whole path for the listed rows: indexer -> top-K -> attention over the
+    selected keys (or all keys for heads routed full) -> gate mix.
+
+    Returns (idx, cnt, out, lse)."""
+    L = L or lib()
+    idx, cnt = topk(inp["qI"], inp["kI"], inp["wI"], shape, K, rows=rows, L=L)
+    out, lse = attention(inp["q"], inp["k"], inp["v"], idx, cnt, shape, K,
+                         g=inp["g"] if gate else None, lin=inp["lin"] if gate else None,
+                         route=inp.get("route"), rows=rows, L=L)
+    return idx, cnt, out, lse
+
+
+def threshold(scores: np.ndarray, K: int, L=None):
+    """(T, ties_taken) of a score row: the K-th largest score and how many
+    positions scoring exactly T the index set holds."""
+    L = L or lib()
+    s = np.ascontiguousarray(scores, dtype=np.int32)
+    T = ctypes.c_int32()
+    tt = ctypes.c_long()
+    L.oracle_threshold_row(_ptr(s), len(s), K, ctypes.byref(T), ctypes.byref(tt))
+    return int(T.value), int(tt.value)

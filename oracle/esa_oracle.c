@@ -1,0 +1,249 @@
+/*
+ * CPU oracle for gated fine-grained sparse attention — TEST INFRASTRUCTURE.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load this code. It is deliberately plain and slow: every quantity follows
+ * its definition on the pages, in 64-bit integers or fp64, with no tiling,
+ * no fusion and no reordering.
+ *
+ * Sources (the pages this follows):
+ *  - "超大规模MoE架构中稀疏注意力机制的演进与实践" (Gated DSA), section 二.1
+ *    (Indexer + Top-K: an indexer scores the query against every history
+ *    position, the K best positions go on to full attention), section 二.2
+ *    (the indexer uses no RoPE), section 二.3 and the pseudo-code of section
+ *    四.1 (matmul scores, top-k, gather, scaled dot-product attention, then
+ *    final = g*attn + (1-g)*linear_output).
+ *  - "混合注意力架构演进：从线性注意力到稀疏门控的技术权衡", section 三
+ *    (sparse_attention: indexer_score, topk, gather, softmax(Q K_sel^T/sqrt(d)) V_sel).
+ *  - "Elastic Attention：动态路由优化大模型长文本处理", sections 2.2 and 3.1
+ *    (per-head routing: a head runs either full or sparse attention).
+ *
+ * Readings taken where the pages are silent (each is restated in the tests):
+ *  the prefix of query position p is keys 0..p inclusive; the indexer is a
+ *  plain weighted sum over indexer heads of int8 dot products (no
+ *  nonlinearity), with one indexer key per position shared by all indexer
+ *  heads; ties in the score go to the lower position; the index set is
+ *  returned in ascending position order, padded with -1, with
+ *  cnt = min(K, p+1); one index set per (sequence, query) is shared by every
+ *  query head; the gate is one value in (0,1) per query head; heads routed to
+ *  full attention output the attention result without the gate mix; query
+ *  head h reads key/value head floor(h / (Hq/Hkv)).
+ *
+ * Parity pins: every function here is pinned by the CPU tests against brute
+ * force, closed forms, invariants and library routines (numpy, torch).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bit pattern -> exact double */
+static double bf16_to_double(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Indexer score of query row (b, t) against keys 0..p, p = q_offset + t:
+ *   s_j = sum_h w_h * sum_c qI[b,t,h,c] * kI[b,j,c]      (no RoPE anywhere)
+ * computed in int64. Writes p+1 scores; returns p+1, or -1 when a score
+ * does not fit in int32 (the interface promises int32 scores).
+ */
+long oracle_indexer_row(const int8_t *qI, const int8_t *kI, const int32_t *wI,
+                        long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
+                        long b, long t, int32_t *scores) {
+    (void)B;
+    long p = q_offset + t;
+    long n = p + 1;
+    if (n > Tk) return -2;
+    for (long j = 0; j < n; j++) {
+        int64_t s = 0;
+        for (int h = 0; h < H_I; h++) {
+            int64_t dot = 0;
+            for (int c = 0; c < D_I; c++) {
+                int64_t a = qI[((b * Tq + t) * H_I + h) * D_I + c];
+                int64_t k = kI[(b * Tk + j) * D_I + c];
+                dot += a * k;
+            }
+            s += (int64_t)wI[h] * dot;
+        }
+        if (s > INT32_MAX || s < INT32_MIN) return -1;
+        scores[j] = (int32_t)s;
+    }
+    return n;
+}
+
+typedef struct {
+    int32_t s;
+    int32_t j;
+} scored_pos;
+
+/* (score descending, position ascending) */
+static int by_score_then_position(const void *x, const void *y) {
+    const scored_pos *a = (const scored_pos *)x, *b = (const scored_pos *)y;
+    if (a->s != b->s) return (a->s > b->s) ? -1 : 1;
+    return (a->j < b->j) ? -1 : (a->j > b->j);
+}
+
+static int ascending_i32(const void *x, const void *y) {
+    int32_t a = *(const int32_t *)x, b = *(const int32_t *)y;
+    return (a < b) ? -1 : (a > b);
+}
+
+/*
+ * Top-K selection for a list of query rows (flat row id r = b*Tq + t).
+ * For each row: order positions 0..p by (score descending, position
+ * ascending), keep the first min(K, p+1), sort them ascending, pad with -1.
+ * idx is [n_rows, K], cnt is [n_rows]. Returns 0, or -1 on int32 overflow.
+ */
+int oracle_topk_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
+                     long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
+                     int K, const int64_t *rows, long n_rows,
+                     int32_t *idx, int32_t *cnt, int n_threads) {
+    int bad = 0;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#endif
+    for (long r = 0; r < n_rows; r++) {
+        long b = rows[r] / Tq, t = rows[r] % Tq;
+        long n = q_offset + t + 1;
+        int32_t *sc = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+        scored_pos *order = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
+        if (oracle_indexer_row(qI, kI, wI, B, Tq, Tk, q_offset, H_I, D_I, b, t, sc) != n) {
+            bad |= 1;
+        } else {
+            for (long j = 0; j < n; j++) {
+                order[j].s = sc[j];
+                order[j].j = (int32_t)j;
+            }
+            qsort(order, (size_t)n, sizeof(scored_pos), by_score_then_position);
+            long kk = n < K ? n : K;
+            int32_t *row = idx + r * (long)K;
+            for (long i = 0; i < kk; i++) row[i] = order[i].j;
+            qsort(row, (size_t)kk, sizeof(int32_t), ascending_i32);
+            for (long i = kk; i < K; i++) row[i] = -1;
+            cnt[r] = (int32_t)kk;
+        }
+        free(sc);
+        free(order);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Attention for a list of query rows, all query heads, in fp64.
+ *  - Head h of row (b,t) reads key/value head kh = h / (Hq/Hkv).
+ *  - Key set: when route is given and route[b*Hq+h] == 0 (a full head), all
+ *    positions 0..p; otherwise the row's index set idx[r, 0..cnt[r]).
+ *  - logit_j = scale * sum_c q[b,t,h,c] * k[b,j,kh,c];  m = max logit;
+ *    o = sum_j e^(logit_j - m) v[b,j,kh,:] / sum_j e^(logit_j - m);
+ *    lse = m + ln sum_j e^(logit_j - m).
+ *  - Sparse heads with g given: out = g[h]*o + (1-g[h])*lin[b,t,h,:];
+ *    full heads (and sparse heads without g): out = o.
+ * q, lin: [B,Tq,Hq,D] bf16 bits; k, v: [B,Tk,Hkv,D] bf16 bits; idx/cnt are
+ * per listed row. out [n_rows,Hq,D], lse [n_rows,Hq] (lse may be NULL).
+ * Returns 0, or -1 when an index lies outside 0..p.
+ */
+int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const int32_t *idx, const int32_t *cnt, int K,
+                          long B, long Tq, long Tk, long q_offset,
+                          int Hq, int Hkv, int D, double scale,
+                          const float *g, const uint16_t *lin, const uint8_t *route,
+                          const int64_t *rows, long n_rows,
+                          double *out, double *lse, int n_threads) {
+    (void)B;
+    int bad = 0;
+    int G = Hq / Hkv;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#endif
+    for (long r = 0; r < n_rows; r++) {
+        long b = rows[r] / Tq, t = rows[r] % Tq;
+        long p = q_offset + t;
+        double *logit = (double *)malloc(sizeof(double) * (size_t)(p + 1));
+        int32_t *keys = (int32_t *)malloc(sizeof(int32_t) * (size_t)(p + 1));
+        double *acc = (double *)malloc(sizeof(double) * (size_t)D);
+        for (int h = 0; h < Hq; h++) {
+            int kh = h / G;
+            int full = (route != NULL) && (route[b * Hq + h] == 0);
+            long nk;
+            if (full) {
+                nk = p + 1;
+                for (long j = 0; j < nk; j++) keys[j] = (int32_t)j;
+            } else {
+                nk = cnt[r];
+                for (long i = 0; i < nk; i++) {
+                    int32_t j = idx[r * (long)K + i];
+                    if (j < 0 || j > p) {
+                        bad |= 1;
+                        j = 0;
+                    }
+                    keys[i] = j;
+                }
+            }
+            const uint16_t *qrow = q + ((b * Tq + t) * Hq + h) * (long)D;
+            double m = -INFINITY;
+            for (long i = 0; i < nk; i++) {
+                const uint16_t *krow = k + ((b * Tk + keys[i]) * Hkv + kh) * (long)D;
+                double dot = 0.0;
+                for (int c = 0; c < D; c++) dot += bf16_to_double(qrow[c]) * bf16_to_double(krow[c]);
+                logit[i] = dot * scale;
+                if (logit[i] > m) m = logit[i];
+            }
+            double den = 0.0;
+            for (int c = 0; c < D; c++) acc[c] = 0.0;
+            for (long i = 0; i < nk; i++) {
+                double e = exp(logit[i] - m);
+                den += e;
+                const uint16_t *vrow = v + ((b * Tk + keys[i]) * Hkv + kh) * (long)D;
+                for (int c = 0; c < D; c++) acc[c] += e * bf16_to_double(vrow[c]);
+            }
+            double *o = out + (r * Hq + h) * (long)D;
+            const uint16_t *lrow = lin ? lin + ((b * Tq + t) * Hq + h) * (long)D : NULL;
+            for (int c = 0; c < D; c++) {
+                double oc = acc[c] / den;
+                if (!full && g != NULL && lrow != NULL) {
+                    double gh = (double)g[h];
+                    oc = gh * oc + (1.0 - gh) * bf16_to_double(lrow[c]);
+                }
+                o[c] = oc;
+            }
+            if (lse) lse[r * Hq + h] = m + log(den);
+        }
+        free(logit);
+        free(keys);
+        free(acc);
+    }
+    return bad ? -1 : 0;
+}
+
+/* Threshold form of a row's index set, used to explain parity failures:
+ * T = the K-th largest score (or INT32_MIN when p+1 <= K) and the number of
+ * positions with score == T that the set holds. Returns 0. */
+int oracle_threshold_row(const int32_t *scores, long n, int K, int32_t *T, long *ties_taken) {
+    if (n <= K) {
+        *T = INT32_MIN;
+        *ties_taken = 0;
+        return 0;
+    }
+    scored_pos *order = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
+    for (long j = 0; j < n; j++) {
+        order[j].s = scores[j];
+        order[j].j = (int32_t)j;
+    }
+    qsort(order, (size_t)n, sizeof(scored_pos), by_score_then_position);
+    *T = order[K - 1].s;
+    long tt = 0;
+    for (long i = 0; i < K; i++) tt += (order[i].s == *T);
+    *ties_taken = tt;
+    free(order);
+    return 0;
+}

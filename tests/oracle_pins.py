@@ -1,0 +1,303 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each ``pin_*`` function takes a compiled oracle handle (``oracle.lib()`` or a
+deliberately broken copy built by the mutation tests) and raises
+AssertionError when the oracle disagrees with:
+  * the hand-worked example in ``tests/golden/indexer_tiny.txt``;
+  * brute force on tiny inputs (the counting definition of top-K);
+  * library routines (numpy int64 einsum, numpy lexsort, torch fp64
+    scaled_dot_product_attention with a causal or explicit mask);
+  * closed forms and invariants (t=0 gives v_0, V=1 gives 1, softmax sums to
+    one, permutation invariance, gate end points and affinity, needles).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+import esa_inputs as E
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "indexer_tiny.txt")
+
+
+def _golden():
+    vals = {}
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *rest = line.split()
+            vals[key] = [int(x) for x in rest]
+    return vals
+
+
+def _bf16_f64(t: torch.Tensor) -> torch.Tensor:
+    return t.to(torch.float64)
+
+
+def _small(seed=11, **over):
+    cfg = E.small_config(seed=seed, **over)
+    return cfg, E.shape_of(cfg), E.make_inputs(cfg)
+
+
+def _sdpa_masked(inp, shape, allowed, rows):
+    """fp64 torch SDPA for the listed flat rows with boolean mask allowed[r, j]."""
+    B, Tq, Hq, Hkv, D = shape["B"], shape["Tq"], shape["Hq"], shape["Hkv"], shape["D"]
+    G = Hq // Hkv
+    q = _bf16_f64(inp["q"]).reshape(B * Tq, Hq, D)[torch.as_tensor(rows)]
+    out = torch.empty(len(rows), Hq, D, dtype=torch.float64)
+    lse = torch.empty(len(rows), Hq, dtype=torch.float64)
+    for i, r in enumerate(rows):
+        b = r // Tq
+        k = _bf16_f64(inp["k"][b]).repeat_interleave(G, dim=1).transpose(0, 1)  # [Hq, Tk, D]
+        v = _bf16_f64(inp["v"][b]).repeat_interleave(G, dim=1).transpose(0, 1)
+        m = torch.as_tensor(allowed[i])[None, None, :]
+        o = torch.nn.functional.scaled_dot_product_attention(q[i][:, None, :], k, v, attn_mask=m)
+        out[i] = o[:, 0, :]
+        logits = (q[i][:, None, :] @ k.transpose(-1, -2))[:, 0, :] / math.sqrt(D)
+        lse[i] = torch.logsumexp(logits.masked_fill(~m[0], -math.inf), dim=-1)
+    return out.numpy(), lse.numpy()
+
+
+# ---------------------------------------------------------------- indexer
+def pin_indexer_golden(L):
+    gv = _golden()
+    qI = np.array(gv["qI"], dtype=np.int8).reshape(1, 3, 2, 3)
+    kI = np.array(gv["kI"], dtype=np.int8).reshape(1, 3, 3)
+    w = np.array(gv["w"], dtype=np.int32)
+    sh = dict(B=1, Tq=3, Tk=3, q_offset=0, Hq=1, Hkv=1, D=64, H_I=2, D_I=3)
+    for t in range(3):
+        got = O.indexer_row(qI, kI, w, sh, 0, t, L=L)
+        assert got.tolist() == gv[f"scores_t{t}"], (t, got)
+    idx1, _ = O.topk(qI, kI, w, sh, 1, L=L)
+    assert idx1.reshape(-1).tolist() == gv["top1"], idx1
+    idx2, cnt2 = O.topk(qI, kI, w, sh, 2, L=L)
+    assert idx2.reshape(-1).tolist() == gv["top2"], idx2
+    assert cnt2.tolist() == gv["cnt2"], cnt2
+
+
+def pin_indexer_numpy(L, seed=3):
+    rng = np.random.default_rng(seed)
+    for (B, Tq, Tk, qo, HI, DI) in [(2, 5, 9, 4, 3, 16), (1, 1, 40, 39, 1, 64), (3, 7, 7, 0, 4, 8)]:
+        qI = rng.integers(-128, 128, (B, Tq, HI, DI), dtype=np.int8)
+        kI = rng.integers(-128, 128, (B, Tk, DI), dtype=np.int8)
+        w = rng.integers(-3, 5, HI).astype(np.int32)
+        sh = dict(B=B, Tq=Tq, Tk=Tk, q_offset=qo, Hq=1, Hkv=1, D=64, H_I=HI, D_I=DI)
+        ref = np.einsum("bthc,bjc,h->btj", qI.astype(np.int64), kI.astype(np.int64), w.astype(np.int64))
+        for b in range(B):
+            for t in range(Tq):
+                got = O.indexer_row(qI, kI, w, sh, b, t, L=L)
+                assert np.array_equal(got, ref[b, t, :qo + t + 1]), (b, t)
+
+
+def pin_indexer_onehot(L):
+    rng = np.random.default_rng(5)
+    kI = rng.integers(-8, 8, (1, 12, 8), dtype=np.int8)
+    for h, c, w in [(0, 3, 1), (2, 7, 4), (1, 0, 2)]:
+        qI = np.zeros((1, 12, 3, 8), dtype=np.int8)
+        qI[0, 11, h, c] = 1
+        wv = np.array([1, 2, 4], dtype=np.int32)
+        sh = dict(B=1, Tq=12, Tk=12, q_offset=0, Hq=1, Hkv=1, D=64, H_I=3, D_I=8)
+        got = O.indexer_row(qI, kI, wv, sh, 0, 11, L=L)
+        assert np.array_equal(got, wv[h] * kI[0, :, c].astype(np.int32)), (h, c, w)
+
+
+def pin_indexer_bound(L):
+    cfg, sh, inp = _small(seed=21, Tq=32, Tk=32, H_I=4, D_I=64, weights="1to4")
+    bound = int(inp["wI"].abs().sum()) * 64 * 64
+    for t in (0, 15, 31):
+        s = O.indexer_row(inp["qI"], inp["kI"], inp["wI"], sh, 0, t, L=L)
+        assert np.abs(s).max() <= bound
+
+
+# ---------------------------------------------------------------- top-K
+def _topk_bruteforce(s: np.ndarray, K: int):
+    """Counting definition: j is kept iff fewer than K positions beat it
+    (higher score, or equal score at a lower position)."""
+    n = len(s)
+    keep = [j for j in range(n) if sum(1 for i in range(n) if s[i] > s[j] or (s[i] == s[j] and i < j)) < K]
+    return keep
+
+
+def pin_topk_bruteforce(L, seed=9):
+    rng = np.random.default_rng(seed)
+    for trial in range(6):
+        B, Tq, Tk, qo = 2, 6, 30, 24
+        DI = 4
+        qI = rng.integers(-2, 2, (B, Tq, 1, DI), dtype=np.int8)  # small range: many ties
+        kI = rng.integers(-2, 2, (B, Tk, DI), dtype=np.int8)
+        w = np.ones(1, dtype=np.int32)
+        sh = dict(B=B, Tq=Tq, Tk=Tk, q_offset=qo, Hq=1, Hkv=1, D=64, H_I=1, D_I=DI)
+        K = [1, 3, 7, 25, 26, 40][trial]
+        idx, cnt = O.topk(qI, kI, w, sh, K, L=L)
+        for r in range(B * Tq):
+            b, t = divmod(r, Tq)
+            s = O.indexer_row(qI, kI, w, sh, b, t, L=L)
+            keep = _topk_bruteforce(s, K)
+            assert cnt[r] == len(keep) == min(K, qo + t + 1)
+            assert idx[r, :cnt[r]].tolist() == keep, (trial, r)
+            assert (idx[r, cnt[r]:] == -1).all()
+
+
+def pin_topk_lexsort(L, seed=13):
+    cfg, sh, inp = _small(seed=seed, Tq=48, Tk=48, H_I=2, D_I=16, top_k=20, weights="1to4")
+    K = 20
+    idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K, L=L)
+    qI = inp["qI"].numpy().astype(np.int64)
+    kI = inp["kI"].numpy().astype(np.int64)
+    w = inp["wI"].numpy().astype(np.int64)
+    for t in range(48):
+        s = np.einsum("hc,jc,h->j", qI[0, t], kI[0, :t + 1], w)
+        order = np.lexsort((np.arange(t + 1), -s))  # score desc, then position asc
+        ref = np.sort(order[:K])
+        assert idx[t, :cnt[t]].tolist() == ref.tolist(), t
+
+
+def pin_topk_special(L):
+    cfg, sh, inp = _small(seed=17, Tq=40, Tk=40, D_I=32)
+    idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, 64, L=L)  # K >= every prefix
+    for t in range(40):
+        assert cnt[t] == t + 1
+        assert idx[t, :t + 1].tolist() == list(range(t + 1))
+        assert (idx[t, t + 1:] == -1).all()
+    kz = torch.zeros_like(inp["kI"])  # all scores equal: the first K positions win
+    idx, cnt = O.topk(inp["qI"], kz, inp["wI"], sh, 5, L=L)
+    for t in range(40):
+        assert idx[t, :cnt[t]].tolist() == list(range(min(5, t + 1)))
+
+
+def pin_topk_needles(L):
+    cfg = E.small_config(B=1, Tq=1, Tk=16384, q_offset=16383, Hq=4, Hkv=1, D=64, H_I=1, D_I=64,
+                         top_k=256, needles=64, seed=2005)
+    inp = E.make_inputs(cfg)
+    sh = E.shape_of(cfg)
+    idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, 256, L=L)
+    assert set(inp["needles"].tolist()) <= set(idx[0].tolist())
+
+
+# ---------------------------------------------------------------- attention
+def pin_attention_full_is_sdpa(L):
+    for over in [dict(Tq=33, Tk=33, Hq=4, Hkv=1, D=64), dict(Tq=20, Tk=20, Hq=8, Hkv=2, D=128),
+                 dict(B=2, Tq=5, Tk=29, q_offset=24, Hq=6, Hkv=3, D=64)]:
+        cfg, sh, inp = _small(seed=23, **over)
+        K = sh["Tk"]
+        rows = list(range(sh["B"] * sh["Tq"]))
+        idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K, L=L)
+        out, lse = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, L=L)
+        allowed = np.array([[j <= sh["q_offset"] + r % sh["Tq"] for j in range(sh["Tk"])] for r in rows])
+        ref, ref_lse = _sdpa_masked(inp, sh, allowed, rows)
+        assert np.abs(out - ref).max() < 1e-12, np.abs(out - ref).max()
+        assert np.abs(lse - ref_lse).max() < 1e-12
+        if sh["q_offset"] == 0:  # also the library's own causal flag
+            B, Tq, Hq, Hkv, D = sh["B"], sh["Tq"], sh["Hq"], sh["Hkv"], sh["D"]
+            G = Hq // Hkv
+            q = _bf16_f64(inp["q"]).permute(0, 2, 1, 3)
+            k = _bf16_f64(inp["k"]).repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+            v = _bf16_f64(inp["v"]).repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+            o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+            assert np.abs(out - o.permute(0, 2, 1, 3).reshape(B * Tq, Hq, D).numpy()).max() < 1e-12
+
+
+def pin_attention_sparse_is_masked_sdpa(L):
+    cfg, sh, inp = _small(seed=29, Tq=40, Tk=40, Hq=8, Hkv=2, D=64, D_I=16)
+    K = 9
+    idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K, L=L)
+    out, lse = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, L=L)
+    rows = list(range(40))
+    allowed = np.zeros((40, 40), dtype=bool)
+    for r in rows:
+        allowed[r, idx[r, :cnt[r]]] = True
+    ref, ref_lse = _sdpa_masked(inp, sh, allowed, rows)
+    assert np.abs(out - ref).max() < 1e-12
+    assert np.abs(lse - ref_lse).max() < 1e-12
+
+
+def pin_attention_closed_forms(L):
+    cfg, sh, inp = _small(seed=31, Tq=16, Tk=16, Hq=4, Hkv=2, D=64)
+    K = 6
+    idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K, L=L)
+    out, lse = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, L=L)
+    v0 = _bf16_f64(inp["v"][0, 0]).numpy()  # [Hkv, D]
+    for h in range(4):
+        assert np.array_equal(out[0, h], v0[h // 2])  # row 0 attends to key 0 alone
+        assert lse[0, h] == _bf16_f64(inp["q"][0, 0, h]).dot(_bf16_f64(inp["k"][0, 0, h // 2])).item() / 8.0
+    ones = torch.ones_like(inp["v"])
+    o1, _ = O.attention(inp["q"], inp["k"], ones, idx, cnt, sh, K, L=L)
+    assert np.abs(o1 - 1.0).max() < 1e-14
+    perm = idx.copy()
+    rng = np.random.default_rng(0)
+    for r in range(16):
+        perm[r, :cnt[r]] = rng.permutation(perm[r, :cnt[r]])
+    op, lp = O.attention(inp["q"], inp["k"], inp["v"], perm, cnt, sh, K, L=L)
+    assert np.abs(op - out).max() < 1e-13 and np.abs(lp - lse).max() < 1e-13
+    # softmax over the selected keys sums to one: sum_j exp(logit_j - lse) = 1
+    q = _bf16_f64(inp["q"][0])
+    k = _bf16_f64(inp["k"][0])
+    for r in (3, 9, 15):
+        for h in range(4):
+            sel = torch.as_tensor(idx[r, :cnt[r]], dtype=torch.long)
+            logits = (k[sel, h // 2] @ q[r, h]) / 8.0
+            assert abs(torch.exp(logits - lse[r, h]).sum().item() - 1.0) < 1e-13
+
+
+def pin_gate(L):
+    cfg, sh, inp = _small(seed=37, Tq=24, Tk=24, Hq=4, Hkv=1, D=64)
+    K = 7
+    idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K, L=L)
+    plain, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, L=L)
+    lin = _bf16_f64(inp["lin"]).reshape(24, 4, 64).numpy()
+    g0, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, g=torch.zeros(4), lin=inp["lin"], L=L)
+    g1, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, g=torch.ones(4), lin=inp["lin"], L=L)
+    assert np.array_equal(g0, lin)  # g = 0 gives the linear branch exactly
+    assert np.array_equal(g1, plain)  # g = 1 gives the sparse attention exactly
+    gv = torch.tensor([0.25, 0.5, 0.75, 0.125])
+    gm, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, g=gv, lin=inp["lin"], L=L)
+    for h in range(4):  # affine in g between the two end points
+        ref = g0[:, h] + gv[h].item() * (g1[:, h] - g0[:, h])
+        assert np.abs(gm[:, h] - ref).max() < 1e-12
+
+
+def pin_routing(L):
+    cfg, sh, inp = _small(seed=41, B=2, Tq=20, Tk=20, Hq=4, Hkv=4, D=64, routed=True)
+    K = 5
+    idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K, L=L)
+    rows = list(range(40))
+    full = torch.zeros(2, 4, dtype=torch.uint8)
+    of, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, g=inp["g"], lin=inp["lin"], route=full, L=L)
+    allowed = np.array([[j <= r % 20 for j in range(20)] for r in rows])
+    ref, _ = _sdpa_masked(inp, sh, allowed, rows)
+    assert np.abs(of - ref).max() < 1e-12  # full heads: causal attention, no gate
+    sparse = torch.ones(2, 4, dtype=torch.uint8)
+    osp, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, g=inp["g"], lin=inp["lin"], route=sparse, L=L)
+    ou, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, g=inp["g"], lin=inp["lin"], L=L)
+    assert np.array_equal(osp, ou)
+    mixed = torch.tensor([[1, 0, 1, 0], [0, 0, 1, 1]], dtype=torch.uint8)
+    om, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, g=inp["g"], lin=inp["lin"], route=mixed, L=L)
+    for b in range(2):
+        for h in range(4):
+            src = osp if mixed[b, h] else of
+            assert np.array_equal(om[b * 20:(b + 1) * 20, h], src[b * 20:(b + 1) * 20, h])
+
+
+def pin_needles_closed_form(L):
+    cfg = E.small_config(B=1, Tq=1, Tk=16384, q_offset=16383, Hq=4, Hkv=1, D=128, H_I=1, D_I=64,
+                         top_k=256, needles=64, seed=2005)
+    inp = E.make_inputs(cfg)
+    sh = E.shape_of(cfg)
+    idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, 256, L=L)
+    out, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, 256, L=L)
+    # head 0's query meets 64 identical needle keys 4*q: their logits sit ~40
+    # above the rest, so the output is the plain mean of the needles' values.
+    vmean = _bf16_f64(inp["v"][0, torch.as_tensor(inp["needles"]), 0]).mean(0).numpy()
+    assert np.abs(out[0, 0] - vmean).max() < 1e-9
+
+
+ALL_PINS = [pin_indexer_golden, pin_indexer_numpy, pin_indexer_onehot, pin_indexer_bound,
+            pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special, pin_topk_needles,
+            pin_attention_full_is_sdpa, pin_attention_sparse_is_masked_sdpa, pin_attention_closed_forms,
+            pin_gate, pin_routing, pin_needles_closed_form]

@@ -1,0 +1,50 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one of them (the mistakes live only in a temporary copy; the
+oracle itself is untouched)."""
+import os
+import tempfile
+
+import pytest
+
+import oracle as O
+from oracle_pins import ALL_PINS
+
+SRC = open(O._SRC).read()
+
+MUTANTS = {
+    "dropped indexer weight": ("s += (int64_t)wI[h] * dot;", "s += dot;"),
+    "indexer head/channel transposed": ("qI[((b * Tq + t) * H_I + h) * D_I + c]", "qI[((b * Tq + t) * D_I + c) * H_I + h]"),
+    "diagonal left out of the prefix": ("long n = q_offset + t + 1;", "long n = q_offset + t;"),
+    "ties go to the higher position": ("return (a->j < b->j) ? -1 : (a->j > b->j);", "return (a->j > b->j) ? -1 : (a->j < b->j);"),
+    "score order flipped": ("return (a->s > b->s) ? -1 : 1;", "return (a->s < b->s) ? -1 : 1;"),
+    "index set not sorted ascending": ("int32_t a = *(const int32_t *)x, b = *(const int32_t *)y;\n    return (a < b) ? -1 : (a > b);",
+                                       "int32_t a = *(const int32_t *)x, b = *(const int32_t *)y;\n    return (a > b) ? -1 : (a < b);"),
+    "wrong key/value head": ("int kh = h / G;", "int kh = h % Hkv;"),
+    "scale dropped": ("logit[i] = dot * scale;", "logit[i] = dot;"),
+    "gate sides swapped": ("oc = gh * oc + (1.0 - gh) * bf16_to_double(lrow[c]);", "oc = (1.0 - gh) * oc + gh * bf16_to_double(lrow[c]);"),
+    "gate applied to full heads": ("if (!full && g != NULL && lrow != NULL)", "if (g != NULL && lrow != NULL)"),
+    "lse misses the max": ("lse[r * Hq + h] = m + log(den);", "lse[r * Hq + h] = log(den);"),
+    "value row from the key cache": ("const uint16_t *vrow = v + ", "const uint16_t *vrow = k + "),
+    "full heads skip the diagonal": ("nk = p + 1;\n                for (long j = 0; j < nk; j++)", "nk = p;\n                for (long j = 0; j < nk; j++)"),
+}
+
+
+def _caught(lib):
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except Exception:
+            return True
+    return False
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    old, new = MUTANTS[name]
+    assert SRC.count(old) == 1, f"mutation site not unique: {name}"
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "mutant.c")
+        with open(src, "w") as f:
+            f.write(SRC.replace(old, new))
+        so = O.build(src=src, out=os.path.join(d, "libmutant.so"))
+        assert _caught(O.lib(so)), f"no pin catches: {name}"
