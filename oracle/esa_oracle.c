@@ -145,6 +145,7 @@ int oracle_topk_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
  *  - logit_j = scale * sum_c q[b,t,h,c] * k[b,j,kh,c];  m = max logit;
  *    o = sum_j e^(logit_j - m) v[b,j,kh,:] / sum_j e^(logit_j - m);
  *    lse = m + ln sum_j e^(logit_j - m).
+ *  - An empty key set (cnt = 0) gives o = 0 and lse = -inf.
  *  - Sparse heads with g given: out = g[h]*o + (1-g[h])*lin[b,t,h,:];
  *    full heads (and sparse heads without g): out = o.
  * q, lin: [B,Tq,Hq,D] bf16 bits; k, v: [B,Tk,Hkv,D] bf16 bits; idx/cnt are
@@ -209,7 +210,8 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
             double *o = out + (r * Hq + h) * (long)D;
             const uint16_t *lrow = lin ? lin + ((b * Tq + t) * Hq + h) * (long)D : NULL;
             for (int c = 0; c < D; c++) {
-                double oc = acc[c] / den;
+                /* an empty key set (cnt = 0) attends to nothing: o = 0 */
+                double oc = nk > 0 ? acc[c] / den : 0.0;
                 if (!full && g != NULL && lrow != NULL) {
                     double gh = (double)g[h];
                     oc = gh * oc + (1.0 - gh) * bf16_to_double(lrow[c]);

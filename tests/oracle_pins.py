@@ -245,6 +245,20 @@ def pin_attention_closed_forms(L):
             assert abs(torch.exp(logits - lse[r, h]).sum().item() - 1.0) < 1e-13
 
 
+def pin_empty_set(L):
+    """cnt = 0: no key is attended: o = 0, lse = -inf, gated out = (1-g) lin."""
+    cfg, sh, inp = _small(seed=43, Tq=8, Tk=8, Hq=2, Hkv=1, D=64)
+    K = 4
+    idx = np.full((8, K), -1, dtype=np.int32)
+    cnt = np.zeros(8, dtype=np.int32)
+    o, lse = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, L=L)
+    assert (o == 0).all() and np.isneginf(lse).all()
+    og, _ = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, g=inp["g"], lin=inp["lin"], L=L)
+    lin = _bf16_f64(inp["lin"]).reshape(8, 2, 64).numpy()
+    g = inp["g"].double().numpy()
+    assert np.array_equal(og, (1.0 - g)[None, :, None] * lin)
+
+
 def pin_gate(L):
     cfg, sh, inp = _small(seed=37, Tq=24, Tk=24, Hq=4, Hkv=1, D=64)
     K = 7
@@ -300,4 +314,4 @@ def pin_needles_closed_form(L):
 ALL_PINS = [pin_indexer_golden, pin_indexer_numpy, pin_indexer_onehot, pin_indexer_bound,
             pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special, pin_topk_needles,
             pin_attention_full_is_sdpa, pin_attention_sparse_is_masked_sdpa, pin_attention_closed_forms,
-            pin_gate, pin_routing, pin_needles_closed_form]
+            pin_empty_set, pin_gate, pin_routing, pin_needles_closed_form]
