@@ -1,0 +1,371 @@
+"""Benchmark of the gated fine-grained sparse attention hot path on B300.
+
+One step = one decode pass of the whole path for every sequence of the batch:
+indexer scores over the full 131,072-key cache, exact top-2048 selection
+(esa_topk_select), gathered sparse attention with the gate mix fused
+(esa_sparse_attn). Workload: 8 sequences, 1 new token each, 32 query heads
+sharing 1 KV head, head dim 128, indexer 1 head x 64 (int8), synthetic seeded
+inputs. Multi-GPU runs are replicas (each rank its own batch, no collective
+on the data path): scaling "weak", value = tokens of all ranks / max time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl esa|reference]
+  python bench.py --workload long_prefill|routed_prefill|million_decode|tiny_prefill
+
+Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "sparse-attn prefill tok/s + decode µs/step @1 B300; % HBM/tensor roofline"
+NSETS = 4  # rotating input sets: their kI caches together exceed the 126 MB L2
+
+
+def _load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d.get("bf16_tflops"), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while a region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _traffic_for(kernel: str, src_files: list[str]):
+    """dram bytes per launch recorded from an ncu capture, if the kernel source
+    is unchanged since (the capture stores a hash of its sources)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d:
+        return None
+    h = hashlib.sha256()
+    for f in src_files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return d["bytes_per_launch"] if d.get("src_sha256") == h.hexdigest() else None
+
+
+SELECT_SRC = ["long_context_sparse_20_b300/csrc/k_select_split.cu", "long_context_sparse_20_b300/csrc/esa_device.cuh"]
+ATTN_SRC = ["long_context_sparse_20_b300/csrc/k_sparse_attn.cu", "long_context_sparse_20_b300/csrc/esa_device.cuh"]
+
+
+def decode_bytes(sh: dict, K: int):
+    """Algorithmic HBM bytes of one decode step, per kernel (DESIGN: roofline)."""
+    B, L, Hq, Hkv, D, HI, DI = (sh[k] for k in ("B", "Tk", "Hq", "Hkv", "D", "H_I", "D_I"))
+    sel = B * L * DI + B * HI * DI + B * K * 4 + B * 4            # kI stream, qI, idx + cnt written
+    k_sel = min(K, L)
+    attn = B * k_sel * Hkv * D * 2 * 2 + B * k_sel * 4 + B * 4      # gathered K and V rows, idx + cnt read
+    attn += B * Hq * D * 2 * 2 + B * Hq * D * 4 + Hq * 4            # q, lin in; out (fp32) out; g
+    return sel, attn
+
+
+def run_cpu_baseline(cfg: dict, inp: dict, seconds: float = 10.0):
+    """The oracle, as it stands, on whole decode steps (all rows of the batch),
+    repeated for about `seconds`; returns tok/s, threads, sample text."""
+    sys.path.insert(0, ROOT)
+    import esa_inputs as E
+    import oracle as O
+    sh = E.shape_of(cfg)
+    K = cfg["top_k"]
+    O.lib()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        O.gated_sparse_attention(inp, sh, K)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    rows = sh["B"] * sh["Tq"]
+    threads = min(O.threads(), rows)
+    return rows * reps / el, threads, f"{reps} full decode steps ({rows} rows each), {el:.1f} s"
+
+
+def reference_arm(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    sys.path.insert(0, ROOT)
+    import esa_inputs as E
+    cfg = E.CONFIGS[args.workload]
+    inp = E.make_inputs(cfg)
+    import oracle as O
+    sh = E.shape_of(cfg)
+    K = cfg["top_k"]
+    O.lib()
+    rows = sh["B"] * sh["Tq"]
+    # each step: one query row of the workload, in turn (a bounded sample)
+    for i in range(args.warmup):
+        O.gated_sparse_attention(inp, sh, K, rows=[i % rows])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        O.gated_sparse_attention(inp, sh, K, rows=[i % rows])
+    el = time.perf_counter() - t0
+    val = args.steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "B": sh["B"], "cache_len": sh["Tk"], "Hq": sh["Hq"],
+                       "Hkv": sh["Hkv"], "D": sh["D"], "D_I": sh["D_I"], "top_k": K},
+            "cpu_baseline": {"value": val, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} steps of one query row each (rows taken in turn)"},
+            "e2e": {"value": val, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def esa_arm(args):
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sys.path.insert(0, ROOT)
+    import esa_inputs as E
+    import long_context_sparse_20_b300 as esa
+
+    cfg = dict(E.CONFIGS[args.workload])
+    assert cfg["Tq"] == 1, "the step benchmark runs decode workloads"
+    sh = E.shape_of(cfg)
+    K = cfg["top_k"]
+    B, L, Hq, Hkv, D, HI, DI = (sh[k] for k in ("B", "Tk", "Hq", "Hkv", "D", "H_I", "D_I"))
+    host = E.make_inputs(cfg, seed=cfg["seed"] + 1000 * rank)
+    shape = esa.shape_from(sh)
+    scale = 1.0 / math.sqrt(D)
+
+    # NSETS rotating copies of the whole decode state, each with its outputs
+    sets = []
+    for _ in range(NSETS):
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+        d["idx"] = torch.empty(B, 1, K, dtype=torch.int32, device=dev)
+        d["cnt"] = torch.empty(B, 1, dtype=torch.int32, device=dev)
+        d["out"] = torch.empty(B, 1, Hq, D, dtype=torch.float32, device=dev)
+        d["ws_sel"] = esa.workspace_for(esa.OP_TOPK_SELECT, shape, K, dev)
+        d["ws_att"] = esa.workspace_for(esa.OP_SPARSE_ATTN, shape, K, dev)
+        sets.append(d)
+
+    def step(d, ev=None):
+        st = torch.cuda.current_stream(dev)
+        if ev:
+            ev[0].record(st)
+        esa.esa_topk_select(d["qI"], d["kI"], d["wI"], shape, K, d["idx"], d["cnt"], d["ws_sel"], st)
+        if ev:
+            ev[1].record(st)
+        esa.esa_sparse_attn(d["q"], d["k"], d["v"], d["idx"], d["cnt"], shape, K, scale, d["g"], d["lin"], d["out"],
+                            None, d["ws_att"], st)
+        if ev:
+            ev[2].record(st)
+
+    for i in range(max(3, args.warmup)):
+        step(sets[i % NSETS])
+    torch.cuda.synchronize()
+    for d in sets:
+        for w in (d["ws_sel"], d["ws_att"]):
+            assert esa.esa_read_status(w) == 0
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # The K timed steps are captured once into a CUDA graph (kernel launches
+    # and per-kernel event records), so that host launch overhead does not
+    # starve the GPU; the graph is replayed once untimed, then once timed.
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] for _ in range(args.steps)]
+    timing = "cuda-graph"
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                step(sets[i % NSETS], evs[i])
+        graph.replay()
+        torch.cuda.synchronize()
+        run = graph.replay
+    except Exception as exc:  # capture unsupported: time eager launches
+        timing = f"eager ({type(exc).__name__})"
+        torch.cuda.synchronize()
+
+        def run():
+            for i in range(args.steps):
+                step(sets[i % NSETS], evs[i])
+    with Clocks(local) as clk:
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        run()
+        t1.record()
+        barrier()
+    clocks = clk.summary()
+    total_ms = t0.elapsed_time(t1)
+    sel_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    att_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    for d in sets:
+        for w in (d["ws_sel"], d["ws_att"]):
+            assert esa.esa_read_status(w) == 0
+
+    # ---- end to end through host buffers: per step copy the new token's
+    # inputs in (q, qI, lin, its K/V/kI rows written at position L-1) and the
+    # output back
+    pin = lambda t: t.pin_memory()
+    h_q, h_qI, h_lin = pin(host["q"]), pin(host["qI"]), pin(host["lin"])
+    h_knew, h_vnew = pin(host["k"][:, L - 1:L].contiguous()), pin(host["v"][:, L - 1:L].contiguous())
+    h_kInew = pin(host["kI"][:, L - 1:L].contiguous())
+    h_out = torch.empty(B, 1, Hq, D, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_qI, h_lin, h_knew, h_vnew, h_kInew))
+    d2h = h_out.numel() * 4
+
+    def e2e_step(d):
+        d["q"].copy_(h_q, non_blocking=True)
+        d["qI"].copy_(h_qI, non_blocking=True)
+        d["lin"].copy_(h_lin, non_blocking=True)
+        d["k"][:, L - 1:L].copy_(h_knew, non_blocking=True)
+        d["v"][:, L - 1:L].copy_(h_vnew, non_blocking=True)
+        d["kI"][:, L - 1:L].copy_(h_kInew, non_blocking=True)
+        step(d)
+        h_out.copy_(d["out"], non_blocking=True)
+
+    for i in range(3):
+        e2e_step(sets[i % NSETS])
+    barrier()
+    a0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(sets[i % NSETS])
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - a0) * 1e3
+    barrier()
+
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms, e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = tt.tolist()
+    ms_step = total_ms / args.steps
+    tok_per_step = B * world
+    value = tok_per_step / (ms_step / 1e3)
+
+    sel_bytes, att_bytes = decode_bytes(sh, K)
+    sel_avg, att_avg = statistics.mean(sel_ms), statistics.mean(att_ms)
+    peak_gbs, _, peak_kind = _load_peaks()
+    dom_is_sel = sel_avg >= att_avg
+    dom_ms, dom_bytes = (sel_avg, sel_bytes) if dom_is_sel else (att_avg, att_bytes)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    traffic = _traffic_for("split_select" if dom_is_sel else "sparse_attn", SELECT_SRC if dom_is_sel else ATTN_SRC)
+
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            v, cores, sample = run_cpu_baseline(cfg, host, seconds=args.cpu_seconds)
+            cpu = {"value": v, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": f"{args.workload}: B={B} x 1 new token, cache {L}, Hq={Hq}, Hkv={Hkv}, D={D}, "
+                                   f"indexer {HI}x{DI} int8, top_k={K}",
+                       "global_batch": B * world, "seq_len": L, "parallelism": f"replicas x{world}",
+                       "l2": f"{NSETS} rotating input sets (kI caches {NSETS * B * L * DI / 2**20:.0f} MiB > 126 MB L2)",
+                       "timing": timing},
+            "roofline": {"bound": "hbm", "kernel": "split_select" if dom_is_sel else "sparse_attn",
+                         "achieved": achieved, "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
+                         "peak_kind": peak_kind, "traffic": traffic, "algorithmic_bytes": dom_bytes,
+                         "avg_launch_us": dom_ms * 1e3},
+            "kernels_us": {"split_select": sel_avg * 1e3, "sparse_attn": att_avg * 1e3},
+            "step_roofline": {"achieved": (sel_bytes + att_bytes) / (ms_step / 1e3) / 1e9, "peak": peak_gbs,
+                              "frac": (sel_bytes + att_bytes) / (ms_step / 1e3) / 1e9 / peak_gbs,
+                              "algorithmic_bytes": sel_bytes + att_bytes},
+            "gpu_launches": 2 * args.steps,
+            "e2e": {"value": tok_per_step / (e2e_ms / args.steps / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="esa", choices=["esa", "reference"])
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        esa_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -24,8 +24,10 @@ Generator (its definition, so that anyone can re-derive every value):
 """
 from __future__ import annotations
 
+import ctypes
 import math
 import os
+import subprocess
 from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
@@ -99,12 +101,45 @@ def _normal_f64(seed: int, tid: int, start: int, n: int) -> np.ndarray:
     return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
 
 
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_GEN_SRC = os.path.join(_HERE, "gen.c")
+_GEN_SO = os.path.join(_HERE, "_build", "libesa_gen.so")
+_gen = None
+
+
+def _genlib():
+    """The C version of the same generator (bulk tensors), built on first use."""
+    global _gen
+    if _gen is None:
+        if not os.path.exists(_GEN_SO) or os.path.getmtime(_GEN_SO) < os.path.getmtime(_GEN_SRC):
+            os.makedirs(os.path.dirname(_GEN_SO), exist_ok=True)
+            subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", _GEN_SO, _GEN_SRC, "-lm"], check=True)
+        _gen = ctypes.CDLL(_GEN_SO)
+        for f in (_gen.gen_normal_bf16, _gen.gen_int8_uniform):
+            f.restype = None
+            f.argtypes = [ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    return _gen
+
+
 def normal_bf16_bits(seed: int, tid: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint16)
+    _genlib().gen_normal_bf16(stream_key(seed, tid), 0, n, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def int8_uniform(seed: int, tid: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.int8)
+    _genlib().gen_int8_uniform(stream_key(seed, tid), 0, n, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def normal_bf16_bits_np(seed: int, tid: int, n: int) -> np.ndarray:
+    """numpy restatement of :func:`normal_bf16_bits` (checks the C loop)."""
     out = np.empty(n, dtype=np.uint16)
     return _chunked(n, lambda s, c: _f32_to_bf16_bits(_normal_f64(seed, tid, s, c).astype(np.float32)), out)
 
 
-def int8_uniform(seed: int, tid: int, n: int) -> np.ndarray:
+def int8_uniform_np(seed: int, tid: int, n: int) -> np.ndarray:
     out = np.empty(n, dtype=np.int8)
     return _chunked(n, lambda s, c: ((words(seed, tid, s, c) >> np.uint64(60)).astype(np.int16) - 8).astype(np.int8), out)
 

@@ -1,0 +1,187 @@
+/*
+ * esa.h — C ABI of the gated fine-grained sparse attention library (libesa.so).
+ *
+ * The method (sources named per call below):
+ *   1. an Indexer scores each query against every causal-prefix key, without
+ *      RoPE ("超大规模MoE架构中稀疏注意力机制的演进与实践", sections 二.1 and 二.2);
+ *   2. a per-query Top-K keeps the K best positions (same page, section 二.1;
+ *      "混合注意力架构演进…", section 三);
+ *   3. K/V are gathered at those positions and exact softmax attention runs
+ *      over them (the pseudo-code of section 四.1 of the first page; section
+ *      三 of the second, softmax(Q K_sel^T / sqrt(d)) V_sel);
+ *   4. a per-head gate mixes that output with a linear-attention branch,
+ *      final = g*attn + (1-g)*linear_output (first page, sections 二.3, 四.1);
+ *   5. optionally a per-head route sends each head to full causal attention or
+ *      to the sparse path inside one launch ("Elastic Attention…", 2.2, 3.1).
+ *
+ * Conventions shared by every call
+ *   - Pointers named as tensors are DEVICE pointers owned by the caller; all
+ *     tensors are dense, row-major, with the layouts stated below. bf16 data
+ *     is passed as its 16-bit patterns (uint16_t).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Every call is asynchronous on it.
+ *   - Host-detectable errors (null pointers, bad sizes, unsupported shapes,
+ *     workspace too small) are returned before anything is launched.
+ *   - Device-side errors never trap: kernels record the first error code in
+ *     the workspace status word and return; read it with esa_read_status().
+ *   - The library allocates no device memory and keeps no global state; it
+ *     is thread-safe as long as concurrent calls use distinct workspaces.
+ *   - Workspace: a caller-allocated device buffer of at least
+ *     esa_workspace_size() bytes, 256-byte aligned, zero-filled once before
+ *     its first use (esa_workspace_init). Calls leave it ready for the next
+ *     call (they clear what they use), except after a device error, after
+ *     which it must be re-initialised. Calls that share a workspace must not
+ *     overlap in time (use one stream per workspace).
+ *
+ * Shapes (esa_shape):
+ *   B sequences; Tq query rows per sequence; Tk key positions per sequence;
+ *   query row t sits at absolute position p = q_offset + t and its causal
+ *   prefix is keys 0..p inclusive (n = p+1 keys). Prefill: Tq = Tk,
+ *   q_offset = 0. Decode: Tq = 1, q_offset = Tk-1 (the cache already holds
+ *   the new token). Chunked prefill: q_offset + Tq <= Tk.
+ *   Hq query heads, Hkv key/value heads (Hq % Hkv == 0; query head h reads
+ *   key/value head h / (Hq/Hkv)), head dim D in {64, 128};
+ *   H_I indexer heads (1..16) of dim D_I in {16, 32, 64, 128}.
+ *
+ * Tensor layouts:
+ *   qI  int8  [B, Tq, H_I, D_I]     indexer queries
+ *   kI  int8  [B, Tk, D_I]          indexer keys, one per position, shared by
+ *                                    all indexer heads
+ *   wI  int32 [H_I]                 indexer head weights
+ *   q   bf16  [B, Tq, Hq, D]
+ *   k,v bf16  [B, Tk, Hkv, D]
+ *   idx int32 [B, Tq, top_k]        selected positions, ascending, -1 padded
+ *   cnt int32 [B, Tq]               min(top_k, p+1)
+ *   g   fp32  [Hq]                  gate, already in (0,1)
+ *   lin bf16  [B, Tq, Hq, D]        linear-attention branch output
+ *   out fp32  [B, Tq, Hq, D]
+ *   lse fp32  [B, Tq, Hq]           natural-log sum-exp of the scaled logits
+ *   route uint8 [B, Hq]             1 = sparse head, 0 = full head
+ */
+#ifndef ESA_H
+#define ESA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ESA_API __attribute__((visibility("default")))
+#else
+#define ESA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t esa_status;
+
+#define ESA_OK 0
+#define ESA_ERR_INVALID 1     /* bad argument (null pointer, size, shape, top_k) */
+#define ESA_ERR_UNSUPPORTED 2 /* well-formed but outside what this build handles */
+#define ESA_ERR_CUDA 3        /* a CUDA runtime call failed (launch, copy, sync) */
+#define ESA_ERR_TIMEOUT 4     /* device: a bounded inter-block wait gave up */
+#define ESA_ERR_BAD_INDEX 5   /* device: an index outside the causal prefix, or cnt
+                                 outside 0..min(top_k, p+1); the row is skipped */
+#define ESA_ERR_WORKSPACE 6   /* workspace null, misaligned or too small */
+#define ESA_ERR_INTERNAL 7    /* device: a kernel's own consistency check failed; the
+                                 outputs of that call are not valid */
+
+typedef struct esa_shape {
+    int64_t B;
+    int64_t Tq;
+    int64_t Tk;
+    int64_t q_offset;
+    int32_t Hq;
+    int32_t Hkv;
+    int32_t D;
+    int32_t H_I;
+    int32_t D_I;
+} esa_shape;
+
+/* Operation ids for esa_workspace_size. */
+#define ESA_OP_INDEXER_SCORE 0
+#define ESA_OP_TOPK_SELECT 1
+#define ESA_OP_SPARSE_ATTN 2
+#define ESA_OP_GATED_MIX 3
+#define ESA_OP_ROUTED_ATTN 4
+
+/* Bytes of workspace that `op` needs for shape `s` and `top_k` (0 when the
+ * op needs none beyond the status word, which every op may write; the
+ * minimum returned is 256). Returns 0 for an invalid op or shape. */
+ESA_API size_t esa_workspace_size(int op, const esa_shape *s, int top_k);
+
+/* Zero-fill a workspace (cudaMemsetAsync on `stream`). Needed once before
+ * first use and after any device error. */
+ESA_API esa_status esa_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Indexer scores (Gated DSA page, section 二.1: the query's relevance to every
+ * history position; section 二.2: no RoPE):
+ *   scores[b,t,j] = sum_h wI[h] * sum_c qI[b,t,h,c] * kI[b,j,c]   for j <= p,
+ *   scores[b,t,j] = INT32_MIN                                      for j > p.
+ * scores int32 [B, Tq, Tk] (a diagnostic: the selection never materialises
+ * this). Every score must fit in int32, which holds when
+ * sum_h |wI[h]| * D_I * 16384 < 2^31. */
+ESA_API esa_status esa_indexer_score(const int8_t *qI, const int8_t *kI, const int32_t *wI, const esa_shape *s,
+                             int32_t *scores, void *ws, size_t ws_bytes, void *stream);
+
+/* Top-K selection (Gated DSA page, section 二.1, K = 2048 in its setting;
+ * the hybrid-architecture page, section 三: idx = topk(indexer_score(Q,K))).
+ * For each query row: the min(top_k, p+1) positions j <= p with the largest
+ * indexer score, ties going to the lower position, written ascending to
+ * idx[b,t,:], -1 padded; cnt[b,t] = min(top_k, p+1). Exact (integer) and
+ * deterministic. top_k in 1..65536. The full score row is never written to
+ * device memory. */
+ESA_API esa_status esa_topk_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const esa_shape *s, int top_k,
+                           int32_t *idx, int32_t *cnt, void *ws, size_t ws_bytes, void *stream);
+
+/* Attention over the selected keys (Gated DSA pseudo-code, section 四.1:
+ * gather then scaled_dot_product_attention; hybrid page, section 三). For
+ * each row and query head h (key/value head kh = h / (Hq/Hkv)):
+ *   l_j = scale * q[b,t,h,:] . k[b,j,kh,:]  over j in idx[b,t,0..cnt-1],
+ *   o   = sum_j softmax(l)_j v[b,j,kh,:],   lse = log sum_j exp(l_j),
+ *   out = g[h]*o + (1-g[h])*lin[b,t,h,:]    when g and lin are both given
+ *         (the gate mix of sections 二.3/四.1, fused), else out = o.
+ * fp32 accumulation, fp32 output. scale is normally 1/sqrt(D). g, lin and
+ * lse may be NULL (g and lin together). A row with cnt = 0 gets out = 0 (or
+ * the linear branch share when gated) and lse = -inf. Indices outside
+ * 0..p, or cnt outside 0..min(top_k, p+1), set ESA_ERR_BAD_INDEX in the
+ * status word; the offending row is left unwritten. */
+ESA_API esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,
+                           const int32_t *cnt, const esa_shape *s, int top_k, float scale, const float *g,
+                           const uint16_t *lin, float *out, float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* Gate mix on its own (Gated DSA page, sections 二.3 and 四.1 step 5):
+ *   out[b,t,h,:] = g[h]*attn[b,t,h,:] + (1-g[h])*lin[b,t,h,:]
+ * for heads with head_mask[b,h] != 0 (all heads when head_mask is NULL);
+ * other heads copy attn. attn/out fp32 [B,Tq,Hq,D] (out may alias attn),
+ * lin bf16 [B,Tq,Hq,D], g fp32 [Hq], head_mask uint8 [B,Hq]. */
+ESA_API esa_status esa_gated_mix(const float *attn, const uint16_t *lin, const float *g, const uint8_t *head_mask,
+                         const esa_shape *s, float *out, void *stream);
+
+/* Per-head routed attention (Elastic Attention page, sections 2.2 and 3.1:
+ * each head runs either full or sparse attention, decided per head, inside
+ * one fused kernel). route[b,h] = 0: exact causal attention over all keys
+ * 0..p, output without the gate. route[b,h] = 1: the sparse path — the
+ * index set of esa_topk_select (one set per (b,t), shared by all sparse
+ * heads), attention over it, then the gate mix with lin when g and lin are
+ * given. Every head of the layer runs in one attention launch. scale is
+ * normally 1/sqrt(D). Requires D_I >= 32 and H_I * D_I <= 512. */
+ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
+                           const int8_t *kI, const int32_t *wI, const uint8_t *route, const esa_shape *s, int top_k,
+                           float scale, const float *g, const uint16_t *lin, float *out, void *ws, size_t ws_bytes,
+                           void *stream);
+
+/* Synchronise `stream`, read the workspace status word into *dev_status
+ * (ESA_OK when no kernel recorded an error) and clear it. Returns ESA_OK, or
+ * ESA_ERR_CUDA when the synchronisation or the copy failed. */
+ESA_API esa_status esa_read_status(void *ws, void *stream, int32_t *dev_status);
+
+/* A static, human-readable name for a status code. */
+ESA_API const char *esa_status_string(esa_status st);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ESA_H */

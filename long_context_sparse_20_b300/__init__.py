@@ -1,0 +1,162 @@
+"""Python binding of libesa.so — gated fine-grained sparse attention on B300.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. Functions carry the names of the C entry points (see
+``include/esa.h``) and take torch CUDA tensors (device memory) plus an
+optional stream; they raise :class:`EsaError` when a call returns a non-zero
+status. There is no CPU fallback: importing this package without the built
+library raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libesa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m long_context_sparse_20_b300.build`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_INDEX, ERR_WORKSPACE, ERR_INTERNAL = range(8)
+OP_INDEXER_SCORE, OP_TOPK_SELECT, OP_SPARSE_ATTN, OP_GATED_MIX, OP_ROUTED_ATTN = range(5)
+
+
+class esa_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("Tq", ctypes.c_int64), ("Tk", ctypes.c_int64), ("q_offset", ctypes.c_int64),
+                ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32), ("H_I", ctypes.c_int32),
+                ("D_I", ctypes.c_int32)]
+
+
+class EsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+_sp = ctypes.POINTER(esa_shape)
+_SIGS = {
+    "esa_workspace_size": (_sz, [ctypes.c_int, _sp, ctypes.c_int]),
+    "esa_workspace_init": (_i32, [_vp, _sz, _vp]),
+    "esa_indexer_score": (_i32, [_vp, _vp, _vp, _sp, _vp, _vp, _sz, _vp]),
+    "esa_topk_select": (_i32, [_vp, _vp, _vp, _sp, ctypes.c_int, _vp, _vp, _vp, _sz, _vp]),
+    "esa_sparse_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
+                               _sz, _vp]),
+    "esa_gated_mix": (_i32, [_vp, _vp, _vp, _vp, _sp, _vp, _vp]),
+    "esa_routed_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp,
+                               _vp, _sz, _vp]),
+    "esa_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
+    "esa_status_string": (ctypes.c_char_p, [_i32]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype, _f.argtypes = _res, _args
+
+
+def exported_symbols():
+    return sorted(_SIGS)
+
+
+def status_string(st: int) -> str:
+    return _lib.esa_status_string(st).decode()
+
+
+def make_shape(B, Tq, Tk, q_offset, Hq=1, Hkv=1, D=64, H_I=1, D_I=64) -> esa_shape:
+    return esa_shape(B, Tq, Tk, q_offset, Hq, Hkv, D, H_I, D_I)
+
+
+def shape_from(d: dict) -> esa_shape:
+    return make_shape(*(d[k] for k in ("B", "Tq", "Tk", "q_offset", "Hq", "Hkv", "D", "H_I", "D_I")))
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, ref: torch.Tensor):
+    if stream is None:
+        stream = torch.cuda.current_stream(ref.device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(st: int, where: str):
+    if st != OK:
+        raise EsaError(st, where)
+
+
+class Workspace:
+    """A zero-initialised device workspace (torch-allocated uint8 buffer)."""
+
+    def __init__(self, nbytes: int, device="cuda"):
+        self.nbytes = max(256, int(nbytes))
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+    def fits(self, nbytes: int) -> bool:
+        return nbytes <= self.nbytes
+
+
+def esa_workspace_size(op: int, shape: esa_shape, top_k: int = 1) -> int:
+    return int(_lib.esa_workspace_size(op, ctypes.byref(shape), top_k))
+
+
+def esa_workspace_init(ws: Workspace, stream=None):
+    _check(_lib.esa_workspace_init(ws.ptr, ws.nbytes, _stream(stream, ws.buf)), "esa_workspace_init")
+
+
+def workspace_for(op: int, shape: esa_shape, top_k: int = 1, device="cuda") -> Workspace:
+    n = esa_workspace_size(op, shape, top_k)
+    if n == 0:
+        raise EsaError(ERR_INVALID, "esa_workspace_size")
+    return Workspace(n, device)
+
+
+def esa_indexer_score(qI, kI, wI, shape: esa_shape, scores, ws: Workspace, stream=None):
+    _check(_lib.esa_indexer_score(_p(qI), _p(kI), _p(wI), ctypes.byref(shape), _p(scores), ws.ptr, ws.nbytes,
+                                  _stream(stream, qI)), "esa_indexer_score")
+
+
+def esa_topk_select(qI, kI, wI, shape: esa_shape, top_k: int, idx, cnt, ws: Workspace, stream=None):
+    _check(_lib.esa_topk_select(_p(qI), _p(kI), _p(wI), ctypes.byref(shape), top_k, _p(idx), _p(cnt), ws.ptr,
+                                ws.nbytes, _stream(stream, qI)), "esa_topk_select")
+
+
+def _bits(t):
+    """bf16 tensors travel as their 16-bit patterns."""
+    if t is None:
+        return None
+    assert t.dtype == torch.bfloat16, t.dtype
+    return t
+
+
+def esa_sparse_attn(q, k, v, idx, cnt, shape: esa_shape, top_k: int, scale: float, g, lin, out, lse,
+                    ws: Workspace, stream=None):
+    _check(_lib.esa_sparse_attn(_p(_bits(q)), _p(_bits(k)), _p(_bits(v)), _p(idx), _p(cnt), ctypes.byref(shape),
+                                top_k, float(scale), _p(g), _p(_bits(lin)), _p(out), _p(lse), ws.ptr, ws.nbytes,
+                                _stream(stream, q)), "esa_sparse_attn")
+
+
+def esa_gated_mix(attn, lin, g, head_mask, shape: esa_shape, out, stream=None):
+    _check(_lib.esa_gated_mix(_p(attn), _p(_bits(lin)), _p(g), _p(head_mask), ctypes.byref(shape), _p(out),
+                              _stream(stream, attn)), "esa_gated_mix")
+
+
+def esa_routed_attn(q, k, v, qI, kI, wI, route, shape: esa_shape, top_k: int, scale: float, g, lin, out,
+                    ws: Workspace, stream=None):
+    _check(_lib.esa_routed_attn(_p(_bits(q)), _p(_bits(k)), _p(_bits(v)), _p(qI), _p(kI), _p(wI), _p(route),
+                                ctypes.byref(shape), top_k, float(scale), _p(g), _p(_bits(lin)), _p(out), ws.ptr,
+                                ws.nbytes, _stream(stream, q)), "esa_routed_attn")
+
+
+def esa_read_status(ws: Workspace, stream=None) -> int:
+    st = _i32(0)
+    _check(_lib.esa_read_status(ws.ptr, _stream(stream, ws.buf), ctypes.byref(st)), "esa_read_status")
+    return int(st.value)

@@ -1,0 +1,262 @@
+// extern "C" entry points of libesa.so: argument checks, workspace planning
+// and dispatch to the kernels. See include/esa.h for the contract.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "esa_internal.h"
+
+namespace esa {
+
+DevInfo device_info() {
+    static std::mutex mu;
+    static DevInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 0 && dev < 64 && have[dev]) return cache[dev];
+    DevInfo di{};
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    di.sms = v > 0 ? v : 1;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    di.smem_optin = (size_t)v;
+    if (dev >= 0 && dev < 64) {
+        cache[dev] = di;
+        have[dev] = true;
+    }
+    return di;
+}
+
+bool ensure_smem(const void *fn, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, size_t> set_to;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(dev, fn);
+    auto it = set_to.find(key);
+    if (it != set_to.end() && it->second >= smem) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    set_to[key] = smem;
+    return true;
+}
+
+int occupancy(const void *fn, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    auto key = std::make_tuple(dev, fn, threads, smem);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    if (!ensure_smem(fn, smem)) return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        per_sm = 0;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = per_sm;
+    return per_sm;
+}
+
+long long wait_limit_ns() {
+    const char *e = getenv("ESA_WAIT_LIMIT_NS");
+    long long v = e ? atoll(e) : 0;
+    return v > 0 ? v : 1000000000ll;  // 1 s
+}
+
+int debug_extra_arrivals() {
+    const char *e = getenv("ESA_DEBUG_EXTRA_ARRIVALS");
+    int v = e ? atoi(e) : 0;
+    return v > 0 ? v : 0;
+}
+
+}  // namespace esa
+
+using namespace esa;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks common to every call; `need_attn` adds the attention fields,
+// `need_index` the indexer fields.
+esa_status check_shape(const esa_shape *s, bool need_attn, bool need_index) {
+    if (!s) return ESA_ERR_INVALID;
+    if (s->B < 0 || s->Tq < 0 || s->Tk < 0 || s->q_offset < 0) return ESA_ERR_INVALID;
+    if (s->q_offset + s->Tq > s->Tk) return ESA_ERR_INVALID;
+    if (s->Tk > (int64_t)INT32_MAX) return ESA_ERR_UNSUPPORTED;
+    if (need_attn) {
+        if (s->Hq <= 0 || s->Hkv <= 0 || s->Hq % s->Hkv) return ESA_ERR_INVALID;
+        if (s->D != 64 && s->D != 128) return ESA_ERR_UNSUPPORTED;
+    }
+    if (need_index) {
+        if (s->H_I <= 0 || s->H_I > 16) return ESA_ERR_UNSUPPORTED;
+        if (s->D_I != 16 && s->D_I != 32 && s->D_I != 64 && s->D_I != 128) return ESA_ERR_UNSUPPORTED;
+    }
+    return ESA_OK;
+}
+
+Shape to_shape(const esa_shape *s) {
+    Shape x;
+    x.B = s->B;
+    x.Tq = s->Tq;
+    x.Tk = s->Tk;
+    x.q_offset = s->q_offset;
+    x.Hq = s->Hq;
+    x.Hkv = s->Hkv;
+    x.D = s->D;
+    x.H_I = s->H_I;
+    x.D_I = s->D_I;
+    return x;
+}
+
+esa_status check_ws(void *ws, size_t ws_bytes, size_t need) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return ESA_ERR_WORKSPACE;
+    if (ws_bytes < need) return ESA_ERR_WORKSPACE;
+    return ESA_OK;
+}
+
+size_t topk_ws(const Shape &s, int K) {
+    SplitPlan sp = plan_split_select(s, K);
+    size_t w = sp.ok ? sp.ws_bytes : ws_row_select(s, K);
+    return w < kStatusBytes ? kStatusBytes : w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t esa_workspace_size(int op, const esa_shape *s, int top_k) {
+    bool attn = op == ESA_OP_SPARSE_ATTN || op == ESA_OP_ROUTED_ATTN || op == ESA_OP_GATED_MIX;
+    bool index = op == ESA_OP_INDEXER_SCORE || op == ESA_OP_TOPK_SELECT || op == ESA_OP_ROUTED_ATTN;
+    if (op < 0 || op > 4 || check_shape(s, attn, index) != ESA_OK) return 0;
+    if ((op == ESA_OP_TOPK_SELECT || op == ESA_OP_SPARSE_ATTN || op == ESA_OP_ROUTED_ATTN) && top_k <= 0) return 0;
+    Shape x = to_shape(s);
+    switch (op) {
+        case ESA_OP_TOPK_SELECT: return topk_ws(x, top_k);
+        case ESA_OP_SPARSE_ATTN: return plan_sparse_attn(x, top_k).ws_bytes;
+        case ESA_OP_ROUTED_ATTN: return ws_routed(x, top_k);
+        default: return kStatusBytes;
+    }
+}
+
+esa_status esa_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+    if (!ws || ws_bytes == 0) return ESA_ERR_WORKSPACE;
+    return cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
+}
+
+esa_status esa_indexer_score(const int8_t *qI, const int8_t *kI, const int32_t *wI, const esa_shape *s,
+                             int32_t *scores, void *ws, size_t ws_bytes, void *stream) {
+    esa_status e = check_shape(s, false, true);
+    if (e) return e;
+    if (!qI || !kI || !wI || !scores) return ESA_ERR_INVALID;
+    if (!aligned16(qI) || !aligned16(kI) || !aligned16(scores)) return ESA_ERR_INVALID;
+    if ((e = check_ws(ws, ws_bytes, kStatusBytes))) return e;
+    return launch_indexer_score(qI, kI, wI, to_shape(s), scores, (cudaStream_t)stream) == cudaSuccess ? ESA_OK
+                                                                                                      : ESA_ERR_CUDA;
+}
+
+esa_status esa_topk_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const esa_shape *s, int top_k,
+                           int32_t *idx, int32_t *cnt, void *ws, size_t ws_bytes, void *stream) {
+    esa_status e = check_shape(s, false, true);
+    if (e) return e;
+    if (!qI || !kI || !wI || !idx || !cnt) return ESA_ERR_INVALID;
+    if (top_k <= 0 || top_k > 65536) return ESA_ERR_INVALID;
+    if (!aligned16(qI) || !aligned16(kI)) return ESA_ERR_INVALID;
+    Shape x = to_shape(s);
+    if (x.B * x.Tq == 0) return ESA_OK;
+    SplitPlan sp = plan_split_select(x, top_k);
+    if ((e = check_ws(ws, ws_bytes, sp.ok ? sp.ws_bytes : ws_row_select(x, top_k)))) return e;
+    if (sp.ok) return launch_split_select(qI, kI, wI, x, top_k, idx, cnt, ws, sp, (cudaStream_t)stream);
+    return launch_row_select(qI, kI, wI, x, top_k, idx, cnt, nullptr, ws, (cudaStream_t)stream);
+}
+
+esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,
+                           const int32_t *cnt, const esa_shape *s, int top_k, float scale, const float *g,
+                           const uint16_t *lin, float *out, float *lse, void *ws, size_t ws_bytes, void *stream) {
+    esa_status e = check_shape(s, true, false);
+    if (e) return e;
+    if (!q || !k || !v || !idx || !cnt || !out) return ESA_ERR_INVALID;
+    if ((g == nullptr) != (lin == nullptr)) return ESA_ERR_INVALID;
+    if (top_k <= 0 || top_k > 65536) return ESA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (lin && !aligned16(lin)))
+        return ESA_ERR_INVALID;
+    if (!(scale > 0.f) || scale != scale) return ESA_ERR_INVALID;
+    Shape x = to_shape(s);
+    if (x.B * x.Tq == 0) return ESA_OK;
+    AttnPlan p = plan_sparse_attn(x, top_k);
+    if ((e = check_ws(ws, ws_bytes, p.ws_bytes))) return e;
+    return launch_sparse_attn(q, k, v, idx, cnt, x, top_k, scale, g, lin, out, lse, ws, p, (cudaStream_t)stream);
+}
+
+esa_status esa_gated_mix(const float *attn, const uint16_t *lin, const float *g, const uint8_t *head_mask,
+                         const esa_shape *s, float *out, void *stream) {
+    esa_status e = check_shape(s, true, false);
+    if (e) return e;
+    if (!attn || !lin || !g || !out) return ESA_ERR_INVALID;
+    if (!aligned16(attn) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lin) & 7u)) return ESA_ERR_INVALID;
+    return launch_gated_mix(attn, lin, g, head_mask, to_shape(s), out, (cudaStream_t)stream) == cudaSuccess
+               ? ESA_OK
+               : ESA_ERR_CUDA;
+}
+
+esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
+                           const int8_t *kI, const int32_t *wI, const uint8_t *route, const esa_shape *s, int top_k,
+                           float scale, const float *g, const uint16_t *lin, float *out, void *ws, size_t ws_bytes,
+                           void *stream) {
+    esa_status e = check_shape(s, true, true);
+    if (e) return e;
+    if (s->D_I == 16 || s->H_I * s->D_I > 512) return ESA_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !qI || !kI || !wI || !route || !out) return ESA_ERR_INVALID;
+    if ((g == nullptr) != (lin == nullptr)) return ESA_ERR_INVALID;
+    if (top_k <= 0 || top_k > 65536) return ESA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(qI) || !aligned16(kI) || !aligned16(out) ||
+        (lin && !aligned16(lin)))
+        return ESA_ERR_INVALID;
+    if (!(scale > 0.f) || scale != scale) return ESA_ERR_INVALID;
+    Shape x = to_shape(s);
+    if (x.B * x.Tq == 0) return ESA_OK;
+    if ((e = check_ws(ws, ws_bytes, ws_routed(x, top_k)))) return e;
+    return launch_routed_attn(q, k, v, qI, kI, wI, route, x, top_k, scale, g, lin, out, ws, (cudaStream_t)stream);
+}
+
+esa_status esa_read_status(void *ws, void *stream, int32_t *dev_status) {
+    if (!ws || !dev_status) return ESA_ERR_INVALID;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return ESA_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return ESA_ERR_CUDA;
+    *dev_status = v;
+    if (v != 0 && cudaMemset(ws, 0, sizeof v) != cudaSuccess) return ESA_ERR_CUDA;
+    return ESA_OK;
+}
+
+const char *esa_status_string(esa_status st) {
+    switch (st) {
+        case ESA_OK: return "ok";
+        case ESA_ERR_INVALID: return "invalid argument";
+        case ESA_ERR_UNSUPPORTED: return "unsupported shape or size";
+        case ESA_ERR_CUDA: return "CUDA runtime error";
+        case ESA_ERR_TIMEOUT: return "device wait timed out";
+        case ESA_ERR_BAD_INDEX: return "index outside the causal prefix";
+        case ESA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case ESA_ERR_INTERNAL: return "kernel consistency check failed";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// Internal launchers of libesa.so. Not part of the C ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/esa.h"
+
+namespace esa {
+
+struct Shape {
+    long long B, Tq, Tk, q_offset;
+    int Hq, Hkv, D, H_I, D_I;
+};
+
+struct DevInfo {
+    int sms;
+    size_t smem_optin;
+};
+
+// Immutable attributes of the current device (cached per device ordinal).
+DevInfo device_info();
+
+// Raise a kernel's dynamic shared-memory limit to at least `smem` on the
+// current device (the attribute is set once per kernel, device and size).
+bool ensure_smem(const void *fn, size_t smem);
+// Resident blocks per SM for (kernel, threads, smem) on the current device,
+// cached; 0 on failure.
+int occupancy(const void *fn, int threads, size_t smem);
+
+// Workspace carving: [0,256) status word area, then 256-aligned regions.
+constexpr size_t kStatusBytes = 256;
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---- gate mix -----------------------------------------------------------
+cudaError_t launch_gated_mix(const float *attn, const uint16_t *lin, const float *g, const uint8_t *head_mask,
+                             const Shape &s, float *out, cudaStream_t st);
+
+// ---- indexer scores (diagnostic) ----------------------------------------
+cudaError_t launch_indexer_score(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s,
+                                 int32_t *scores, cudaStream_t st);
+
+// ---- top-K selection ----------------------------------------------------
+// Split plan: rows whose keys are spread over several co-resident blocks that
+// meet at bounded inter-block barriers (few rows, long prefixes).
+struct SplitPlan {
+    bool ok;
+    int chunks;     // blocks per row
+    int grid;       // rows * chunks
+    size_t smem;    // dynamic shared memory per block
+    size_t ctrl_words;
+    size_t ws_bytes;
+};
+SplitPlan plan_split_select(const Shape &s, int K);
+esa_status launch_split_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
+                               int32_t *idx, int32_t *cnt, void *ws, const SplitPlan &plan, cudaStream_t st);
+
+// Row-tiled selection: 32 query rows per block, several passes over the
+// keys. Writes idx/cnt when idx != nullptr and the threshold form (T, P)
+// of every row to thr (int32 pairs [rows][2]) when thr != nullptr.
+size_t ws_row_select(const Shape &s, int K);
+esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
+                             int32_t *idx, int32_t *cnt, int32_t *thr, void *ws, cudaStream_t st);
+
+// ---- attention over gathered keys ---------------------------------------
+struct AttnPlan {
+    int gt;      // query heads per block (16, 32 or 64)
+    int hg;      // head groups per key/value head
+    int splits;  // key splits per (row, kv head, head group)
+    int keys_per_split;
+    long long grid;
+    size_t smem;
+    size_t ws_bytes;
+};
+AttnPlan plan_sparse_attn(const Shape &s, int K);
+esa_status launch_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,
+                              const int32_t *cnt, const Shape &s, int K, float scale, const float *g,
+                              const uint16_t *lin, float *out, float *lse, void *ws, const AttnPlan &plan,
+                              cudaStream_t st);
+
+// ---- routed (full | sparse per head) attention ---------------------------
+size_t ws_routed(const Shape &s, int K);
+esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
+                              const int8_t *kI, const int32_t *wI, const uint8_t *route, const Shape &s, int K,
+                              float scale, const float *g, const uint16_t *lin, float *out, void *ws,
+                              cudaStream_t st);
+
+// Wait limit for inter-block waits, in ns (ESA_WAIT_LIMIT_NS overrides) and
+// the count of extra arrivals a barrier waits for (ESA_DEBUG_EXTRA_ARRIVALS;
+// 0 normally — a positive value makes every barrier wait run out, which the
+// timeout test uses).
+long long wait_limit_ns();
+int debug_extra_arrivals();
+
+}  // namespace esa

@@ -1,0 +1,102 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol that
+include/*.h declares, and rejects bad arguments on the host before any
+launch (no CUDA call is made by these checks)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names |= set(re.findall(r"ESA_API\s+[\w\s\*]*?\b(esa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_five_calls():
+    d = _declared()
+    for name in ["esa_indexer_score", "esa_topk_select", "esa_sparse_attn", "esa_gated_mix", "esa_routed_attn",
+                 "esa_workspace_size", "esa_read_status"]:
+        assert name in d
+
+
+def test_library_exports_every_declared_symbol():
+    import long_context_sparse_20_b300 as esa
+    lib = ctypes.CDLL(esa.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) <= set(esa.exported_symbols())
+
+
+def test_library_is_built_for_sm_103a_only():
+    import long_context_sparse_20_b300 as esa
+    out = os.popen(f"cuobjdump --list-elf {esa.LIB_PATH} 2>/dev/null").read()
+    if not out:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out and "sm_100" not in out.replace("sm_103a", "")
+
+
+def _shape(esa, **kw):
+    d = dict(B=1, Tq=4, Tk=4, q_offset=0, Hq=4, Hkv=1, D=64, H_I=1, D_I=32)
+    d.update(kw)
+    return esa.shape_from(d)
+
+
+def test_host_validation_rejects_before_launch():
+    import long_context_sparse_20_b300 as esa
+    L = esa._lib
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    s = _shape(esa)
+    # null pointers
+    assert L.esa_topk_select(None, fake, fake, ctypes.byref(s), 4, fake, fake, fake, 1 << 20, None) == esa.ERR_INVALID
+    # top_k out of range
+    assert L.esa_topk_select(fake, fake, fake, ctypes.byref(s), 0, fake, fake, fake, 1 << 20, None) == esa.ERR_INVALID
+    # q_offset + Tq > Tk
+    bad = _shape(esa, Tq=5)
+    assert L.esa_topk_select(fake, fake, fake, ctypes.byref(bad), 4, fake, fake, fake, 1 << 20, None) == esa.ERR_INVALID
+    # Hq not a multiple of Hkv; unsupported D; unsupported D_I / H_I
+    for kw, code in [(dict(Hq=6, Hkv=4), esa.ERR_INVALID), (dict(D=96), esa.ERR_UNSUPPORTED)]:
+        sh = _shape(esa, **kw)
+        assert L.esa_sparse_attn(fake, fake, fake, fake, fake, ctypes.byref(sh), 4, 0.125, None, None, fake, None,
+                                 fake, 1 << 20, None) == code
+    for kw in [dict(D_I=48), dict(H_I=17), dict(H_I=0)]:
+        sh = _shape(esa, **kw)
+        assert L.esa_topk_select(fake, fake, fake, ctypes.byref(sh), 4, fake, fake, fake, 1 << 20, None) == \
+            esa.ERR_UNSUPPORTED
+    # gate without lin (both or neither)
+    assert L.esa_sparse_attn(fake, fake, fake, fake, fake, ctypes.byref(s), 4, 0.125, fake, None, fake, None, fake,
+                             1 << 20, None) == esa.ERR_INVALID
+    # non-positive scale
+    assert L.esa_sparse_attn(fake, fake, fake, fake, fake, ctypes.byref(s), 4, 0.0, None, None, fake, None, fake,
+                             1 << 20, None) == esa.ERR_INVALID
+    # misaligned tensor
+    odd = ctypes.c_void_p(0x1008)
+    assert L.esa_gated_mix(odd, fake, fake, None, ctypes.byref(s), fake, None) == esa.ERR_INVALID
+    # routed attention does not take D_I = 16
+    sh = _shape(esa, D_I=16)
+    assert L.esa_routed_attn(fake, fake, fake, fake, fake, fake, fake, ctypes.byref(sh), 4, 0.125, None, None, fake,
+                             fake, 1 << 20, None) == esa.ERR_UNSUPPORTED
+    # workspace: null or misaligned
+    assert L.esa_indexer_score(fake, fake, fake, ctypes.byref(s), fake, None, 1 << 20, None) == esa.ERR_WORKSPACE
+    assert L.esa_indexer_score(fake, fake, fake, ctypes.byref(s), fake, ctypes.c_void_p(0x1010), 1 << 20, None) == \
+        esa.ERR_WORKSPACE
+
+
+def test_workspace_size_rejects_bad_shapes():
+    import long_context_sparse_20_b300 as esa
+    assert esa.esa_workspace_size(esa.OP_TOPK_SELECT, _shape(esa, Tq=9), 4) == 0
+    assert esa.esa_workspace_size(99, _shape(esa), 4) == 0
+    assert esa.esa_workspace_size(esa.OP_SPARSE_ATTN, _shape(esa), 0) == 0
+
+
+def test_status_strings():
+    import long_context_sparse_20_b300 as esa
+    assert esa.status_string(esa.ERR_TIMEOUT) == "device wait timed out"
+    assert esa.status_string(esa.OK) == "ok"
+    assert esa.status_string(123) == "unknown status"

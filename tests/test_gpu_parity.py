@@ -1,0 +1,300 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+Index sets and counts must match bit-exactly; fp32 outputs within 2e-3
+max-abs (bf16 inputs, fp32 accumulation). Small cases span several tiles
+and ragged tails; the five workloads run at full size, compared on all rows
+(decode) or on seeded row samples plus edge rows (prefill)."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import esa_inputs as E
+import oracle as O
+from gpu_helpers import (ATOL, assert_close, assert_idx_equal, esa, gpu_attn, gpu_routed, gpu_topk, sample_rows,
+                         to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(**over):
+    cfg = E.small_config(**over)
+    return cfg, E.shape_of(cfg), E.make_inputs(cfg)
+
+
+# ------------------------------------------------------------------ top-K
+TOPK_CASES = [
+    # prefill, row-tiled selection: ragged row tiles, t around K, several key tiles
+    dict(B=1, Tq=300, Tk=300, top_k=64, D_I=32),
+    dict(B=2, Tq=200, Tk=200, top_k=100, D_I=64, H_I=4, weights="1to4"),
+    dict(B=1, Tq=130, Tk=130, top_k=1, D_I=16),
+    dict(B=1, Tq=257, Tk=257, top_k=256, D_I=128, H_I=2, weights="1to4"),
+    # chunked prefill: queries at positions q_offset..q_offset+Tq-1
+    dict(B=2, Tq=70, Tk=600, q_offset=530, top_k=128, D_I=64),
+    # decode, split selection across blocks
+    dict(B=1, Tq=1, Tk=5000, q_offset=4999, top_k=2048, D_I=64),
+    dict(B=3, Tq=1, Tk=40000, q_offset=39999, top_k=700, D_I=32, H_I=3, weights="1to4"),
+    dict(B=8, Tq=1, Tk=1500, q_offset=1499, top_k=2048, D_I=64),   # n <= K: whole prefix
+    dict(B=2, Tq=1, Tk=9000, q_offset=8999, top_k=2048, D_I=128),
+    dict(B=1, Tq=1, Tk=3000, q_offset=2999, top_k=2999, D_I=16),   # K = n-1
+    dict(B=4, Tq=2, Tk=6000, q_offset=5998, top_k=1000, D_I=64),   # two query rows per sequence
+]
+
+
+@pytest.mark.parametrize("over", TOPK_CASES, ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
+def test_topk_small(over):
+    cfg, sh, inp = _case(seed=101, **over)
+    K = cfg["top_k"]
+    gi, gc = gpu_topk(to_dev(inp), sh, K)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    assert_idx_equal(gi, gc, oi, oc)
+
+
+@pytest.mark.parametrize("decode", [False, True])
+def test_topk_all_equal_scores(decode):
+    """Every score equal: the K lowest positions win (worst case for ties)."""
+    over = dict(B=2, Tq=1, Tk=20000, q_offset=19999, top_k=2048) if decode else dict(B=1, Tq=200, Tk=200, top_k=50)
+    cfg, sh, inp = _case(seed=5, D_I=64, **over)
+    inp["kI"] = torch.zeros_like(inp["kI"])
+    K = cfg["top_k"]
+    gi, gc = gpu_topk(to_dev(inp), sh, K)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    assert_idx_equal(gi, gc, oi, oc)
+
+
+@pytest.mark.parametrize("decode", [False, True])
+def test_topk_wide_scores(decode):
+    """Full-range int8 and large, mixed-sign weights: scores near 2^30 take
+    the deeper histogram levels, and the indexer heads cannot be collapsed."""
+    over = dict(B=2, Tq=1, Tk=30000, q_offset=29999, top_k=1500) if decode else dict(B=1, Tq=160, Tk=160, top_k=40)
+    cfg, sh, inp = _case(seed=77, D_I=64, H_I=4, **over)
+    g = torch.Generator().manual_seed(3)
+    inp["qI"] = torch.randint(-128, 128, inp["qI"].shape, dtype=torch.int8, generator=g)
+    inp["kI"] = torch.randint(-128, 128, inp["kI"].shape, dtype=torch.int8, generator=g)
+    inp["wI"] = torch.tensor([500, -300, 200, 7], dtype=torch.int32)
+    K = cfg["top_k"]
+    gi, gc = gpu_topk(to_dev(inp), sh, K)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    assert_idx_equal(gi, gc, oi, oc)
+
+
+def test_topk_repeated_calls_reuse_workspace():
+    """The split selection returns its workspace to zero: back-to-back calls
+    with different shapes on one workspace stay exact."""
+    m = esa()
+    shapes = [dict(B=4, Tq=1, Tk=30000, q_offset=29999, top_k=512), dict(B=1, Tq=1, Tk=90000, q_offset=89999,
+                                                                         top_k=2048)]
+    cases = [_case(seed=200 + i, D_I=64, **s) for i, s in enumerate(shapes)]
+    need = max(m.esa_workspace_size(m.OP_TOPK_SELECT, m.shape_from(c[1]), c[0]["top_k"]) for c in cases)
+    ws = m.Workspace(need)
+    for rep in range(3):
+        for cfg, sh, inp in cases:
+            gi, gc = gpu_topk(to_dev(inp), sh, cfg["top_k"], ws=ws)
+            oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, cfg["top_k"])
+            assert_idx_equal(gi, gc, oi, oc)
+
+
+# ------------------------------------------------------------------ attention
+ATTN_CASES = [
+    dict(B=1, Tq=150, Tk=150, Hq=4, Hkv=1, D=64, top_k=40),
+    dict(B=2, Tq=90, Tk=90, Hq=16, Hkv=2, D=128, top_k=70, D_I=64, H_I=4, weights="1to4"),
+    dict(B=1, Tq=65, Tk=65, Hq=6, Hkv=3, D=64, top_k=200),               # K >= every prefix
+    dict(B=2, Tq=1, Tk=9000, q_offset=8999, Hq=32, Hkv=1, D=128, top_k=2048, D_I=64),   # decode, splits
+    dict(B=1, Tq=1, Tk=20000, q_offset=19999, Hq=64, Hkv=1, D=128, top_k=2048, D_I=64),  # 64 heads per KV head
+    dict(B=3, Tq=1, Tk=4000, q_offset=3999, Hq=8, Hkv=2, D=64, top_k=300, D_I=32),
+    dict(B=1, Tq=40, Tk=500, q_offset=460, Hq=48, Hkv=1, D=128, top_k=100, D_I=64),     # chunked, 48 heads
+]
+
+
+@pytest.mark.parametrize("over", ATTN_CASES, ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
+@pytest.mark.parametrize("gate", [True, False])
+def test_sparse_attn_small(over, gate):
+    cfg, sh, inp = _case(seed=303, **over)
+    K = cfg["top_k"]
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    ref, ref_lse = O.attention(inp["q"], inp["k"], inp["v"], oi, oc, sh, K, g=inp["g"] if gate else None,
+                               lin=inp["lin"] if gate else None)
+    st, out, lse = gpu_attn(to_dev(inp), sh, K, oi, oc, gate=gate)
+    assert st == 0
+    assert_close(out, ref)
+    assert_close(lse, ref_lse, what="lse")
+
+
+def test_sparse_attn_edge_counts():
+    """cnt = 0 (empty set: out = linear share, lse = -inf), cnt = 1, and an
+    index list given in non-ascending order (attention is order-free)."""
+    cfg, sh, inp = _case(seed=9, B=1, Tq=1, Tk=3000, q_offset=2999, Hq=32, Hkv=1, D=128, top_k=512, D_I=64)
+    K = 512
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    d = to_dev(inp)
+    for c in (0, 1, 511):
+        idx = oi.copy()
+        idx[0, c:] = -1
+        cnt = np.array([c], dtype=np.int32)
+        idx[0, :c] = idx[0, :c][::-1].copy()
+        ref, ref_lse = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, sh, K, g=inp["g"], lin=inp["lin"])
+        st, out, lse = gpu_attn(d, sh, K, idx, cnt)
+        assert st == 0
+        assert_close(out, ref)
+        if c == 0:
+            assert np.isneginf(lse).all()
+        else:
+            assert_close(lse, ref_lse, what="lse")
+
+
+@pytest.mark.parametrize("decode", [False, True])
+def test_sparse_attn_bad_index_sets_status(decode):
+    """An index past the causal prefix is reported in the status word (no
+    fault); the row is left unwritten and the other rows are exact."""
+    over = dict(B=2, Tq=1, Tk=5000, q_offset=4999, Hq=32, D=128, D_I=64, top_k=1024) if decode else \
+        dict(B=1, Tq=50, Tk=50, Hq=4, D=64, top_k=16)
+    cfg, sh, inp = _case(seed=12, Hkv=1, **over)
+    K = cfg["top_k"]
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    bad_row = 1 if decode else 20
+    idx = oi.copy()
+    idx[bad_row, 0] = (sh["q_offset"] + bad_row % sh["Tq"]) + 1  # one past the prefix
+    st, out, _ = gpu_attn(to_dev(inp), sh, K, idx, oc)
+    assert st == esa().ERR_BAD_INDEX
+    assert np.isnan(out[bad_row]).all()
+    ref, _ = O.attention(inp["q"], inp["k"], inp["v"], oi, oc, sh, K, g=inp["g"], lin=inp["lin"])
+    keep = [r for r in range(len(oc)) if r != bad_row]
+    assert_close(out[keep], ref[keep])
+
+
+def test_gated_mix():
+    m = esa()
+    cfg, sh, inp = _case(seed=41, B=2, Tq=33, Tk=33, Hq=8, Hkv=2, D=128, top_k=9, routed=True)
+    K = 9
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    plain, _ = O.attention(inp["q"], inp["k"], inp["v"], oi, oc, sh, K)
+    gated, _ = O.attention(inp["q"], inp["k"], inp["v"], oi, oc, sh, K, g=inp["g"], lin=inp["lin"])
+    attn = torch.as_tensor(plain, dtype=torch.float32).reshape(2, 33, 8, 128).cuda()
+    out = torch.empty_like(attn)
+    d = to_dev(inp)
+    m.esa_gated_mix(attn, d["lin"], d["g"], None, m.shape_from(sh), out)
+    assert_close(out.reshape(66, 8, 128).cpu().numpy(), gated)
+    # with a head mask: unmasked heads copy attn; also in place (out aliases attn)
+    m.esa_gated_mix(attn, d["lin"], d["g"], d["route"], m.shape_from(sh), attn)
+    got = attn.reshape(66, 8, 128).cpu().numpy()
+    route = inp["route"].numpy()
+    for b in range(2):
+        for h in range(8):
+            src = gated if route[b, h] else plain
+            assert_close(got[b * 33:(b + 1) * 33, h], src[b * 33:(b + 1) * 33, h])
+
+
+# ------------------------------------------------------------------ routed
+ROUTED_CASES = [
+    dict(B=2, Tq=200, Tk=200, Hq=8, Hkv=8, D=128, top_k=50, D_I=64),
+    dict(B=1, Tq=130, Tk=130, Hq=4, Hkv=2, D=64, top_k=16, D_I=32, H_I=2, weights="1to4"),
+    dict(B=1, Tq=64, Tk=300, q_offset=236, Hq=6, Hkv=6, D=128, top_k=100, D_I=128),
+]
+
+
+@pytest.mark.parametrize("over", ROUTED_CASES, ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
+@pytest.mark.parametrize("routes", ["drawn", "all_full", "all_sparse"])
+def test_routed_small(over, routes):
+    cfg, sh, inp = _case(seed=55, routed=True, **over)
+    if routes == "all_full":
+        inp["route"] = torch.zeros_like(inp["route"])
+    elif routes == "all_sparse":
+        inp["route"] = torch.ones_like(inp["route"])
+    K = cfg["top_k"]
+    oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K)
+    out = gpu_routed(to_dev(inp), sh, K)
+    assert_close(out, ref)
+
+
+def test_routed_equal_scores():
+    """All-equal indexer scores: sparse heads keep the K lowest positions."""
+    cfg, sh, inp = _case(seed=8, routed=True, B=1, Tq=150, Tk=150, Hq=4, Hkv=4, D=64, top_k=20, D_I=64)
+    inp["kI"] = torch.zeros_like(inp["kI"])
+    inp["route"] = torch.tensor([[1, 0, 1, 1]], dtype=torch.uint8)
+    oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, 20)
+    assert_close(gpu_routed(to_dev(inp), sh, 20), ref)
+
+
+# ------------------------------------------------------------------ the five workloads at full size
+def _full(name):
+    cfg = E.CONFIGS[name]
+    return cfg, E.shape_of(cfg), E.make_inputs(cfg)
+
+
+def test_tiny_prefill_full():
+    cfg, sh, inp = _full("tiny_prefill")
+    K = cfg["top_k"]
+    d = to_dev(inp)
+    gi, gc = gpu_topk(d, sh, K)
+    oi, oc, ref, ref_lse = O.gated_sparse_attention(inp, sh, K)
+    assert_idx_equal(gi, gc, oi, oc)
+    st, out, lse = gpu_attn(d, sh, K, gi, gc)
+    assert st == 0
+    assert_close(out, ref)
+    assert_close(lse, ref_lse, what="lse")
+
+
+@pytest.mark.parametrize("name", ["decode", "million_decode"])
+def test_decode_full(name):
+    cfg, sh, inp = _full(name)
+    K = cfg["top_k"]
+    d = to_dev(inp)
+    gi, gc = gpu_topk(d, sh, K)
+    oi, oc, ref, ref_lse = O.gated_sparse_attention(inp, sh, K)
+    assert_idx_equal(gi, gc, oi, oc)
+    if inp["needles"] is not None:
+        assert set(inp["needles"].tolist()) <= set(gi[0].tolist())
+    st, out, lse = gpu_attn(d, sh, K, gi, gc)
+    assert st == 0
+    assert_close(out, ref)
+    assert_close(lse, ref_lse, what="lse")
+
+
+def test_long_prefill_full():
+    cfg, sh, inp = _full("long_prefill")
+    K = cfg["top_k"]
+    d = to_dev(inp)
+    gi, gc = gpu_topk(d, sh, K)
+    rows = sample_rows(sh["B"], sh["Tq"], K, 1024, seed=1)
+    oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
+    assert_idx_equal(gi, gc, oi, oc, rows=rows)
+    assert (gc == np.minimum(K, np.arange(sh["Tq"]) + 1)).all()
+    st, out, _ = gpu_attn(d, sh, K, gi, gc)
+    assert st == 0
+    assert_close(out[rows], ref)
+
+
+def test_routed_prefill_full():
+    cfg, sh, inp = _full("routed_prefill")
+    K = cfg["top_k"]
+    rows = sample_rows(sh["B"], sh["Tq"], K, 256, seed=2)
+    out = gpu_routed(to_dev(inp), sh, K)
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
+    assert_close(out[rows], ref)
+
+
+# ------------------------------------------------------------------ bounded waits
+def test_wait_timeout_reports_status(monkeypatch):
+    """A barrier made unreachable (extra arrivals nobody provides) runs out
+    after its short limit: the call returns, the status word says TIMEOUT,
+    and the context stays usable (a parity check follows on a fresh
+    workspace)."""
+    m = esa()
+    cfg, sh, inp = _case(seed=31, B=2, Tq=1, Tk=20000, q_offset=19999, top_k=512, D_I=64)
+    d = to_dev(inp)
+    shape = m.shape_from(sh)
+    ws = m.workspace_for(m.OP_TOPK_SELECT, shape, 512)
+    idx = torch.empty(2, 1, 512, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(2, 1, dtype=torch.int32, device="cuda")
+    monkeypatch.setenv("ESA_DEBUG_EXTRA_ARRIVALS", "1")
+    monkeypatch.setenv("ESA_WAIT_LIMIT_NS", "20000000")
+    m.esa_topk_select(d["qI"], d["kI"], d["wI"], shape, 512, idx, cnt, ws)
+    assert m.esa_read_status(ws) == m.ERR_TIMEOUT
+    monkeypatch.delenv("ESA_DEBUG_EXTRA_ARRIVALS")
+    monkeypatch.delenv("ESA_WAIT_LIMIT_NS")
+    m.esa_workspace_init(ws)
+    gi, gc = gpu_topk(d, sh, 512, ws=ws)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, 512)
+    assert_idx_equal(gi, gc, oi, oc)
