@@ -172,6 +172,33 @@ ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const u
                            float scale, const float *g, const uint16_t *lin, float *out, void *ws, size_t ws_bytes,
                            void *stream);
 
+/* Top-K selection without a caller workspace. The pages have no counterpart
+ * to this call: it is a convenience of this library.
+ *
+ * For callers that cannot allocate device memory themselves — code running
+ * inside a runtime that owns every device allocation (a framework's caching
+ * allocator, a serving engine with a reserved memory pool) and may not call
+ * cudaMalloc. Same inputs, outputs and results as esa_topk_select(), but the
+ * scratch state (status word, barrier counters, histograms) lives in one
+ * fixed device array inside this library, ESA_NOALLOC_SCRATCH_BYTES large,
+ * which every GPU that loads the library holds until the process exits. The
+ * call itself allocates nothing (no cudaMalloc or cudaFree).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on the device.
+ *   - Shapes whose scratch would exceed ESA_NOALLOC_SCRATCH_BYTES return
+ *     ESA_ERR_UNSUPPORTED (decode with up to 8 query rows and prefill of any
+ *     size fit).
+ *   - Every call shares the one array: it clears the parts that must start
+ *     at zero on `stream` before launching, and calls whose GPU work overlaps
+ *     in time (different streams, or several host threads) race on it.
+ *   - dev_status (nullable): a caller-owned device int32 that receives this
+ *     call's device status code (ESA_OK, ESA_ERR_TIMEOUT, ...), copied on
+ *     `stream` after the kernel. */
+#define ESA_NOALLOC_SCRATCH_BYTES (8u << 20)
+ESA_API esa_status esa_topk_select_noalloc(const int8_t *qI, const int8_t *kI, const int32_t *wI, const esa_shape *s,
+                                           int top_k, int32_t *idx, int32_t *cnt, int32_t *dev_status, void *stream);
+
 /* Synchronise `stream`, read the workspace status word into *dev_status
  * (ESA_OK when no kernel recorded an error) and clear it. Returns ESA_OK, or
  * ESA_ERR_CUDA when the synchronisation or the copy failed. */

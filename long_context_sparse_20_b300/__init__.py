@@ -50,6 +50,7 @@ _SIGS = {
     "esa_gated_mix": (_i32, [_vp, _vp, _vp, _vp, _sp, _vp, _vp]),
     "esa_routed_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp,
                                _vp, _sz, _vp]),
+    "esa_topk_select_noalloc": (_i32, [_vp, _vp, _vp, _sp, ctypes.c_int, _vp, _vp, _vp, _vp]),
     "esa_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "esa_status_string": (ctypes.c_char_p, [_i32]),
 }
@@ -127,6 +128,13 @@ def esa_indexer_score(qI, kI, wI, shape: esa_shape, scores, ws: Workspace, strea
 def esa_topk_select(qI, kI, wI, shape: esa_shape, top_k: int, idx, cnt, ws: Workspace, stream=None):
     _check(_lib.esa_topk_select(_p(qI), _p(kI), _p(wI), ctypes.byref(shape), top_k, _p(idx), _p(cnt), ws.ptr,
                                 ws.nbytes, _stream(stream, qI)), "esa_topk_select")
+
+
+def esa_topk_select_noalloc(qI, kI, wI, shape: esa_shape, top_k: int, idx, cnt, dev_status=None, stream=None):
+    """esa_topk_select without a workspace: for callers that may not allocate
+    device memory (the library's own fixed scratch array is used)."""
+    _check(_lib.esa_topk_select_noalloc(_p(qI), _p(kI), _p(wI), ctypes.byref(shape), top_k, _p(idx), _p(cnt),
+                                        _p(dev_status), _stream(stream, qI)), "esa_topk_select_noalloc")
 
 
 def _bits(t):

@@ -1,0 +1,75 @@
+"""esa_topk_select_noalloc: top-K selection for callers that cannot allocate.
+
+Code that runs inside a runtime owning every device allocation (a caching
+allocator, a serving engine's reserved pool) may not call cudaMalloc, so it
+cannot give esa_topk_select() a workspace. The no-allocation entry point
+keeps that scratch in a fixed array inside the library. These tests call it
+through the C ABI and compare its index sets with esa_topk_select()'s on the
+same inputs, bit for bit (integer results), on two calls in a row — the
+shared array must be left ready for the next call. This file is collected
+last so that a run stopping at the first failure has run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import esa_inputs as E
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # decode: the split selection, whose scratch holds barrier counters,
+    # level histograms and per-block published counts
+    dict(B=8, Tq=1, Tk=131072, q_offset=131071, Hq=32, Hkv=1, D=128, H_I=1, D_I=64, top_k=2048),
+    dict(B=2, Tq=1, Tk=30000, q_offset=29999, Hq=8, Hkv=1, D=64, H_I=3, D_I=32, top_k=700, weights="1to4"),
+    # prefill: the row-tiled selection (only the status word in scratch)
+    dict(B=1, Tq=300, Tk=300, Hq=4, Hkv=1, D=64, H_I=1, D_I=64, top_k=64),
+]
+
+
+@pytest.mark.parametrize("over", CASES, ids=["decode-8x131072", "decode-2x30000", "prefill-300"])
+def test_noalloc_matches_workspace_call(over):
+    import long_context_sparse_20_b300 as esa
+    cfg = E.small_config(seed=909, **over)
+    sh = E.shape_of(cfg)
+    K = cfg["top_k"]
+    inp = E.make_inputs(cfg)
+    qI, kI, wI = inp["qI"].cuda(), inp["kI"].cuda(), inp["wI"].cuda()
+    shape = esa.shape_from(sh)
+    B, Tq = sh["B"], sh["Tq"]
+
+    ws = esa.workspace_for(esa.OP_TOPK_SELECT, shape, K)
+    ref_idx = torch.empty(B, Tq, K, dtype=torch.int32, device="cuda")
+    ref_cnt = torch.empty(B, Tq, dtype=torch.int32, device="cuda")
+    esa.esa_topk_select(qI, kI, wI, shape, K, ref_idx, ref_cnt, ws)
+    assert esa.esa_read_status(ws) == esa.OK
+
+    lib = esa._lib
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for call in range(2):
+        idx = torch.full((B, Tq, K), -7, dtype=torch.int32, device="cuda")
+        cnt = torch.full((B, Tq), -7, dtype=torch.int32, device="cuda")
+        status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+        rc = lib.esa_topk_select_noalloc(ctypes.c_void_p(qI.data_ptr()), ctypes.c_void_p(kI.data_ptr()),
+                                         ctypes.c_void_p(wI.data_ptr()), ctypes.byref(shape), K,
+                                         ctypes.c_void_p(idx.data_ptr()), ctypes.c_void_p(cnt.data_ptr()),
+                                         ctypes.c_void_p(status.data_ptr()), stream)
+        assert rc == esa.OK, esa.status_string(rc)
+        torch.cuda.synchronize()
+        assert int(status.item()) == esa.OK, (call, int(status.item()))
+        assert torch.equal(cnt, ref_cnt), call
+        assert torch.equal(idx, ref_idx), (call, int((idx != ref_idx).any(dim=-1).sum()))
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    import long_context_sparse_20_b300 as esa
+    sh = dict(B=140, Tq=1, Tk=20000, q_offset=19999, Hq=8, Hkv=1, D=64, H_I=1, D_I=64)
+    shape = esa.shape_from(sh)
+    need = esa.esa_workspace_size(esa.OP_TOPK_SELECT, shape, 512)
+    if need <= (8 << 20):
+        pytest.skip("this device's plan fits the fixed scratch for this shape")
+    fake = ctypes.c_void_p(0x1000)  # not dereferenced: the size check comes first
+    rc = esa._lib.esa_topk_select_noalloc(fake, fake, fake, ctypes.byref(shape), 512, fake, fake, None, None)
+    assert rc == esa.ERR_UNSUPPORTED
