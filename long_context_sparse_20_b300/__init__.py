@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libesa.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m long_context_sparse_20_b300.build`")
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python long_context_sparse_20_b300/build.py`")
 
 _lib = ctypes.CDLL(LIB_PATH)
 

@@ -1,6 +1,8 @@
 """Build libesa.so in-tree for sm_103a (B300).
 
-    python -m long_context_sparse_20_b300.build
+    python long_context_sparse_20_b300/build.py
+
+(run as a script: importing the package itself needs the built library).
 
 Compiles every ``csrc/*.cu`` with nvcc (``-gencode arch=compute_103a,code=sm_103a
 -O3 -lineinfo``) into ``_build/*.o`` and links ``libesa.so`` next to this file.

@@ -28,6 +28,10 @@ __device__ __forceinline__ void red_release_add_u32(unsigned *p, unsigned v) {
 // Wait (thread 0 of the block) until *ctr >= target, for at most limit_ns.
 // Returns false on timeout. Never traps.
 __device__ __forceinline__ bool bounded_wait_geq(const unsigned *ctr, unsigned target, long long limit_ns) {
+    // tight polling first (the waits on the hot path are a few microseconds),
+    // then back off with nanosleep; the global timer bounds the whole wait
+    for (int i = 0; i < 4096; i++)
+        if (ld_acquire_u32(ctr) >= target) return true;
     unsigned long long t0;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
     unsigned ns = 32;

@@ -92,15 +92,21 @@ struct Smem {
     // followed by the scores of the block's span (int32)
 };
 
-// Block-wide: among bins [0,nb) of h (global when `gmem`), find v with
-// sum_{u>v} h[u] < need <= sum_{u>=v} h[u]. Result in sm.bin / sm.above.
-__device__ void find_crossing(const unsigned *h, int nb, unsigned need, bool gmem, Smem &sm) {
+// Block-wide: among bins [0,nb) of the global histogram h, find v with
+// sum_{u>v} h[u] < need <= sum_{u>=v} h[u]. Result in sm.bin / sm.above
+// (sm.bin = -1 if there is none). The bins are first staged into `stage`
+// (shared, >= nb words) with independent loads, so the search costs one L2
+// round trip.
+__device__ void find_crossing(const unsigned *h, int nb, unsigned need, unsigned *stage, Smem &sm) {
     int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) sm.bin = -1;
+#pragma unroll 8
+    for (int i = tid; i < nb; i += kThreads) stage[i] = __ldcg(h + i);
+    __syncthreads();
     int per = (nb + kThreads - 1) / kThreads;
     int b0 = tid * per, b1 = min(nb, b0 + per);
     unsigned seg = 0;
-    for (int v = b0; v < b1; v++) seg += gmem ? __ldcg(h + v) : h[v];
+    for (int v = b0; v < b1; v++) seg += stage[v];
     // inclusive suffix sum within the warp (lanes with higher index = higher bins)
     unsigned x = seg;
 #pragma unroll
@@ -116,7 +122,7 @@ __device__ void find_crossing(const unsigned *h, int nb, unsigned need, bool gme
     if (excl < need && need <= incl) {
         unsigned a = excl;
         for (int v = b1 - 1; v >= b0; v--) {
-            unsigned c = gmem ? __ldcg(h + v) : h[v];
+            unsigned c = stage[v];
             if (a + c >= need) {
                 sm.bin = v;
                 sm.above = a;
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(kThreads) split_select_kernel(
         int T = 0;
         int shift = 0, nb = 1, levels_used = 1;
         if (ok) {
-            find_crossing(g1, kNB1, (unsigned)K, true, sm);
+            find_crossing(g1, kNB1, (unsigned)K, sm.h1, sm);
             if (sm.bin < 0) {
                 if (tid == 0) set_status(status, ESA_ERR_INTERNAL);
                 ok = false;
@@ -301,7 +307,7 @@ __global__ void __launch_bounds__(kThreads) split_select_kernel(
                 int per = (pn + chunks - 1) / chunks;
                 for (int i = ci * per + tid; i < min(pn, (ci + 1) * per); i += kThreads) prev[i] = 0u;
             }
-            find_crossing(gdst, nb, (unsigned)K - above, true, sm);
+            find_crossing(gdst, nb, (unsigned)K - above, sm.h2, sm);
             if (sm.bin < 0) {
                 if (tid == 0) set_status(status, ESA_ERR_INTERNAL);
                 ok = false;

@@ -38,6 +38,7 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kKeys = 64;  // keys per stage
 constexpr int kMaxSplits = 16;
+constexpr int kIdxWin = 1024;  // staged indices (a multiple of kKeys)
 
 template <int D>
 struct Cfg {
@@ -72,6 +73,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
     __shared__ int bad_row;
     __shared__ float Pm[GT], Pl[GT];  // this block's partial: max and sum per head
     __shared__ int Pbad;
+    __shared__ int kidx[kIdxWin];  // a window of this split's key positions (-1: invalid)
 
     cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -114,7 +116,24 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
     const int k_end = min(c, k_begin + a.kps);
     const int nkeys = max(0, k_end - k_begin);
 
-    const int32_t *idx_row = a.idx + row * (long long)a.K;
+    // this split's indices, staged in windows of kIdxWin (validated here,
+    // then read by the gathers of the following stages)
+    const int32_t *idx_row = a.idx + row * (long long)a.K + k_begin;
+    int win0 = 0;
+    auto fill_idx = [&](int base) {
+#pragma unroll 8
+        for (int i = tid; i < kIdxWin && base + i < nkeys; i += kThreads) {
+            int j = __ldg(idx_row + base + i);
+            if (j < 0 || j > p) {
+                bad_row = 1;
+                j = -1;
+            }
+            kidx[i] = j;
+        }
+        win0 = base;
+        __syncthreads();
+    };
+    fill_idx(0);
     const uint16_t *kbase = a.k + (b * a.Tk * a.Hkv + kvh) * (long long)D;
     const uint16_t *vbase = a.v + (b * a.Tk * a.Hkv + kvh) * (long long)D;
     const long long kstride = (long long)a.Hkv * D;
@@ -124,17 +143,10 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
         constexpr int CH = D / 8;
         for (int i = tid; i < kKeys * CH; i += kThreads) {
             int key = i / CH, ch = i % CH;
-            int pos = kb + key;
-            bool valid = pos < k_end;
-            long long j = 0;
-            if (valid) {
-                j = __ldg(idx_row + pos);
-                if (j < 0 || j > p) {
-                    bad_row = 1;
-                    valid = false;
-                    j = 0;
-                }
-            }
+            int pos = kb + key;  // position within this split
+            long long j = pos < nkeys ? kidx[pos - win0] : -1;
+            bool valid = j >= 0;
+            if (!valid) j = 0;
             cp_async16_zfill(smem_u32(Kt + key * RS + ch * 8), kbase + j * kstride + ch * 8, valid);
             cp_async16_zfill(smem_u32(Vt + key * RS + ch * 8), vbase + j * kstride + ch * 8, valid);
         }
@@ -142,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
     };
 
     const int nstages = (nkeys + kKeys - 1) / kKeys;
-    if (nstages > 0) load_stage(0, k_begin);
+    if (nstages > 0) load_stage(0, 0);
     cp_async_wait<0>();  // Q tile (and maybe stage 0)
     __syncthreads();
 
@@ -160,7 +172,8 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
 
     for (int s = 0; s < nstages; s++) {
         if (s + 1 < nstages) {
-            load_stage((s + 1) & 1, k_begin + (s + 1) * kKeys);
+            if ((s + 1) * kKeys - win0 >= kIdxWin) fill_idx((s + 1) * kKeys);
+            load_stage((s + 1) & 1, (s + 1) * kKeys);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
@@ -327,7 +340,12 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
             const int h = h0 + hr;
             for (int d = tid; d < D; d += kThreads) {
                 float O = 0.f;
-                for (int s2 = 0; s2 < a.splits; s2++) O += *cluster.map_shared_rank(&PO[hr * D + d], s2) * wts[s2];
+                float part[kMaxSplits];
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxSplits; s2++)  // independent remote loads, issued together
+                    part[s2] = s2 < a.splits ? *cluster.map_shared_rank(&PO[hr * D + d], s2) : 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < kMaxSplits; s2++) O += s2 < a.splits ? part[s2] * wts[s2] : 0.f;
                 float res = L > 0.f ? O / L : 0.f;
                 const long long off = (row * a.Hq + h) * (long long)D + d;
                 if (gated) {
