@@ -200,7 +200,7 @@ def esa_arm(args):
 
     # NSETS rotating copies of the whole decode state, each with its outputs
     sets = []
-    for _ in range(NSETS):
+    for _ in range(args.sets):
         d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
         d["idx"] = torch.empty(B, 1, K, dtype=torch.int32, device=dev)
         d["cnt"] = torch.empty(B, 1, dtype=torch.int32, device=dev)
@@ -222,7 +222,7 @@ def esa_arm(args):
             ev[2].record(st)
 
     for i in range(max(3, args.warmup)):
-        step(sets[i % NSETS])
+        step(sets[i % len(sets)])
     torch.cuda.synchronize()
     for d in sets:
         for w in (d["ws_sel"], d["ws_att"]):
@@ -242,7 +242,7 @@ def esa_arm(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for i in range(args.steps):
-                step(sets[i % NSETS], evs[i])
+                step(sets[i % len(sets)], evs[i])
         graph.replay()
         torch.cuda.synchronize()
         run = graph.replay
@@ -252,7 +252,7 @@ def esa_arm(args):
 
         def run():
             for i in range(args.steps):
-                step(sets[i % NSETS], evs[i])
+                step(sets[i % len(sets)], evs[i])
     with Clocks(local) as clk:
         barrier()
         t0 = torch.cuda.Event(enable_timing=True)
@@ -291,11 +291,11 @@ def esa_arm(args):
         h_out.copy_(d["out"], non_blocking=True)
 
     for i in range(3):
-        e2e_step(sets[i % NSETS])
+        e2e_step(sets[i % len(sets)])
     barrier()
     a0 = time.perf_counter()
     for i in range(args.steps):
-        e2e_step(sets[i % NSETS])
+        e2e_step(sets[i % len(sets)])
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - a0) * 1e3
     barrier()
@@ -330,7 +330,8 @@ def esa_arm(args):
             "config": {"workload": f"{args.workload}: B={B} x 1 new token, cache {L}, Hq={Hq}, Hkv={Hkv}, D={D}, "
                                    f"indexer {HI}x{DI} int8, top_k={K}",
                        "global_batch": B * world, "seq_len": L, "parallelism": f"replicas x{world}",
-                       "l2": f"{NSETS} rotating input sets (kI caches {NSETS * B * L * DI / 2**20:.0f} MiB > 126 MB L2)",
+                       "l2": f"{args.sets} rotating input sets (kI caches {args.sets * B * L * DI / 2**20:.0f} MiB"
+                             f"{' > 126 MB L2' if args.sets * B * L * DI > 126e6 else ', within L2'})",
                        "timing": timing},
             "roofline": {"bound": "hbm", "kernel": "split_select" if dom_is_sel else "sparse_attn",
                          "achieved": achieved, "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
@@ -360,6 +361,7 @@ def main():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sets", type=int, default=NSETS, help="rotating input sets (small profiling cases use 1)")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)
