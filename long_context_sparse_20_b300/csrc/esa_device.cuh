@@ -86,6 +86,27 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+// wait_group with a run-time count (0..15; larger counts wait for everything)
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+    switch (n) {
+        case 15: cp_async_wait<15>(); break;
+        case 14: cp_async_wait<14>(); break;
+        case 13: cp_async_wait<13>(); break;
+        case 12: cp_async_wait<12>(); break;
+        case 11: cp_async_wait<11>(); break;
+        case 10: cp_async_wait<10>(); break;
+        case 9: cp_async_wait<9>(); break;
+        case 8: cp_async_wait<8>(); break;
+        case 7: cp_async_wait<7>(); break;
+        case 6: cp_async_wait<6>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 1: cp_async_wait<1>(); break;
+        default: cp_async_wait<0>(); break;
+    }
+}
 
 // ---------------------------------------------------------------- warp MMA
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -114,6 +135,55 @@ __device__ __forceinline__ void mma_s8_16832(int *d, const uint32_t *a, uint32_t
         "{%0,%1,%2,%3};"
         : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+// One-shot transaction barriers in shared memory, fed by the bulk-copy (TMA)
+// engine: the producer posts the byte count, the copy completes it.
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+// Make barrier initialisation visible to the bulk-copy engine.
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for phase `parity` of the barrier to complete, for at most limit_ns.
+// Returns false on timeout. Never traps.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit_ns) {
+    for (int i = 0; i < 64; i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    while (!mbar_try_wait(bar, parity)) {
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if ((long long)(t - t0) > limit_ns) return false;
+    }
+    return true;
+}
+// L2 policy for data read once (streamed past the cache).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// Bulk copy global -> shared (16-byte aligned addresses, size a multiple of
+// 16), completing `bytes` transactions on the barrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, unsigned bytes, uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
 }
 
 // ---------------------------------------------------------------- misc

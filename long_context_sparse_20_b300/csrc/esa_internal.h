@@ -45,10 +45,14 @@ cudaError_t launch_indexer_score(const int8_t *qI, const int8_t *kI, const int32
 // meet at bounded inter-block barriers (few rows, long prefixes).
 struct SplitPlan {
     bool ok;
-    int chunks;     // blocks per row
-    int grid;       // rows * chunks
-    size_t smem;    // dynamic shared memory per block
-    size_t ctrl_words;
+    int chunks;         // blocks per row
+    int grid;           // rows * chunks
+    size_t smem;        // dynamic shared memory per block
+    int stages;         // depth of the kI stage ring
+    size_t hdr_off;     // workspace: call-counter header (zero before first use)
+    size_t pub_off;     // per-block publications (written before read; no zeroing)
+    size_t ctrl_off;    // per-row control state, two parities (zero before first use)
+    size_t ctrl_bytes;
     size_t ws_bytes;
 };
 SplitPlan plan_split_select(const Shape &s, int K);

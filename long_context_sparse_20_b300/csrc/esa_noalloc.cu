@@ -69,9 +69,12 @@ extern "C" ESA_API esa_status esa_topk_select_noalloc(const int8_t *qI, const in
     if (!scratch) return err;
     cudaStream_t st = (cudaStream_t)stream;
     // The array keeps the previous call's contents: clear the status word and
-    // the control state (counters, histograms) that must start at zero.
-    const size_t clear = sp.ok ? kStatusBytes + align256(sp.ctrl_words * 4) : kStatusBytes;
+    // the control state (call counter, barrier counters, histograms) that must
+    // start at zero.
+    const size_t clear = sp.ok ? sp.pub_off : kStatusBytes;
     if (cudaMemsetAsync(scratch, 0, clear, st) != cudaSuccess) return ESA_ERR_CUDA;
+    if (sp.ok && cudaMemsetAsync(static_cast<char *>(scratch) + sp.ctrl_off, 0, sp.ctrl_bytes, st) != cudaSuccess)
+        return ESA_ERR_CUDA;
     esa_status e = sp.ok ? launch_split_select(qI, kI, wI, x, top_k, idx, cnt, scratch, sp, st)
                          : launch_row_select(qI, kI, wI, x, top_k, idx, cnt, nullptr, scratch, st);
     if (e != ESA_OK) return e;

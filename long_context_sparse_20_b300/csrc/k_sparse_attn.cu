@@ -12,13 +12,16 @@
 // heads at once. Rows are gathered with 16-byte cp.async into padded shared
 // tiles (bank-conflict-free ldmatrix), two 64-key stages in flight. Q K^T
 // and P V run on bf16 warp MMAs (m16n8k16, fp32 accumulation), 16 heads per
-// MMA row tile; P stays in registers and enters P V as a bf16 hi + lo pair
-// (two MMAs), so the probabilities keep ~16 significant bits.
+// MMA row tile; the warps that share a head tile each score the whole stage
+// and split the output columns of P V between them, so a block's partial
+// needs no merge across its warps. P stays in registers and enters P V as a
+// bf16 hi + lo pair (two MMAs), so the probabilities keep ~16 significant bits.
 // Decode rows split the index list over the blocks of one thread-block
-// cluster: each block leaves its (max, sum, unnormalised output) in its own
-// shared memory and, after a cluster barrier, merges a share of the heads by
-// reading every block's partial through distributed shared memory — no
-// partials in global memory and no serial merge.
+// cluster: each block pushes every head's (max, sum, unnormalised output)
+// into the shared memory of the block that finalises that head (distributed
+// shared memory stores, no round trip), and after one cluster barrier each
+// block merges its heads from its own shared memory — no partials in global
+// memory. Rows that are not split finish straight from registers.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -61,23 +64,22 @@ struct AttnArgs {
 template <int D, int GT>
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
     constexpr int RS = Cfg<D>::RS;
-    constexpr int HT = GT / 16;       // head tiles
-    constexpr int KS = 4 / HT;        // key subsets (warps per head tile)
-    constexpr int KW = kKeys / KS;    // keys per warp per stage
-    constexpr int NT = KW / 8;        // n-tiles of 8 keys per warp
+    constexpr int HT = GT / 16;       // head tiles of 16 heads
+    constexpr int WPH = 4 / HT;       // warps per head tile: they split the output columns
+    constexpr int NT = kKeys / 8;     // n-tiles of 8 keys (every warp scores the whole stage)
     constexpr int DK = D / 16;        // k-steps over the head dim
-    constexpr int DN = D / 8;         // n-tiles over the head dim
+    constexpr int DW = D / WPH;       // output columns per warp
+    constexpr int DNW = DW / 8;       // output n-tiles per warp
+    static_assert(DNW % 2 == 0, "pairs of output n-tiles");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     uint16_t *Qs = reinterpret_cast<uint16_t *>(smem_raw);
     uint16_t *KVs = Qs + GT * RS;  // [2 stages][K tile, V tile]
     __shared__ int bad_row;
-    __shared__ float Pm[GT], Pl[GT];  // this block's partial: max and sum per head
-    __shared__ int Pbad;
     __shared__ int kidx[kIdxWin];  // a window of this split's key positions (-1: invalid)
 
     cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ht = warp % HT, ks = warp / HT;
+    const int ht = warp % HT, dsl = warp / HT;
     const int g8 = lane >> 2, c4 = lane & 3;
 
     long long bid = blockIdx.x;
@@ -165,10 +167,11 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
         ldmatrix_x4(smem_u32(Qs + r * RS + col), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
     }
 
-    float o[DN][4];
+    float o[DNW][4];
 #pragma unroll
-    for (int i = 0; i < DN; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < DNW; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+    const int col0 = dsl * DW;  // this warp's first output column
 
     for (int s = 0; s < nstages; s++) {
         if (s + 1 < nstages) {
@@ -181,7 +184,6 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
         __syncthreads();
         const uint16_t *Kt = KVs + (s & 1) * 2 * Cfg<D>::TILE;
         const uint16_t *Vt = Kt + Cfg<D>::TILE;
-        const int kw0 = ks * KW;  // this warp's first key in the stage
         const int kvalid = min(kKeys, nkeys - s * kKeys);
 
         float sc[NT][4];
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
 #pragma unroll
             for (int kk = 0; kk < DK; kk += 2) {
                 uint32_t b0, b1, b2, b3;
-                int key = kw0 + nt * 8 + (lane & 7), col = kk * 16 + (lane >> 3) * 8;
+                int key = nt * 8 + (lane & 7), col = kk * 16 + (lane >> 3) * 8;
                 ldmatrix_x4(smem_u32(Kt + key * RS + col), b0, b1, b2, b3);
                 mma_bf16_16816(sc[nt], qf[kk], b0, b1);
                 mma_bf16_16816(sc[nt], qf[kk + 1], b2, b3);
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
         for (int nt = 0; nt < NT; nt++) {
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                int key = kw0 + nt * 8 + 2 * c4 + (e & 1);
+                int key = nt * 8 + 2 * c4 + (e & 1);
                 float x = key < kvalid ? sc[nt][e] * a.scale_log2 : -INFINITY;
                 sc[nt][e] = x;
                 mx[e >> 1] = fmaxf(mx[e >> 1], x);
@@ -240,22 +242,23 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
             l_r[r] = l_r[r] * corr[r] + rs[r];
         }
 #pragma unroll
-        for (int dn = 0; dn < DN; dn++) {
+        for (int dn = 0; dn < DNW; dn++) {
             o[dn][0] *= corr[0];
             o[dn][1] *= corr[0];
             o[dn][2] *= corr[1];
             o[dn][3] *= corr[1];
         }
-        // P V: A = P (16 heads x 16 keys) straight from the score registers
+        // P V over this warp's output columns: A = P (16 heads x 16 keys)
+        // straight from the score registers
 #pragma unroll
         for (int kk2 = 0; kk2 < NT / 2; kk2++) {
             uint32_t ah[4] = {ph[2 * kk2][0], ph[2 * kk2][1], ph[2 * kk2 + 1][0], ph[2 * kk2 + 1][1]};
             uint32_t al[4] = {pl[2 * kk2][0], pl[2 * kk2][1], pl[2 * kk2 + 1][0], pl[2 * kk2 + 1][1]};
 #pragma unroll
-            for (int dn = 0; dn < DN / 2; dn++) {
+            for (int dn = 0; dn < DNW / 2; dn++) {
                 uint32_t b0, b1, b2, b3;
-                int key = kw0 + kk2 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                int col = dn * 16 + (lane >> 4) * 8;
+                int key = kk2 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                int col = col0 + dn * 16 + (lane >> 4) * 8;
                 ldmatrix_x4_trans(smem_u32(Vt + key * RS + col), b0, b1, b2, b3);
                 mma_bf16_16816(o[2 * dn], ah, b0, b1);
                 mma_bf16_16816(o[2 * dn + 1], ah, b2, b3);
@@ -266,107 +269,131 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
         __syncthreads();
     }
 
-    // ---- merge the KS warps of each head tile into this block's partial
-    float *mo = reinterpret_cast<float *>(KVs);  // [KS][HT][16][D] per-warp outputs
-    float *mm = mo + KS * HT * 16 * D;           // [KS][HT][16]
-    float *ml = mm + KS * HT * 16;
-    float *PO = ml + KS * HT * 16;               // [GT][D] this block's partial output
-    {
-        float *myo = mo + ((ks * HT + ht) * 16) * D;
-#pragma unroll
-        for (int dn = 0; dn < DN; dn++) {
-            int col = dn * 8 + 2 * c4;
-            *reinterpret_cast<float2 *>(myo + g8 * D + col) = make_float2(o[dn][0], o[dn][1]);
-            *reinterpret_cast<float2 *>(myo + (g8 + 8) * D + col) = make_float2(o[dn][2], o[dn][3]);
-        }
-        if (c4 == 0) {
-            mm[(ks * HT + ht) * 16 + g8] = m_r[0];
-            mm[(ks * HT + ht) * 16 + g8 + 8] = m_r[1];
-            ml[(ks * HT + ht) * 16 + g8] = l_r[0];
-            ml[(ks * HT + ht) * 16 + g8 + 8] = l_r[1];
-        }
-    }
-    __syncthreads();
-    for (int e = tid; e < GT * D; e += kThreads) {
-        int hr = e / D, d = e % D, htt = hr / 16, r = hr % 16;
-        float M = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < KS; q++) M = fmaxf(M, mm[(q * HT + htt) * 16 + r]);
-        float Mu = M == -INFINITY ? 0.f : M, L = 0.f, O = 0.f;
-#pragma unroll
-        for (int q = 0; q < KS; q++) {
-            float w = exp2f(mm[(q * HT + htt) * 16 + r] - Mu);
-            L += ml[(q * HT + htt) * 16 + r] * w;
-            O += mo[((q * HT + htt) * 16 + r) * D + d] * w;
-        }
-        PO[hr * D + d] = O;
-        if (d == 0) {
-            Pm[hr] = M;
-            Pl[hr] = L;
-        }
-    }
-    if (tid == 0) Pbad = bad_row;
-    // ---- merge the splits of the cluster: every partial stays in its block's
-    // shared memory; block `split` finalises heads split, split+S, ...
-    cluster.sync();
+    // ---- epilogue
     const bool gated = a.g != nullptr && a.lin != nullptr;
+    const int S = a.splits;
+    __syncthreads();  // bad_row is final
+    if (S == 1) {
+        // the whole index list was this block's: every warp finishes its own
+        // rows and columns straight from registers
+        if (bad_row) {
+            if (tid == 0) set_status(a.status, ESA_ERR_BAD_INDEX);
+            return;
+        }
+#pragma unroll
+        for (int rr = 0; rr < 2; rr++) {
+            const int hr = ht * 16 + g8 + rr * 8;
+            if (hr >= nh) continue;
+            const int h = h0 + hr;
+            const float L = l_r[rr];
+            const float gh = gated ? a.g[h] : 1.f;
+            const long long base = (row * a.Hq + h) * (long long)D;
+#pragma unroll
+            for (int dn = 0; dn < DNW; dn++) {
+                const int col = col0 + dn * 8 + 2 * c4;
+                float v0 = L > 0.f ? o[dn][2 * rr] / L : 0.f, v1 = L > 0.f ? o[dn][2 * rr + 1] / L : 0.f;
+                if (gated) {
+                    const uint32_t lw = *reinterpret_cast<const uint32_t *>(a.lin + base + col);
+                    v0 = fmaf(gh, v0, (1.0f - gh) * bf16lo(lw));
+                    v1 = fmaf(gh, v1, (1.0f - gh) * bf16hi(lw));
+                }
+                *reinterpret_cast<float2 *>(a.out + base + col) = make_float2(v0, v1);
+            }
+            if (a.lse && dsl == 0 && c4 == 0)
+                a.lse[row * a.Hq + h] = L > 0.f ? (m_r[rr] + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        }
+        return;
+    }
+    // several splits (one cluster): push each head's partial (unnormalised
+    // output, max, sum) into the shared memory of the block that finalises
+    // it (head hr -> block hr % S, slot hr / S), then one cluster barrier;
+    // every block then reduces only from its own shared memory
+    const int MM = (GT + S - 1) / S;  // heads per finalising block, at most
+    float *RB = reinterpret_cast<float *>(KVs + 2 * 2 * Cfg<D>::TILE);  // [MM][S][D]
+    float *RM = RB + (size_t)MM * S * D;                               // [MM][S]
+    float *RL = RM + MM * S;                                           // [MM][S]
+    int *RBad = reinterpret_cast<int *>(RL + MM * S);                  // [S]
+    float *Wt = reinterpret_cast<float *>(RBad + S);                   // [MM][S] merge weights
+    float *Mf = Wt + MM * S, *Lf = Mf + MM;                            // [MM]
+#pragma unroll
+    for (int rr = 0; rr < 2; rr++) {
+        const int hr = ht * 16 + g8 + rr * 8;
+        if (hr < nh) {
+            const int dst = hr % S, i = hr / S;
+            float *rb = cluster.map_shared_rank(RB + ((size_t)i * S + split) * D, dst);
+#pragma unroll
+            for (int dn = 0; dn < DNW; dn++) {
+                const int col = col0 + dn * 8 + 2 * c4;
+                *reinterpret_cast<float2 *>(rb + col) = make_float2(o[dn][2 * rr], o[dn][2 * rr + 1]);
+            }
+            if (dsl == 0 && c4 == 0) {
+                *cluster.map_shared_rank(RM + i * S + split, dst) = m_r[rr];
+                *cluster.map_shared_rank(RL + i * S + split, dst) = l_r[rr];
+            }
+        }
+    }
+    if (tid < S) *cluster.map_shared_rank(RBad + split, tid) = bad_row;
+    cluster.sync();  // every push has landed; nobody touches another block's memory after this
     int any_bad = 0;
-    for (int s2 = 0; s2 < a.splits; s2++) any_bad |= *cluster.map_shared_rank(&Pbad, s2);
+    for (int s2 = 0; s2 < S; s2++) any_bad |= RBad[s2];
     if (any_bad) {
         if (split == 0 && tid == 0) set_status(a.status, ESA_ERR_BAD_INDEX);
-    } else {
-        __shared__ float wts[kMaxSplits];
-        __shared__ float Msh, Lsh;
-        for (int hr = split; hr < nh; hr += a.splits) {
-            if (warp == 0) {  // the head's merge weights 2^(m_s - M) and total sum
-                float mloc = lane < a.splits ? *cluster.map_shared_rank(&Pm[hr], lane) : -INFINITY;
-                float lloc = lane < a.splits ? *cluster.map_shared_rank(&Pl[hr], lane) : 0.f;
-                float M = mloc;
-#pragma unroll
-                for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, d));
-                const float Mu = M == -INFINITY ? 0.f : M;
-                float w = lane < a.splits ? exp2f(mloc - Mu) : 0.f;
-                float L = lloc * w;
-#pragma unroll
-                for (int d = 16; d > 0; d >>= 1) L += __shfl_xor_sync(0xffffffffu, L, d);
-                if (lane < a.splits) wts[lane] = w;
-                if (lane == 0) {
-                    Msh = M;
-                    Lsh = L;
-                }
-            }
-            __syncthreads();
-            const float L = Lsh, M = Msh;
-            const int h = h0 + hr;
-            for (int d = tid; d < D; d += kThreads) {
-                float O = 0.f;
-                float part[kMaxSplits];
-#pragma unroll
-                for (int s2 = 0; s2 < kMaxSplits; s2++)  // independent remote loads, issued together
-                    part[s2] = s2 < a.splits ? *cluster.map_shared_rank(&PO[hr * D + d], s2) : 0.f;
-#pragma unroll
-                for (int s2 = 0; s2 < kMaxSplits; s2++) O += s2 < a.splits ? part[s2] * wts[s2] : 0.f;
-                float res = L > 0.f ? O / L : 0.f;
-                const long long off = (row * a.Hq + h) * (long long)D + d;
-                if (gated) {
-                    float gh = a.g[h];
-                    res = fmaf(gh, res, (1.0f - gh) * __uint_as_float((uint32_t)a.lin[off] << 16));
-                }
-                a.out[off] = res;
-            }
-            if (a.lse && tid == 0)
-                a.lse[row * a.Hq + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-            __syncthreads();
-        }
+        return;
     }
-    cluster.sync();  // keep every partial alive until all blocks have read it
+    const int mine = nh > split ? (nh - split + S - 1) / S : 0;  // heads this block finalises
+    if (tid < mine) {
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < S; s2++) M = fmaxf(M, RM[tid * S + s2]);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        float L = 0.f;
+        for (int s2 = 0; s2 < S; s2++) {
+            const float w = exp2f(RM[tid * S + s2] - Mu);
+            Wt[tid * S + s2] = w;
+            L += RL[tid * S + s2] * w;
+        }
+        Mf[tid] = M;
+        Lf[tid] = L;
+    }
+    __syncthreads();
+    for (int e = tid; e < mine * (D / 4); e += kThreads) {
+        const int i = e / (D / 4), d4 = (e % (D / 4)) * 4;
+        const int h = h0 + split + i * S;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s2 = 0; s2 < S; s2++) {
+            const float w = Wt[i * S + s2];
+            const float4 v = *reinterpret_cast<const float4 *>(RB + ((size_t)i * S + s2) * D + d4);
+            O.x = fmaf(v.x, w, O.x);
+            O.y = fmaf(v.y, w, O.y);
+            O.z = fmaf(v.z, w, O.z);
+            O.w = fmaf(v.w, w, O.w);
+        }
+        const float L = Lf[i];
+        float4 res = L > 0.f ? make_float4(O.x / L, O.y / L, O.z / L, O.w / L) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const long long off = (row * a.Hq + h) * (long long)D + d4;
+        if (gated) {
+            const float gh = a.g[h], gl = 1.0f - gh;
+            const uint2 lw = *reinterpret_cast<const uint2 *>(a.lin + off);
+            res.x = fmaf(gh, res.x, gl * bf16lo(lw.x));
+            res.y = fmaf(gh, res.y, gl * bf16hi(lw.x));
+            res.z = fmaf(gh, res.z, gl * bf16lo(lw.y));
+            res.w = fmaf(gh, res.w, gl * bf16hi(lw.y));
+        }
+        *reinterpret_cast<float4 *>(a.out + off) = res;
+        if (a.lse && d4 == 0)
+            a.lse[row * a.Hq + h] = L > 0.f ? (Mf[i] + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
 }
 
 template <int D, int GT>
 size_t attn_smem() {
-    size_t stage = (size_t)2 * 2 * Cfg<D>::TILE * 2;  // 2 stages x (K,V) x bf16
-    size_t merge = ((size_t)4 * 16 * D + 2 * 4 * 16 + (size_t)GT * D) * 4;
-    return (size_t)GT * Cfg<D>::RS * 2 + (stage > merge ? stage : merge);
+    return (size_t)GT * Cfg<D>::RS * 2 + (size_t)2 * 2 * Cfg<D>::TILE * 2;  // Q tile + 2 stages x (K, V)
+}
+
+// Shared memory that the cluster merge adds when the index list is split S ways.
+size_t recv_smem(int D, int GT, int S) {
+    if (S <= 1) return 0;
+    size_t MM = (size_t)(GT + S - 1) / S;
+    return (MM * S * D + 3 * MM * S + S + 2 * MM) * 4;
 }
 
 void *attn_kernel(int D, int GT, size_t *smem) {
@@ -449,14 +476,16 @@ AttnPlan plan_sparse_attn(const Shape &s, int K) {
     int kps = (K + splits - 1) / splits;
     kps = (kps + kKeys - 1) / kKeys * kKeys;
     splits = (K + kps - 1) / kps;
-    void *fn = attn_kernel(s.D, gt, &p.smem);
+    size_t base = 0;
+    void *fn = attn_kernel(s.D, gt, &base);
     // shrink the cluster until the device can hold one
-    while (splits > 1 && !cluster_fits(fn, p.smem, splits)) {
+    while (splits > 1 && !cluster_fits(fn, base + recv_smem(s.D, gt, splits), splits)) {
         splits = (splits + 1) / 2;
         kps = (K + splits - 1) / splits;
         kps = (kps + kKeys - 1) / kKeys * kKeys;
         splits = (K + kps - 1) / kps;
     }
+    p.smem = base + recv_smem(s.D, gt, splits);
     p.splits = splits;
     p.keys_per_split = kps;
     p.grid = units * p.hg * splits;
@@ -490,8 +519,9 @@ esa_status launch_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16
     a.splits = plan.splits;
     a.kps = plan.keys_per_split;
     a.scale_log2 = scale * 1.4426950408889634f;
-    size_t smem = 0;
-    void *fn = attn_kernel(s.D, plan.gt, &smem);
+    size_t base = 0;
+    void *fn = attn_kernel(s.D, plan.gt, &base);
+    const size_t smem = plan.smem;
     if (!prepare_attn(fn, smem)) return ESA_ERR_CUDA;
     void *args[] = {(void *)&a};
     cudaLaunchConfig_t cfg{};

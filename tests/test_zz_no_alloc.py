@@ -65,7 +65,7 @@ def test_noalloc_matches_workspace_call(over):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     import long_context_sparse_20_b300 as esa
-    sh = dict(B=140, Tq=1, Tk=20000, q_offset=19999, Hq=8, Hkv=1, D=64, H_I=1, D_I=64)
+    sh = dict(B=64, Tq=1, Tk=20000, q_offset=19999, Hq=8, Hkv=1, D=64, H_I=1, D_I=64)
     shape = esa.shape_from(sh)
     need = esa.esa_workspace_size(esa.OP_TOPK_SELECT, shape, 512)
     if need <= (8 << 20):
