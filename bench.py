@@ -8,7 +8,11 @@ sharing 1 KV head, head dim 128, indexer 1 head x 64 (int8), synthetic seeded
 inputs. Multi-GPU runs are replicas (each rank its own batch, no collective
 on the data path): scaling "weak", value = tokens of all ranks / max time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl esa|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl esa|reference] [--no-prefill]
+
+The JSON line's "prefill" object adds one forward of each prefill workload
+(long_prefill: Top-K selection + gathered attention; routed_prefill: the
+routed launch) with tokens/s and algorithmic TFLOP/s against the bf16 peak.
   python bench.py --workload long_prefill|routed_prefill|million_decode|tiny_prefill
 
 Prints one JSON line.
@@ -178,6 +182,74 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def prefill_section(dev, esa, E, reps: int = 2) -> dict:
+    """The two prefill workloads, one forward each (after one untimed warm-up),
+    timed with CUDA events on the launching stream. Inputs (hundreds of MB to
+    GBs) exceed the 126 MB L2. Algorithmic flops count what the method
+    computes: causal pairs for full heads, selected pairs (min(K, p+1) per
+    row) for sparse heads, 4*D flops per pair (Q.K and P.V)."""
+    _, tf_peak, kind = _load_peaks()
+    res = {}
+    st = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    for name in ("long_prefill", "routed_prefill"):
+        cfg = dict(E.CONFIGS[name])
+        sh = E.shape_of(cfg)
+        K = cfg["top_k"]
+        host = E.make_inputs(cfg)
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+        shape = esa.shape_from(sh)
+        B, S, Hq, D = sh["B"], sh["Tq"], sh["Hq"], sh["D"]
+        scale = 1.0 / math.sqrt(D)
+        out = torch.empty(B, S, Hq, D, dtype=torch.float32, device=dev)
+        n = np.arange(1, S + 1, dtype=np.float64)
+        sel_pairs = float(np.minimum(n, K).sum())  # per (sequence, head)
+        causal_pairs = float(n.sum())
+        entry = {"workload": f"{name}: B={B} S={S} Hq={Hq} Hkv={sh['Hkv']} D={D} indexer {sh['H_I']}x{sh['D_I']} top_k={K}"}
+        if cfg.get("routed"):
+            ws = esa.workspace_for(esa.OP_ROUTED_ATTN, shape, K, dev)
+            ms = timed(lambda: esa.esa_routed_attn(d["q"], d["k"], d["v"], d["qI"], d["kI"], d["wI"], d["route"], shape,
+                                                   K, scale, d["g"], d["lin"], out, ws, st))
+            assert esa.esa_read_status(ws, st) == 0
+            nfull = int((host["route"] == 0).sum())
+            nsparse = B * Hq - nfull
+            flops = 4.0 * D * (nfull * causal_pairs + nsparse * sel_pairs)
+            entry.update({"full_heads": nfull, "sparse_heads": nsparse, "kernels_ms": {"routed_attn": ms}})
+        else:
+            wsel = esa.workspace_for(esa.OP_TOPK_SELECT, shape, K, dev)
+            watt = esa.workspace_for(esa.OP_SPARSE_ATTN, shape, K, dev)
+            idx = torch.empty(B, S, K, dtype=torch.int32, device=dev)
+            cnt = torch.empty(B, S, dtype=torch.int32, device=dev)
+            ms_sel = timed(lambda: esa.esa_topk_select(d["qI"], d["kI"], d["wI"], shape, K, idx, cnt, wsel, st))
+            ms_att = timed(lambda: esa.esa_sparse_attn(d["q"], d["k"], d["v"], idx, cnt, shape, K, scale, d["g"],
+                                                       d["lin"], out, None, watt, st))
+            assert esa.esa_read_status(wsel, st) == 0 and esa.esa_read_status(watt, st) == 0
+            ms = ms_sel + ms_att
+            flops = 4.0 * D * B * Hq * sel_pairs
+            entry["kernels_ms"] = {"topk_select": ms_sel, "sparse_attn": ms_att}
+        entry.update({"ms": ms, "tok_per_s": B * S / (ms / 1e3), "algorithmic_tflops": flops / (ms / 1e3) / 1e12,
+                      "tensor_peak_tflops": tf_peak, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tf_peak,
+                      "peak_kind": kind})
+        res[name] = entry
+        del d, host, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def esa_arm(args):
     world, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -317,6 +389,9 @@ def esa_arm(args):
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     traffic = _traffic_for("split_select" if dom_is_sel else "sparse_attn", SELECT_SRC if dom_is_sel else ATTN_SRC)
 
+    prefill = None
+    if rank == 0 and not args.no_prefill:
+        prefill = prefill_section(dev, esa, E)
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -346,6 +421,7 @@ def esa_arm(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "prefill": prefill,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -362,6 +438,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sets", type=int, default=NSETS, help="rotating input sets (small profiling cases use 1)")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workloads' timings")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)

@@ -165,8 +165,8 @@ ESA_API esa_status esa_gated_mix(const float *attn, const uint16_t *lin, const f
  * 0..p, output without the gate. route[b,h] = 1: the sparse path — the
  * index set of esa_topk_select (one set per (b,t), shared by all sparse
  * heads), attention over it, then the gate mix with lin when g and lin are
- * given. Every head of the layer runs in one attention launch. scale is
- * normally 1/sqrt(D). Requires D_I >= 32 and H_I * D_I <= 512. */
+ * given. Every head of the layer runs in one attention launch (on the
+ * tensor cores, accumulators in tensor memory). scale is normally 1/sqrt(D). */
 ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
                            const int8_t *kI, const int32_t *wI, const uint8_t *route, const esa_shape *s, int top_k,
                            float scale, const float *g, const uint16_t *lin, float *out, void *ws, size_t ws_bytes,

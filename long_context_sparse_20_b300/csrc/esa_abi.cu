@@ -220,7 +220,6 @@ esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t 
                            void *stream) {
     esa_status e = check_shape(s, true, true);
     if (e) return e;
-    if (s->D_I == 16 || s->H_I * s->D_I > 512) return ESA_ERR_UNSUPPORTED;
     if (!q || !k || !v || !qI || !kI || !wI || !route || !out) return ESA_ERR_INVALID;
     if ((g == nullptr) != (lin == nullptr)) return ESA_ERR_INVALID;
     if (top_k <= 0 || top_k > 65536) return ESA_ERR_INVALID;

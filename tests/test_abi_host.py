@@ -78,8 +78,8 @@ def test_host_validation_rejects_before_launch():
     # misaligned tensor
     odd = ctypes.c_void_p(0x1008)
     assert L.esa_gated_mix(odd, fake, fake, None, ctypes.byref(s), fake, None) == esa.ERR_INVALID
-    # routed attention does not take D_I = 16
-    sh = _shape(esa, D_I=16)
+    # routed attention: head dim outside {64, 128}
+    sh = _shape(esa, D=96)
     assert L.esa_routed_attn(fake, fake, fake, fake, fake, fake, fake, ctypes.byref(sh), 4, 0.125, None, None, fake,
                              fake, 1 << 20, None) == esa.ERR_UNSUPPORTED
     # workspace: null or misaligned

@@ -191,6 +191,8 @@ ROUTED_CASES = [
     dict(B=2, Tq=200, Tk=200, Hq=8, Hkv=8, D=128, top_k=50, D_I=64),
     dict(B=1, Tq=130, Tk=130, Hq=4, Hkv=2, D=64, top_k=16, D_I=32, H_I=2, weights="1to4"),
     dict(B=1, Tq=64, Tk=300, q_offset=236, Hq=6, Hkv=6, D=128, top_k=100, D_I=128),
+    dict(B=1, Tq=70, Tk=70, Hq=4, Hkv=1, D=64, top_k=12, D_I=16),
+    dict(B=1, Tq=300, Tk=300, Hq=2, Hkv=1, D=128, top_k=64, D_I=64, H_I=4, weights="1to4"),
 ]
 
 
@@ -215,6 +217,20 @@ def test_routed_equal_scores():
     inp["route"] = torch.tensor([[1, 0, 1, 1]], dtype=torch.uint8)
     oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, 20)
     assert_close(gpu_routed(to_dev(inp), sh, 20), ref)
+
+
+def test_routed_wide_scores():
+    """Full-range int8 indexer vectors with large, mixed-sign weights: the
+    collapsed indexer query is not exact in fp16, so the tensor-core kernel
+    takes its exact integer mask path; results must still match."""
+    cfg, sh, inp = _case(seed=19, routed=True, B=1, Tq=200, Tk=200, Hq=4, Hkv=2, D=128, top_k=30, D_I=64, H_I=4)
+    g = torch.Generator().manual_seed(5)
+    inp["qI"] = torch.randint(-128, 128, inp["qI"].shape, dtype=torch.int8, generator=g)
+    inp["kI"] = torch.randint(-128, 128, inp["kI"].shape, dtype=torch.int8, generator=g)
+    inp["wI"] = torch.tensor([500, -300, 200, 7], dtype=torch.int32)
+    inp["route"] = torch.tensor([[1, 0, 1, 1]], dtype=torch.uint8)
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, 30)
+    assert_close(gpu_routed(to_dev(inp), sh, 30), ref)
 
 
 # ------------------------------------------------------------------ the five workloads at full size
