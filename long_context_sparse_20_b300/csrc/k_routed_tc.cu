@@ -7,11 +7,14 @@
 // Top-K positions of the Indexer ("超大规模MoE架构中稀疏注意力机制的演进与实践",
 // sections 二.1-二.3) and are mixed with the linear branch by the gate.
 //
-// Design: one CTA per (sequence, head, 128-row query tile); thread r owns
-// query row r, which is also tensor-memory lane r. Keys are visited in
+// Design: one CTA per (sequence, head, 128-row query tile); query row r is
+// tensor-memory lane r, owned by two threads that split each tile's columns
+// (and O's columns) and exchange row maxima and sums. Keys are visited in
 // 64-key tiles, K/V (and, for sparse heads, the int8 indexer keys) staged by
-// cp.async in a ring of shared-memory slots in the tensor cores' no-swizzle
-// core-matrix layout. One thread issues the MMAs:
+// the tensor memory accelerator (TMA: 3-D tensor maps over [tokens, heads,
+// D], 128-byte swizzled 64-element panels that are the tensor cores' operand
+// layout as loaded) in a ring of shared-memory slots completed on mbarriers.
+// One thread issues the TMA copies and the MMAs:
 //   S  = Q K^T                       bf16 x bf16 -> fp32 (TMEM, 3 buffers)
 //   SI = q_eff kI^T                  fp16 x fp16 -> fp32 (TMEM, 2 buffers):
 //        the indexer scores, exact — q_eff = sum_h w_h qI_h and kI are small
@@ -25,9 +28,12 @@
 // than 2^8, so O (in tensor memory) is rescaled rarely. A CTA whose
 // collapsed indexer query is not exact in fp16 computes its mask scores
 // with dp4a instead.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "esa_device.cuh"
 #include "esa_internal.h"
@@ -36,8 +42,8 @@ namespace esa {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kBM = 128;  // query rows per CTA (tensor-memory lanes)
+constexpr int kThreads = 256;  // two threads per query row
+constexpr int kBM = 128;       // query rows per CTA (tensor-memory lanes)
 constexpr int kBN = 64;   // keys per tile
 constexpr uint32_t kColS = 0;     // 3 x 64 columns: scores, then P (hi 32 + lo 32)
 constexpr uint32_t kColSI = 192;  // 2 x 64 columns: indexer scores
@@ -47,14 +53,16 @@ constexpr float kRescaleLog2 = 8.f;  // raise the running max only past 2^8 grow
 
 template <int D, int DI>
 struct Lay {
-    static constexpr int Q = 0;                          // kBM x D bf16
+    // 128-byte swizzled operands come in 64-element panels, 1024-byte aligned
+    static constexpr int NP = D / 64;                    // panels per row of D elements
+    static constexpr int Q = 0;                          // NP x (kBM rows x 128 B) bf16
     static constexpr int QE = Q + kBM * D * 2;           // kBM x DI fp16 (collapsed indexer query)
     static constexpr int KH = QE + kBM * DI * 2;         // 2 x kBN x DI fp16 (indexer keys)
     static constexpr int RING = KH + 2 * kBN * DI * 2;
-    static constexpr int SK = 0, SV = kBN * D * 2, SKI = 2 * kBN * D * 2;  // within a slot
-    static constexpr int SLOT = SKI + kBN * DI;
-    static constexpr int SLOTS = RING + 4 * SLOT <= 220 * 1024 ? 4 : 3;
-    static constexpr int TOTAL = RING + SLOTS * SLOT;
+    static constexpr int SK = 0, SV = kBN * D * 2, SKI = 2 * kBN * D * 2;  // within a slot: K, V panels, raw kI
+    static constexpr int SLOT = (SKI + kBN * DI + 1023) / 1024 * 1024;
+    static constexpr int SLOTS = RING + 4 * SLOT <= 219 * 1024 ? 4 : 3;
+    static constexpr int TOTAL = RING + SLOTS * SLOT + 1024;  // + alignment slack
 };
 
 struct TcArgs {
@@ -71,9 +79,27 @@ struct TcArgs {
     float scale_log2;
 };
 
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// shared-memory matrix descriptor; swz = 0: no swizzle (core matrices of
+// 8 rows x 16 B; LBO = stride between core matrices along K, SBO = along
+// M/N), swz = 2: 128-byte swizzle (8-row x 128-byte atoms; SBO = 1024, and
+// for an MN-major operand LBO = stride between 64-element panels)
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swz = 0) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
+}
+__device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma2(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
 }
 // instruction descriptor: fp32 accumulate, M = 128; ab = 1 for bf16, 0 for fp16
 __host__ __device__ constexpr uint32_t idesc(int N, uint32_t ab, uint32_t b_mn_major) {
@@ -129,16 +155,56 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// 32 consecutive columns -> 16 columns of packed pairs
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// barrier of the two warps (64 threads) that share one quarter of the rows
+__device__ __forceinline__ void pair_sync(int quarter) {
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
+}
+
 template <int D, int DI>
-__global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    routed_tc_kernel(const __grid_constant__ TcArgs a, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_ki) {
     using L = Lay<D, DI>;
     constexpr int NS = L::SLOTS;
-    extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) unsigned long long bar_s[3], bar_pv;
+    constexpr int NP = L::NP;
+    constexpr int HD = D / 2;    // output columns per thread
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // swizzled panels need 1024-byte alignment
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ __align__(8) unsigned long long bar_s[3], bar_pv, bar_full[4], bar_q;
     __shared__ uint32_t tmem_base;
-    __shared__ int flag_bad;
+    __shared__ float xmax[2][kThreads];  // per-thread partial row max, by tile parity
+    __shared__ float xsum[kThreads];
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    // thread = (row quarter, column half, lane): warps w and w+4 share rows
+    // 32*(w%4) .. +31 (their tensor-memory lanes) and split the columns
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int r = 32 * q4 + lane;  // query row within the tile
+    const int partner = tid ^ 128;
+
     const long long nqt = (a.Tq + kBM - 1) / kBM;
     // query tiles of one (sequence, head) are consecutive, longest prefixes
     // first: the CTAs running together share that head's K/V through L2
@@ -154,13 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
     const long long row0 = b * a.Tq + t0;
     const long long kend = a.q_offset + t0 + rows;  // keys 0..kend-1 are visible to some row
     const int nt = (int)((kend + kBN - 1) / kBN);
-    const long long pos = tid < rows ? a.q_offset + t0 + tid : -1;  // this thread's query position
+    const long long pos = r < rows ? a.q_offset + t0 + r : -1;  // this row's query position
 
     const uint32_t sbase = smem_u32(smem);
-    const uint16_t *kb = a.k + (b * a.Tk * a.Hkv + kvh) * (long long)D;
-    const uint16_t *vb = a.v + (b * a.Tk * a.Hkv + kvh) * (long long)D;
-    const long long kst = (long long)a.Hkv * D;
-    const int8_t *kib = a.kI + b * a.Tk * (long long)DI;
 
     // ---- tensor memory and barriers
     if (warp == 0) {
@@ -168,60 +230,53 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
                      "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    // key tile t -> ring slot t % NS, completed on bar_full[slot] (thread 0
+    // issues; rows past the tensor read as zeros, rows past kend are masked)
+    auto issue_tile = [&](int t) {
+        const int slot = t % NS;
+        const uint32_t sl = sbase + L::RING + slot * L::SLOT;
+        const uint32_t bar = smem_u32(&bar_full[slot]);
+        const int krow = (int)(b * a.Tk + (long long)t * kBN);
+        mbar_expect_tx(bar, (unsigned)(2 * kBN * D * 2 + (sparse ? kBN * DI : 0)));
+#pragma unroll
+        for (int p = 0; p < NP; p++) {
+            tma3(sl + L::SK + p * (kBN * 128), &tm_k, p * 64, kvh, krow, bar);
+            tma3(sl + L::SV + p * (kBN * 128), &tm_v, p * 64, kvh, krow, bar);
+        }
+        if (sparse) tma2(sl + L::SKI, &tm_ki, 0, krow, bar);
+    };
+    int issued = -1;  // last tile issued (thread 0)
     if (tid == 0) {
         for (int i = 0; i < 3; i++) mbar_init(smem_u32(&bar_s[i]), 1);
+        for (int i = 0; i < NS; i++) mbar_init(smem_u32(&bar_full[i]), 1);
         mbar_init(smem_u32(&bar_pv), 1);
+        mbar_init(smem_u32(&bar_q), 1);
         mbar_fence_init();
-        flag_bad = 0;
-    }
-
-    // ---- Q tile (zero rows past the sequence), one cp.async group
-    for (int i = tid; i < kBM * (D / 8); i += kThreads) {
-        const int r = i / (D / 8), c = i % (D / 8);
-        const bool ok = r < rows;
-        cp_async16_zfill(sbase + L::Q + (r / 8) * (D / 8 * 128) + c * 128 + (r % 8) * 16,
-                         a.q + ((row0 + (ok ? r : 0)) * a.Hq + h) * (long long)D + c * 8, ok);
-    }
-    cp_async_commit();
-    // key tile t -> ring slot t % NS (zero-filled past kend); one group per tile
-    auto load_tile = [&](int t) {
-        const uint32_t sl = sbase + L::RING + (t % NS) * L::SLOT;
-        const long long j0 = (long long)t * kBN;
-        for (int i = tid; i < kBN * (D / 8); i += kThreads) {
-            const int kk = i / (D / 8), c = i % (D / 8);
-            const long long j = j0 + kk;
-            const bool ok = j < kend;
-            const long long js = ok ? j : 0;
-            cp_async16_zfill(sl + L::SK + (kk / 8) * (D / 8 * 128) + c * 128 + (kk % 8) * 16, kb + js * kst + c * 8, ok);
-            cp_async16_zfill(sl + L::SV + c * (kBN / 8 * 128) + (kk / 8) * 128 + (kk % 8) * 16, vb + js * kst + c * 8, ok);
+        // Q tile (rows past the sequence are never written out)
+        mbar_expect_tx(smem_u32(&bar_q), (unsigned)(kBM * D * 2));
+#pragma unroll
+        for (int p = 0; p < NP; p++) tma3(sbase + L::Q + p * (kBM * 128), &tm_q, p * 64, h, (int)row0, smem_u32(&bar_q));
+        for (int t = 0; t < NS - 1 && t < nt; t++) {
+            issue_tile(t);
+            issued = t;
         }
-        if (sparse) {
-            for (int i = tid; i < kBN * DI / 16; i += kThreads) {
-                const long long j = j0 + (i * 16) / DI;
-                const bool ok = j < kend;
-                cp_async16_zfill(sl + L::SKI + i * 16, kib + (ok ? j0 * DI + i * 16 : 0), ok);
-            }
-        }
-    };
-    for (int t = 0; t < NS - 1; t++) {
-        if (t < nt) load_tile(t);
-        cp_async_commit();
     }
 
     // ---- sparse heads: threshold form and the collapsed indexer query
+    // (each of a row's two threads collapses half of its components)
     float Tf = 0.f;
     int Tint = 0, Pp = -1;
     bool exact = true;
     if (sparse) {
-        if (tid < rows) {
-            Tint = a.thr[2 * (row0 + tid)];
-            Pp = a.thr[2 * (row0 + tid) + 1];
+        if (r < rows) {
+            Tint = a.thr[2 * (row0 + r)];
+            Pp = a.thr[2 * (row0 + r) + 1];
         }
         Tf = (float)Tint;
         long long absum = 0;
         bool fits = true;
-        const int8_t *qrow = a.qI + (row0 + (tid < rows ? tid : 0)) * (long long)a.H_I * DI;
-        for (int c0 = 0; c0 < DI; c0 += 8) {
+        const int8_t *qrow = a.qI + (row0 + (r < rows ? r : 0)) * (long long)a.H_I * DI;
+        for (int c0 = hf * (DI / 2); c0 < (hf + 1) * (DI / 2); c0 += 8) {
             int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
             for (int hh = 0; hh < a.H_I; hh++) {
                 const int wv = a.wI[hh];
@@ -240,26 +295,28 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
             }
 #pragma unroll
             for (int e = 0; e < 4; e++) pk[e] = pack_f16((float)acc[2 * e], (float)acc[2 * e + 1]);
-            if (tid >= rows) pk[0] = pk[1] = pk[2] = pk[3] = 0u;
-            *reinterpret_cast<uint4 *>(smem + L::QE + (tid / 8) * (DI / 8 * 128) + (c0 / 8) * 128 + (tid % 8) * 16) =
+            if (r >= rows) pk[0] = pk[1] = pk[2] = pk[3] = 0u;
+            *reinterpret_cast<uint4 *>(smem + L::QE + (r / 8) * (DI / 8 * 128) + (c0 / 8) * 128 + (r % 8) * 16) =
                 make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        // every partial sum of q_eff . kI (|kI| <= 128) must stay below 2^24
-        fits = fits && absum * 128 < (1ll << 24);
-        exact = __syncthreads_and(fits || tid >= rows) != 0;
+        // every partial sum of q_eff . kI (|kI| <= 128) must stay below 2^24:
+        // each half of the components below 2^23
+        fits = fits && absum * 128 < (1ll << 23);
+        exact = __syncthreads_and(fits || r >= rows) != 0;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
 
-    // convert tile t's raw indexer keys to fp16 into KH buffer t % 2
+    // convert tile t's raw indexer keys to fp16 into KH buffer t % 2 (eight
+    // consecutive lanes write one 128-byte core-matrix row)
     auto convert_ki = [&](int t) {
         const unsigned char *raw = smem + L::RING + (t % NS) * L::SLOT + L::SKI;
         unsigned char *dst = smem + L::KH + (t % 2) * (kBN * DI * 2);
         for (int i = tid; i < kBN * DI / 8; i += kThreads) {
-            const int kk = i / (DI / 8), c8 = i % (DI / 8);
+            const int c8 = (i / 8) % (DI / 8), kk = (i % 8) + 8 * ((i / 8) / (DI / 8));
             const uint2 rv = *reinterpret_cast<const uint2 *>(raw + kk * DI + c8 * 8);
             uint32_t pk[4];
 #pragma unroll
@@ -278,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
         constexpr uint32_t id_s = idesc(kBN, 1u, 0u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk++)
-            mma_ss(tmem + kColS + (t % 3) * 64, sdesc(sbase + L::Q + kk * 256, 128, D / 8 * 128),
-                   sdesc(sl + L::SK + kk * 256, 128, D / 8 * 128), id_s, kk > 0);
+            mma_ss(tmem + kColS + (t % 3) * 64,
+                   sdesc(sbase + L::Q + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024, 2),
+                   sdesc(sl + L::SK + (kk / 4) * (kBN * 128) + (kk % 4) * 32, 16, 1024, 2), id_s, kk > 0);
         if (sparse && exact) {
             constexpr uint32_t id_i = idesc(kBN, 0u, 0u);
             const uint32_t kh = sbase + L::KH + (t % 2) * (kBN * DI * 2);
@@ -293,11 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
 
     // ---- prologue: Q, tile 0 -> scores of tile 0
     bool bad = false;
-    cp_async_wait_dyn(NS - 2);  // Q and tile 0 have landed (this thread's copies)
-    if (sparse && exact && nt > 0) {
-        __syncthreads();  // ... and everyone's, before converting them
-        convert_ki(0);
-    }
+    if (!mbar_wait_bounded(smem_u32(&bar_q), 0u, a.wait_ns)) bad = true;
+    if (nt > 0 && !mbar_wait_bounded(smem_u32(&bar_full[0]), 0u, a.wait_ns)) bad = true;
+    if (sparse && exact && nt > 0) convert_ki(0);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -306,16 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
         issue_scores(0);
     }
 
-    float m_used = -INFINITY, l = 0.f;
+    float m_used = -INFINITY, l = 0.f;  // l: this thread's half of the row sum
     for (int j = 0; j < nt; j++) {
         // A. tile j+1 landed: its scores go to the tensor cores while this
         //    tile's softmax runs
         if (j + 1 < nt) {
-            cp_async_wait_dyn(NS - 3);  // tile t is cp.async group t + 1
-            if (sparse && exact) {
-                __syncthreads();  // every thread's copies of tile j+1 have landed
-                convert_ki(j + 1);
-            }
+            if (!mbar_wait_bounded(smem_u32(&bar_full[(j + 1) % NS]), (unsigned)((j + 1) / NS) & 1u, a.wait_ns))
+                bad = true;
+            if (sparse && exact) convert_ki(j + 1);
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -327,31 +381,26 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
         // B. scores of tile j
         if (!mbar_wait_bounded(smem_u32(&bar_s[j % 3]), (unsigned)(j / 3) & 1u, a.wait_ns)) bad = true;
         tc_fence_after();
-        // C. softmax of tile j -> P (hi, lo) over the consumed S columns
-        uint32_t sr[64];
-        tmem_ld32(tmem + lane_base + kColS + (j % 3) * 64, sr);
-        tmem_ld32(tmem + lane_base + kColS + (j % 3) * 64 + 32, sr + 32);
-        const long long j0 = (long long)j * kBN;
-        // keep bit c: key j0+c passes the Top-K test (sparse heads)
-        uint64_t keep = ~0ull;
+        // C. softmax of tile j (this thread: keys 32*hf .. +31 of the tile) ->
+        //    P (hi, lo) over the consumed S columns
+        uint32_t sr[32];
+        tmem_ld32(tmem + lane_base + kColS + (j % 3) * 64 + hf * 32, sr);
+        const long long j0 = (long long)j * kBN + hf * 32;
+        uint32_t keep = 0xffffffffu;  // bit c: key j0+c passes the Top-K test
         if (sparse && exact) {
+            uint32_t ir[32];
+            tmem_ld32(tmem + lane_base + kColSI + (j % 2) * 64 + hf * 32, ir);
+            tmem_wait_ld();
 #pragma unroll
-            for (int half = 0; half < 2; half++) {
-                uint32_t ir[32];
-                tmem_ld32(tmem + lane_base + kColSI + (j % 2) * 64 + half * 32, ir);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; c++) {
-                    const float si = __uint_as_float(ir[c]);
-                    const bool sel = si > Tf || (si == Tf && j0 + half * 32 + c <= Pp);
-                    if (!sel) keep &= ~(1ull << (half * 32 + c));
-                }
+            for (int c = 0; c < 32; c++) {
+                const float si = __uint_as_float(ir[c]);
+                if (!(si > Tf || (si == Tf && j0 + c <= Pp))) keep &= ~(1u << c);
             }
         } else if (sparse) {
             // exact integer mask scores with dp4a (collapsed query not exact in fp16)
-            const unsigned char *raw = smem + L::RING + (j % NS) * L::SLOT + L::SKI;
-            const int8_t *qrow = a.qI + (row0 + (tid < rows ? tid : 0)) * (long long)a.H_I * DI;
-            for (int c = 0; c < 64; c++) {
+            const unsigned char *raw = smem + L::RING + (j % NS) * L::SLOT + L::SKI + hf * 32 * DI;
+            const int8_t *qrow = a.qI + (row0 + (r < rows ? r : 0)) * (long long)a.H_I * DI;
+            for (int c = 0; c < 32; c++) {
                 unsigned acc = 0;
                 for (int hh = 0; hh < a.H_I; hh++) {
                     int d = 0;
@@ -362,63 +411,70 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
                     acc += (unsigned)a.wI[hh] * (unsigned)d;
                 }
                 const int si = (int)acc;
-                if (!(si > Tint || (si == Tint && j0 + c <= Pp))) keep &= ~(1ull << c);
+                if (!(si > Tint || (si == Tint && j0 + c <= Pp))) keep &= ~(1u << c);
             }
         }
         tmem_wait_ld();
         // causal: key j0+c is visible to this row iff c <= pos - j0
-        const int lim = (int)max(-1ll, min(64ll, pos - j0));
-        float mt = -INFINITY;
+        const int lim = (int)max(-1ll, min(32ll, pos - j0));
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 64; c++) {
-            const bool valid = c <= lim && ((keep >> c) & 1ull);
+        for (int c = 0; c < 32; c++) {
+            const bool valid = c <= lim && ((keep >> c) & 1u);
             const float xv = valid ? __uint_as_float(sr[c]) * a.scale_log2 : -INFINITY;
             sr[c] = __float_as_uint(xv);
-            mt = fmaxf(mt, xv);
+            mx4[c & 3] = fmaxf(mx4[c & 3], xv);
         }
+        // row max: this half and the partner thread's half
+        xmax[j & 1][tid] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        pair_sync(q4);
+        const float mt = fmaxf(xmax[j & 1][tid], xmax[j & 1][partner]);
         float corr = 1.f;
         bool rescale = false;
         if (mt > m_used + kRescaleLog2 || (m_used == -INFINITY && mt > -INFINITY)) {
             rescale = m_used != -INFINITY;  // O is still zero before the first kept key
-            corr = rescale ? exp2f(m_used - mt) : 1.f;
+            corr = rescale ? ex2_approx(m_used - mt) : 1.f;
             l *= corr;
             m_used = mt;
         }
         const float mu = m_used == -INFINITY ? 0.f : m_used;
-        uint32_t phi[32], plo[32];
-        float ls = 0.f;
+        uint32_t phi[16], plo[16];
+        float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-            const float p0 = exp2f(__uint_as_float(sr[c]) - mu), p1 = exp2f(__uint_as_float(sr[c + 1]) - mu);
-            ls += p0 + p1;
+        for (int c = 0; c < 32; c += 2) {
+            const float p0 = ex2_approx(__uint_as_float(sr[c]) - mu), p1 = ex2_approx(__uint_as_float(sr[c + 1]) - mu);
+            ls0 += p0;
+            ls1 += p1;
             const uint32_t hw = pack_bf16(p0, p1);
             phi[c / 2] = hw;
             plo[c / 2] = pack_bf16(p0 - bf16lo(hw), p1 - bf16hi(hw));
         }
-        l += ls;
-        tmem_st32(tmem + lane_base + kColS + (j % 3) * 64, phi);
-        tmem_st32(tmem + lane_base + kColS + (j % 3) * 64 + 32, plo);
+        l += ls0 + ls1;
+        tmem_st16(tmem + lane_base + kColS + (j % 3) * 64 + hf * 16, phi);
+        tmem_st16(tmem + lane_base + kColS + (j % 3) * 64 + 32 + hf * 16, plo);
         tmem_wait_st();
         // D. the previous tile's P V has finished: O is stable, its slot is free
         if (j > 0 && !mbar_wait_bounded(smem_u32(&bar_pv), (unsigned)(j - 1) & 1u, a.wait_ns)) bad = true;
         tc_fence_after();
-        // E. rescale O rows whose running max was raised (warp-wide: tensor
-        //    memory access is collective)
+        // E. rescale this thread's half of the O row when the running max was
+        //    raised (warp-wide: tensor memory access is collective)
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < HD; c0 += 32) {
                 uint32_t o_raw[32];
-                tmem_ld32(tmem + lane_base + kColO + c0, o_raw);
+                tmem_ld32(tmem + lane_base + kColO + hf * HD + c0, o_raw);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; e++) o_raw[e] = __float_as_uint(__uint_as_float(o_raw[e]) * corr);
-                tmem_st32(tmem + lane_base + kColO + c0, o_raw);
+                tmem_st32(tmem + lane_base + kColO + hf * HD + c0, o_raw);
             }
             tmem_wait_st();
         }
         // F. the slot of tile j-1 is free (its S and P V are done): load tile j-1+NS
-        if (j - 1 + NS < nt) load_tile(j - 1 + NS);
-        cp_async_commit();
+        if (tid == 0 && j - 1 + NS < nt && !bad) {
+            issue_tile(j - 1 + NS);
+            issued = j - 1 + NS;
+        }
         // G. P V of tile j
         tc_fence_before();
         if (__syncthreads_or(bad)) {
@@ -427,8 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
                 set_status(a.status, ESA_ERR_TIMEOUT);
                 if (j > 0) mbar_wait_bounded(smem_u32(&bar_pv), (unsigned)(j - 1) & 1u, a.wait_ns);
                 if (j + 1 < nt) mbar_wait_bounded(smem_u32(&bar_s[(j + 1) % 3]), (unsigned)((j + 1) / 3) & 1u, a.wait_ns);
+                for (int t = j + 2; t <= issued; t++)  // copies still in flight
+                    mbar_wait_bounded(smem_u32(&bar_full[t % NS]), (unsigned)(t / NS) & 1u, a.wait_ns);
             }
-            cp_async_wait<0>();
             tc_fence_before();
             __syncthreads();
             if (warp == 0) {
@@ -446,46 +503,48 @@ __global__ void __launch_bounds__(kThreads, 1) routed_tc_kernel(TcArgs a) {
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; kk++)
                     mma_ts(tmem + kColO, tmem + kColS + (j % 3) * 64 + part * 32 + kk * 8,
-                           sdesc(sl + L::SV + kk * 256, 128, kBN / 8 * 128), id_o, (j > 0 || part > 0 || kk > 0));
+                           sdesc(sl + L::SV + kk * 2048, kBN * 128, 1024, 2), id_o, (j > 0 || part > 0 || kk > 0));
             mma_commit(smem_u32(&bar_pv));
         }
     }
 
-    // ---- epilogue: O / l, gate mix for sparse heads
+    // ---- epilogue: O / l (both halves of the row sum), gate mix for sparse heads
     if (nt > 0 && !mbar_wait_bounded(smem_u32(&bar_pv), (unsigned)(nt - 1) & 1u, a.wait_ns)) {
         set_status(a.status, ESA_ERR_TIMEOUT);
         bad = true;
     }
     tc_fence_after();
+    xsum[tid] = l;
+    pair_sync(q4);
+    const float lt = l + xsum[partner];
     const bool gated = sparse && a.g != nullptr && a.lin != nullptr;
     const float gh = gated ? a.g[h] : 1.f, gl = 1.f - gh;
-    const long long obase = ((row0 + tid) * a.Hq + h) * (long long)D;
+    const long long obase = ((row0 + r) * a.Hq + h) * (long long)D + hf * HD;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = 0; c0 < HD; c0 += 32) {
         uint32_t o_raw[32];
         if (nt > 0) {
-            tmem_ld32(tmem + lane_base + kColO + c0, o_raw);
+            tmem_ld32(tmem + lane_base + kColO + hf * HD + c0, o_raw);
             tmem_wait_ld();
         }
-        if (tid < rows && !bad) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (r < rows && !bad) {
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
-                float4 r = nt > 0 ? make_float4(__uint_as_float(o_raw[e]) * inv, __uint_as_float(o_raw[e + 1]) * inv,
-                                                __uint_as_float(o_raw[e + 2]) * inv, __uint_as_float(o_raw[e + 3]) * inv)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                float4 v4 = nt > 0 ? make_float4(__uint_as_float(o_raw[e]) * inv, __uint_as_float(o_raw[e + 1]) * inv,
+                                                 __uint_as_float(o_raw[e + 2]) * inv, __uint_as_float(o_raw[e + 3]) * inv)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
                 if (gated) {
                     const uint2 lw = *reinterpret_cast<const uint2 *>(a.lin + obase + c0 + e);
-                    r.x = fmaf(gh, r.x, gl * bf16lo(lw.x));
-                    r.y = fmaf(gh, r.y, gl * bf16hi(lw.x));
-                    r.z = fmaf(gh, r.z, gl * bf16lo(lw.y));
-                    r.w = fmaf(gh, r.w, gl * bf16hi(lw.y));
+                    v4.x = fmaf(gh, v4.x, gl * bf16lo(lw.x));
+                    v4.y = fmaf(gh, v4.y, gl * bf16hi(lw.x));
+                    v4.z = fmaf(gh, v4.z, gl * bf16lo(lw.y));
+                    v4.w = fmaf(gh, v4.w, gl * bf16hi(lw.y));
                 }
-                *reinterpret_cast<float4 *>(a.out + obase + c0 + e) = r;
+                *reinterpret_cast<float4 *>(a.out + obase + c0 + e) = v4;
             }
         }
     }
-    cp_async_wait<0>();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -508,6 +567,49 @@ void *tc_kernel_d(int DI, size_t *smem) {
         case 64: return tc_kernel<D, 64>(smem);
         default: return tc_kernel<D, 128>(smem);
     }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library)
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// [rows, heads, D] bf16 as 64-element x 1-head x box_rows boxes, 128-byte swizzle
+bool map_rows_heads_d(CUtensorMap *m, const void *base, long long rows, int heads, int D, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows, DI] int8 as DI x box_rows boxes, no swizzle
+bool map_rows_bytes(CUtensorMap *m, const void *base, long long rows, int DI, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)DI, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)DI};
+    cuuint32_t box[2] = {(cuuint32_t)DI, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -540,10 +642,15 @@ esa_status launch_routed_tc(const uint16_t *q, const uint16_t *k, const uint16_t
     a.scale_log2 = scale * 1.4426950408889634f;
     long long blocks = s.B * s.Hq * ((s.Tq + kBM - 1) / kBM);
     if (blocks == 0) return ESA_OK;
+    if (s.B * s.Tq >= (1ll << 31) || s.B * s.Tk >= (1ll << 31)) return ESA_ERR_UNSUPPORTED;  // TMA coordinates
+    CUtensorMap tq, tk, tv, tki;
+    if (!map_rows_heads_d(&tq, q, s.B * s.Tq, s.Hq, s.D, kBM) || !map_rows_heads_d(&tk, k, s.B * s.Tk, s.Hkv, s.D, kBN) ||
+        !map_rows_heads_d(&tv, v, s.B * s.Tk, s.Hkv, s.D, kBN) || !map_rows_bytes(&tki, kI, s.B * s.Tk, s.D_I, kBN))
+        return ESA_ERR_CUDA;
     size_t smem = 0;
     void *fn = s.D == 64 ? tc_kernel_d<64>(s.D_I, &smem) : tc_kernel_d<128>(s.D_I, &smem);
     if (!ensure_smem(fn, smem)) return ESA_ERR_CUDA;
-    void *args[] = {(void *)&a};
+    void *args[] = {(void *)&a, (void *)&tq, (void *)&tk, (void *)&tv, (void *)&tki};
     cudaError_t ce = cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(kThreads), args, smem, st);
     return ce == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }
