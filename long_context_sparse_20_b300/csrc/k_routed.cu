@@ -10,7 +10,8 @@
 // Two launches: the row-tiled selection reduces every query row's index set
 // to its threshold form (T, P) — key j <= p is selected iff s_j > T, or
 // s_j == T and j <= P, which is exactly the top-K set with ties to the lower
-// position — and the tensor-core kernel (k_routed_tc.cu) runs every head,
+// position — and a tensor-core kernel runs every head (k_routed_pp.cu, warp-
+// specialised over two query tiles, where its buffers fit; else k_routed_tc.cu),
 // full and sparse, rebuilding the sparse heads' masks from exact indexer
 // scores. For multi-head prefill at 64K tokens this moves 64 bytes of indexer
 // key per key tile instead of gathering 512 bytes per selected key per head
@@ -30,8 +31,10 @@ esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16
     int32_t *thr = reinterpret_cast<int32_t *>(base + kStatusBytes);
     esa_status e = launch_row_select(qI, kI, wI, s, K, nullptr, nullptr, thr, ws, st);
     if (e != ESA_OK) return e;
-    return launch_routed_tc(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, reinterpret_cast<int32_t *>(ws),
-                            st);
+    int32_t *status = reinterpret_cast<int32_t *>(ws);
+    if (routed_pp_supported(s))
+        return launch_routed_pp(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, status, st);
+    return launch_routed_tc(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, status, st);
 }
 
 }  // namespace esa

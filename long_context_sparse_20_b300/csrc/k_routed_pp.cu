@@ -1,0 +1,580 @@
+// Per-head routed attention on the tensor cores, warp-specialised: two
+// query tiles per CTA so that one tile's softmax overlaps the other tile's
+// matrix products.
+//
+// Method ("Elastic Attention：动态路由优化大模型长文本处理", sections 2.2 and
+// 3.1): every head runs either full causal attention or the sparse path,
+// decided per head, inside one launch; sparse heads attend to exactly the
+// Top-K positions of the Indexer ("超大规模MoE架构中稀疏注意力机制的演进与实践",
+// sections 二.1-二.3) and are mixed with the linear branch by the gate.
+//
+// Roles in one CTA (one sequence, one head, query tiles A and B of 128 rows):
+//   warps 0-3  softmax of tile A, one thread per query row (TMEM lane)
+//   warps 4-7  softmax of tile B
+//   warp 8     TMA producer: Q once, then K, V (and raw int8 indexer keys)
+//              per 64-key tile into a ring of shared-memory slots; converts
+//              the indexer keys to fp16 for the tensor cores
+//   warp 9     one thread issues every tcgen05.mma:
+//                S  = Q K^T            (bf16, fp32 in TMEM)
+//                SI = q_eff kI^T       (fp16 holding exact small integers; the
+//                                       Top-K mask of sparse heads)
+//                O += P_hi V + P_lo V  (P from TMEM)
+// All hand-offs are mbarriers (scores ready, scores read, P ready, P V done,
+// slot free, indexer keys converted / consumed); no CTA-wide barrier runs
+// inside the key loop. Per query tile the tensor memory holds S (64
+// columns), SI and then P over the same 64 columns, and O (D columns).
+// The mask, the softmax (running max raised only past 2^8 growth, so O is
+// rescaled rarely), the bf16 hi + lo split of P and the gate epilogue are as
+// in k_routed_tc.cu, which serves the shapes whose buffers do not fit here.
+#include <algorithm>
+
+#include "esa_device.cuh"
+#include "esa_internal.h"
+#include "tc_util.cuh"
+
+namespace esa {
+
+namespace {
+
+constexpr int kRowsT = 128;  // rows per query tile (TMEM lanes)
+constexpr int kBN = 64;      // keys per key tile
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kSlots = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColsPerTile = 256;  // per query tile: S 64 | SI, P 64 | O D
+constexpr float kRescaleLog2 = 8.f;
+
+template <int D, int DI>
+struct PLay {
+    static constexpr int NP = D / 64;                 // 64-element swizzled panels per row
+    static constexpr int QT = kRowsT * D * 2;         // one query tile
+    static constexpr int Q = 0;                       // 2 query tiles
+    static constexpr int QET = kRowsT * DI * 2;       // one collapsed indexer query tile (fp16)
+    static constexpr int QE = Q + 2 * QT;
+    static constexpr int KHB = kBN * DI * 2;          // fp16 indexer keys of one key tile
+    static constexpr int KH = QE + 2 * QET;           // 2 buffers
+    static constexpr int RING = KH + 2 * KHB;
+    static constexpr int SK = 0, SV = kBN * D * 2, SKI = 2 * kBN * D * 2;
+    static constexpr int SLOT = (SKI + kBN * DI + 1023) / 1024 * 1024;
+    static constexpr int TOTAL = RING + kSlots * SLOT + 1024;  // + alignment slack
+    static constexpr bool FITS = TOTAL <= 227 * 1024;
+};
+
+struct PpArgs {
+    const uint16_t *lin;
+    const int8_t *qI;
+    const int32_t *wI;
+    const uint8_t *route;
+    const int32_t *thr;
+    const float *g;
+    float *out;
+    int32_t *status;
+    long long B, Tq, Tk, q_offset, wait_ns;
+    int Hq, Hkv, H_I;
+    float scale_log2;
+};
+
+struct PpBars {
+    unsigned long long full[kSlots], slot_free[kSlots], kh_ready[2], kh_free[2];
+    unsigned long long s_ready[2], s_free[2], p_ready[2], pv_done[2];
+    unsigned long long bar_q, qe_ready, mma_end;
+};
+
+// Bounded wait that also gives up when another role has aborted the CTA.
+__device__ __forceinline__ bool pp_wait(uint32_t bar, uint32_t parity, long long limit_ns, volatile int *abort,
+                                        int32_t *status) {
+    for (int i = 0; i < 64; i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if ((long long)(t - t0) > limit_ns) {
+            *abort = 1;
+            set_status(status, ESA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+template <int D, int DI>
+__global__ void __launch_bounds__(kThreads, 1)
+    routed_pp_kernel(const __grid_constant__ PpArgs a, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_ki) {
+    using L = PLay<D, DI>;
+    constexpr int NP = L::NP;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ __align__(8) PpBars bars;
+    __shared__ uint32_t tmem_base;
+    __shared__ int exact_all;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long nqt = (a.Tq + kRowsT - 1) / kRowsT;
+    const long long npair = (nqt + 1) / 2;
+    // pairs of query tiles of one (sequence, head) are consecutive, longest
+    // prefixes first: the CTAs running together share that head's K/V in L2
+    long long bid = blockIdx.x;
+    const long long qp = npair - 1 - bid % npair;
+    bid /= npair;
+    const int h = (int)(bid % a.Hq);
+    const long long b = bid / a.Hq;
+    const int kvh = h / (a.Hq / a.Hkv);
+    const bool sparse = a.route[b * a.Hq + h] != 0;
+    long long t0x[2];
+    int rowsx[2], ntx[2];
+    for (int x = 0; x < 2; x++) {
+        t0x[x] = (2 * qp + x) * kRowsT;
+        rowsx[x] = (int)max(0ll, min((long long)kRowsT, a.Tq - t0x[x]));
+        ntx[x] = rowsx[x] > 0 ? (int)((a.q_offset + t0x[x] + rowsx[x] + kBN - 1) / kBN) : 0;
+    }
+    const int nt = max(ntx[0], ntx[1]);
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [](unsigned long long &x) { return smem_u32(&x); };
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == kProducerWarp * 32) {
+        for (int i = 0; i < kSlots; i++) {
+            mbar_init(bar(bars.full[i]), 1);
+            mbar_init(bar(bars.slot_free[i]), 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(bar(bars.kh_ready[i]), 1);
+            mbar_init(bar(bars.kh_free[i]), 1);
+            mbar_init(bar(bars.s_ready[i]), 1);
+            mbar_init(bar(bars.s_free[i]), kRowsT);
+            mbar_init(bar(bars.p_ready[i]), kRowsT);
+            mbar_init(bar(bars.pv_done[i]), 1);
+        }
+        mbar_init(bar(bars.bar_q), 1);
+        mbar_init(bar(bars.qe_ready), 2 * kRowsT);
+        mbar_init(bar(bars.mma_end), 1);
+        mbar_fence_init();
+        exact_all = 1;
+        abort_flag = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    if (warp < 8) {
+        // ================================================= softmax warps
+        const int x = warp >> 2, q4 = warp & 3;
+        const int r = 32 * q4 + lane;  // row within tile x, and its TMEM lane
+        const int rows = rowsx[x], ntt = ntx[x];
+        const long long row0 = b * a.Tq + t0x[x];
+        const long long pos = r < rows ? a.q_offset + t0x[x] + r : -1;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        const uint32_t colS = x * kColsPerTile, colSI = colS + 64, colO = colS + 128;
+        float Tf = 0.f;
+        int Tint = 0, Pp = -1;
+        if (sparse) {
+            if (r < rows) {
+                Tint = a.thr[2 * (row0 + r)];
+                Pp = a.thr[2 * (row0 + r) + 1];
+            }
+            Tf = (float)Tint;
+            // collapsed indexer query q_eff = sum_h w_h qI_h (fp16, exact while
+            // |q_eff| <= 2048 and every partial sum of q_eff . kI stays below 2^24)
+            long long absum = 0;
+            bool fits = true;
+            const int8_t *qrow = a.qI + (row0 + (r < rows ? r : 0)) * (long long)a.H_I * DI;
+            for (int c0 = 0; c0 < DI; c0 += 8) {
+                int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                for (int hh = 0; hh < a.H_I; hh++) {
+                    const int wv = a.wI[hh];
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + hh * DI + c0);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const int8_t qv = (int8_t)(((e < 4 ? raw.x : raw.y) >> (8 * (e & 3))) & 0xFF);
+                        acc[e] += wv * (int)qv;
+                    }
+                }
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    fits = fits && acc[e] >= -2048 && acc[e] <= 2048;
+                    absum += acc[e] < 0 ? -(long long)acc[e] : acc[e];
+                }
+#pragma unroll
+                for (int e = 0; e < 4; e++) pk[e] = pack_f16((float)acc[2 * e], (float)acc[2 * e + 1]);
+                if (r >= rows) pk[0] = pk[1] = pk[2] = pk[3] = 0u;
+                *reinterpret_cast<uint4 *>(smem + L::QE + x * L::QET + (r / 8) * (DI / 8 * 128) + (c0 / 8) * 128 +
+                                           (r % 8) * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            fits = fits && absum * 128 < (1ll << 24);
+            if (!fits && r < rows) atomicAnd(&exact_all, 0);
+            fence_async_smem();
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // every softmax thread has voted
+        const bool exact = exact_all != 0;
+        mbar_arrive(bar(bars.qe_ready));
+
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < ntt && ok; t++) {
+            if (!pp_wait(bar(bars.s_ready[x]), (uint32_t)t & 1u, a.wait_ns, &abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[64];
+            tmem_ld32(tmem + lane_base + colS, sr);
+            tmem_ld32(tmem + lane_base + colS + 32, sr + 32);
+            const long long j0 = (long long)t * kBN;
+            uint64_t keep = ~0ull;  // bit c: key j0+c passes the Top-K test
+            if (sparse && exact) {
+#pragma unroll
+                for (int half = 0; half < 2; half++) {
+                    uint32_t ir[32];
+                    tmem_ld32(tmem + lane_base + colSI + half * 32, ir);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; c++) {
+                        const float si = __uint_as_float(ir[c]);
+                        if (!(si > Tf || (si == Tf && j0 + half * 32 + c <= Pp))) keep &= ~(1ull << (half * 32 + c));
+                    }
+                }
+            } else if (sparse) {
+                // exact integer mask scores with dp4a from the raw keys of the slot
+                const int slot = t % kSlots;
+                if (!pp_wait(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                const unsigned char *raw = smem + L::RING + slot * L::SLOT + L::SKI;
+                const int8_t *qrow = a.qI + (row0 + (r < rows ? r : 0)) * (long long)a.H_I * DI;
+                for (int c = 0; c < 64; c++) {
+                    unsigned acc = 0;
+                    for (int hh = 0; hh < a.H_I; hh++) {
+                        int d = 0;
+#pragma unroll
+                        for (int w4 = 0; w4 < DI / 4; w4++)
+                            d = __dp4a(reinterpret_cast<const int *>(qrow + hh * DI)[w4],
+                                       reinterpret_cast<const int *>(raw + c * DI)[w4], d);
+                        acc += (unsigned)a.wI[hh] * (unsigned)d;
+                    }
+                    const int si = (int)acc;
+                    if (!(si > Tint || (si == Tint && j0 + c <= Pp))) keep &= ~(1ull << c);
+                }
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(bars.s_free[x]));  // S (and SI) are in registers
+            // causal: key j0+c is visible to this row iff c <= pos - j0
+            const int lim = (int)max(-1ll, min(64ll, pos - j0));
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < 64; c++) {
+                const bool valid = c <= lim && ((keep >> c) & 1ull);
+                const float xv = valid ? __uint_as_float(sr[c]) * a.scale_log2 : -INFINITY;
+                sr[c] = __float_as_uint(xv);
+                mx4[c & 3] = fmaxf(mx4[c & 3], xv);
+            }
+            const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            float corr = 1.f;
+            bool rescale = false;
+            if (mt > m_used + kRescaleLog2 || (m_used == -INFINITY && mt > -INFINITY)) {
+                rescale = m_used != -INFINITY;  // O is still zero before the first kept key
+                corr = rescale ? ex2_approx(m_used - mt) : 1.f;
+                l *= corr;
+                m_used = mt;
+            }
+            const float mu = m_used == -INFINITY ? 0.f : m_used;
+            uint32_t phi[32], plo[32];
+            float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                const float p0 = ex2_approx(__uint_as_float(sr[c]) - mu),
+                            p1 = ex2_approx(__uint_as_float(sr[c + 1]) - mu);
+                ls0 += p0;
+                ls1 += p1;
+                const uint32_t hw = pack_bf16(p0, p1);
+                phi[c / 2] = hw;
+                plo[c / 2] = pack_bf16(p0 - bf16lo(hw), p1 - bf16hi(hw));
+            }
+            l += ls0 + ls1;
+            // the previous tile's P V is done: P's columns are free, O is stable
+            if (t > 0 && !pp_wait(bar(bars.pv_done[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o_raw[32];
+                    tmem_ld32(tmem + lane_base + colO + c0, o_raw);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e++) o_raw[e] = __float_as_uint(__uint_as_float(o_raw[e]) * corr);
+                    tmem_st32(tmem + lane_base + colO + c0, o_raw);
+                }
+            }
+            tmem_st32(tmem + lane_base + colSI, phi);
+            tmem_st32(tmem + lane_base + colSI + 32, plo);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(bars.p_ready[x]));
+        }
+        // ---- epilogue: O / l, gate mix for sparse heads
+        if (ok && ntt > 0 &&
+            pp_wait(bar(bars.pv_done[x]), (uint32_t)(ntt - 1) & 1u, a.wait_ns, &abort_flag, a.status)) {
+            tc_fence_after();
+            const bool gated = sparse && a.g != nullptr && a.lin != nullptr;
+            const float gh = gated ? a.g[h] : 1.f, gl = 1.f - gh;
+            const long long obase = ((row0 + r) * a.Hq + h) * (long long)D;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o_raw[32];
+                tmem_ld32(tmem + lane_base + colO + c0, o_raw);
+                tmem_wait_ld();
+                if (r < rows) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        float4 v4 = make_float4(__uint_as_float(o_raw[e]) * inv, __uint_as_float(o_raw[e + 1]) * inv,
+                                                __uint_as_float(o_raw[e + 2]) * inv, __uint_as_float(o_raw[e + 3]) * inv);
+                        if (gated) {
+                            const uint2 lw = *reinterpret_cast<const uint2 *>(a.lin + obase + c0 + e);
+                            v4.x = fmaf(gh, v4.x, gl * bf16lo(lw.x));
+                            v4.y = fmaf(gh, v4.y, gl * bf16hi(lw.x));
+                            v4.z = fmaf(gh, v4.z, gl * bf16lo(lw.y));
+                            v4.w = fmaf(gh, v4.w, gl * bf16hi(lw.y));
+                        }
+                        *reinterpret_cast<float4 *>(a.out + obase + c0 + e) = v4;
+                    }
+                }
+            }
+        }
+    } else if (warp == kProducerWarp) {
+        // ================================================= TMA producer
+        int issued = -1;
+        auto issue = [&](int t) {  // lane 0 issues; the whole warp waits for the slot
+            const int slot = t % kSlots;
+            if (t >= kSlots &&
+                !pp_wait(bar(bars.slot_free[slot]), (uint32_t)(t / kSlots - 1) & 1u, a.wait_ns, &abort_flag, a.status))
+                return false;
+            if (lane == 0) {
+                const uint32_t sl = sbase + L::RING + slot * L::SLOT;
+                const uint32_t fb = bar(bars.full[slot]);
+                const int krow = (int)(b * a.Tk + (long long)t * kBN);
+                mbar_expect_tx(fb, (unsigned)(2 * kBN * D * 2 + (sparse ? kBN * DI : 0)));
+#pragma unroll
+                for (int p = 0; p < NP; p++) {
+                    tma3(sl + L::SK + p * (kBN * 128), &tm_k, p * 64, kvh, krow, fb);
+                    tma3(sl + L::SV + p * (kBN * 128), &tm_v, p * 64, kvh, krow, fb);
+                }
+                if (sparse) tma2(sl + L::SKI, &tm_ki, 0, krow, fb);
+            }
+            issued = t;
+            return true;
+        };
+        bool ok = true;
+        if (lane == 0) {
+            unsigned bytes = 0;
+            for (int x = 0; x < 2; x++) bytes += rowsx[x] > 0 ? (unsigned)L::QT : 0u;
+            mbar_expect_tx(bar(bars.bar_q), bytes);
+            for (int x = 0; x < 2; x++)
+                if (rowsx[x] > 0)
+#pragma unroll
+                    for (int p = 0; p < NP; p++)
+                        tma3(sbase + L::Q + x * L::QT + p * (kRowsT * 128), &tm_q, p * 64, h, (int)(b * a.Tq + t0x[x]),
+                             bar(bars.bar_q));
+        }
+        for (int t = 0; t < kSlots - 1 && t < nt && ok; t++) ok = issue(t);
+        bool exact = true;
+        if (sparse) {
+            ok = ok && pp_wait(bar(bars.qe_ready), 0u, a.wait_ns, &abort_flag, a.status);
+            exact = exact_all != 0;
+        }
+        for (int t = 0; t < nt && ok; t++) {
+            if (sparse && exact) {
+                // tile t's raw indexer keys -> fp16 KH buffer t % 2 (its previous
+                // user, tile t-2, has had its indexer products read)
+                const int slot = t % kSlots;
+                if (!pp_wait(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status) ||
+                    (t >= 2 &&
+                     !pp_wait(bar(bars.kh_free[t % 2]), (uint32_t)((t - 2) / 2) & 1u, a.wait_ns, &abort_flag, a.status))) {
+                    ok = false;
+                    break;
+                }
+                const unsigned char *raw = smem + L::RING + slot * L::SLOT + L::SKI;
+                unsigned char *dst = smem + L::KH + (t % 2) * L::KHB;
+                for (int i = lane; i < kBN * DI / 8; i += 32) {
+                    const int c8 = (i / 8) % (DI / 8), kk = (i % 8) + 8 * ((i / 8) / (DI / 8));
+                    const uint2 rv = *reinterpret_cast<const uint2 *>(raw + kk * DI + c8 * 8);
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const uint32_t w = e < 2 ? rv.x : rv.y;
+                        const int sh = (e & 1) * 16;
+                        pk[e] = pack_f16((float)(int8_t)((w >> sh) & 0xFF), (float)(int8_t)((w >> (sh + 8)) & 0xFF));
+                    }
+                    *reinterpret_cast<uint4 *>(dst + (kk / 8) * (DI / 8 * 128) + c8 * 128 + (kk % 8) * 16) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bars.kh_ready[t % 2]));
+            }
+            if (t + kSlots - 1 < nt) ok = issue(t + kSlots - 1);
+        }
+        // copies still in flight after an abort: wait for them (bounded)
+        if (!ok && lane == 0)
+            for (int t = 0; t <= issued; t++) mbar_wait_bounded(bar(bars.full[t % kSlots]), (uint32_t)(t / kSlots) & 1u, a.wait_ns);
+    } else if (warp == kMmaWarp) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            bool ok = pp_wait(bar(bars.bar_q), 0u, a.wait_ns, &abort_flag, a.status) &&
+                      pp_wait(bar(bars.qe_ready), 0u, a.wait_ns, &abort_flag, a.status);
+            const bool exact = exact_all != 0;
+            const bool use_si = sparse && exact;
+            constexpr uint32_t id_s = idesc(kBN, 1u, 0u), id_i = idesc(kBN, 0u, 0u), id_o = idesc(D, 1u, 1u);
+            for (int t = 0; t < nt && ok; t++) {
+                const int slot = t % kSlots;
+                const uint32_t sl = sbase + L::RING + slot * L::SLOT;
+                ok = pp_wait(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status) &&
+                     (!use_si || pp_wait(bar(bars.kh_ready[t % 2]), (uint32_t)(t / 2) & 1u, a.wait_ns, &abort_flag,
+                                         a.status));
+                if (!ok) break;
+                for (int x = 0; x < 2 && ok; x++) {
+                    if (t >= ntx[x]) continue;
+                    if (t > 0)
+                        ok = pp_wait(bar(bars.s_free[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag, a.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t colS = x * kColsPerTile;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; kk++)
+                        mma_ss(tmem + colS,
+                               sdesc(sbase + L::Q + x * L::QT + (kk / 4) * (kRowsT * 128) + (kk % 4) * 32, 16, 1024, 2),
+                               sdesc(sl + L::SK + (kk / 4) * (kBN * 128) + (kk % 4) * 32, 16, 1024, 2), id_s, kk > 0);
+                    if (use_si) {
+                        // SI overwrites the columns that held P of tile t-1
+                        if (t > 0)
+                            ok = pp_wait(bar(bars.pv_done[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag,
+                                         a.status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t kh = sbase + L::KH + (t % 2) * L::KHB;
+#pragma unroll
+                        for (int kk = 0; kk < DI / 16; kk++)
+                            mma_ss(tmem + colS + 64, sdesc(sbase + L::QE + x * L::QET + kk * 256, 128, DI / 8 * 128),
+                                   sdesc(kh + kk * 256, 128, DI / 8 * 128), id_i, kk > 0);
+                    }
+                    mma_commit(bar(bars.s_ready[x]));
+                }
+                if (!ok) break;
+                if (use_si) mma_commit(bar(bars.kh_free[t % 2]));
+                for (int x = 0; x < 2 && ok; x++) {
+                    if (t >= ntx[x]) continue;
+                    ok = pp_wait(bar(bars.p_ready[x]), (uint32_t)t & 1u, a.wait_ns, &abort_flag, a.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t colS = x * kColsPerTile;
+#pragma unroll
+                    for (int part = 0; part < 2; part++)
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; kk++)
+                            mma_ts(tmem + colS + 128, tmem + colS + 64 + part * 32 + kk * 8,
+                                   sdesc(sl + L::SV + kk * 2048, kBN * 128, 1024, 2), id_o,
+                                   (t > 0 || part > 0 || kk > 0));
+                    mma_commit(bar(bars.pv_done[x]));
+                }
+                if (ok) mma_commit(bar(bars.slot_free[slot]));
+            }
+            // every MMA issued has completed before the CTA frees tensor memory
+            mma_commit(bar(bars.mma_end));
+            mbar_wait_bounded(bar(bars.mma_end), 0u, a.wait_ns);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+template <int D, int DI>
+void *pp_kernel(size_t *smem) {
+    if constexpr (!PLay<D, DI>::FITS) {
+        return nullptr;
+    } else {
+        *smem = PLay<D, DI>::TOTAL;
+        return (void *)routed_pp_kernel<D, DI>;
+    }
+}
+
+template <int D>
+void *pp_kernel_d(int DI, size_t *smem) {
+    switch (DI) {
+        case 16: return pp_kernel<D, 16>(smem);
+        case 32: return pp_kernel<D, 32>(smem);
+        case 64: return pp_kernel<D, 64>(smem);
+        default: return pp_kernel<D, 128>(smem);
+    }
+}
+
+}  // namespace
+
+bool routed_pp_supported(const Shape &s) {
+    size_t smem = 0;
+    void *fn = s.D == 64 ? pp_kernel_d<64>(s.D_I, &smem) : pp_kernel_d<128>(s.D_I, &smem);
+    return fn != nullptr && s.B * s.Tq < (1ll << 31) && s.B * s.Tk < (1ll << 31);
+}
+
+esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
+                            const int8_t *kI, const int32_t *wI, const uint8_t *route, const int32_t *thr,
+                            const Shape &s, float scale, const float *g, const uint16_t *lin, float *out,
+                            int32_t *status, cudaStream_t st) {
+    PpArgs a{};
+    a.lin = lin;
+    a.qI = qI;
+    a.wI = wI;
+    a.route = route;
+    a.thr = thr;
+    a.g = g;
+    a.out = out;
+    a.status = status;
+    a.B = s.B;
+    a.Tq = s.Tq;
+    a.Tk = s.Tk;
+    a.q_offset = s.q_offset;
+    a.wait_ns = wait_limit_ns();
+    a.Hq = s.Hq;
+    a.Hkv = s.Hkv;
+    a.H_I = s.H_I;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    const long long nqt = (s.Tq + kRowsT - 1) / kRowsT;
+    const long long blocks = s.B * s.Hq * ((nqt + 1) / 2);
+    if (blocks == 0) return ESA_OK;
+    size_t smem = 0;
+    void *fn = s.D == 64 ? pp_kernel_d<64>(s.D_I, &smem) : pp_kernel_d<128>(s.D_I, &smem);
+    if (!fn) return ESA_ERR_UNSUPPORTED;
+    CUtensorMap tq, tk, tv, tki;
+    if (!map_rows_heads_d(&tq, q, s.B * s.Tq, s.Hq, s.D, kRowsT) || !map_rows_heads_d(&tk, k, s.B * s.Tk, s.Hkv, s.D, kBN) ||
+        !map_rows_heads_d(&tv, v, s.B * s.Tk, s.Hkv, s.D, kBN) || !map_rows_bytes(&tki, kI, s.B * s.Tk, s.D_I, kBN))
+        return ESA_ERR_CUDA;
+    if (!ensure_smem(fn, smem)) return ESA_ERR_CUDA;
+    void *args[] = {(void *)&a, (void *)&tq, (void *)&tk, (void *)&tv, (void *)&tki};
+    cudaError_t ce = cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(kThreads), args, smem, st);
+    return ce == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
+}
+
+}  // namespace esa
