@@ -139,6 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int nt = max(ntx[0], ntx[1]);
     const uint32_t sbase = smem_u32(smem);
+    // param-space addresses of the tensor maps (never copies of them)
+    const CUtensorMap *mq = &tm_q, *mk = &tm_k, *mv = &tm_v, *mki = &tm_ki;
     auto bar = [](unsigned long long &x) { return smem_u32(&x); };
 
     if (warp == 0) {
@@ -243,10 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t ir[32];
                     tmem_ld32(tmem + lane_base + colSI + half * 32, ir);
                     tmem_wait_ld();
+                    const int pl = (int)max(-1ll, min(64ll, (long long)Pp - j0));  // ties kept for c <= pl
 #pragma unroll
                     for (int c = 0; c < 32; c++) {
                         const float si = __uint_as_float(ir[c]);
-                        if (!(si > Tf || (si == Tf && j0 + half * 32 + c <= Pp))) keep &= ~(1ull << (half * 32 + c));
+                        if (!(si > Tf || (si == Tf && half * 32 + c <= pl))) sr[half * 32 + c] = 0xff800000u;  // -inf
                     }
                 }
             } else if (sparse) {
@@ -275,17 +278,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(bars.s_free[x]));  // S (and SI) are in registers
-            // causal: key j0+c is visible to this row iff c <= pos - j0
+            // causal: key j0+c is visible to this row iff c <= pos - j0; the
+            // maximum is taken over the raw scores (scale > 0 keeps the order)
             const int lim = (int)max(-1ll, min(64ll, pos - j0));
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (sparse && !exact) {
 #pragma unroll
-            for (int c = 0; c < 64; c++) {
-                const bool valid = c <= lim && ((keep >> c) & 1ull);
-                const float xv = valid ? __uint_as_float(sr[c]) * a.scale_log2 : -INFINITY;
-                sr[c] = __float_as_uint(xv);
-                mx4[c & 3] = fmaxf(mx4[c & 3], xv);
+                for (int c = 0; c < 64; c++) {
+                    const bool valid = c <= lim && ((keep >> c) & 1ull);
+                    const float xv = valid ? __uint_as_float(sr[c]) : -INFINITY;
+                    sr[c] = __float_as_uint(xv);
+                    mx4[c & 3] = fmaxf(mx4[c & 3], xv);
+                }
+            } else {  // the Top-K mask (if any) is already in sr
+#pragma unroll
+                for (int c = 0; c < 64; c++) {
+                    const float xv = c <= lim ? __uint_as_float(sr[c]) : -INFINITY;
+                    sr[c] = __float_as_uint(xv);
+                    mx4[c & 3] = fmaxf(mx4[c & 3], xv);
+                }
             }
-            const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
             float corr = 1.f;
             bool rescale = false;
             if (mt > m_used + kRescaleLog2 || (m_used == -INFINITY && mt > -INFINITY)) {
@@ -295,19 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = mt;
             }
             const float mu = m_used == -INFINITY ? 0.f : m_used;
-            uint32_t phi[32], plo[32];
-            float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-                const float p0 = ex2_approx(__uint_as_float(sr[c]) - mu),
-                            p1 = ex2_approx(__uint_as_float(sr[c + 1]) - mu);
-                ls0 += p0;
-                ls1 += p1;
-                const uint32_t hw = pack_bf16(p0, p1);
-                phi[c / 2] = hw;
-                plo[c / 2] = pack_bf16(p0 - bf16lo(hw), p1 - bf16hi(hw));
-            }
-            l += ls0 + ls1;
             // the previous tile's P V is done: P's columns are free, O is stable
             if (t > 0 && !pp_wait(bar(bars.pv_done[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag, a.status)) {
                 ok = false;
@@ -325,8 +325,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(tmem + lane_base + colO + c0, o_raw);
                 }
             }
-            tmem_st32(tmem + lane_base + colSI, phi);
-            tmem_st32(tmem + lane_base + colSI + 32, plo);
+            // p = 2^(s*scale - mu) (0 for masked keys), as bf16 hi + lo, written
+            // over the indexer-score columns in two 32-key halves
+            float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+                uint32_t phi[16], plo[16];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const int cc = half * 32 + c;
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[cc]), a.scale_log2, -mu)),
+                                p1 = ex2_approx(fmaf(__uint_as_float(sr[cc + 1]), a.scale_log2, -mu));
+                    ls0 += p0;
+                    ls1 += p1;
+                    const uint32_t hw = pack_bf16(p0, p1);
+                    phi[c / 2] = hw;
+                    plo[c / 2] = pack_bf16(p0 - bf16lo(hw), p1 - bf16hi(hw));
+                }
+                tmem_st16(tmem + lane_base + colSI + half * 16, phi);
+                tmem_st16(tmem + lane_base + colSI + 32 + half * 16, plo);
+            }
+            l += ls0 + ls1;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(bars.p_ready[x]));
@@ -376,10 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_expect_tx(fb, (unsigned)(2 * kBN * D * 2 + (sparse ? kBN * DI : 0)));
 #pragma unroll
                 for (int p = 0; p < NP; p++) {
-                    tma3(sl + L::SK + p * (kBN * 128), &tm_k, p * 64, kvh, krow, fb);
-                    tma3(sl + L::SV + p * (kBN * 128), &tm_v, p * 64, kvh, krow, fb);
+                    tma3(sl + L::SK + p * (kBN * 128), mk, p * 64, kvh, krow, fb);
+                    tma3(sl + L::SV + p * (kBN * 128), mv, p * 64, kvh, krow, fb);
                 }
-                if (sparse) tma2(sl + L::SKI, &tm_ki, 0, krow, fb);
+                if (sparse) tma2(sl + L::SKI, mki, 0, krow, fb);
             }
             issued = t;
             return true;
@@ -393,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (rowsx[x] > 0)
 #pragma unroll
                     for (int p = 0; p < NP; p++)
-                        tma3(sbase + L::Q + x * L::QT + p * (kRowsT * 128), &tm_q, p * 64, h, (int)(b * a.Tq + t0x[x]),
+                        tma3(sbase + L::Q + x * L::QT + p * (kRowsT * 128), mq, p * 64, h, (int)(b * a.Tq + t0x[x]),
                              bar(bars.bar_q));
         }
         for (int t = 0; t < kSlots - 1 && t < nt && ok; t++) ok = issue(t);

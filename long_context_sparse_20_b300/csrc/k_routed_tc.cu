@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long pos = r < rows ? a.q_offset + t0 + r : -1;  // this row's query position
 
     const uint32_t sbase = smem_u32(smem);
+    // param-space addresses of the tensor maps (never copies of them)
+    const CUtensorMap *mq = &tm_q, *mk = &tm_k, *mv = &tm_v, *mki = &tm_ki;
 
     // ---- tensor memory and barriers
     if (warp == 0) {
@@ -134,10 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar, (unsigned)(2 * kBN * D * 2 + (sparse ? kBN * DI : 0)));
 #pragma unroll
         for (int p = 0; p < NP; p++) {
-            tma3(sl + L::SK + p * (kBN * 128), &tm_k, p * 64, kvh, krow, bar);
-            tma3(sl + L::SV + p * (kBN * 128), &tm_v, p * 64, kvh, krow, bar);
+            tma3(sl + L::SK + p * (kBN * 128), mk, p * 64, kvh, krow, bar);
+            tma3(sl + L::SV + p * (kBN * 128), mv, p * 64, kvh, krow, bar);
         }
-        if (sparse) tma2(sl + L::SKI, &tm_ki, 0, krow, bar);
+        if (sparse) tma2(sl + L::SKI, mki, 0, krow, bar);
     };
     int issued = -1;  // last tile issued (thread 0)
     if (tid == 0) {
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Q tile (rows past the sequence are never written out)
         mbar_expect_tx(smem_u32(&bar_q), (unsigned)(kBM * D * 2));
 #pragma unroll
-        for (int p = 0; p < NP; p++) tma3(sbase + L::Q + p * (kBM * 128), &tm_q, p * 64, h, (int)row0, smem_u32(&bar_q));
+        for (int p = 0; p < NP; p++) tma3(sbase + L::Q + p * (kBM * 128), mq, p * 64, h, (int)row0, smem_u32(&bar_q));
         for (int t = 0; t < NS - 1 && t < nt; t++) {
             issue_tile(t);
             issued = t;
