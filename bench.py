@@ -182,7 +182,7 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-def prefill_section(dev, esa, E, reps: int = 2) -> dict:
+def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0) -> dict:
     """The two prefill workloads, one forward each (after one untimed warm-up),
     timed with CUDA events on the launching stream. Inputs (hundreds of MB to
     GBs) exceed the 126 MB L2. Algorithmic flops count what the method
@@ -208,6 +208,8 @@ def prefill_section(dev, esa, E, reps: int = 2) -> dict:
 
     for name in ("long_prefill", "routed_prefill"):
         cfg = dict(E.CONFIGS[name])
+        if seq:  # a shorter sequence (profiling of small cases)
+            cfg["Tq"] = cfg["Tk"] = seq
         sh = E.shape_of(cfg)
         K = cfg["top_k"]
         host = E.make_inputs(cfg)
@@ -254,6 +256,13 @@ def esa_arm(args):
     world, rank, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.prefill_only:  # profiling aid: the prefill workloads alone
+        sys.path.insert(0, ROOT)
+        import esa_inputs as E
+        import long_context_sparse_20_b300 as esa
+        if rank == 0:
+            print(json.dumps({"prefill": prefill_section(dev, esa, E, seq=args.prefill_seq)}), flush=True)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
@@ -406,7 +415,7 @@ def esa_arm(args):
 
     prefill = None
     if rank == 0 and not args.no_prefill:
-        prefill = prefill_section(dev, esa, E)
+        prefill = prefill_section(dev, esa, E, seq=args.prefill_seq)
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -455,6 +464,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sets", type=int, default=NSETS, help="rotating input sets (small profiling cases use 1)")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workloads' timings")
+    ap.add_argument("--prefill-only", action="store_true", help="time the prefill workloads only (profiling)")
+    ap.add_argument("--prefill-seq", type=int, default=0, help="override the prefill sequence length (profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)
