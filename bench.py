@@ -11,8 +11,9 @@ on the data path): scaling "weak", value = tokens of all ranks / max time.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl esa|reference] [--no-prefill]
 
 The JSON line's "prefill" object adds one forward of each prefill workload
-(long_prefill: Top-K selection + gathered attention; routed_prefill: the
-routed launch) with tokens/s and algorithmic TFLOP/s against the bf16 peak.
+(long_prefill and chunked_prefill: Top-K selection + gathered attention;
+routed_prefill: the routed launch) with tokens/s and algorithmic TFLOP/s
+against the bf16 peak.
   python bench.py --workload long_prefill|routed_prefill|million_decode|tiny_prefill
 
 Prints one JSON line.
@@ -206,10 +207,12 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0) -> dict:
             best = ms if best is None else min(best, ms)
         return best
 
-    for name in ("long_prefill", "routed_prefill"):
+    for name in ("long_prefill", "chunked_prefill", "routed_prefill"):
         cfg = dict(E.CONFIGS[name])
         if seq:  # a shorter sequence (profiling of small cases)
-            cfg["Tq"] = cfg["Tk"] = seq
+            cfg["Tk"] = cfg["Tk"] * seq // cfg["Tq"]
+            cfg["q_offset"] = cfg["Tk"] - seq
+            cfg["Tq"] = seq
         sh = E.shape_of(cfg)
         K = cfg["top_k"]
         host = E.make_inputs(cfg)
@@ -218,10 +221,12 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0) -> dict:
         B, S, Hq, D = sh["B"], sh["Tq"], sh["Hq"], sh["D"]
         scale = 1.0 / math.sqrt(D)
         out = torch.empty(B, S, Hq, D, dtype=torch.float32, device=dev)
-        n = np.arange(1, S + 1, dtype=np.float64)
+        n = np.arange(sh["q_offset"] + 1, sh["q_offset"] + S + 1, dtype=np.float64)  # prefix lengths
         sel_pairs = float(np.minimum(n, K).sum())  # per (sequence, head)
         causal_pairs = float(n.sum())
-        entry = {"workload": f"{name}: B={B} S={S} Hq={Hq} Hkv={sh['Hkv']} D={D} indexer {sh['H_I']}x{sh['D_I']} top_k={K}"}
+        entry = {"workload": f"{name}: B={B} S={S} (queries at {sh['q_offset']}..{sh['q_offset'] + S - 1} of a "
+                             f"{sh['Tk']}-key cache) Hq={Hq} Hkv={sh['Hkv']} D={D} indexer {sh['H_I']}x{sh['D_I']} "
+                             f"top_k={K}"}
         if cfg.get("routed"):
             ws = esa.workspace_for(esa.OP_ROUTED_ATTN, shape, K, dev)
             ms = timed(lambda: esa.esa_routed_attn(d["q"], d["k"], d["v"], d["qI"], d["kI"], d["wI"], d["route"], shape,

@@ -168,6 +168,10 @@ CONFIGS = {
                          top_k=2048, weights="1to4", routed=False, needles=0, seed=2003),
     "routed_prefill": dict(B=2, Tq=65536, Tk=65536, q_offset=0, Hq=32, Hkv=32, D=128, H_I=1, D_I=64,
                            top_k=2048, weights="ones", routed=True, needles=0, seed=2004),
+    # chunked prefill against an existing cache: the last 16384 tokens of a
+    # 131072-token context, with the long_prefill head and indexer layout
+    "chunked_prefill": dict(B=1, Tq=16384, Tk=131072, q_offset=114688, Hq=16, Hkv=2, D=128, H_I=4, D_I=64,
+                            top_k=2048, weights="1to4", routed=False, needles=0, seed=2006),
     "million_decode": dict(B=1, Tq=1, Tk=1048576, q_offset=1048575, Hq=64, Hkv=1, D=128, H_I=1, D_I=64,
                            top_k=2048, weights="ones", routed=False, needles=64, seed=2005),
 }

@@ -282,6 +282,22 @@ def test_long_prefill_full():
     assert_close(out[rows], ref)
 
 
+def test_chunked_prefill_full():
+    """A 16384-token chunk at the end of a 131072-token cache (queries at
+    positions 114688..131071): sampled rows plus the chunk's edge rows."""
+    cfg, sh, inp = _full("chunked_prefill")
+    K = cfg["top_k"]
+    d = to_dev(inp)
+    gi, gc = gpu_topk(d, sh, K)
+    rows = sample_rows(sh["B"], sh["Tq"], K, 384, seed=3)
+    oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
+    assert_idx_equal(gi, gc, oi, oc, rows=rows)
+    assert (gc == K).all()
+    st, out, _ = gpu_attn(d, sh, K, gi, gc)
+    assert st == 0
+    assert_close(out[rows], ref)
+
+
 def test_routed_prefill_full():
     cfg, sh, inp = _full("routed_prefill")
     K = cfg["top_k"]
