@@ -182,7 +182,7 @@ esa_status esa_topk_select(const int8_t *qI, const int8_t *kI, const int32_t *wI
     SplitPlan sp = plan_split_select(x, top_k);
     if ((e = check_ws(ws, ws_bytes, sp.ok ? sp.ws_bytes : ws_row_select(x, top_k)))) return e;
     if (sp.ok) return launch_split_select(qI, kI, wI, x, top_k, idx, cnt, ws, sp, (cudaStream_t)stream);
-    return launch_row_select(qI, kI, wI, x, top_k, idx, cnt, nullptr, ws, (cudaStream_t)stream);
+    return launch_row_select(qI, kI, wI, x, top_k, idx, cnt, nullptr, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,

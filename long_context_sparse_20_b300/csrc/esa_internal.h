@@ -59,12 +59,20 @@ SplitPlan plan_split_select(const Shape &s, int K);
 esa_status launch_split_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
                                int32_t *idx, int32_t *cnt, void *ws, const SplitPlan &plan, cudaStream_t st);
 
-// Row-tiled selection: 32 query rows per block, several passes over the
-// keys. Writes idx/cnt when idx != nullptr and the threshold form (T, P)
-// of every row to thr (int32 pairs [rows][2]) when thr != nullptr.
+// Row-tiled selection of many query rows. Writes idx/cnt when idx !=
+// nullptr and the threshold form (T, P) of every row to thr (int32 pairs
+// [rows][2]) when thr != nullptr. Workspace: [status word][tensor-core
+// scratch]; ws_row_select() is the size that enables the tensor-core kernel
+// (fp16 indexer keys and per-tile flags), and any smaller workspace of at
+// least kStatusBytes runs the dp4a kernel alone.
 size_t ws_row_select(const Shape &s, int K);
 esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
-                             int32_t *idx, int32_t *cnt, int32_t *thr, void *ws, cudaStream_t st);
+                             int32_t *idx, int32_t *cnt, int32_t *thr, void *ws, size_t ws_bytes, cudaStream_t st);
+// The dp4a kernel (32 query rows per block); with only_flagged != nullptr
+// it does only the 128-row query tiles whose flag is 1.
+esa_status launch_rows_dp4a(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
+                            int32_t *idx, int32_t *cnt, int32_t *thr, const int32_t *only_flagged, int32_t *status,
+                            cudaStream_t st);
 
 // ---- attention over gathered keys ---------------------------------------
 struct AttnPlan {

@@ -61,7 +61,9 @@ extern "C" ESA_API esa_status esa_topk_select_noalloc(const int8_t *qI, const in
     if (x.B * x.Tq == 0) return ESA_OK;
 
     SplitPlan sp = plan_split_select(x, top_k);
-    const size_t need = sp.ok ? sp.ws_bytes : ws_row_select(x, top_k);
+    // the row-tiled path needs only the status word; it takes the tensor-core
+    // kernel when that kernel's scratch fits too
+    const size_t need = sp.ok ? sp.ws_bytes : kStatusBytes;
     if (need > (size_t)ESA_NOALLOC_SCRATCH_BYTES) return ESA_ERR_UNSUPPORTED;  // beyond the fixed scratch size
 
     esa_status err = ESA_OK;
@@ -76,7 +78,8 @@ extern "C" ESA_API esa_status esa_topk_select_noalloc(const int8_t *qI, const in
     if (sp.ok && cudaMemsetAsync(static_cast<char *>(scratch) + sp.ctrl_off, 0, sp.ctrl_bytes, st) != cudaSuccess)
         return ESA_ERR_CUDA;
     esa_status e = sp.ok ? launch_split_select(qI, kI, wI, x, top_k, idx, cnt, scratch, sp, st)
-                         : launch_row_select(qI, kI, wI, x, top_k, idx, cnt, nullptr, scratch, st);
+                         : launch_row_select(qI, kI, wI, x, top_k, idx, cnt, nullptr, scratch,
+                                             (size_t)ESA_NOALLOC_SCRATCH_BYTES, st);
     if (e != ESA_OK) return e;
     if (dev_status && cudaMemcpyAsync(dev_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
         return ESA_ERR_CUDA;

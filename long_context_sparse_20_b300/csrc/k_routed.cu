@@ -21,15 +21,17 @@
 
 namespace esa {
 
-size_t ws_routed(const Shape &s, int) { return kStatusBytes + align256((size_t)s.B * s.Tq * 2 * 4); }
+// workspace: [row selection: status word, tensor-core scratch][thr]
+size_t ws_routed(const Shape &s, int K) { return align256(ws_row_select(s, K)) + align256((size_t)s.B * s.Tq * 2 * 4); }
 
 esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
                               const int8_t *kI, const int32_t *wI, const uint8_t *route, const Shape &s, int K,
                               float scale, const float *g, const uint16_t *lin, float *out, void *ws,
                               cudaStream_t st) {
     char *base = static_cast<char *>(ws);
-    int32_t *thr = reinterpret_cast<int32_t *>(base + kStatusBytes);
-    esa_status e = launch_row_select(qI, kI, wI, s, K, nullptr, nullptr, thr, ws, st);
+    const size_t sel_bytes = align256(ws_row_select(s, K));
+    int32_t *thr = reinterpret_cast<int32_t *>(base + sel_bytes);
+    esa_status e = launch_row_select(qI, kI, wI, s, K, nullptr, nullptr, thr, ws, sel_bytes, st);
     if (e != ESA_OK) return e;
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     if (routed_pp_supported(s))

@@ -82,28 +82,6 @@ struct PpBars {
 };
 
 // Bounded wait that also gives up when another role has aborted the CTA.
-__device__ __forceinline__ bool pp_wait(uint32_t bar, uint32_t parity, long long limit_ns, volatile int *abort,
-                                        int32_t *status) {
-    for (int i = 0; i < 64; i++)
-        if (mbar_try_wait(bar, parity)) return true;
-    unsigned long long t0, t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort) return false;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-        if ((long long)(t - t0) > limit_ns) {
-            *abort = 1;
-            set_status(status, ESA_ERR_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 template <int D, int DI>
 __global__ void __launch_bounds__(kThreads, 1)
     routed_pp_kernel(const __grid_constant__ PpArgs a, const __grid_constant__ CUtensorMap tm_q,
@@ -196,14 +174,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool fits = true;
             const int8_t *qrow = a.qI + (row0 + (r < rows ? r : 0)) * (long long)a.H_I * DI;
             for (int c0 = 0; c0 < DI; c0 += 8) {
-                int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // 64-bit: any int32 weight
                 for (int hh = 0; hh < a.H_I; hh++) {
-                    const int wv = a.wI[hh];
+                    const long long wv = a.wI[hh];
                     const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + hh * DI + c0);
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         const int8_t qv = (int8_t)(((e < 4 ? raw.x : raw.y) >> (8 * (e & 3))) & 0xFF);
-                        acc[e] += wv * (int)qv;
+                        acc[e] += wv * qv;
                     }
                 }
                 uint32_t pk[4];
@@ -229,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int t = 0; t < ntt && ok; t++) {
-            if (!pp_wait(bar(bars.s_ready[x]), (uint32_t)t & 1u, a.wait_ns, &abort_flag, a.status)) {
+            if (!wait_or_abort(bar(bars.s_ready[x]), (uint32_t)t & 1u, a.wait_ns, &abort_flag, a.status)) {
                 ok = false;
                 break;
             }
@@ -255,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (sparse) {
                 // exact integer mask scores with dp4a from the raw keys of the slot
                 const int slot = t % kSlots;
-                if (!pp_wait(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status)) {
+                if (!wait_or_abort(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
@@ -309,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mu = m_used == -INFINITY ? 0.f : m_used;
             // the previous tile's P V is done: P's columns are free, O is stable
-            if (t > 0 && !pp_wait(bar(bars.pv_done[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag, a.status)) {
+            if (t > 0 && !wait_or_abort(bar(bars.pv_done[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag, a.status)) {
                 ok = false;
                 break;
             }
@@ -352,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- epilogue: O / l, gate mix for sparse heads
         if (ok && ntt > 0 &&
-            pp_wait(bar(bars.pv_done[x]), (uint32_t)(ntt - 1) & 1u, a.wait_ns, &abort_flag, a.status)) {
+            wait_or_abort(bar(bars.pv_done[x]), (uint32_t)(ntt - 1) & 1u, a.wait_ns, &abort_flag, a.status)) {
             tc_fence_after();
             const bool gated = sparse && a.g != nullptr && a.lin != nullptr;
             const float gh = gated ? a.g[h] : 1.f, gl = 1.f - gh;
@@ -386,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue = [&](int t) {  // lane 0 issues; the whole warp waits for the slot
             const int slot = t % kSlots;
             if (t >= kSlots &&
-                !pp_wait(bar(bars.slot_free[slot]), (uint32_t)(t / kSlots - 1) & 1u, a.wait_ns, &abort_flag, a.status))
+                !wait_or_abort(bar(bars.slot_free[slot]), (uint32_t)(t / kSlots - 1) & 1u, a.wait_ns, &abort_flag, a.status))
                 return false;
             if (lane == 0) {
                 const uint32_t sl = sbase + L::RING + slot * L::SLOT;
@@ -418,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kSlots - 1 && t < nt && ok; t++) ok = issue(t);
         bool exact = true;
         if (sparse) {
-            ok = ok && pp_wait(bar(bars.qe_ready), 0u, a.wait_ns, &abort_flag, a.status);
+            ok = ok && wait_or_abort(bar(bars.qe_ready), 0u, a.wait_ns, &abort_flag, a.status);
             exact = exact_all != 0;
         }
         for (int t = 0; t < nt && ok; t++) {
@@ -426,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile t's raw indexer keys -> fp16 KH buffer t % 2 (its previous
                 // user, tile t-2, has had its indexer products read)
                 const int slot = t % kSlots;
-                if (!pp_wait(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status) ||
+                if (!wait_or_abort(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status) ||
                     (t >= 2 &&
-                     !pp_wait(bar(bars.kh_free[t % 2]), (uint32_t)((t - 2) / 2) & 1u, a.wait_ns, &abort_flag, a.status))) {
+                     !wait_or_abort(bar(bars.kh_free[t % 2]), (uint32_t)((t - 2) / 2) & 1u, a.wait_ns, &abort_flag, a.status))) {
                     ok = false;
                     break;
                 }
@@ -459,22 +437,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ================================================= MMA issuer
         if (lane == 0) {
-            bool ok = pp_wait(bar(bars.bar_q), 0u, a.wait_ns, &abort_flag, a.status) &&
-                      pp_wait(bar(bars.qe_ready), 0u, a.wait_ns, &abort_flag, a.status);
+            bool ok = wait_or_abort(bar(bars.bar_q), 0u, a.wait_ns, &abort_flag, a.status) &&
+                      wait_or_abort(bar(bars.qe_ready), 0u, a.wait_ns, &abort_flag, a.status);
             const bool exact = exact_all != 0;
             const bool use_si = sparse && exact;
             constexpr uint32_t id_s = idesc(kBN, 1u, 0u), id_i = idesc(kBN, 0u, 0u), id_o = idesc(D, 1u, 1u);
             for (int t = 0; t < nt && ok; t++) {
                 const int slot = t % kSlots;
                 const uint32_t sl = sbase + L::RING + slot * L::SLOT;
-                ok = pp_wait(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status) &&
-                     (!use_si || pp_wait(bar(bars.kh_ready[t % 2]), (uint32_t)(t / 2) & 1u, a.wait_ns, &abort_flag,
+                ok = wait_or_abort(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status) &&
+                     (!use_si || wait_or_abort(bar(bars.kh_ready[t % 2]), (uint32_t)(t / 2) & 1u, a.wait_ns, &abort_flag,
                                          a.status));
                 if (!ok) break;
                 for (int x = 0; x < 2 && ok; x++) {
                     if (t >= ntx[x]) continue;
                     if (t > 0)
-                        ok = pp_wait(bar(bars.s_free[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag, a.status);
+                        ok = wait_or_abort(bar(bars.s_free[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag, a.status);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t colS = x * kColsPerTile;
@@ -486,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (use_si) {
                         // SI overwrites the columns that held P of tile t-1
                         if (t > 0)
-                            ok = pp_wait(bar(bars.pv_done[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag,
+                            ok = wait_or_abort(bar(bars.pv_done[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag,
                                          a.status);
                         if (!ok) break;
                         tc_fence_after();
@@ -502,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (use_si) mma_commit(bar(bars.kh_free[t % 2]));
                 for (int x = 0; x < 2 && ok; x++) {
                     if (t >= ntx[x]) continue;
-                    ok = pp_wait(bar(bars.p_ready[x]), (uint32_t)t & 1u, a.wait_ns, &abort_flag, a.status);
+                    ok = wait_or_abort(bar(bars.p_ready[x]), (uint32_t)t & 1u, a.wait_ns, &abort_flag, a.status);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t colS = x * kColsPerTile;

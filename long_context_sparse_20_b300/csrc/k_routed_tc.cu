@@ -173,14 +173,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool fits = true;
         const int8_t *qrow = a.qI + (row0 + (r < rows ? r : 0)) * (long long)a.H_I * DI;
         for (int c0 = hf * (DI / 2); c0 < (hf + 1) * (DI / 2); c0 += 8) {
-            int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // 64-bit: any int32 weight
             for (int hh = 0; hh < a.H_I; hh++) {
                 const int wv = a.wI[hh];
                 const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + hh * DI + c0);
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
                     const int8_t qv = (int8_t)(((e < 4 ? raw.x : raw.y) >> (8 * (e & 3))) & 0xFF);
-                    acc[e] += wv * (int)qv;
+                    acc[e] += (long long)wv * qv;
                 }
             }
             uint32_t pk[4];

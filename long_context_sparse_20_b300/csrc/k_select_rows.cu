@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
                                                               int32_t *__restrict__ cnt, int32_t *__restrict__ thr,
                                                               long long B, long long Tq, long long Tk,
                                                               long long q_offset, int H_I, int K,
+                                                              const int32_t *__restrict__ only_flagged,
                                                               int32_t *__restrict__ status) {
     constexpr int W = DI / 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -107,6 +108,9 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
     const long long row0 = b * Tq + t0;
     const int nrows = (int)min((long long)kRows, Tq - t0);
     const long long nmax = q_offset + t0 + nrows;  // keys to visit
+    // second launch after the tensor-core selection: only the 128-row query
+    // tiles that it left (flag 1) are done here
+    if (only_flagged && only_flagged[b * ((Tq + 127) / 128) + t0 / 128] == 0) return;
 
     // ---- prologue: row state and indexer queries
     if (tid < kRows) {
@@ -138,9 +142,9 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
         bool fits = true;
         for (int i = tid; i < kRows * DI; i += kThreads) {
             int r = i / DI, c = i % DI;
-            int acc = 0;
+            long long acc = 0;  // 64-bit: any int32 weight
             for (int h = 0; h < H_I; h++)
-                acc += wsm[h] * (int)reinterpret_cast<const int8_t *>(qs + (r * H_I + h) * W)[c];
+                acc += (long long)wsm[h] * reinterpret_cast<const int8_t *>(qs + (r * H_I + h) * W)[c];
             fits = fits && acc >= -128 && acc <= 127;
         }
         if (!__syncthreads_and(fits)) {
@@ -156,10 +160,11 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
             int v[4];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                int acc = 0;
+                unsigned acc = 0;  // exact modulo 2^32; the value fits int8 here
                 for (int h = 0; h < H_I; h++)
-                    acc += wsm[h] * (int)reinterpret_cast<const int8_t *>(qs + (lane * H_I + h) * W)[4 * c + e];
-                v[e] = acc;
+                    acc += (unsigned)wsm[h] *
+                           (unsigned)(int)reinterpret_cast<const int8_t *>(qs + (lane * H_I + h) * W)[4 * c + e];
+                v[e] = (int)acc;
             }
             qr[c] = (uint32_t)(v[0] & 255) | ((uint32_t)(v[1] & 255) << 8) | ((uint32_t)(v[2] & 255) << 16) |
                     ((uint32_t)(v[3] & 255) << 24);
@@ -434,10 +439,9 @@ void *row_kernel(int DI) {
 
 }  // namespace
 
-size_t ws_row_select(const Shape &, int) { return kStatusBytes; }
-
-esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
-                             int32_t *idx, int32_t *cnt, int32_t *thr, void *ws, cudaStream_t st) {
+esa_status launch_rows_dp4a(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
+                            int32_t *idx, int32_t *cnt, int32_t *thr, const int32_t *only_flagged, int32_t *status,
+                            cudaStream_t st) {
     long long tiles = s.B * ((s.Tq + kRows - 1) / kRows);
     if (tiles == 0) return ESA_OK;
     size_t smem = row_smem(s.D_I, s.H_I);
@@ -445,9 +449,9 @@ esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *
     if (!ensure_smem(fn, smem)) return ESA_ERR_CUDA;
     long long B = s.B, Tq = s.Tq, Tk = s.Tk, qo = s.q_offset;
     int H_I = s.H_I;
-    int32_t *status = reinterpret_cast<int32_t *>(ws);
-    void *args[] = {(void *)&qI, (void *)&kI, (void *)&wI, (void *)&idx, (void *)&cnt, (void *)&thr,
-                    (void *)&B,  (void *)&Tq, (void *)&Tk, (void *)&qo, (void *)&H_I, (void *)&K, (void *)&status};
+    void *args[] = {(void *)&qI, (void *)&kI, (void *)&wI, (void *)&idx,          (void *)&cnt,
+                    (void *)&thr, (void *)&B, (void *)&Tq, (void *)&Tk,          (void *)&qo,
+                    (void *)&H_I, (void *)&K, (void *)&only_flagged, (void *)&status};
     cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)tiles), dim3(kThreads), args, smem, st);
     return e == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }

@@ -1,0 +1,652 @@
+// Top-K selection for many query rows on the tensor cores (prefill, chunked
+// prefill, and the thresholds that the routed kernel rebuilds its masks from).
+//
+// Method: per query row, the Indexer score against every causal-prefix key
+// (no RoPE) and the K best positions, ties to the lower position
+// ("超大规模MoE架构中稀疏注意力机制的演进与实践", sections 二.1-二.2), computed
+// blockwise over the queries without materialising the score matrix
+// ("大模型推理架构演进：从稀疏注意力到隐式专家路由", section 2.3).
+//
+// Design. The scores of 128 query rows against a tile of 128 keys are one
+// M=128 N=128 K=D_I matrix product. The indexer heads collapse into
+// q_eff = sum_h w_h qI_h (integer algebra, since every indexer head scores
+// the same key vector); q_eff and kI are held as fp16, which represents them
+// exactly while |q_eff| <= 2048, and the fp32 accumulator of tcgen05.mma then
+// holds every partial sum exactly while sum_c |q_eff[c]| * 128 < 2^24: the
+// scores leave tensor memory as exact integers. A query tile that fails that
+// test is flagged and left to the dp4a kernel (k_select_rows.cu), which a
+// second launch runs on the flagged tiles only.
+//
+// Roles in one CTA (320 threads; one sequence, 128 query rows):
+//   warps 0-7  read scores from tensor memory, two warps per 32-row quarter
+//              (warp w takes key columns 64*(w/4) .. +63 of every tile)
+//   warp 8     bulk-copies fp16 key tiles (converted once per call by
+//              kh_convert_kernel into the tensor cores' core-matrix layout,
+//              so that a tile is one contiguous 16-KiB block) into a ring
+//   warp 9     one thread issues the MMAs into four 128-column buffers
+// Passes over the keys; the scores are recomputed by every pass:
+//   1      a log histogram per row (4 classes per octave); keys below a
+//          running lower bound on the row's K-th largest score are not
+//          counted, so most keys cost one comparison;
+//   2 ..   256 bins over the bucket that holds the K-th score, until the
+//          threshold T is exact (one pass while that bucket spans at most
+//          256 integers);
+//   final  selected = s > T, or s == T among the first K - #{s > T} ties in
+//          position order, written in ascending order; also the threshold
+//          form (T, P), P the position of the last tie taken.
+#include <stdlib.h>
+#include <string.h>
+
+#include "esa_device.cuh"
+#include "esa_internal.h"
+#include "tc_util.cuh"
+
+namespace esa {
+
+namespace {
+
+constexpr int kRowsT = 128;   // query rows per CTA (TMEM lanes)
+constexpr int kKT = 128;      // keys per tile (MMA N)
+constexpr int kTBufs = 4;     // TMEM score buffers of kKT columns
+constexpr int kCons = 256;    // score-reading threads
+constexpr int kProdWarp = 8, kMmaWarp = 9;
+constexpr int kThreadsTc = 320;
+constexpr int kNB = 256;      // histogram bins per row
+constexpr int kHS = kNB + 1;  // row stride of the histograms (words)
+constexpr int kLog0 = 100;    // level-1 bin of the score 0
+constexpr int kRing = 65536;  // bytes of key-tile ring
+constexpr int kMaxStages = 8;
+constexpr int kMaxLevels = 6;
+
+enum { kModeStart = -1, kModeHist = 0, kModeFinal = 1, kModeDone = 2 };
+
+template <int DI>
+struct TcLay {
+    static constexpr int KT_BYTES = kKT * DI * 2;
+    static constexpr int STAGES = kRing / KT_BYTES < kMaxStages ? kRing / KT_BYTES : kMaxStages;
+    static constexpr int RING = 0;
+    static constexpr int QE = RING + STAGES * KT_BYTES;
+    static constexpr int HIST = QE + kRowsT * DI * 2;
+    static constexpr int TOTAL = HIST + kRowsT * kHS * 4;
+};
+
+struct TcShared {
+    unsigned long long full[kMaxStages], sfree[kMaxStages], tfull[kTBufs], tfree[kTBufs], mma_end;
+    int n[kRowsT];      // prefix length of the row (0 past the last row)
+    int lo[kRowsT], hi[kRowsT], sh[kRowsT];  // level >= 2: bucket [lo, hi], bin width 2^sh
+    int T[kRowsT], P[kRowsT];
+    unsigned need[kRowsT];   // ties at T to take
+    unsigned above[kRowsT];  // keys above the current bucket
+    int open[kRowsT];        // threshold not exact yet
+    int top[kRowsT];         // highest level-1 bin counted so far
+    uint32_t tmem_base;
+    int mode, level, exact_all;
+};
+
+struct TcSelArgs {
+    const int8_t *qI;
+    const uint16_t *kh;
+    const int32_t *wI;
+    int32_t *idx, *cnt, *thr, *flags, *status;
+    long long B, Tq, Tk, Tkp, q_offset, wait_ns;
+    int H_I, K;
+};
+
+// ---- level-1 (log) classes of an exact integer score held in fp32:
+// class m = 0 for 0, else 4 * floor(log2|s|) + (two bits below the leading
+// one) + 1; bin = kLog0 +- m. |s| < 2^24 keeps m <= 97.
+__device__ __forceinline__ int log_bin(float f) {
+    const unsigned u = __float_as_uint(f);
+    const int m = max(0, (int)((u & 0x7fffffffu) >> 21) - 507);
+    return (int)u < 0 ? kLog0 - m : kLog0 + m;
+}
+// integers of magnitude class m: [lo, hi] (empty when lo > hi)
+__device__ __forceinline__ void mag_range(int m, int &lo, int &hi) {
+    if (m == 0) {
+        lo = hi = 0;
+        return;
+    }
+    const int E = (m - 1) >> 2, m2 = (m - 1) & 3;
+    lo = (int)((((long long)(4 + m2) << E) + 3) >> 2);
+    hi = (int)((((long long)(5 + m2) << E) + 3) >> 2) - 1;
+}
+__device__ __forceinline__ void bin_range1(int bin, int &lo, int &hi) {
+    int l, h;
+    mag_range(bin >= kLog0 ? bin - kLog0 : kLog0 - bin, l, h);
+    if (bin >= kLog0) {
+        lo = l;
+        hi = h;
+    } else {
+        lo = -h;
+        hi = -l;
+    }
+}
+// lowest score of level-1 bin `bin` or above: every key in a bin >= bin
+// scores at least this
+__device__ __forceinline__ float bin_floor1(int bin) {
+    int lo, hi;
+    bin_range1(bin, lo, hi);
+    return (float)lo;  // also for an empty bin: every higher bin starts above it
+}
+// walk a row's level-1 histogram down from its top bin: the floor of the
+// bin where the count reaches `need` bounds the row's need-th largest score
+// from below (the counts only ever grow, so a racing read is conservative)
+__device__ __forceinline__ float rescan1(const volatile unsigned *h, int top, unsigned need) {
+    unsigned cum = 0;
+    for (int bn = top; bn >= 0; bn--) {
+        cum += h[bn];
+        if (cum >= need) return bin_floor1(bn);
+    }
+    return -INFINITY;
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_constant__ TcSelArgs a) {
+    using L = TcLay<DI>;
+    constexpr int S = L::STAGES;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ TcShared st;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int K = a.K;
+    const long long ntile = (a.Tq + kRowsT - 1) / kRowsT;
+    const long long b = (long long)blockIdx.x % a.B;
+    const long long tile = ntile - 1 - (long long)blockIdx.x / a.B;  // longest prefixes first
+    const long long t0 = tile * kRowsT;
+    const long long row0 = b * a.Tq + t0;
+    const int nrows = (int)min((long long)kRowsT, a.Tq - t0);
+    const long long nmax = a.q_offset + t0 + nrows;
+    const int ntk = (int)((nmax + kKT - 1) / kKT);  // key tiles per pass
+    const uint32_t sbase = smem_u32(smem);
+    unsigned *hist = reinterpret_cast<unsigned *>(smem + L::HIST);
+    auto bar = [](unsigned long long &x) { return smem_u32(&x); };
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&st.tmem_base)),
+                     "r"(kTBufs * kKT));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == kProdWarp * 32) {
+        for (int i = 0; i < S; i++) {
+            mbar_init(bar(st.full[i]), 1);
+            mbar_init(bar(st.sfree[i]), 1);
+        }
+        for (int i = 0; i < kTBufs; i++) {
+            mbar_init(bar(st.tfull[i]), 1);
+            mbar_init(bar(st.tfree[i]), kCons);
+        }
+        mbar_init(bar(st.mma_end), 1);
+        mbar_fence_init();
+        abort_flag = 0;
+        st.exact_all = 1;
+        st.mode = kModeStart;
+        st.level = 0;
+    }
+    __syncthreads();
+    if (warp < 8) {
+        // collapsed indexer query of row r, fp16 in the core-matrix layout
+        // (8 rows x 16 B per core matrix; K-adjacent core matrices 128 B
+        // apart, 8-row groups DI*16 B apart); thread half hf writes columns
+        // hf*DI/2 .. +DI/2 and checks the whole row
+        const int r = tid & (kRowsT - 1), hf = tid >> 7;
+        const int8_t *qrow = a.qI + (row0 + (r < nrows ? r : 0)) * (long long)a.H_I * DI;
+        long long absum = 0;
+        bool fits = true;
+        for (int c0 = 0; c0 < DI; c0 += 8) {
+            long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int hh = 0; hh < a.H_I; hh++) {
+                const long long wv = a.wI[hh];
+                const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + hh * DI + c0);
+#pragma unroll
+                for (int e = 0; e < 8; e++)
+                    acc[e] += wv * (int8_t)(((e < 4 ? raw.x : raw.y) >> (8 * (e & 3))) & 0xFF);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                fits = fits && acc[e] >= -2048 && acc[e] <= 2048;
+                absum += acc[e] < 0 ? -acc[e] : acc[e];
+            }
+            if ((c0 < DI / 2) == (hf == 0)) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; e++) pk[e] = pack_f16((float)acc[2 * e], (float)acc[2 * e + 1]);
+                if (r >= nrows || !fits) pk[0] = pk[1] = pk[2] = pk[3] = 0u;
+                *reinterpret_cast<uint4 *>(smem + L::QE + (r >> 3) * (DI * 16) + (c0 >> 3) * 128 + (r & 7) * 16) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+        fits = fits && absum * 128 < (1ll << 24);
+        if (r < nrows && !fits) atomicAnd(&st.exact_all, 0);
+        if (hf == 0) {
+            const int n = r < nrows ? (int)(a.q_offset + t0 + r + 1) : 0;
+            st.n[r] = n;
+            st.open[r] = n > K;  // a prefix of at most K keys is taken whole
+            st.T[r] = INT32_MIN;
+            st.P[r] = n - 1;
+            st.need[r] = (unsigned)K;
+            st.above[r] = 0u;
+            st.top[r] = -1;
+            st.lo[r] = st.hi[r] = st.sh[r] = 0;
+        }
+        fence_async_smem();  // q_eff is read by the tensor cores
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = st.tmem_base;
+    const bool exact = st.exact_all != 0;
+    if (tid == 0) a.flags[b * ntile + tile] = exact ? 0 : 1;
+
+    if (exact) {
+        int g0 = 0;  // key tiles issued by earlier passes (barrier phases run on across passes)
+        // per-thread state of the consumer threads
+        const int q4 = warp & 3, hf = (warp >> 2) & 1, r = 32 * q4 + lane;
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        for (;;) {
+            if (tid == 0) {
+                int any = 0;
+                for (int i = 0; i < kRowsT; i++) any |= st.open[i];
+                const int m = st.mode;
+                int next = m == kModeFinal ? kModeDone : (any ? kModeHist : kModeFinal);
+                if (abort_flag) next = kModeDone;
+                if (next == kModeHist) {
+                    st.level = m == kModeHist ? st.level + 1 : 1;
+                    if (st.level > kMaxLevels) {  // consistency check; never reached
+                        set_status(a.status, ESA_ERR_INTERNAL);
+                        next = kModeDone;
+                    }
+                }
+                st.mode = next;
+            }
+            __syncthreads();
+            const int mode = st.mode, level = st.level;
+            if (mode == kModeDone) break;
+
+            if (warp == kProdWarp) {
+                // ---------------------------------------------- key tiles
+                if (lane == 0) {
+                    const uint64_t pol = l2_evict_last_policy();
+                    const char *src = reinterpret_cast<const char *>(a.kh) + (size_t)(b * a.Tkp) * DI * 2;
+                    for (int t = 0; t < ntk; t++) {
+                        const int g = g0 + t, slot = g % S;
+                        if (g >= S && !wait_or_abort(bar(st.sfree[slot]), (uint32_t)(g / S - 1) & 1u, a.wait_ns,
+                                                     &abort_flag, a.status))
+                            break;
+                        mbar_expect_tx(bar(st.full[slot]), (unsigned)L::KT_BYTES);
+                        bulk_g2s(sbase + L::RING + slot * L::KT_BYTES, src + (size_t)t * L::KT_BYTES,
+                                 (unsigned)L::KT_BYTES, bar(st.full[slot]), pol);
+                    }
+                }
+                __syncwarp();
+            } else if (warp == kMmaWarp) {
+                // ---------------------------------------------- MMA issue
+                if (lane == 0) {
+                    constexpr uint32_t id = idesc(kKT, 0u, 0u);  // fp16 x fp16 -> fp32, N = 128
+                    for (int t = 0; t < ntk; t++) {
+                        const int g = g0 + t, slot = g % S, buf = g % kTBufs;
+                        if (!wait_or_abort(bar(st.full[slot]), (uint32_t)(g / S) & 1u, a.wait_ns, &abort_flag,
+                                           a.status))
+                            break;
+                        if (g >= kTBufs && !wait_or_abort(bar(st.tfree[buf]), (uint32_t)(g / kTBufs - 1) & 1u,
+                                                          a.wait_ns, &abort_flag, a.status))
+                            break;
+                        tc_fence_after();
+                        const uint32_t ks = sbase + L::RING + slot * L::KT_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < DI / 16; kk++)
+                            mma_ss(tmem + buf * kKT, sdesc(sbase + L::QE + kk * 256, 128, DI * 16),
+                                   sdesc(ks + kk * 256, 128, DI * 16), id, kk > 0);
+                        mma_commit(bar(st.sfree[slot]));
+                        mma_commit(bar(st.tfull[buf]));
+                    }
+                }
+                __syncwarp();
+            } else {
+                // ---------------------------------------------- scores
+                const int n_r = st.n[r];
+                const bool open_r = st.open[r] != 0;
+                unsigned *h = hist + r * kHS;
+                if (mode == kModeHist) {
+                    for (int i = tid; i < kRowsT * kHS; i += kCons) hist[i] = 0u;
+                    __syncwarp();
+                    asm volatile("bar.sync 5, 256;" ::: "memory");  // histograms cleared
+                }
+                const int lo = st.lo[r], hi = st.hi[r], sh = st.sh[r];
+                const float flo = (float)lo, fhi = (float)hi;
+                const float Tf = (float)st.T[r];
+                const unsigned need = st.need[r];
+                float fb = -INFINITY;  // level 1: running lower bound on the K-th largest score
+                int mytop = -1, since = 0;
+                unsigned tie_run = 0, out_run = 0;  // final pass: ties seen, positions written
+                int32_t *orow = (a.idx && r < nrows) ? a.idx + (row0 + r) * (long long)K : nullptr;
+                uint2 *xch = reinterpret_cast<uint2 *>(hist);  // final pass: [2][kRowsT][2] (g, e)
+                for (int t = 0; t < ntk; t++) {
+                    const int g = g0 + t, buf = g % kTBufs;
+                    wait_or_abort(bar(st.tfull[buf]), (uint32_t)(g / kTBufs) & 1u, a.wait_ns, &abort_flag, a.status);
+                    __syncwarp();  // tcgen05.ld is warp-collective
+                    tc_fence_after();
+                    uint32_t x[64];
+                    tmem_ld32(tmem + lane_base + buf * kKT + hf * 64, x);
+                    tmem_ld32(tmem + lane_base + buf * kKT + hf * 64 + 32, x + 32);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(bar(st.tfree[buf]));  // the scores are in registers
+                    const int j0 = t * kKT + hf * 64;
+                    const int lim = max(0, min(64, n_r - j0));  // columns c < lim are in the prefix
+                    if (mode == kModeHist) {
+                        if (!open_r || lim == 0) continue;
+                        if (level == 1) {
+                            int added = 0;
+                            if (lim == 64) {
+#pragma unroll
+                                for (int c = 0; c < 64; c++) {
+                                    const float f = __uint_as_float(x[c]);
+                                    if (f >= fb) {
+                                        const int bn = log_bin(f);
+                                        atomicAdd(h + bn, 1u);
+                                        mytop = max(mytop, bn);
+                                        added++;
+                                    }
+                                }
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < 64; c++) {
+                                    const float f = __uint_as_float(x[c]);
+                                    if (c < lim && f >= fb) {
+                                        const int bn = log_bin(f);
+                                        atomicAdd(h + bn, 1u);
+                                        mytop = max(mytop, bn);
+                                        added++;
+                                    }
+                                }
+                            }
+                            if (added) {
+                                atomicMax(&st.top[r], mytop);
+                                since += added;
+                                if (since >= 64) {
+                                    since = 0;
+                                    fb = rescan1(h, *(volatile int *)&st.top[r], (unsigned)K);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 64; c++) {
+                                const float f = __uint_as_float(x[c]);
+                                if (c < lim && f >= flo && f <= fhi)
+                                    atomicAdd(h + ((__float2int_rz(f) - lo) >> sh), 1u);
+                            }
+                        }
+                    } else {
+                        // final pass: ordered write of the selected positions
+                        uint64_t gt = 0, eq = 0;
+                        if (lim > 0) {
+#pragma unroll
+                            for (int c = 0; c < 64; c++) {
+                                const float f = __uint_as_float(x[c]);
+                                const bool in = c < lim;
+                                gt |= (uint64_t)(in && f > Tf) << c;
+                                eq |= (uint64_t)(in && f == Tf) << c;
+                            }
+                        }
+                        const int slot = ((t & 1) * kRowsT + r) * 2;
+                        xch[slot + hf] = make_uint2((unsigned)__popcll(gt), (unsigned)__popcll(eq));
+                        __syncwarp();
+                        pair_sync(q4);
+                        const uint2 c0 = xch[slot], c1 = xch[slot + 1];
+                        const unsigned take0 = tie_run >= need ? 0u : min(c0.y, need - tie_run);
+                        const unsigned tie1 = tie_run + c0.y;
+                        const unsigned take1 = tie1 >= need ? 0u : min(c1.y, need - tie1);
+                        const unsigned tb = hf ? tie1 : tie_run, take = hf ? take1 : take0;
+                        unsigned ob = out_run + (hf ? c0.x + take0 : 0u);
+                        uint64_t sel = gt, ee = eq;
+                        int last = -1;
+                        for (unsigned i = 0; i < take; i++) {
+                            const uint64_t lb = ee & (0ull - ee);
+                            sel |= lb;
+                            ee ^= lb;
+                            last = __ffsll((long long)lb) - 1;
+                        }
+                        if (take > 0 && tb + take == need) st.P[r] = j0 + last;
+                        if (orow) {
+                            while (sel) {
+                                const int bit = __ffsll((long long)sel) - 1;
+                                sel &= sel - 1;
+                                if (ob < (unsigned)K) orow[ob] = j0 + bit;
+                                else set_status(a.status, ESA_ERR_INTERNAL);
+                                ob++;
+                            }
+                        }
+                        out_run += c0.x + take0 + c1.x + take1;
+                        tie_run += c0.y + c1.y;
+                    }
+                }
+                if (mode == kModeFinal && r < nrows && hf == 0 && !abort_flag &&
+                    out_run != (unsigned)min(K, n_r))  // consistency check; never reached
+                    set_status(a.status, ESA_ERR_INTERNAL);
+            }
+            g0 += ntk;
+            __syncthreads();  // pass drained: every MMA read, every histogram count in
+            if (mode == kModeHist && warp < 8 && !abort_flag) {
+                // ---------------------------------------------- next bucket
+                // warp w resolves rows w, w+8, ...: lane l sums bins 8l..8l+7
+                for (int rr = warp; rr < kRowsT; rr += 8) {
+                    if (!st.open[rr]) continue;
+                    const unsigned need = (unsigned)K - st.above[rr];
+                    const unsigned *hh = hist + rr * kHS;
+                    const int b0 = lane * 8;
+                    unsigned seg = 0;
+#pragma unroll
+                    for (int v = 0; v < 8; v++) seg += hh[b0 + v];
+                    unsigned xs = seg;  // keys in the bins of lanes >= lane
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const unsigned y = __shfl_down_sync(0xffffffffu, xs, d);
+                        if (lane + d < 32) xs += y;
+                    }
+                    const unsigned excl = xs - seg;
+                    int found = -1;
+                    unsigned above_in = 0;
+                    if (excl < need && need <= xs) {
+                        unsigned acc = excl;
+                        for (int v = b0 + 7; v >= b0; v--) {
+                            if (acc + hh[v] >= need) {
+                                found = v;
+                                above_in = acc;
+                                break;
+                            }
+                            acc += hh[v];
+                        }
+                    }
+                    const unsigned fl = __ballot_sync(0xffffffffu, found >= 0);
+                    if (fl == 0u) {  // consistency check; never reached
+                        if (lane == 0) {
+                            set_status(a.status, ESA_ERR_INTERNAL);
+                            st.open[rr] = 0;
+                        }
+                        continue;
+                    }
+                    const int src = __ffs(fl) - 1;
+                    found = __shfl_sync(0xffffffffu, found, src);
+                    above_in = __shfl_sync(0xffffffffu, above_in, src);
+                    if (lane == 0) {
+                        int nlo, nhi;
+                        if (level == 1) {
+                            bin_range1(found, nlo, nhi);
+                        } else {
+                            nlo = st.lo[rr] + (found << st.sh[rr]);
+                            nhi = (int)min((long long)st.hi[rr], (long long)nlo + (1ll << st.sh[rr]) - 1);
+                        }
+                        st.above[rr] += above_in;
+                        if (nlo == nhi) {
+                            st.open[rr] = 0;
+                            st.T[rr] = nlo;
+                            st.need[rr] = (unsigned)K - st.above[rr];
+                        } else {
+                            int s2 = 0;
+                            while ((((long long)nhi - nlo) >> s2) >= kNB) s2++;
+                            st.lo[rr] = nlo;
+                            st.hi[rr] = nhi;
+                            st.sh[rr] = s2;
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+
+        // ---- counts, padding and threshold form (one warp per row)
+        if (warp < 8) {
+            for (int rr = warp; rr < nrows; rr += 8) {
+                const int n = st.n[rr];
+                const int c = min(K, n);
+                if (a.idx) {
+                    int32_t *orr = a.idx + (row0 + rr) * (long long)K;
+                    for (int i = c + lane; i < K; i += 32) orr[i] = -1;
+                    if (lane == 0) a.cnt[row0 + rr] = c;
+                }
+                if (a.thr && lane == 0) {
+                    a.thr[2 * (row0 + rr)] = st.T[rr];
+                    a.thr[2 * (row0 + rr) + 1] = st.P[rr];
+                }
+            }
+        }
+        if (warp == kMmaWarp && lane == 0) {
+            // every MMA issued has completed before tensor memory is freed
+            mma_commit(bar(st.mma_end));
+            mbar_wait_bounded(bar(st.mma_end), 0u, a.wait_ns);
+        }
+        if (warp == kProdWarp && lane == 0 && abort_flag) {
+            // after an abort: let bulk copies still in flight land
+            for (int g = max(0, g0 - S); g < g0; g++)
+                mbar_wait_bounded(bar(st.full[g % S]), (uint32_t)(g / S) & 1u, a.wait_ns);
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTBufs * kKT));
+    }
+}
+
+// int8 indexer keys [B, Tk, DI] -> fp16 [B, Tkp, DI] in the core-matrix
+// layout: the 16-byte unit U holds keys 8*grp + (U & 7), columns 8*c8 .. +7,
+// with U = (grp * DI/8 + c8) * 8 + (U & 7); keys Tk .. Tkp-1 are zero.
+__global__ void __launch_bounds__(256) kh_convert_kernel(const int8_t *__restrict__ kI, uint4 *__restrict__ kh,
+                                                         long long B, long long Tk, long long Tkp, int DI) {
+    const int G = DI / 8;
+    const long long units = B * Tkp * G;
+    for (long long U = blockIdx.x * (long long)blockDim.x + threadIdx.x; U < units;
+         U += (long long)gridDim.x * blockDim.x) {
+        const long long rest = U >> 3;
+        const int c8 = (int)(rest % G);
+        const long long row = (rest / G) * 8 + (U & 7);
+        const long long bb = row / Tkp, j = row - bb * Tkp;
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (j < Tk) {
+            const uint2 raw = *reinterpret_cast<const uint2 *>(kI + (bb * Tk + j) * DI + c8 * 8);
+            auto cv = [](uint32_t w, int e) { return (float)(int8_t)((w >> (8 * e)) & 0xFFu); };
+            o.x = pack_f16(cv(raw.x, 0), cv(raw.x, 1));
+            o.y = pack_f16(cv(raw.x, 2), cv(raw.x, 3));
+            o.z = pack_f16(cv(raw.y, 0), cv(raw.y, 1));
+            o.w = pack_f16(cv(raw.y, 2), cv(raw.y, 3));
+        }
+        kh[U] = o;
+    }
+}
+
+template <int DI>
+constexpr size_t tc_smem() {
+    return (size_t)TcLay<DI>::TOTAL;
+}
+
+void *tc_kernel(int DI, size_t *smem) {
+    switch (DI) {
+        case 16: *smem = tc_smem<16>(); return (void *)rows_tc_kernel<16>;
+        case 32: *smem = tc_smem<32>(); return (void *)rows_tc_kernel<32>;
+        case 64: *smem = tc_smem<64>(); return (void *)rows_tc_kernel<64>;
+        default: return nullptr;  // D_I = 128: its buffers do not fit; the dp4a kernel runs it
+    }
+}
+
+struct TcPlan {
+    bool ok;
+    long long Tkp, ntile;
+    size_t kh_off, flag_off, bytes;
+};
+
+// ESA_ROW_SELECT=dp4a keeps the row-tiled selection on the dp4a kernel
+// (a switch for comparing the two kernels; both give identical results)
+bool tc_disabled() {
+    const char *e = getenv("ESA_ROW_SELECT");
+    return e && strcmp(e, "dp4a") == 0;
+}
+
+TcPlan plan_tc(const Shape &s, int) {
+    TcPlan p{};
+    size_t smem = 0;
+    if (!tc_kernel(s.D_I, &smem) || tc_disabled()) return p;
+    if (smem + sizeof(TcShared) + 1024 > device_info().smem_optin) return p;
+    p.Tkp = (s.Tk + kKT - 1) / kKT * kKT;
+    p.ntile = (s.Tq + kRowsT - 1) / kRowsT;
+    p.kh_off = kStatusBytes;
+    p.flag_off = p.kh_off + align256((size_t)s.B * p.Tkp * s.D_I * 2);
+    p.bytes = p.flag_off + align256((size_t)s.B * p.ntile * 4);
+    p.ok = true;
+    return p;
+}
+
+}  // namespace
+
+size_t ws_row_select(const Shape &s, int K) {
+    TcPlan p = plan_tc(s, K);
+    return p.ok ? p.bytes : kStatusBytes;
+}
+
+esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
+                             int32_t *idx, int32_t *cnt, int32_t *thr, void *ws, size_t ws_bytes, cudaStream_t st) {
+    int32_t *status = reinterpret_cast<int32_t *>(ws);
+    if (s.B * s.Tq == 0) return ESA_OK;
+    TcPlan p = plan_tc(s, K);
+    if (!p.ok || ws_bytes < p.bytes)
+        return launch_rows_dp4a(qI, kI, wI, s, K, idx, cnt, thr, nullptr, status, st);
+    char *base = static_cast<char *>(ws);
+    uint16_t *kh = reinterpret_cast<uint16_t *>(base + p.kh_off);
+    int32_t *flags = reinterpret_cast<int32_t *>(base + p.flag_off);
+    {
+        const long long units = s.B * p.Tkp * (s.D_I / 8);
+        const long long want = (units + 255) / 256, cap = (long long)device_info().sms * 16;
+        kh_convert_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, st>>>(kI, reinterpret_cast<uint4 *>(kh), s.B,
+                                                                            s.Tk, p.Tkp, s.D_I);
+        if (cudaGetLastError() != cudaSuccess) return ESA_ERR_CUDA;
+    }
+    size_t smem = 0;
+    void *fn = tc_kernel(s.D_I, &smem);
+    if (!ensure_smem(fn, smem)) return ESA_ERR_CUDA;
+    TcSelArgs a{};
+    a.qI = qI;
+    a.kh = kh;
+    a.wI = wI;
+    a.idx = idx;
+    a.cnt = cnt;
+    a.thr = thr;
+    a.flags = flags;
+    a.status = status;
+    a.B = s.B;
+    a.Tq = s.Tq;
+    a.Tk = s.Tk;
+    a.Tkp = p.Tkp;
+    a.q_offset = s.q_offset;
+    a.wait_ns = wait_limit_ns();
+    a.H_I = s.H_I;
+    a.K = K;
+    void *args[] = {(void *)&a};
+    if (cudaLaunchKernel(fn, dim3((unsigned)(s.B * p.ntile)), dim3(kThreadsTc), args, smem, st) != cudaSuccess)
+        return ESA_ERR_CUDA;
+    // query tiles whose collapsed indexer query is not exact in fp16
+    return launch_rows_dp4a(qI, kI, wI, s, K, idx, cnt, thr, flags, status, st);
+}
+
+}  // namespace esa

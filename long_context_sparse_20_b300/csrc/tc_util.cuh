@@ -114,6 +114,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// Wait for phase `parity` of an mbarrier for at most limit_ns. Gives up at
+// once when another thread of the CTA has set *abort; on its own timeout it
+// sets *abort and the status word (ESA_ERR_TIMEOUT). Never traps.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, long long limit_ns, volatile int *abort,
+                                              int32_t *status) {
+    for (int i = 0; i < 64; i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if ((long long)(t - t0) > limit_ns) {
+            *abort = 1;
+            set_status(status, ESA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // barrier of the two warps (64 threads) that share one quarter of the rows
 __device__ __forceinline__ void pair_sync(int quarter) {
     asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");

@@ -96,6 +96,60 @@ def test_topk_repeated_calls_reuse_workspace():
             assert_idx_equal(gi, gc, oi, oc)
 
 
+# ------------------------------------------------------------------ prefill selection: tensor-core and dp4a kernels
+def test_topk_prefill_two_sequences_offset():
+    """Two sequences, a ragged 128-row tail and queries deep in the cache:
+    the fp16 key copy of each sequence starts at its own padded offset."""
+    cfg, sh, inp = _case(seed=404, B=2, Tq=300, Tk=5000, q_offset=4700, top_k=1024, D_I=64, H_I=2,
+                         weights="1to4")
+    gi, gc = gpu_topk(to_dev(inp), sh, 1024)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, 1024)
+    assert_idx_equal(gi, gc, oi, oc)
+
+
+def test_topk_prefill_deep_levels():
+    """Full-range int8 vectors and weight 8: the collapsed query still fits
+    fp16 exactly, and scores up to ~2^21 take three histogram levels."""
+    cfg, sh, inp = _case(seed=405, B=1, Tq=260, Tk=2600, q_offset=2340, top_k=300, D_I=64, H_I=1)
+    g = torch.Generator().manual_seed(11)
+    inp["qI"] = torch.randint(-128, 128, inp["qI"].shape, dtype=torch.int8, generator=g)
+    inp["kI"] = torch.randint(-128, 128, inp["kI"].shape, dtype=torch.int8, generator=g)
+    inp["wI"] = torch.tensor([8], dtype=torch.int32)
+    gi, gc = gpu_topk(to_dev(inp), sh, 300)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, 300)
+    assert_idx_equal(gi, gc, oi, oc)
+
+
+def test_topk_prefill_mixed_tiles():
+    """One 128-row query tile whose collapsed indexer query leaves the exact
+    fp16 range goes to the dp4a kernel; the other tiles stay on the tensor
+    cores. Both halves of the result must match."""
+    cfg, sh, inp = _case(seed=406, B=2, Tq=400, Tk=400, top_k=96, D_I=32, H_I=2, weights="1to4")
+    inp["qI"] = inp["qI"].clone()
+    inp["wI"] = torch.tensor([20, 1], dtype=torch.int32)  # |q_eff| = |20 q_0 + q_1| <= 168 ...
+    inp["qI"][1, 130, 0, 5] = 127  # ... except row 130 of sequence 1: 2540 + q_1 > 2048
+    gi, gc = gpu_topk(to_dev(inp), sh, 96)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, 96)
+    assert_idx_equal(gi, gc, oi, oc)
+
+
+def test_topk_prefill_kernels_agree(monkeypatch):
+    """The tensor-core selection and the dp4a kernel (ESA_ROW_SELECT=dp4a)
+    give identical index sets on a chunk of 1000 queries over 6000 keys."""
+    cfg, sh, inp = _case(seed=407, B=1, Tq=1000, Tk=6000, q_offset=5000, top_k=2048, D_I=64, H_I=4,
+                         weights="1to4")
+    d = to_dev(inp)
+    ti, tc = gpu_topk(d, sh, 2048)
+    monkeypatch.setenv("ESA_ROW_SELECT", "dp4a")
+    di, dc = gpu_topk(d, sh, 2048)
+    monkeypatch.delenv("ESA_ROW_SELECT")
+    assert np.array_equal(tc, dc)
+    assert np.array_equal(ti, di)
+    rows = sample_rows(sh["B"], sh["Tq"], 2048, 64, seed=9)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, 2048, rows=rows)
+    assert_idx_equal(ti, tc, oi, oc, rows=rows)
+
+
 # ------------------------------------------------------------------ attention
 ATTN_CASES = [
     dict(B=1, Tq=150, Tk=150, Hq=4, Hkv=1, D=64, top_k=40),
