@@ -183,7 +183,8 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0) -> dict:
+def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
+                    names=("long_prefill", "chunked_prefill", "routed_prefill")) -> dict:
     """The two prefill workloads, one forward each (after one untimed warm-up),
     timed with CUDA events on the launching stream. Inputs (hundreds of MB to
     GBs) exceed the 126 MB L2. Algorithmic flops count what the method
@@ -207,7 +208,7 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0) -> dict:
             best = ms if best is None else min(best, ms)
         return best
 
-    for name in ("long_prefill", "chunked_prefill", "routed_prefill"):
+    for name in names:
         cfg = dict(E.CONFIGS[name])
         if seq:  # a shorter sequence (profiling of small cases)
             cfg["Tk"] = cfg["Tk"] * seq // cfg["Tq"]
@@ -266,7 +267,8 @@ def esa_arm(args):
         import esa_inputs as E
         import long_context_sparse_20_b300 as esa
         if rank == 0:
-            print(json.dumps({"prefill": prefill_section(dev, esa, E, seq=args.prefill_seq)}), flush=True)
+            print(json.dumps({"prefill": prefill_section(dev, esa, E, seq=args.prefill_seq,
+                                                         names=args.prefill_names.split(","))}), flush=True)
         return
     if world > 1:
         import torch.distributed as dist
@@ -471,6 +473,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workloads' timings")
     ap.add_argument("--prefill-only", action="store_true", help="time the prefill workloads only (profiling)")
     ap.add_argument("--prefill-seq", type=int, default=0, help="override the prefill sequence length (profiling)")
+    ap.add_argument("--prefill-names", default="long_prefill,chunked_prefill,routed_prefill",
+                    help="comma-separated prefill workloads for --prefill-only (profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)

@@ -78,7 +78,7 @@ struct TcShared {
     unsigned need[kRowsT];   // ties at T to take
     unsigned above[kRowsT];  // keys above the current bucket
     int open[kRowsT];        // threshold not exact yet
-    int top[kRowsT];         // highest level-1 bin counted so far
+    int w16[kRowsT];         // level >= 2: 512 16-bit bins
     uint32_t tmem_base;
     int mode, level, exact_all;
 };
@@ -140,6 +140,12 @@ __device__ __forceinline__ float rescan1(const volatile unsigned *h, int top, un
     return -INFINITY;
 }
 
+// bins of a level >= 2 histogram: 256 x 32-bit counters, or 512 x 16-bit
+// counters (two per word) when the bucket holds fewer than 2^16 keys
+__device__ __forceinline__ unsigned bin_count(const unsigned *h, int b, bool w16) {
+    return w16 ? (h[b >> 1] >> ((b & 1) * 16)) & 0xFFFFu : h[b];
+}
+
 template <int DI>
 __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_constant__ TcSelArgs a) {
     using L = TcLay<DI>;
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
         }
         for (int i = 0; i < kTBufs; i++) {
             mbar_init(bar(st.tfull[i]), 1);
-            mbar_init(bar(st.tfree[i]), kCons);
+            mbar_init(bar(st.tfree[i]), kCons / 32);
         }
         mbar_init(bar(st.mma_end), 1);
         mbar_fence_init();
@@ -226,7 +232,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
             st.P[r] = n - 1;
             st.need[r] = (unsigned)K;
             st.above[r] = 0u;
-            st.top[r] = -1;
+            st.w16[r] = 0;
             st.lo[r] = st.hi[r] = st.sh[r] = 0;
         }
         fence_async_smem();  // q_eff is read by the tensor cores
@@ -316,8 +322,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 const float flo = (float)lo, fhi = (float)hi;
                 const float Tf = (float)st.T[r];
                 const unsigned need = st.need[r];
-                float fb = -INFINITY;  // level 1: running lower bound on the K-th largest score
-                int mytop = -1, since = 0;
+                const bool w16 = st.w16[r] != 0;
+                // level 1: running lower bound on the K-th largest score; it starts
+                // below every score (|s| < 2^24) and above the -inf that marks
+                // keys past the prefix, which therefore never count
+                float fb = -33554432.f;
+                int since_scan = 0;
                 unsigned tie_run = 0, out_run = 0;  // final pass: ties seen, positions written
                 int32_t *orow = (a.idx && r < nrows) ? a.idx + (row0 + r) * (long long)K : nullptr;
                 uint2 *xch = reinterpret_cast<uint2 *>(hist);  // final pass: [2][kRowsT][2] (g, e)
@@ -331,63 +341,53 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                     tmem_ld32(tmem + lane_base + buf * kKT + hf * 64 + 32, x + 32);
                     tmem_wait_ld();
                     tc_fence_before();
-                    mbar_arrive(bar(st.tfree[buf]));  // the scores are in registers
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(st.tfree[buf]));  // the warp's scores are in registers
                     const int j0 = t * kKT + hf * 64;
                     const int lim = max(0, min(64, n_r - j0));  // columns c < lim are in the prefix
                     if (mode == kModeHist) {
                         if (!open_r || lim == 0) continue;
+                        if (lim < 64) {  // keys past the row's prefix never count
+#pragma unroll
+                            for (int c = 0; c < 64; c++)
+                                if (c >= lim) x[c] = 0xff800000u;  // -inf
+                        }
                         if (level == 1) {
-                            int added = 0;
-                            if (lim == 64) {
 #pragma unroll
-                                for (int c = 0; c < 64; c++) {
-                                    const float f = __uint_as_float(x[c]);
-                                    if (f >= fb) {
-                                        const int bn = log_bin(f);
-                                        atomicAdd(h + bn, 1u);
-                                        mytop = max(mytop, bn);
-                                        added++;
-                                    }
-                                }
-                            } else {
-#pragma unroll
-                                for (int c = 0; c < 64; c++) {
-                                    const float f = __uint_as_float(x[c]);
-                                    if (c < lim && f >= fb) {
-                                        const int bn = log_bin(f);
-                                        atomicAdd(h + bn, 1u);
-                                        mytop = max(mytop, bn);
-                                        added++;
-                                    }
-                                }
+                            for (int c = 0; c < 64; c++) {
+                                const float f = __uint_as_float(x[c]);
+                                if (f >= fb) atomicAdd(h + log_bin(f), 1u);
                             }
-                            if (added) {
-                                atomicMax(&st.top[r], mytop);
-                                since += added;
-                                if (since >= 64) {
-                                    since = 0;
-                                    fb = rescan1(h, *(volatile int *)&st.top[r], (unsigned)K);
-                                }
+                            // raise the bound: every tile until it is positive, then every 8th
+                            if (fb <= 0.f || ++since_scan == 8) {
+                                since_scan = 0;
+                                fb = fmaxf(fb, rescan1(h, 2 * kLog0, (unsigned)K));
                             }
                         } else {
 #pragma unroll
                             for (int c = 0; c < 64; c++) {
                                 const float f = __uint_as_float(x[c]);
-                                if (c < lim && f >= flo && f <= fhi)
-                                    atomicAdd(h + ((__float2int_rz(f) - lo) >> sh), 1u);
+                                if (f >= flo && f <= fhi) {
+                                    const int bn = (__float2int_rz(f) - lo) >> sh;
+                                    if (w16) atomicAdd(h + (bn >> 1), 1u << ((bn & 1) * 16));
+                                    else atomicAdd(h + bn, 1u);
+                                }
                             }
                         }
                     } else {
                         // final pass: ordered write of the selected positions
                         uint64_t gt = 0, eq = 0;
                         if (lim > 0) {
+                            unsigned g2[2] = {0u, 0u}, e2[2] = {0u, 0u};
 #pragma unroll
                             for (int c = 0; c < 64; c++) {
                                 const float f = __uint_as_float(x[c]);
-                                const bool in = c < lim;
-                                gt |= (uint64_t)(in && f > Tf) << c;
-                                eq |= (uint64_t)(in && f == Tf) << c;
+                                g2[c >> 5] |= (unsigned)(f > Tf) << (c & 31);
+                                e2[c >> 5] |= (unsigned)(f == Tf) << (c & 31);
                             }
+                            const uint64_t in = lim == 64 ? ~0ull : (1ull << lim) - 1;  // keys in the prefix
+                            gt = (g2[0] | (uint64_t)g2[1] << 32) & in;
+                            eq = (e2[0] | (uint64_t)e2[1] << 32) & in;
                         }
                         const int slot = ((t & 1) * kRowsT + r) * 2;
                         xch[slot + hf] = make_uint2((unsigned)__popcll(gt), (unsigned)__popcll(eq));
@@ -429,15 +429,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
             __syncthreads();  // pass drained: every MMA read, every histogram count in
             if (mode == kModeHist && warp < 8 && !abort_flag) {
                 // ---------------------------------------------- next bucket
-                // warp w resolves rows w, w+8, ...: lane l sums bins 8l..8l+7
+                // warp w resolves rows w, w+8, ...: lane l sums bins bpl*l .. +bpl-1
                 for (int rr = warp; rr < kRowsT; rr += 8) {
                     if (!st.open[rr]) continue;
                     const unsigned need = (unsigned)K - st.above[rr];
                     const unsigned *hh = hist + rr * kHS;
-                    const int b0 = lane * 8;
+                    const bool wide = level > 1 && st.w16[rr] != 0;  // 512 16-bit bins
+                    const int bpl = wide ? 16 : 8;                    // bins per lane
+                    const int b0 = lane * bpl;
                     unsigned seg = 0;
-#pragma unroll
-                    for (int v = 0; v < 8; v++) seg += hh[b0 + v];
+                    for (int v = 0; v < bpl; v++) seg += bin_count(hh, b0 + v, wide);
                     unsigned xs = seg;  // keys in the bins of lanes >= lane
 #pragma unroll
                     for (int d = 1; d < 32; d <<= 1) {
@@ -446,16 +447,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                     }
                     const unsigned excl = xs - seg;
                     int found = -1;
-                    unsigned above_in = 0;
+                    unsigned above_in = 0, in_bin = 0;
                     if (excl < need && need <= xs) {
                         unsigned acc = excl;
-                        for (int v = b0 + 7; v >= b0; v--) {
-                            if (acc + hh[v] >= need) {
+                        for (int v = b0 + bpl - 1; v >= b0; v--) {
+                            const unsigned hv = bin_count(hh, v, wide);
+                            if (acc + hv >= need) {
                                 found = v;
                                 above_in = acc;
+                                in_bin = hv;
                                 break;
                             }
-                            acc += hh[v];
+                            acc += hv;
                         }
                     }
                     const unsigned fl = __ballot_sync(0xffffffffu, found >= 0);
@@ -469,6 +472,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                     const int src = __ffs(fl) - 1;
                     found = __shfl_sync(0xffffffffu, found, src);
                     above_in = __shfl_sync(0xffffffffu, above_in, src);
+                    in_bin = __shfl_sync(0xffffffffu, in_bin, src);
                     if (lane == 0) {
                         int nlo, nhi;
                         if (level == 1) {
@@ -483,11 +487,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                             st.T[rr] = nlo;
                             st.need[rr] = (unsigned)K - st.above[rr];
                         } else {
+                            // the next level counts only this bucket's keys: 16-bit
+                            // counters suffice below 2^16 of them
+                            const bool w = in_bin < 65536u;
+                            const int nb = w ? 2 * kNB : kNB;
                             int s2 = 0;
-                            while ((((long long)nhi - nlo) >> s2) >= kNB) s2++;
+                            while ((((long long)nhi - nlo) >> s2) >= nb) s2++;
                             st.lo[rr] = nlo;
                             st.hi[rr] = nhi;
                             st.sh[rr] = s2;
+                            st.w16[rr] = w ? 1 : 0;
                         }
                     }
                 }

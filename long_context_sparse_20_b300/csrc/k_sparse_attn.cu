@@ -41,7 +41,7 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kKeys = 64;  // keys per stage
 constexpr int kMaxSplits = 16;
-constexpr int kIdxWin = 1024;  // staged indices (a multiple of kKeys)
+constexpr int kIdxWin = 512;  // staged indices (a multiple of kKeys; small enough for 3 blocks per SM)
 
 template <int D>
 struct Cfg {
@@ -417,7 +417,9 @@ bool prepare_attn(void *fn, size_t smem) {
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lk(mu);
     if (done.count({dev, fn})) return ensure_smem(fn, smem);
+    // the largest shared-memory carveout: several blocks of ~77 KB per SM
     if (!ensure_smem(fn, smem) ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
         cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
         cudaGetLastError();
         return false;

@@ -30,6 +30,7 @@ TOPK_CASES = [
     dict(B=1, Tq=300, Tk=300, top_k=64, D_I=32),
     dict(B=2, Tq=200, Tk=200, top_k=100, D_I=64, H_I=4, weights="1to4"),
     dict(B=1, Tq=130, Tk=130, top_k=1, D_I=16),
+    dict(B=1, Tq=300, Tk=300, top_k=200, D_I=64, H_I=2, weights="1to4"),  # thresholds near 0 and below
     dict(B=1, Tq=257, Tk=257, top_k=256, D_I=128, H_I=2, weights="1to4"),
     # chunked prefill: queries at positions q_offset..q_offset+Tq-1
     dict(B=2, Tq=70, Tk=600, q_offset=530, top_k=128, D_I=64),
