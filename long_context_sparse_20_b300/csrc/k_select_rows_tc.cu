@@ -17,13 +17,13 @@
 // test is flagged and left to the dp4a kernel (k_select_rows.cu), which a
 // second launch runs on the flagged tiles only.
 //
-// Roles in one CTA (320 threads; one sequence, 128 query rows):
-//   warps 0-7  read scores from tensor memory, two warps per 32-row quarter
-//              (warp w takes key columns 64*(w/4) .. +63 of every tile)
-//   warp 8     bulk-copies fp16 key tiles (converted once per call by
+// Roles in one CTA (576 threads; one sequence, 128 query rows):
+//   warps 0-15 read scores from tensor memory, four warps per 32-row quarter
+//              (warp w takes key columns 32*(w/4) .. +31 of every tile)
+//   warp 16    bulk-copies fp16 key tiles (converted once per call by
 //              kh_convert_kernel into the tensor cores' core-matrix layout,
 //              so that a tile is one contiguous 16-KiB block) into a ring
-//   warp 9     one thread issues the MMAs into four 128-column buffers
+//   warp 17    one thread issues the MMAs into four 128-column buffers
 // Passes over the keys; the scores are recomputed by every pass:
 //   1      a log histogram per row (4 classes per octave); keys below a
 //          running lower bound on the row's K-th largest score are not
@@ -48,9 +48,12 @@ namespace {
 constexpr int kRowsT = 128;   // query rows per CTA (TMEM lanes)
 constexpr int kKT = 128;      // keys per tile (MMA N)
 constexpr int kTBufs = 4;     // TMEM score buffers of kKT columns
-constexpr int kCons = 256;    // score-reading threads
-constexpr int kProdWarp = 8, kMmaWarp = 9;
-constexpr int kThreadsTc = 320;
+constexpr int kParts = 4;               // threads per query row (each reads 32 key columns)
+constexpr int kCols = kKT / kParts;     // key columns per thread and tile
+constexpr int kCons = kRowsT * kParts;  // score-reading threads (16 warps)
+constexpr int kConsWarps = kCons / 32;
+constexpr int kProdWarp = kConsWarps, kMmaWarp = kConsWarps + 1;
+constexpr int kThreadsTc = kCons + 64;
 constexpr int kNB = 256;      // histogram bins per row
 constexpr int kHS = kNB + 1;  // row stride of the histograms (words)
 constexpr int kLog0 = 100;    // level-1 bin of the score 0
@@ -190,12 +193,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
         st.level = 0;
     }
     __syncthreads();
-    if (warp < 8) {
+    if (warp < kConsWarps) {
         // collapsed indexer query of row r, fp16 in the core-matrix layout
         // (8 rows x 16 B per core matrix; K-adjacent core matrices 128 B
-        // apart, 8-row groups DI*16 B apart); thread half hf writes columns
-        // hf*DI/2 .. +DI/2 and checks the whole row
-        const int r = tid & (kRowsT - 1), hf = tid >> 7;
+        // apart, 8-row groups DI*16 B apart); thread part pt writes the
+        // 8-column groups g with g % 4 == pt and checks the whole row
+        const int r = tid & (kRowsT - 1), pt = tid >> 7;
         const int8_t *qrow = a.qI + (row0 + (r < nrows ? r : 0)) * (long long)a.H_I * DI;
         long long absum = 0;
         bool fits = true;
@@ -213,7 +216,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 fits = fits && acc[e] >= -2048 && acc[e] <= 2048;
                 absum += acc[e] < 0 ? -acc[e] : acc[e];
             }
-            if ((c0 < DI / 2) == (hf == 0)) {
+            if (((c0 >> 3) & (kParts - 1)) == pt) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int e = 0; e < 4; e++) pk[e] = pack_f16((float)acc[2 * e], (float)acc[2 * e + 1]);
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
         }
         fits = fits && absum * 128 < (1ll << 24);
         if (r < nrows && !fits) atomicAnd(&st.exact_all, 0);
-        if (hf == 0) {
+        if (pt == 0) {
             const int n = r < nrows ? (int)(a.q_offset + t0 + r + 1) : 0;
             st.n[r] = n;
             st.open[r] = n > K;  // a prefix of at most K keys is taken whole
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
     if (exact) {
         int g0 = 0;  // key tiles issued by earlier passes (barrier phases run on across passes)
         // per-thread state of the consumer threads
-        const int q4 = warp & 3, hf = (warp >> 2) & 1, r = 32 * q4 + lane;
+        const int q4 = warp & 3, pt = (warp >> 2) & (kParts - 1), r = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         for (;;) {
             if (tid == 0) {
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 if (mode == kModeHist) {
                     for (int i = tid; i < kRowsT * kHS; i += kCons) hist[i] = 0u;
                     __syncwarp();
-                    asm volatile("bar.sync 5, 256;" ::: "memory");  // histograms cleared
+                    asm volatile("bar.sync 5, %0;" ::"n"(kCons) : "memory");  // histograms cleared
                 }
                 const int lo = st.lo[r], hi = st.hi[r], sh = st.sh[r];
                 const float flo = (float)lo, fhi = (float)hi;
@@ -330,31 +333,30 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 int since_scan = 0;
                 unsigned tie_run = 0, out_run = 0;  // final pass: ties seen, positions written
                 int32_t *orow = (a.idx && r < nrows) ? a.idx + (row0 + r) * (long long)K : nullptr;
-                uint2 *xch = reinterpret_cast<uint2 *>(hist);  // final pass: [2][kRowsT][2] (g, e)
+                uint2 *xch = reinterpret_cast<uint2 *>(hist);  // final pass: [2][kRowsT][kParts] (g, e)
                 for (int t = 0; t < ntk; t++) {
                     const int g = g0 + t, buf = g % kTBufs;
                     wait_or_abort(bar(st.tfull[buf]), (uint32_t)(g / kTBufs) & 1u, a.wait_ns, &abort_flag, a.status);
                     __syncwarp();  // tcgen05.ld is warp-collective
                     tc_fence_after();
-                    uint32_t x[64];
-                    tmem_ld32(tmem + lane_base + buf * kKT + hf * 64, x);
-                    tmem_ld32(tmem + lane_base + buf * kKT + hf * 64 + 32, x + 32);
+                    uint32_t x[kCols];
+                    tmem_ld32(tmem + lane_base + buf * kKT + pt * kCols, x);
                     tmem_wait_ld();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(st.tfree[buf]));  // the warp's scores are in registers
-                    const int j0 = t * kKT + hf * 64;
-                    const int lim = max(0, min(64, n_r - j0));  // columns c < lim are in the prefix
+                    const int j0 = t * kKT + pt * kCols;
+                    const int lim = max(0, min(kCols, n_r - j0));  // columns c < lim are in the prefix
                     if (mode == kModeHist) {
                         if (!open_r || lim == 0) continue;
-                        if (lim < 64) {  // keys past the row's prefix never count
+                        if (lim < kCols) {  // keys past the row's prefix never count
 #pragma unroll
-                            for (int c = 0; c < 64; c++)
+                            for (int c = 0; c < kCols; c++)
                                 if (c >= lim) x[c] = 0xff800000u;  // -inf
                         }
                         if (level == 1) {
 #pragma unroll
-                            for (int c = 0; c < 64; c++) {
+                            for (int c = 0; c < kCols; c++) {
                                 const float f = __uint_as_float(x[c]);
                                 if (f >= fb) atomicAdd(h + log_bin(f), 1u);
                             }
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                             }
                         } else {
 #pragma unroll
-                            for (int c = 0; c < 64; c++) {
+                            for (int c = 0; c < kCols; c++) {
                                 const float f = __uint_as_float(x[c]);
                                 if (f >= flo && f <= fhi) {
                                     const int bn = (__float2int_rz(f) - lo) >> sh;
@@ -376,61 +378,69 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                         }
                     } else {
                         // final pass: ordered write of the selected positions
-                        uint64_t gt = 0, eq = 0;
+                        unsigned gt = 0u, eq = 0u;
                         if (lim > 0) {
-                            unsigned g2[2] = {0u, 0u}, e2[2] = {0u, 0u};
 #pragma unroll
-                            for (int c = 0; c < 64; c++) {
+                            for (int c = 0; c < kCols; c++) {
                                 const float f = __uint_as_float(x[c]);
-                                g2[c >> 5] |= (unsigned)(f > Tf) << (c & 31);
-                                e2[c >> 5] |= (unsigned)(f == Tf) << (c & 31);
+                                gt |= (unsigned)(f > Tf) << c;
+                                eq |= (unsigned)(f == Tf) << c;
                             }
-                            const uint64_t in = lim == 64 ? ~0ull : (1ull << lim) - 1;  // keys in the prefix
-                            gt = (g2[0] | (uint64_t)g2[1] << 32) & in;
-                            eq = (e2[0] | (uint64_t)e2[1] << 32) & in;
+                            const unsigned in = lim == kCols ? ~0u : (1u << lim) - 1u;  // keys in the prefix
+                            gt &= in;
+                            eq &= in;
                         }
-                        const int slot = ((t & 1) * kRowsT + r) * 2;
-                        xch[slot + hf] = make_uint2((unsigned)__popcll(gt), (unsigned)__popcll(eq));
+                        const int slot = ((t & 1) * kRowsT + r) * kParts;
+                        xch[slot + pt] = make_uint2((unsigned)__popc(gt), (unsigned)__popc(eq));
                         __syncwarp();
-                        pair_sync(q4);
-                        const uint2 c0 = xch[slot], c1 = xch[slot + 1];
-                        const unsigned take0 = tie_run >= need ? 0u : min(c0.y, need - tie_run);
-                        const unsigned tie1 = tie_run + c0.y;
-                        const unsigned take1 = tie1 >= need ? 0u : min(c1.y, need - tie1);
-                        const unsigned tb = hf ? tie1 : tie_run, take = hf ? take1 : take0;
-                        unsigned ob = out_run + (hf ? c0.x + take0 : 0u);
-                        uint64_t sel = gt, ee = eq;
+                        asm volatile("bar.sync %0, %1;" ::"r"(1 + q4), "n"(32 * kParts) : "memory");
+                        // the row's parts in key order: ties taken while fewer than
+                        // `need` have been, and this part's first output slot
+                        unsigned tie = tie_run, ob = out_run, my_tb = 0u, my_take = 0u, my_ob = 0u;
+#pragma unroll
+                        for (int i = 0; i < kParts; i++) {
+                            const uint2 ci = xch[slot + i];
+                            const unsigned take_i = tie >= need ? 0u : min(ci.y, need - tie);
+                            if (i == pt) {
+                                my_tb = tie;
+                                my_take = take_i;
+                                my_ob = ob;
+                            }
+                            ob += ci.x + take_i;
+                            tie += ci.y;
+                        }
+                        out_run = ob;
+                        tie_run = tie;
+                        unsigned sel = gt, ee = eq;
                         int last = -1;
-                        for (unsigned i = 0; i < take; i++) {
-                            const uint64_t lb = ee & (0ull - ee);
+                        for (unsigned i = 0; i < my_take; i++) {
+                            const unsigned lb = ee & (0u - ee);
                             sel |= lb;
                             ee ^= lb;
-                            last = __ffsll((long long)lb) - 1;
+                            last = __ffs(lb) - 1;
                         }
-                        if (take > 0 && tb + take == need) st.P[r] = j0 + last;
+                        if (my_take > 0 && my_tb + my_take == need) st.P[r] = j0 + last;
                         if (orow) {
                             while (sel) {
-                                const int bit = __ffsll((long long)sel) - 1;
+                                const int bit = __ffs(sel) - 1;
                                 sel &= sel - 1;
-                                if (ob < (unsigned)K) orow[ob] = j0 + bit;
+                                if (my_ob < (unsigned)K) orow[my_ob] = j0 + bit;
                                 else set_status(a.status, ESA_ERR_INTERNAL);
-                                ob++;
+                                my_ob++;
                             }
                         }
-                        out_run += c0.x + take0 + c1.x + take1;
-                        tie_run += c0.y + c1.y;
                     }
                 }
-                if (mode == kModeFinal && r < nrows && hf == 0 && !abort_flag &&
+                if (mode == kModeFinal && r < nrows && pt == 0 && !abort_flag &&
                     out_run != (unsigned)min(K, n_r))  // consistency check; never reached
                     set_status(a.status, ESA_ERR_INTERNAL);
             }
             g0 += ntk;
             __syncthreads();  // pass drained: every MMA read, every histogram count in
-            if (mode == kModeHist && warp < 8 && !abort_flag) {
+            if (mode == kModeHist && warp < kConsWarps && !abort_flag) {
                 // ---------------------------------------------- next bucket
-                // warp w resolves rows w, w+8, ...: lane l sums bins bpl*l .. +bpl-1
-                for (int rr = warp; rr < kRowsT; rr += 8) {
+                // warp w resolves rows w, w+16, ...: lane l sums bins bpl*l .. +bpl-1
+                for (int rr = warp; rr < kRowsT; rr += kConsWarps) {
                     if (!st.open[rr]) continue;
                     const unsigned need = (unsigned)K - st.above[rr];
                     const unsigned *hh = hist + rr * kHS;
@@ -505,8 +515,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
         }
 
         // ---- counts, padding and threshold form (one warp per row)
-        if (warp < 8) {
-            for (int rr = warp; rr < nrows; rr += 8) {
+        if (warp < kConsWarps) {
+            for (int rr = warp; rr < nrows; rr += kConsWarps) {
                 const int n = st.n[rr];
                 const int c = min(K, n);
                 if (a.idx) {
