@@ -107,11 +107,13 @@ esa_status launch_routed_tc(const uint16_t *q, const uint16_t *k, const uint16_t
 // Warp-specialised variant (two query tiles per CTA; TMA producer warp, MMA
 // warp, two softmax warpgroups); routed_pp_supported() tells whether its
 // buffers fit for this shape.
+// Its workspace (ws_routed_pp bytes): a flag word area and an fp16 copy of V.
 bool routed_pp_supported(const Shape &s);
+size_t ws_routed_pp(const Shape &s);
 esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
                             const int8_t *kI, const int32_t *wI, const uint8_t *route, const int32_t *thr,
                             const Shape &s, float scale, const float *g, const uint16_t *lin, float *out,
-                            int32_t *status, cudaStream_t st);
+                            void *pp_ws, int32_t *status, cudaStream_t st);
 
 // Wait limit for inter-block waits, in ns (ESA_WAIT_LIMIT_NS overrides) and
 // the count of extra arrivals a barrier waits for (ESA_DEBUG_EXTRA_ARRIVALS;

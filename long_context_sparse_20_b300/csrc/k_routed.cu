@@ -21,8 +21,11 @@
 
 namespace esa {
 
-// workspace: [row selection: status word, tensor-core scratch][thr]
-size_t ws_routed(const Shape &s, int K) { return align256(ws_row_select(s, K)) + align256((size_t)s.B * s.Tq * 2 * 4); }
+// workspace: [row selection: status word, tensor-core scratch][thr][routed_pp: flag, fp16 values]
+size_t ws_routed(const Shape &s, int K) {
+    return align256(ws_row_select(s, K)) + align256((size_t)s.B * s.Tq * 2 * 4) +
+           (routed_pp_supported(s) ? ws_routed_pp(s) : 0);
+}
 
 esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
                               const int8_t *kI, const int32_t *wI, const uint8_t *route, const Shape &s, int K,
@@ -34,8 +37,10 @@ esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16
     esa_status e = launch_row_select(qI, kI, wI, s, K, nullptr, nullptr, thr, ws, sel_bytes, st);
     if (e != ESA_OK) return e;
     int32_t *status = reinterpret_cast<int32_t *>(ws);
-    if (routed_pp_supported(s))
-        return launch_routed_pp(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, status, st);
+    if (routed_pp_supported(s)) {
+        void *pp_ws = base + sel_bytes + align256((size_t)s.B * s.Tq * 2 * 4);
+        return launch_routed_pp(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, pp_ws, status, st);
+    }
     return launch_routed_tc(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, status, st);
 }
 

@@ -62,6 +62,7 @@ struct PLay {
 };
 
 struct PpArgs {
+    const int32_t *v_wide;  // set when some |V| is beyond fp16: the fp16-P variant stands down
     const uint16_t *lin;
     const int8_t *qI;
     const int32_t *wI;
@@ -82,7 +83,13 @@ struct PpBars {
 };
 
 // Bounded wait that also gives up when another role has aborted the CTA.
-template <int D, int DI>
+// F16P: P is one fp16 operand and V (tm_v) an fp16 copy of the values: one
+// P V product per key tile. Otherwise P is a bf16 hi + lo pair against the
+// bf16 values: two products. fp16 holds every bf16 value below 65504
+// exactly (smaller ones lose only bits below 2^-24), and rounding p in
+// [0, 256] to fp16 changes the output by < 1e-3 where one bf16 P changes it
+// by up to 5e-3; the variant used follows the values' range.
+template <int D, int DI, bool F16P>
 __global__ void __launch_bounds__(kThreads, 1)
     routed_pp_kernel(const __grid_constant__ PpArgs a, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -96,6 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int exact_all;
     __shared__ volatile int abort_flag;
 
+    // one of the two variants runs each call (uniform over the grid)
+    if ((*a.v_wide != 0) == F16P) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long nqt = (a.Tq + kRowsT - 1) / kRowsT;
     const long long npair = (nqt + 1) / 2;
@@ -303,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(tmem + lane_base + colO + c0, o_raw);
                 }
             }
-            // p = 2^(s*scale - mu) (0 for masked keys), as bf16 hi + lo, written
-            // over the indexer-score columns in two 32-key halves
+            // p = 2^(s*scale - mu) (0 for masked keys), fp16 or bf16 hi + lo,
+            // written over the indexer-score columns in two 32-key halves
             float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
             for (int half = 0; half < 2; half++) {
@@ -316,12 +325,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 p1 = ex2_approx(fmaf(__uint_as_float(sr[cc + 1]), a.scale_log2, -mu));
                     ls0 += p0;
                     ls1 += p1;
-                    const uint32_t hw = pack_bf16(p0, p1);
-                    phi[c / 2] = hw;
-                    plo[c / 2] = pack_bf16(p0 - bf16lo(hw), p1 - bf16hi(hw));
+                    if constexpr (F16P) {
+                        phi[c / 2] = pack_f16(p0, p1);
+                    } else {
+                        const uint32_t hw = pack_bf16(p0, p1);
+                        phi[c / 2] = hw;
+                        plo[c / 2] = pack_bf16(p0 - bf16lo(hw), p1 - bf16hi(hw));
+                    }
                 }
                 tmem_st16(tmem + lane_base + colSI + half * 16, phi);
-                tmem_st16(tmem + lane_base + colSI + 32 + half * 16, plo);
+                if constexpr (!F16P) tmem_st16(tmem + lane_base + colSI + 32 + half * 16, plo);
             }
             l += ls0 + ls1;
             tmem_wait_st();
@@ -441,7 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       wait_or_abort(bar(bars.qe_ready), 0u, a.wait_ns, &abort_flag, a.status);
             const bool exact = exact_all != 0;
             const bool use_si = sparse && exact;
-            constexpr uint32_t id_s = idesc(kBN, 1u, 0u), id_i = idesc(kBN, 0u, 0u), id_o = idesc(D, 1u, 1u);
+            constexpr uint32_t id_s = idesc(kBN, 1u, 0u), id_i = idesc(kBN, 0u, 0u),
+                               id_o = idesc(D, F16P ? 0u : 1u, 1u);
+            constexpr int nparts = F16P ? 1 : 2;
             for (int t = 0; t < nt && ok; t++) {
                 const int slot = t % kSlots;
                 const uint32_t sl = sbase + L::RING + slot * L::SLOT;
@@ -485,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t colS = x * kColsPerTile;
 #pragma unroll
-                    for (int part = 0; part < 2; part++)
+                    for (int part = 0; part < nparts; part++)
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; kk++)
                             mma_ts(tmem + colS + 128, tmem + colS + 64 + part * 32 + kk * 8,
@@ -508,38 +523,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int DI>
+template <int D, int DI, bool F16P>
 void *pp_kernel(size_t *smem) {
     if constexpr (!PLay<D, DI>::FITS) {
         return nullptr;
     } else {
         *smem = PLay<D, DI>::TOTAL;
-        return (void *)routed_pp_kernel<D, DI>;
+        return (void *)routed_pp_kernel<D, DI, F16P>;
     }
 }
 
-template <int D>
+template <int D, bool F16P>
 void *pp_kernel_d(int DI, size_t *smem) {
     switch (DI) {
-        case 16: return pp_kernel<D, 16>(smem);
-        case 32: return pp_kernel<D, 32>(smem);
-        case 64: return pp_kernel<D, 64>(smem);
-        default: return pp_kernel<D, 128>(smem);
+        case 16: return pp_kernel<D, 16, F16P>(smem);
+        case 32: return pp_kernel<D, 32, F16P>(smem);
+        case 64: return pp_kernel<D, 64, F16P>(smem);
+        default: return pp_kernel<D, 128, F16P>(smem);
     }
+}
+
+template <bool F16P>
+void *pp_kernel_for(const Shape &s, size_t *smem) {
+    return s.D == 64 ? pp_kernel_d<64, F16P>(s.D_I, smem) : pp_kernel_d<128, F16P>(s.D_I, smem);
+}
+
+// values (bf16) -> fp16 copy; *wide = 1 when some |v| > 65504 (fp16 cannot hold it)
+__global__ void __launch_bounds__(256) v_to_f16_kernel(const uint4 *__restrict__ v, uint4 *__restrict__ vh,
+                                                       long long n8, int32_t *__restrict__ wide) {
+    bool big = false;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+        const uint4 w = ldg_stream16(v + i);
+        uint32_t in[4] = {w.x, w.y, w.z, w.w}, o[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float lo = bf16lo(in[e]), hi = bf16hi(in[e]);
+            big = big || fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+            o[e] = pack_f16(lo, hi);
+        }
+        vh[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (__syncthreads_or(big) && threadIdx.x == 0) atomicOr(wide, 1);
 }
 
 }  // namespace
 
+size_t ws_routed_pp(const Shape &s) {
+    return align256((size_t)s.B * s.Tk * s.Hkv * s.D * 2) + kStatusBytes;  // fp16 values, range flag
+}
+
 bool routed_pp_supported(const Shape &s) {
     size_t smem = 0;
-    void *fn = s.D == 64 ? pp_kernel_d<64>(s.D_I, &smem) : pp_kernel_d<128>(s.D_I, &smem);
+    void *fn = pp_kernel_for<true>(s, &smem);
     return fn != nullptr && s.B * s.Tq < (1ll << 31) && s.B * s.Tk < (1ll << 31);
 }
 
 esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
                             const int8_t *kI, const int32_t *wI, const uint8_t *route, const int32_t *thr,
                             const Shape &s, float scale, const float *g, const uint16_t *lin, float *out,
-                            int32_t *status, cudaStream_t st) {
+                            void *pp_ws, int32_t *status, cudaStream_t st) {
     PpArgs a{};
     a.lin = lin;
     a.qI = qI;
@@ -561,16 +603,36 @@ esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t
     const long long nqt = (s.Tq + kRowsT - 1) / kRowsT;
     const long long blocks = s.B * s.Hq * ((nqt + 1) / 2);
     if (blocks == 0) return ESA_OK;
-    size_t smem = 0;
-    void *fn = s.D == 64 ? pp_kernel_d<64>(s.D_I, &smem) : pp_kernel_d<128>(s.D_I, &smem);
-    if (!fn) return ESA_ERR_UNSUPPORTED;
-    CUtensorMap tq, tk, tv, tki;
+    size_t smem16 = 0, smem2 = 0;
+    void *fn16 = pp_kernel_for<true>(s, &smem16), *fn2 = pp_kernel_for<false>(s, &smem2);
+    if (!fn16 || !fn2) return ESA_ERR_UNSUPPORTED;
+    // fp16 copy of the values and the flag that picks the variant
+    int32_t *wide = static_cast<int32_t *>(pp_ws);
+    uint16_t *vh = reinterpret_cast<uint16_t *>(static_cast<char *>(pp_ws) + kStatusBytes);
+    a.v_wide = wide;
+    if (cudaMemsetAsync(wide, 0, sizeof(int32_t), st) != cudaSuccess) return ESA_ERR_CUDA;
+    {
+        const long long n8 = s.B * s.Tk * s.Hkv * s.D / 8;
+        const long long want = (n8 + 255) / 256, cap = (long long)device_info().sms * 8;
+        if (n8 > 0)
+            v_to_f16_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, st>>>(
+                reinterpret_cast<const uint4 *>(v), reinterpret_cast<uint4 *>(vh), n8, wide);
+        if (cudaGetLastError() != cudaSuccess) return ESA_ERR_CUDA;
+    }
+    CUtensorMap tq, tk, tv, tvh, tki;
     if (!map_rows_heads_d(&tq, q, s.B * s.Tq, s.Hq, s.D, kRowsT) || !map_rows_heads_d(&tk, k, s.B * s.Tk, s.Hkv, s.D, kBN) ||
-        !map_rows_heads_d(&tv, v, s.B * s.Tk, s.Hkv, s.D, kBN) || !map_rows_bytes(&tki, kI, s.B * s.Tk, s.D_I, kBN))
+        !map_rows_heads_d(&tv, v, s.B * s.Tk, s.Hkv, s.D, kBN) || !map_rows_heads_d(&tvh, vh, s.B * s.Tk, s.Hkv, s.D, kBN) ||
+        !map_rows_bytes(&tki, kI, s.B * s.Tk, s.D_I, kBN))
         return ESA_ERR_CUDA;
-    if (!ensure_smem(fn, smem)) return ESA_ERR_CUDA;
-    void *args[] = {(void *)&a, (void *)&tq, (void *)&tk, (void *)&tv, (void *)&tki};
-    cudaError_t ce = cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(kThreads), args, smem, st);
+    if (!ensure_smem(fn16, smem16) || !ensure_smem(fn2, smem2)) return ESA_ERR_CUDA;
+    // the fp16-P variant; then the bf16 hi + lo variant, whose blocks return at
+    // once unless some value is beyond fp16 (tensor maps copy bits: the fp16
+    // copy uses the same 2-byte map shape)
+    void *args16[] = {(void *)&a, (void *)&tq, (void *)&tk, (void *)&tvh, (void *)&tki};
+    if (cudaLaunchKernel(fn16, dim3((unsigned)blocks), dim3(kThreads), args16, smem16, st) != cudaSuccess)
+        return ESA_ERR_CUDA;
+    void *args2[] = {(void *)&a, (void *)&tq, (void *)&tk, (void *)&tv, (void *)&tki};
+    cudaError_t ce = cudaLaunchKernel(fn2, dim3((unsigned)blocks), dim3(kThreads), args2, smem2, st);
     return ce == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }
 

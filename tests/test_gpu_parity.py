@@ -288,6 +288,23 @@ def test_routed_wide_scores():
     assert_close(gpu_routed(to_dev(inp), sh, 30), ref)
 
 
+def test_routed_values_beyond_fp16():
+    """A value above the fp16 range in V makes the routed launch take its
+    bf16 hi + lo variant for P V (the fp16 one stands down). Only the last
+    query row sees that key: the other rows must match within 2e-3, and the
+    last row, whose outputs are large, within a relative 5e-5 (bf16 hi + lo
+    P keeps ~2^-17; an fp16 P would be off by ~2^-12)."""
+    cfg, sh, inp = _case(seed=23, routed=True, B=1, Tq=300, Tk=300, Hq=4, Hkv=2, D=128, top_k=40, D_I=64)
+    inp["v"] = inp["v"].clone()
+    inp["v"][0, 299, :, 7] = 70000.0  # bf16 70144, > 65504
+    inp["route"] = torch.tensor([[1, 0, 1, 0]], dtype=torch.uint8)
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, 40)
+    got = gpu_routed(to_dev(inp), sh, 40)
+    assert_close(got[:-1], ref[:-1])
+    err = np.abs(got[-1].astype(np.float64) - ref[-1])
+    assert (err <= 5e-5 * np.maximum(1.0, np.abs(ref[-1]))).all(), err.max()
+
+
 # ------------------------------------------------------------------ the five workloads at full size
 def _full(name):
     cfg = E.CONFIGS[name]
