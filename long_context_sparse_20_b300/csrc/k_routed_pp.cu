@@ -233,10 +233,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tmem + lane_base + colSI + half * 32, ir);
                     tmem_wait_ld();
                     const int pl = (int)max(-1ll, min(64ll, (long long)Pp - j0));  // ties kept for c <= pl
+                    if (pl < 0 || pl >= 63) {
+                        // the tie position is outside this tile: kept iff s >= cut,
+                        // with cut = T (ties kept) or T + 1 (exact: integer scores)
+                        const float cut = pl < 0 ? Tf + 1.f : Tf;
 #pragma unroll
-                    for (int c = 0; c < 32; c++) {
-                        const float si = __uint_as_float(ir[c]);
-                        if (!(si > Tf || (si == Tf && half * 32 + c <= pl))) sr[half * 32 + c] = 0xff800000u;  // -inf
+                        for (int c = 0; c < 32; c++)
+                            if (!(__uint_as_float(ir[c]) >= cut)) sr[half * 32 + c] = 0xff800000u;  // -inf
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; c++) {
+                            const float si = __uint_as_float(ir[c]);
+                            if (!(si > Tf || (si == Tf && half * 32 + c <= pl))) sr[half * 32 + c] = 0xff800000u;
+                        }
                     }
                 }
             } else if (sparse) {
@@ -277,7 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sr[c] = __float_as_uint(xv);
                     mx4[c & 3] = fmaxf(mx4[c & 3], xv);
                 }
-            } else {  // the Top-K mask (if any) is already in sr
+            } else if (lim >= 63) {  // the Top-K mask (if any) is already in sr; no key past the row
+#pragma unroll
+                for (int c = 0; c < 64; c++) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(sr[c]));
+            } else {
 #pragma unroll
                 for (int c = 0; c < 64; c++) {
                     const float xv = c <= lim ? __uint_as_float(sr[c]) : -INFINITY;
