@@ -178,7 +178,9 @@ CONFIGS = {
 
 
 def shape_of(cfg: dict) -> dict:
-    return {k: cfg[k] for k in ("B", "Tq", "Tk", "q_offset", "Hq", "Hkv", "D", "H_I", "D_I")}
+    sh = {k: cfg[k] for k in ("B", "Tq", "Tk", "q_offset", "Hq", "Hkv", "D", "H_I", "D_I")}
+    sh["flags"] = int(cfg.get("flags", 0))  # indexer options: 1 = ReLU per head, 2 = per-head index sets
+    return sh
 
 
 def needle_positions(seed: int, L: int, count: int) -> np.ndarray:

@@ -43,6 +43,15 @@ def _bind(path: str):
     lib = ctypes.CDLL(path)
     lib.oracle_indexer_row.restype = c_long
     lib.oracle_indexer_row.argtypes = [vp, vp, vp, c_long, c_long, c_long, c_long, c_int, c_int, c_long, c_long, vp]
+    lib.oracle_indexer_row_mode.restype = c_long
+    lib.oracle_indexer_row_mode.argtypes = [vp, vp, vp, c_long, c_long, c_long, c_long, c_int, c_int, c_long, c_long,
+                                            c_int, c_int, vp]
+    lib.oracle_topk_rows_mode.restype = c_int
+    lib.oracle_topk_rows_mode.argtypes = [vp, vp, vp, c_long, c_long, c_long, c_long, c_int, c_int, c_int, c_int, vp,
+                                          c_long, vp, vp, c_int]
+    lib.oracle_attention_rows_sets.restype = c_int
+    lib.oracle_attention_rows_sets.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_long, c_long, c_long, c_long, c_int,
+                                               c_int, c_int, ctypes.c_double, vp, vp, vp, vp, c_long, vp, vp, c_int]
     lib.oracle_topk_rows.restype = c_int
     lib.oracle_topk_rows.argtypes = [vp, vp, vp, c_long, c_long, c_long, c_long, c_int, c_int, c_int, vp, c_long,
                                      vp, vp, c_int]
@@ -95,28 +104,38 @@ def _rows(B, Tq, rows):
     return np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
 
 
-def indexer_row(qI, kI, wI, shape: dict, b: int, t: int, L=None) -> np.ndarray:
-    """int32 scores of row (b,t) against keys 0..q_offset+t."""
+# shape["flags"] bits (the same values as the C ABI's)
+RELU = 1       # ReLU on each indexer head's dot product before the weighted sum
+PER_HEAD = 2   # one index set per indexer head, scored by that head alone
+
+
+def indexer_row(qI, kI, wI, shape: dict, b: int, t: int, L=None, relu: bool = False, head: int = -1) -> np.ndarray:
+    """int32 scores of row (b,t) against keys 0..q_offset+t: the weighted sum
+    over indexer heads (head < 0) or one head's own unweighted score."""
     L = L or lib()
     qa, ka, wa = _np(qI, np.int8), _np(kI, np.int8), _np(wI, np.int32)
     n = shape["q_offset"] + t + 1
     out = np.empty(n, dtype=np.int32)
-    r = L.oracle_indexer_row(_ptr(qa), _ptr(ka), _ptr(wa), shape["B"], shape["Tq"], shape["Tk"], shape["q_offset"],
-                             shape["H_I"], shape["D_I"], b, t, _ptr(out))
+    r = L.oracle_indexer_row_mode(_ptr(qa), _ptr(ka), _ptr(wa), shape["B"], shape["Tq"], shape["Tk"],
+                                  shape["q_offset"], shape["H_I"], shape["D_I"], b, t, int(relu), head, _ptr(out))
     if r != n:
         raise ValueError(f"oracle_indexer_row failed ({r}): score outside int32 or row beyond Tk")
     return out
 
 
 def topk(qI, kI, wI, shape: dict, K: int, rows=None, L=None):
-    """(idx [n_rows,K] int32, cnt [n_rows] int32) for the listed flat rows."""
+    """(idx, cnt) int32 for the listed flat rows: [n_rows,K] and [n_rows], or
+    with per-head sets (shape flags) [n_rows,H_I,K] and [n_rows,H_I]."""
     L = L or lib()
     qa, ka, wa = _np(qI, np.int8), _np(kI, np.int8), _np(wI, np.int32)
     rr = _rows(shape["B"], shape["Tq"], rows)
-    idx = np.empty((len(rr), K), dtype=np.int32)
-    cnt = np.empty(len(rr), dtype=np.int32)
-    rc = L.oracle_topk_rows(_ptr(qa), _ptr(ka), _ptr(wa), shape["B"], shape["Tq"], shape["Tk"], shape["q_offset"],
-                            shape["H_I"], shape["D_I"], K, _ptr(rr), len(rr), _ptr(idx), _ptr(cnt), threads())
+    flags = int(shape.get("flags", 0))
+    sets = (shape["H_I"],) if flags & PER_HEAD else ()
+    idx = np.empty((len(rr), *sets, K), dtype=np.int32)
+    cnt = np.empty((len(rr), *sets), dtype=np.int32)
+    rc = L.oracle_topk_rows_mode(_ptr(qa), _ptr(ka), _ptr(wa), shape["B"], shape["Tq"], shape["Tk"],
+                                 shape["q_offset"], shape["H_I"], shape["D_I"], K, flags, _ptr(rr), len(rr), _ptr(idx),
+                                 _ptr(cnt), threads())
     if rc != 0:
         raise ValueError("oracle_topk_rows: a score does not fit in int32")
     return idx, cnt
@@ -126,22 +145,24 @@ def attention(q, k, v, idx, cnt, shape: dict, K: int, scale: float | None = None
               rows=None, L=None):
     """(out [n_rows,Hq,D] fp64, lse [n_rows,Hq] fp64) for the listed rows.
 
-    idx/cnt are given per listed row (as returned by :func:`topk`)."""
+    idx/cnt are given per listed row (as returned by :func:`topk`); with
+    per-head sets (shape flags) query head h reads set h // (Hq // H_I)."""
     L = L or lib()
     B, Tq, Hq, D = shape["B"], shape["Tq"], shape["Hq"], shape["D"]
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     qa, ka, va = _np(q, np.uint16), _np(k, np.uint16), _np(v, np.uint16)
     rr = _rows(B, Tq, rows)
-    ia = np.ascontiguousarray(np.asarray(idx, dtype=np.int32).reshape(len(rr), K))
-    ca = np.ascontiguousarray(np.asarray(cnt, dtype=np.int32).reshape(len(rr)))
+    nsets = shape["H_I"] if int(shape.get("flags", 0)) & PER_HEAD else 1
+    ia = np.ascontiguousarray(np.asarray(idx, dtype=np.int32).reshape(len(rr) * nsets, K))
+    ca = np.ascontiguousarray(np.asarray(cnt, dtype=np.int32).reshape(len(rr) * nsets))
     ga = _np(g, np.float32) if g is not None else None
     la = _np(lin, np.uint16) if lin is not None else None
     ra = _np(route, np.uint8) if route is not None else None
     out = np.empty((len(rr), Hq, D), dtype=np.float64)
     lse = np.empty((len(rr), Hq), dtype=np.float64)
-    rc = L.oracle_attention_rows(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ia), _ptr(ca), K, B, Tq, shape["Tk"],
-                                 shape["q_offset"], Hq, shape["Hkv"], D, float(scale), _ptr(ga), _ptr(la), _ptr(ra),
-                                 _ptr(rr), len(rr), _ptr(out), _ptr(lse), threads())
+    rc = L.oracle_attention_rows_sets(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ia), _ptr(ca), K, nsets, B, Tq, shape["Tk"],
+                                      shape["q_offset"], Hq, shape["Hkv"], D, float(scale), _ptr(ga), _ptr(la),
+                                      _ptr(ra), _ptr(rr), len(rr), _ptr(out), _ptr(lse), threads())
     if rc != 0:
         raise ValueError("oracle_attention_rows: an index lies outside the causal prefix")
     return out, lse

@@ -21,8 +21,10 @@
  * Readings taken where the pages are silent (each is restated in the tests):
  *  the prefix of query position p is keys 0..p inclusive; the indexer is a
  *  plain weighted sum over indexer heads of int8 dot products (no
- *  nonlinearity), with one indexer key per position shared by all indexer
- *  heads; ties in the score go to the lower position; the index set is
+ *  nonlinearity; a ReLU per indexer head is an option), with one indexer key
+ *  per position shared by all indexer heads; per-head index sets (an option)
+ *  score each indexer head alone, unweighted, and query head h attends to
+ *  the set of indexer head h / (Hq/H_I); ties in the score go to the lower position; the index set is
  *  returned in ascending position order, padded with -1, with
  *  cnt = min(K, p+1); one index set per (sequence, query) is shared by every
  *  query head; the gate is one value in (0,1) per query head; heads routed to
@@ -49,15 +51,36 @@ static double bf16_to_double(uint16_t h) {
     return (double)f;
 }
 
+/* int8 dot product of indexer head h of query row (b, t) with the indexer
+ * key at position j, in int64 */
+static int64_t indexer_dot(const int8_t *qI, const int8_t *kI, long Tq, long Tk, int H_I, int D_I,
+                           long b, long t, int h, long j) {
+    int64_t dot = 0;
+    for (int c = 0; c < D_I; c++) {
+        int64_t a = qI[((b * Tq + t) * H_I + h) * D_I + c];
+        int64_t k = kI[(b * Tk + j) * D_I + c];
+        dot += a * k;
+    }
+    return dot;
+}
+
 /*
- * Indexer score of query row (b, t) against keys 0..p, p = q_offset + t:
- *   s_j = sum_h w_h * sum_c qI[b,t,h,c] * kI[b,j,c]      (no RoPE anywhere)
- * computed in int64. Writes p+1 scores; returns p+1, or -1 when a score
- * does not fit in int32 (the interface promises int32 scores).
+ * Indexer scores of query row (b, t) against keys 0..p, p = q_offset + t,
+ * in int64 (no RoPE anywhere):
+ *   head < 0 (one index set per query, the Gated DSA indexer):
+ *       s_j = sum_h w_h * f(sum_c qI[b,t,h,c] * kI[b,j,c])
+ *   head >= 0 (one index set per indexer head: the per-head [batch, heads,
+ *   top_k] index shape of the Gated DSA pseudo-code, which scores each head's
+ *   query against the shared history keys without weights):
+ *       s_j = f(sum_c qI[b,t,head,c] * kI[b,j,c])
+ * where f is the identity, or f(x) = max(x, 0) when relu is set (a ReLU on
+ * each indexer head's dot product before the weighted sum).
+ * Writes p+1 scores; returns p+1, or -1 when a score does not fit in int32
+ * (the interface promises int32 scores).
  */
-long oracle_indexer_row(const int8_t *qI, const int8_t *kI, const int32_t *wI,
-                        long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
-                        long b, long t, int32_t *scores) {
+long oracle_indexer_row_mode(const int8_t *qI, const int8_t *kI, const int32_t *wI,
+                             long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
+                             long b, long t, int relu, int head, int32_t *scores) {
     (void)B;
     long p = q_offset + t;
     long n = p + 1;
@@ -65,18 +88,23 @@ long oracle_indexer_row(const int8_t *qI, const int8_t *kI, const int32_t *wI,
     for (long j = 0; j < n; j++) {
         int64_t s = 0;
         for (int h = 0; h < H_I; h++) {
-            int64_t dot = 0;
-            for (int c = 0; c < D_I; c++) {
-                int64_t a = qI[((b * Tq + t) * H_I + h) * D_I + c];
-                int64_t k = kI[(b * Tk + j) * D_I + c];
-                dot += a * k;
-            }
-            s += (int64_t)wI[h] * dot;
+            if (head >= 0 && h != head) continue;
+            int64_t dot = indexer_dot(qI, kI, Tq, Tk, H_I, D_I, b, t, h, j);
+            if (relu && dot < 0) dot = 0;
+            if (head >= 0) s += dot;
+            else s += (int64_t)wI[h] * dot;
         }
         if (s > INT32_MAX || s < INT32_MIN) return -1;
         scores[j] = (int32_t)s;
     }
     return n;
+}
+
+/* The Gated DSA indexer: weighted sum over heads, no nonlinearity. */
+long oracle_indexer_row(const int8_t *qI, const int8_t *kI, const int32_t *wI,
+                        long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
+                        long b, long t, int32_t *scores) {
+    return oracle_indexer_row_mode(qI, kI, wI, B, Tq, Tk, q_offset, H_I, D_I, b, t, 0, -1, scores);
 }
 
 typedef struct {
@@ -98,14 +126,20 @@ static int ascending_i32(const void *x, const void *y) {
 
 /*
  * Top-K selection for a list of query rows (flat row id r = b*Tq + t).
- * For each row: order positions 0..p by (score descending, position
- * ascending), keep the first min(K, p+1), sort them ascending, pad with -1.
- * idx is [n_rows, K], cnt is [n_rows]. Returns 0, or -1 on int32 overflow.
+ * For each row (and, with per-head sets, each indexer head of it): order
+ * positions 0..p by (score descending, position ascending), keep the first
+ * min(K, p+1), sort them ascending, pad with -1.
+ * flags: bit 0 = ReLU per indexer head, bit 1 = one index set per indexer
+ * head (scores as in oracle_indexer_row_mode).
+ * idx is [n_rows, K] (or [n_rows, H_I, K] with per-head sets), cnt is
+ * [n_rows] (or [n_rows, H_I]). Returns 0, or -1 on int32 overflow.
  */
-int oracle_topk_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
-                     long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
-                     int K, const int64_t *rows, long n_rows,
-                     int32_t *idx, int32_t *cnt, int n_threads) {
+int oracle_topk_rows_mode(const int8_t *qI, const int8_t *kI, const int32_t *wI,
+                          long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
+                          int K, int flags, const int64_t *rows, long n_rows,
+                          int32_t *idx, int32_t *cnt, int n_threads) {
+    const int relu = flags & 1, per_head = (flags >> 1) & 1;
+    const int nsets = per_head ? H_I : 1;
     int bad = 0;
 #ifdef _OPENMP
     if (n_threads > 0) omp_set_num_threads(n_threads);
@@ -116,20 +150,24 @@ int oracle_topk_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
         long n = q_offset + t + 1;
         int32_t *sc = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
         scored_pos *order = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
-        if (oracle_indexer_row(qI, kI, wI, B, Tq, Tk, q_offset, H_I, D_I, b, t, sc) != n) {
-            bad |= 1;
-        } else {
+        for (int set = 0; set < nsets; set++) {
+            const long out = r * nsets + set;
+            if (oracle_indexer_row_mode(qI, kI, wI, B, Tq, Tk, q_offset, H_I, D_I, b, t, relu, per_head ? set : -1,
+                                        sc) != n) {
+                bad |= 1;
+                continue;
+            }
             for (long j = 0; j < n; j++) {
                 order[j].s = sc[j];
                 order[j].j = (int32_t)j;
             }
             qsort(order, (size_t)n, sizeof(scored_pos), by_score_then_position);
             long kk = n < K ? n : K;
-            int32_t *row = idx + r * (long)K;
+            int32_t *row = idx + out * (long)K;
             for (long i = 0; i < kk; i++) row[i] = order[i].j;
             qsort(row, (size_t)kk, sizeof(int32_t), ascending_i32);
             for (long i = kk; i < K; i++) row[i] = -1;
-            cnt[r] = (int32_t)kk;
+            cnt[out] = (int32_t)kk;
         }
         free(sc);
         free(order);
@@ -137,11 +175,21 @@ int oracle_topk_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
     return bad ? -1 : 0;
 }
 
+/* The Gated DSA selection: one index set per query row. */
+int oracle_topk_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
+                     long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
+                     int K, const int64_t *rows, long n_rows,
+                     int32_t *idx, int32_t *cnt, int n_threads) {
+    return oracle_topk_rows_mode(qI, kI, wI, B, Tq, Tk, q_offset, H_I, D_I, K, 0, rows, n_rows, idx, cnt, n_threads);
+}
+
 /*
  * Attention for a list of query rows, all query heads, in fp64.
  *  - Head h of row (b,t) reads key/value head kh = h / (Hq/Hkv).
  *  - Key set: when route is given and route[b*Hq+h] == 0 (a full head), all
- *    positions 0..p; otherwise the row's index set idx[r, 0..cnt[r]).
+ *    positions 0..p; otherwise the index set of head h: with nsets = 1 the
+ *    row's one set idx[r, 0..cnt[r]); with nsets > 1 (one set per indexer
+ *    head) the set s = h / (Hq/nsets), idx[r, s, 0..cnt[r, s]).
  *  - logit_j = scale * sum_c q[b,t,h,c] * k[b,j,kh,c];  m = max logit;
  *    o = sum_j e^(logit_j - m) v[b,j,kh,:] / sum_j e^(logit_j - m);
  *    lse = m + ln sum_j e^(logit_j - m).
@@ -152,13 +200,13 @@ int oracle_topk_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
  * per listed row. out [n_rows,Hq,D], lse [n_rows,Hq] (lse may be NULL).
  * Returns 0, or -1 when an index lies outside 0..p.
  */
-int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                          const int32_t *idx, const int32_t *cnt, int K,
-                          long B, long Tq, long Tk, long q_offset,
-                          int Hq, int Hkv, int D, double scale,
-                          const float *g, const uint16_t *lin, const uint8_t *route,
-                          const int64_t *rows, long n_rows,
-                          double *out, double *lse, int n_threads) {
+int oracle_attention_rows_sets(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                               const int32_t *idx, const int32_t *cnt, int K, int nsets,
+                               long B, long Tq, long Tk, long q_offset,
+                               int Hq, int Hkv, int D, double scale,
+                               const float *g, const uint16_t *lin, const uint8_t *route,
+                               const int64_t *rows, long n_rows,
+                               double *out, double *lse, int n_threads) {
     (void)B;
     int bad = 0;
     int G = Hq / Hkv;
@@ -174,15 +222,16 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
         double *acc = (double *)malloc(sizeof(double) * (size_t)D);
         for (int h = 0; h < Hq; h++) {
             int kh = h / G;
+            long set = r * nsets + h / (Hq / nsets);  /* the index set of head h */
             int full = (route != NULL) && (route[b * Hq + h] == 0);
             long nk;
             if (full) {
                 nk = p + 1;
                 for (long j = 0; j < nk; j++) keys[j] = (int32_t)j;
             } else {
-                nk = cnt[r];
+                nk = cnt[set];
                 for (long i = 0; i < nk; i++) {
-                    int32_t j = idx[r * (long)K + i];
+                    int32_t j = idx[set * (long)K + i];
                     if (j < 0 || j > p) {
                         bad |= 1;
                         j = 0;
@@ -225,6 +274,18 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
         free(acc);
     }
     return bad ? -1 : 0;
+}
+
+/* Attention with one index set per query row (nsets = 1). */
+int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const int32_t *idx, const int32_t *cnt, int K,
+                          long B, long Tq, long Tk, long q_offset,
+                          int Hq, int Hkv, int D, double scale,
+                          const float *g, const uint16_t *lin, const uint8_t *route,
+                          const int64_t *rows, long n_rows,
+                          double *out, double *lse, int n_threads) {
+    return oracle_attention_rows_sets(q, k, v, idx, cnt, K, 1, B, Tq, Tk, q_offset, Hq, Hkv, D, scale, g, lin, route,
+                                      rows, n_rows, out, lse, n_threads);
 }
 
 /* Threshold form of a row's index set, used to explain parity failures:

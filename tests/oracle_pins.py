@@ -311,7 +311,97 @@ def pin_needles_closed_form(L):
     assert np.abs(out[0, 0] - vmean).max() < 1e-9
 
 
+
+# ------------------------------------------------------------------ indexer options: ReLU, per-head sets
+def _golden_example():
+    gv = _golden()
+    qI = np.array(gv["qI"], dtype=np.int8).reshape(1, 3, 2, 3)
+    kI = np.array(gv["kI"], dtype=np.int8).reshape(1, 3, 3)
+    w = np.array(gv["w"], dtype=np.int32)
+    sh = dict(B=1, Tq=3, Tk=3, q_offset=0, Hq=2, Hkv=1, D=64, H_I=2, D_I=3, flags=0)
+    return gv, qI, kI, w, sh
+
+
+def pin_indexer_modes_golden(L):
+    """The hand-worked example of tests/golden/indexer_tiny.txt with the ReLU
+    per head and with one index set per head."""
+    gv, qI, kI, w, sh = _golden_example()
+    assert O.indexer_row(qI, kI, w, sh, 0, 2, L=L, relu=True).tolist() == gv["relu_scores_t2"]
+    rs = dict(sh, flags=O.RELU)
+    assert O.topk(qI, kI, w, rs, 1, L=L)[0].reshape(-1).tolist() == gv["relu_top1"]
+    assert O.topk(qI, kI, w, rs, 2, L=L)[0].reshape(-1).tolist() == gv["relu_top2"]
+    heads = O.indexer_row(qI, kI, w, sh, 0, 2, L=L, head=0).tolist() + \
+        O.indexer_row(qI, kI, w, sh, 0, 2, L=L, head=1).tolist()
+    assert heads == gv["head_scores_t2"], heads
+    ph = dict(sh, flags=O.PER_HEAD)
+    idx, cnt = O.topk(qI, kI, w, ph, 2, L=L)
+    assert idx.shape == (3, 2, 2) and cnt.shape == (3, 2)
+    assert idx.reshape(-1).tolist() == gv["head_top2"], idx
+    assert cnt.reshape(-1).tolist() == gv["head_cnt2"], cnt
+    idx, _ = O.topk(qI, kI, w, dict(sh, flags=O.PER_HEAD | O.RELU), 2, L=L)
+    assert idx[2].reshape(-1).tolist() == gv["head_relu_top2_t2"], idx[2]
+
+
+def pin_relu_special_and_numpy(L, seed=19):
+    """ReLU indexer: equal to the linear one when every head's dot product is
+    >= 0; all scores 0 (so the first K positions) when every one is <= 0;
+    and numpy's elementwise maximum of int64 einsum products elsewhere."""
+    rng = np.random.default_rng(seed)
+    B, Tq, Tk, HI, DI = 1, 6, 30, 3, 16
+    sh = dict(B=B, Tq=Tq, Tk=Tk, q_offset=Tk - Tq, Hq=1, Hkv=1, D=64, H_I=HI, D_I=DI, flags=0)
+    w = np.array([2, 1, 3], dtype=np.int32)
+    qpos = rng.integers(0, 8, (B, Tq, HI, DI), dtype=np.int8)
+    kpos = rng.integers(0, 8, (B, Tk, DI), dtype=np.int8)
+    kneg = -kpos
+    for t in range(Tq):
+        assert np.array_equal(O.indexer_row(qpos, kpos, w, sh, 0, t, L=L, relu=True),
+                              O.indexer_row(qpos, kpos, w, sh, 0, t, L=L)), t
+        assert not O.indexer_row(qpos, kneg, w, sh, 0, t, L=L, relu=True).any(), t
+    K = 7
+    idx, cnt = O.topk(qpos, kneg, w, dict(sh, flags=O.RELU), K, L=L)
+    assert (idx == np.arange(K)[None, :]).all() and (cnt == K).all()
+    qI = rng.integers(-128, 128, (2, 5, HI, DI), dtype=np.int8)
+    kI = rng.integers(-128, 128, (2, 11, DI), dtype=np.int8)
+    sh2 = dict(B=2, Tq=5, Tk=11, q_offset=6, Hq=1, Hkv=1, D=64, H_I=HI, D_I=DI, flags=0)
+    dots = np.einsum("bthc,bjc->bthj", qI.astype(np.int64), kI.astype(np.int64))
+    ref = np.einsum("bthj,h->btj", np.maximum(dots, 0), w.astype(np.int64))
+    for b in range(2):
+        for t in range(5):
+            assert np.array_equal(O.indexer_row(qI, kI, w, sh2, b, t, L=L, relu=True), ref[b, t, :7 + t]), (b, t)
+
+
+def pin_per_head_sets_are_sliced_queries(L):
+    """One index set per indexer head: head h's set equals the one-set
+    selection of the query sliced to head h with weight 1 (and the same with
+    the ReLU, which on one head clamps its negative scores to 0)."""
+    cfg, sh, inp = _small(seed=47, B=2, Tq=20, Tk=40, q_offset=20, H_I=3, D_I=16, top_k=9, weights="1to4")
+    K = 9
+    for flags in (O.PER_HEAD, O.PER_HEAD | O.RELU):
+        idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], dict(sh, flags=flags), K, L=L)
+        for h in range(3):
+            q1 = inp["qI"][:, :, h:h + 1, :].contiguous()
+            one = dict(sh, H_I=1, flags=flags & O.RELU)
+            i1, c1 = O.topk(q1, inp["kI"], np.array([1], dtype=np.int32), one, K, L=L)
+            assert np.array_equal(idx[:, h], i1) and np.array_equal(cnt[:, h], c1), (flags, h)
+
+
+def pin_per_head_attention_uses_its_set(L):
+    """With one index set per indexer head, query head h's output equals the
+    one-set attention given head h's set (query head h reads set h // (Hq // H_I))."""
+    cfg, sh, inp = _small(seed=53, Tq=24, Tk=24, Hq=8, Hkv=2, D=64, H_I=4, D_I=16, top_k=6)
+    K = 6
+    ph = dict(sh, flags=O.PER_HEAD)
+    idx, cnt = O.topk(inp["qI"], inp["kI"], inp["wI"], ph, K, L=L)
+    out, lse = O.attention(inp["q"], inp["k"], inp["v"], idx, cnt, ph, K, g=inp["g"], lin=inp["lin"], L=L)
+    for s in range(4):
+        o1, l1 = O.attention(inp["q"], inp["k"], inp["v"], idx[:, s], cnt[:, s], dict(sh, flags=0), K,
+                             g=inp["g"], lin=inp["lin"], L=L)
+        for h in range(2 * s, 2 * s + 2):
+            assert np.array_equal(out[:, h], o1[:, h]) and np.array_equal(lse[:, h], l1[:, h]), (s, h)
+
 ALL_PINS = [pin_indexer_golden, pin_indexer_numpy, pin_indexer_onehot, pin_indexer_bound,
             pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special, pin_topk_needles,
             pin_attention_full_is_sdpa, pin_attention_sparse_is_masked_sdpa, pin_attention_closed_forms,
-            pin_empty_set, pin_gate, pin_routing, pin_needles_closed_form]
+            pin_empty_set, pin_gate, pin_routing, pin_needles_closed_form,
+            pin_indexer_modes_golden, pin_relu_special_and_numpy, pin_per_head_sets_are_sliced_queries,
+            pin_per_head_attention_uses_its_set]

@@ -26,6 +26,11 @@ MUTANTS = {
     "lse misses the max": ("lse[r * Hq + h] = m + log(den);", "lse[r * Hq + h] = log(den);"),
     "value row from the key cache": ("const uint16_t *vrow = v + ", "const uint16_t *vrow = k + "),
     "full heads skip the diagonal": ("nk = p + 1;\n                for (long j = 0; j < nk; j++)", "nk = p;\n                for (long j = 0; j < nk; j++)"),
+    "ReLU not applied": ("if (relu && dot < 0) dot = 0;", ";"),
+    "ReLU clamps the weighted sum instead of each head": ("if (relu && dot < 0) dot = 0;", "if (relu && dot < 0 && H_I == 1) dot = 0;"),
+    "per-head score weighted": ("if (head >= 0) s += dot;", "if (head >= 0) s += (int64_t)wI[h] * dot;"),
+    "per-head set scored by every head": ("if (head >= 0 && h != head) continue;", ";"),
+    "query head reads the wrong set": ("long set = r * nsets + h / (Hq / nsets);", "long set = r * nsets + h % nsets;"),
 }
 
 
