@@ -184,7 +184,7 @@ def reference_arm(args):
 
 
 def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
-                    names=("long_prefill", "chunked_prefill", "routed_prefill")) -> dict:
+                    names=("long_prefill", "chunked_prefill", "per_head_prefill", "routed_prefill")) -> dict:
     """The two prefill workloads, one forward each (after one untimed warm-up),
     timed with CUDA events on the launching stream. Inputs (hundreds of MB to
     GBs) exceed the 126 MB L2. Algorithmic flops count what the method
@@ -225,9 +225,10 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
         n = np.arange(sh["q_offset"] + 1, sh["q_offset"] + S + 1, dtype=np.float64)  # prefix lengths
         sel_pairs = float(np.minimum(n, K).sum())  # per (sequence, head)
         causal_pairs = float(n.sum())
+        opts = {0: "", 1: " ReLU", 2: " per-head sets", 3: " ReLU, per-head sets"}[sh["flags"]]
         entry = {"workload": f"{name}: B={B} S={S} (queries at {sh['q_offset']}..{sh['q_offset'] + S - 1} of a "
-                             f"{sh['Tk']}-key cache) Hq={Hq} Hkv={sh['Hkv']} D={D} indexer {sh['H_I']}x{sh['D_I']} "
-                             f"top_k={K}"}
+                             f"{sh['Tk']}-key cache) Hq={Hq} Hkv={sh['Hkv']} D={D} indexer {sh['H_I']}x{sh['D_I']}"
+                             f"{opts} top_k={K}"}
         if cfg.get("routed"):
             ws = esa.workspace_for(esa.OP_ROUTED_ATTN, shape, K, dev)
             ms = timed(lambda: esa.esa_routed_attn(d["q"], d["k"], d["v"], d["qI"], d["kI"], d["wI"], d["route"], shape,
@@ -240,8 +241,9 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
         else:
             wsel = esa.workspace_for(esa.OP_TOPK_SELECT, shape, K, dev)
             watt = esa.workspace_for(esa.OP_SPARSE_ATTN, shape, K, dev)
-            idx = torch.empty(B, S, K, dtype=torch.int32, device=dev)
-            cnt = torch.empty(B, S, dtype=torch.int32, device=dev)
+            sets = (sh["H_I"],) if sh["flags"] & esa.PER_HEAD_SETS else ()  # per-head index sets
+            idx = torch.empty(B, S, *sets, K, dtype=torch.int32, device=dev)
+            cnt = torch.empty(B, S, *sets, dtype=torch.int32, device=dev)
             ms_sel = timed(lambda: esa.esa_topk_select(d["qI"], d["kI"], d["wI"], shape, K, idx, cnt, wsel, st))
             ms_att = timed(lambda: esa.esa_sparse_attn(d["q"], d["k"], d["v"], idx, cnt, shape, K, scale, d["g"],
                                                        d["lin"], out, None, watt, st))
@@ -473,7 +475,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workloads' timings")
     ap.add_argument("--prefill-only", action="store_true", help="time the prefill workloads only (profiling)")
     ap.add_argument("--prefill-seq", type=int, default=0, help="override the prefill sequence length (profiling)")
-    ap.add_argument("--prefill-names", default="long_prefill,chunked_prefill,routed_prefill",
+    ap.add_argument("--prefill-names", default="long_prefill,chunked_prefill,per_head_prefill,routed_prefill",
                     help="comma-separated prefill workloads for --prefill-only (profiling)")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -174,6 +174,10 @@ CONFIGS = {
                             top_k=2048, weights="1to4", routed=False, needles=0, seed=2006),
     "million_decode": dict(B=1, Tq=1, Tk=1048576, q_offset=1048575, Hq=64, Hkv=1, D=128, H_I=1, D_I=64,
                            top_k=2048, weights="ones", routed=False, needles=64, seed=2005),
+    # one index set per query head (the per-head [batch, heads, top_k] shape),
+    # each scored by its own ReLU'd int8 dot products: flags 1 | 2
+    "per_head_prefill": dict(B=1, Tq=8192, Tk=8192, q_offset=0, Hq=16, Hkv=2, D=128, H_I=16, D_I=64,
+                             top_k=2048, weights="ones", routed=False, needles=0, seed=2007, flags=3),
 }
 
 

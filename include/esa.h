@@ -42,6 +42,20 @@
  *   Hq query heads, Hkv key/value heads (Hq % Hkv == 0; query head h reads
  *   key/value head h / (Hq/Hkv)), head dim D in {64, 128};
  *   H_I indexer heads (1..16) of dim D_I in {16, 32, 64, 128}.
+ *   flags: indexer options, 0 for the Gated DSA indexer (one index set per
+ *   query row, scored by sum_h wI[h] * (qI[h] . kI), shared by every query
+ *   head), or an OR of
+ *     ESA_INDEXER_RELU   score by sum_h wI[h] * max(0, qI[h] . kI): a ReLU on
+ *                        each indexer head's dot product (with one set per
+ *                        head: max(0, qI[h] . kI));
+ *     ESA_PER_HEAD_SETS  one index set per indexer head, scored by that head
+ *                        alone and without its weight (the per-head
+ *                        [batch, heads, top_k] index shape of the Gated DSA
+ *                        page's pseudo-code, section 四.1); query head h
+ *                        attends to the set of indexer head h / (Hq/H_I),
+ *                        which needs Hq % H_I == 0 and, for attention, one of
+ *                        Hq/H_I and Hq/Hkv to divide the other. Not for the
+ *                        routed call (ESA_ERR_UNSUPPORTED).
  *
  * Tensor layouts:
  *   qI  int8  [B, Tq, H_I, D_I]     indexer queries
@@ -51,7 +65,8 @@
  *   q   bf16  [B, Tq, Hq, D]
  *   k,v bf16  [B, Tk, Hkv, D]
  *   idx int32 [B, Tq, top_k]        selected positions, ascending, -1 padded
- *   cnt int32 [B, Tq]               min(top_k, p+1)
+ *                                    ([B, Tq, H_I, top_k] with per-head sets)
+ *   cnt int32 [B, Tq]               min(top_k, p+1) ([B, Tq, H_I] with per-head sets)
  *   g   fp32  [Hq]                  gate, already in (0,1)
  *   lin bf16  [B, Tq, Hq, D]        linear-attention branch output
  *   out fp32  [B, Tq, Hq, D]
@@ -97,7 +112,11 @@ typedef struct esa_shape {
     int32_t D;
     int32_t H_I;
     int32_t D_I;
+    int32_t flags; /* ESA_INDEXER_RELU | ESA_PER_HEAD_SETS, or 0 */
 } esa_shape;
+
+#define ESA_INDEXER_RELU 1
+#define ESA_PER_HEAD_SETS 2
 
 /* Operation ids for esa_workspace_size. */
 #define ESA_OP_INDEXER_SCORE 0
@@ -119,6 +138,10 @@ ESA_API esa_status esa_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * history position; section 二.2: no RoPE):
  *   scores[b,t,j] = sum_h wI[h] * sum_c qI[b,t,h,c] * kI[b,j,c]   for j <= p,
  *   scores[b,t,j] = INT32_MIN                                      for j > p.
+ * With ESA_INDEXER_RELU each head's dot product is max(0, .) before the
+ * weighted sum; with ESA_PER_HEAD_SETS the scores are per indexer head,
+ * scores[b,t,h,j] = (max(0, .) of) sum_c qI[b,t,h,c] * kI[b,j,c], int32
+ * [B, Tq, H_I, Tk].
  * scores int32 [B, Tq, Tk] (a diagnostic: the selection never materialises
  * this). Every score must fit in int32, which holds when
  * sum_h |wI[h]| * D_I * 16384 < 2^31. */

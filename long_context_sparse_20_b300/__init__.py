@@ -24,12 +24,13 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_INDEX, ERR_WORKSPACE, ERR_INTERNAL = range(8)
 OP_INDEXER_SCORE, OP_TOPK_SELECT, OP_SPARSE_ATTN, OP_GATED_MIX, OP_ROUTED_ATTN = range(5)
+INDEXER_RELU, PER_HEAD_SETS = 1, 2  # esa_shape.flags
 
 
 class esa_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("Tq", ctypes.c_int64), ("Tk", ctypes.c_int64), ("q_offset", ctypes.c_int64),
                 ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32), ("H_I", ctypes.c_int32),
-                ("D_I", ctypes.c_int32)]
+                ("D_I", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class EsaError(RuntimeError):
@@ -67,12 +68,13 @@ def status_string(st: int) -> str:
     return _lib.esa_status_string(st).decode()
 
 
-def make_shape(B, Tq, Tk, q_offset, Hq=1, Hkv=1, D=64, H_I=1, D_I=64) -> esa_shape:
-    return esa_shape(B, Tq, Tk, q_offset, Hq, Hkv, D, H_I, D_I)
+def make_shape(B, Tq, Tk, q_offset, Hq=1, Hkv=1, D=64, H_I=1, D_I=64, flags=0) -> esa_shape:
+    return esa_shape(B, Tq, Tk, q_offset, Hq, Hkv, D, H_I, D_I, flags)
 
 
 def shape_from(d: dict) -> esa_shape:
-    return make_shape(*(d[k] for k in ("B", "Tq", "Tk", "q_offset", "Hq", "Hkv", "D", "H_I", "D_I")))
+    return make_shape(*(d[k] for k in ("B", "Tq", "Tk", "q_offset", "Hq", "Hkv", "D", "H_I", "D_I")),
+                      flags=int(d.get("flags", 0)))
 
 
 def _p(t):

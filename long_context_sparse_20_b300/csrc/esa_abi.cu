@@ -84,6 +84,26 @@ int debug_extra_arrivals() {
     return v > 0 ? v : 0;
 }
 
+namespace {
+__device__ int32_t g_unit_weight = 1;
+}  // namespace
+
+const int32_t *unit_weight() {
+    static std::mutex mu;
+    static const int32_t *cache[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_unit_weight) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (dev >= 0 && dev < 64) cache[dev] = static_cast<const int32_t *>(p);
+    return static_cast<const int32_t *>(p);
+}
+
 }  // namespace esa
 
 using namespace esa;
@@ -107,6 +127,15 @@ esa_status check_shape(const esa_shape *s, bool need_attn, bool need_index) {
         if (s->H_I <= 0 || s->H_I > 16) return ESA_ERR_UNSUPPORTED;
         if (s->D_I != 16 && s->D_I != 32 && s->D_I != 64 && s->D_I != 128) return ESA_ERR_UNSUPPORTED;
     }
+    if (s->flags & ~(ESA_INDEXER_RELU | ESA_PER_HEAD_SETS)) return ESA_ERR_INVALID;
+    if ((s->flags & ESA_PER_HEAD_SETS) && (s->H_I <= 0 || s->H_I > 16)) return ESA_ERR_UNSUPPORTED;
+    if ((s->flags & ESA_PER_HEAD_SETS) && need_attn) {
+        // query head h attends to set h / (Hq/H_I); a block of heads that
+        // shares one gather must lie in one set and one key/value head
+        if (s->Hq % s->H_I) return ESA_ERR_INVALID;
+        const int hs = s->Hq / s->H_I, G = s->Hq / s->Hkv;
+        if (hs % G && G % hs) return ESA_ERR_UNSUPPORTED;
+    }
     return ESA_OK;
 }
 
@@ -121,6 +150,8 @@ Shape to_shape(const esa_shape *s) {
     x.D = s->D;
     x.H_I = s->H_I;
     x.D_I = s->D_I;
+    x.flags = s->flags;
+    x.pos_div = 1;
     return x;
 }
 
@@ -131,8 +162,9 @@ esa_status check_ws(void *ws, size_t ws_bytes, size_t need) {
 }
 
 size_t topk_ws(const Shape &s, int K) {
-    SplitPlan sp = plan_split_select(s, K);
-    size_t w = sp.ok ? sp.ws_bytes : ws_row_select(s, K);
+    const Shape r = selection_rows(s);
+    SplitPlan sp = plan_split_select(r, K);
+    size_t w = sp.ok ? sp.ws_bytes : ws_row_select(r, K);
     return w < kStatusBytes ? kStatusBytes : w;
 }
 
@@ -166,8 +198,11 @@ esa_status esa_indexer_score(const int8_t *qI, const int8_t *kI, const int32_t *
     if (!qI || !kI || !wI || !scores) return ESA_ERR_INVALID;
     if (!aligned16(qI) || !aligned16(kI) || !aligned16(scores)) return ESA_ERR_INVALID;
     if ((e = check_ws(ws, ws_bytes, kStatusBytes))) return e;
-    return launch_indexer_score(qI, kI, wI, to_shape(s), scores, (cudaStream_t)stream) == cudaSuccess ? ESA_OK
-                                                                                                      : ESA_ERR_CUDA;
+    // per-head scores are the scores of the per-head selection rows
+    const Shape r = selection_rows(to_shape(s));
+    const int32_t *w = per_head_of(r) ? unit_weight() : wI;
+    if (!w) return ESA_ERR_CUDA;
+    return launch_indexer_score(qI, kI, w, r, scores, (cudaStream_t)stream) == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }
 
 esa_status esa_topk_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const esa_shape *s, int top_k,
@@ -177,12 +212,14 @@ esa_status esa_topk_select(const int8_t *qI, const int8_t *kI, const int32_t *wI
     if (!qI || !kI || !wI || !idx || !cnt) return ESA_ERR_INVALID;
     if (top_k <= 0 || top_k > 65536) return ESA_ERR_INVALID;
     if (!aligned16(qI) || !aligned16(kI)) return ESA_ERR_INVALID;
-    Shape x = to_shape(s);
+    const Shape x = selection_rows(to_shape(s));  // per-head sets: one row per (query, indexer head)
     if (x.B * x.Tq == 0) return ESA_OK;
+    const int32_t *w = per_head_of(x) ? unit_weight() : wI;
+    if (!w) return ESA_ERR_CUDA;
     SplitPlan sp = plan_split_select(x, top_k);
     if ((e = check_ws(ws, ws_bytes, sp.ok ? sp.ws_bytes : ws_row_select(x, top_k)))) return e;
-    if (sp.ok) return launch_split_select(qI, kI, wI, x, top_k, idx, cnt, ws, sp, (cudaStream_t)stream);
-    return launch_row_select(qI, kI, wI, x, top_k, idx, cnt, nullptr, ws, ws_bytes, (cudaStream_t)stream);
+    if (sp.ok) return launch_split_select(qI, kI, w, x, top_k, idx, cnt, ws, sp, (cudaStream_t)stream);
+    return launch_row_select(qI, kI, w, x, top_k, idx, cnt, nullptr, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,
@@ -227,6 +264,7 @@ esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t 
         (lin && !aligned16(lin)))
         return ESA_ERR_INVALID;
     if (!(scale > 0.f) || scale != scale) return ESA_ERR_INVALID;
+    if (s->flags & ESA_PER_HEAD_SETS) return ESA_ERR_UNSUPPORTED;  // one threshold form per row
     Shape x = to_shape(s);
     if (x.B * x.Tq == 0) return ESA_OK;
     if ((e = check_ws(ws, ws_bytes, ws_routed(x, top_k)))) return e;

@@ -11,7 +11,28 @@ namespace esa {
 struct Shape {
     long long B, Tq, Tk, q_offset;
     int Hq, Hkv, D, H_I, D_I;
+    int flags = 0;    // ESA_INDEXER_RELU | ESA_PER_HEAD_SETS
+    int pos_div = 1;  // selection rows per query position (per-head sets: H_I)
 };
+
+inline bool relu_of(const Shape &s) { return (s.flags & ESA_INDEXER_RELU) != 0; }
+inline bool per_head_of(const Shape &s) { return (s.flags & ESA_PER_HEAD_SETS) != 0; }
+
+// The selection problem of a shape. With per-head sets every (query row,
+// indexer head) pair is a row of its own: B x (Tq * H_I) rows of ONE indexer
+// head (weight 1, see unit_weight), H_I consecutive rows per query position,
+// whose idx/cnt rows are exactly the [B, Tq, H_I, K] / [B, Tq, H_I] layout.
+inline Shape selection_rows(const Shape &s) {
+    Shape r = s;
+    if (per_head_of(s)) {
+        r.Tq = s.Tq * s.H_I;
+        r.pos_div = s.H_I;
+        r.H_I = 1;
+    }
+    return r;
+}
+// Device address of an int32 holding 1 (the weight of a per-head row).
+const int32_t *unit_weight();
 
 struct DevInfo {
     int sms;
@@ -78,6 +99,10 @@ esa_status launch_rows_dp4a(const int8_t *qI, const int8_t *kI, const int32_t *w
 struct AttnPlan {
     int gt;      // query heads per block (16, 32 or 64)
     int hg;      // head groups per key/value head
+    int nsets;   // index sets per query row (1, or H_I with per-head sets)
+    int hs;      // query heads per index set
+    int seg;     // heads of one key/value head sharing one index set
+    int gps;     // head groups per segment
     int splits;  // key splits per (row, kv head, head group)
     int keys_per_split;
     long long grid;

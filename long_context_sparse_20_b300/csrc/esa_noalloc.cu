@@ -57,7 +57,11 @@ extern "C" ESA_API esa_status esa_topk_select_noalloc(const int8_t *qI, const in
     if (s->D_I != 16 && s->D_I != 32 && s->D_I != 64 && s->D_I != 128) return ESA_ERR_UNSUPPORTED;
     if (top_k <= 0 || top_k > 65536) return ESA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(qI) & 15u) || (reinterpret_cast<uintptr_t>(kI) & 15u)) return ESA_ERR_INVALID;
-    Shape x{s->B, s->Tq, s->Tk, s->q_offset, s->Hq, s->Hkv, s->D, s->H_I, s->D_I};
+    if (s->flags & ~(ESA_INDEXER_RELU | ESA_PER_HEAD_SETS)) return ESA_ERR_INVALID;
+    Shape x0{s->B, s->Tq, s->Tk, s->q_offset, s->Hq, s->Hkv, s->D, s->H_I, s->D_I};
+    x0.flags = s->flags;
+    const Shape x = selection_rows(x0);  // per-head sets: one row per (query, indexer head)
+    if (per_head_of(x) && !(wI = unit_weight())) return ESA_ERR_CUDA;
     if (x.B * x.Tq == 0) return ESA_OK;
 
     SplitPlan sp = plan_split_select(x, top_k);

@@ -52,18 +52,19 @@ cudaError_t launch_gated_mix(const float *attn, const uint16_t *lin, const float
 template <int DI>
 __global__ void __launch_bounds__(256) indexer_score_kernel(const int8_t *__restrict__ qI, const int8_t *__restrict__ kI,
                                                             const int32_t *__restrict__ wI, int32_t *__restrict__ scores,
-                                                            long long Tq, long long Tk, long long q_offset, int H_I) {
+                                                            long long Tq, long long Tk, long long q_offset, int H_I,
+                                                            int pos_div, int relu) {
     constexpr int W = DI / 4;  // 32-bit words per vector
     __shared__ int32_t qs[16 * W];
     __shared__ int32_t ws_[16];
-    long long row = blockIdx.y;  // b*Tq + t
-    long long b = row / Tq, t = row % Tq;
+    long long row = blockIdx.x;  // b*Tq + t (pos_div rows per query position)
+    long long b = row / Tq, t = (row % Tq) / pos_div;
     long long p = q_offset + t;
     const int32_t *qrow = reinterpret_cast<const int32_t *>(qI + row * (long long)H_I * DI);
     for (int i = threadIdx.x; i < H_I * W; i += blockDim.x) qs[i] = qrow[i];
     if (threadIdx.x < H_I) ws_[threadIdx.x] = wI[threadIdx.x];
     __syncthreads();
-    long long j = blockIdx.x * 1024ll + threadIdx.x;
+    long long j = blockIdx.y * 1024ll + threadIdx.x;
     for (int it = 0; it < 4; it++, j += 256) {
         if (j >= Tk) break;
         int32_t outv = INT32_MIN;
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(256) indexer_score_kernel(const int8_t *__rest
                 int d = 0;
 #pragma unroll
                 for (int c = 0; c < W; c++) d = __dp4a(qs[h * W + c], kw[c], d);
-                acc += (unsigned)ws_[h] * (unsigned)d;
+                acc += (unsigned)ws_[h] * (unsigned)(relu ? max(d, 0) : d);
             }
             outv = (int32_t)acc;
         }
@@ -95,12 +96,14 @@ cudaError_t launch_indexer_score(const int8_t *qI, const int8_t *kI, const int32
                                  int32_t *scores, cudaStream_t st) {
     long long rows = s.B * s.Tq;
     if (rows == 0 || s.Tk == 0) return cudaSuccess;
-    dim3 grid((unsigned)((s.Tk + 1023) / 1024), (unsigned)rows);
+    if ((s.Tk + 1023) / 1024 > 65535 || rows > 0x7fffffffll) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)rows, (unsigned)((s.Tk + 1023) / 1024));
+    const int pd = s.pos_div, relu = relu_of(s) ? 1 : 0;
     switch (s.D_I) {
-        case 16: indexer_score_kernel<16><<<grid, 256, 0, st>>>(qI, kI, wI, scores, s.Tq, s.Tk, s.q_offset, s.H_I); break;
-        case 32: indexer_score_kernel<32><<<grid, 256, 0, st>>>(qI, kI, wI, scores, s.Tq, s.Tk, s.q_offset, s.H_I); break;
-        case 64: indexer_score_kernel<64><<<grid, 256, 0, st>>>(qI, kI, wI, scores, s.Tq, s.Tk, s.q_offset, s.H_I); break;
-        default: indexer_score_kernel<128><<<grid, 256, 0, st>>>(qI, kI, wI, scores, s.Tq, s.Tk, s.q_offset, s.H_I); break;
+        case 16: indexer_score_kernel<16><<<grid, 256, 0, st>>>(qI, kI, wI, scores, s.Tq, s.Tk, s.q_offset, s.H_I, pd, relu); break;
+        case 32: indexer_score_kernel<32><<<grid, 256, 0, st>>>(qI, kI, wI, scores, s.Tq, s.Tk, s.q_offset, s.H_I, pd, relu); break;
+        case 64: indexer_score_kernel<64><<<grid, 256, 0, st>>>(qI, kI, wI, scores, s.Tq, s.Tk, s.q_offset, s.H_I, pd, relu); break;
+        default: indexer_score_kernel<128><<<grid, 256, 0, st>>>(qI, kI, wI, scores, s.Tq, s.Tk, s.q_offset, s.H_I, pd, relu); break;
     }
     return cudaGetLastError();
 }

@@ -73,6 +73,7 @@ struct PpArgs {
     int32_t *status;
     long long B, Tq, Tk, q_offset, wait_ns;
     int Hq, Hkv, H_I;
+    int relu;  // ReLU on each indexer head's dot product (mask scores on dp4a)
     float scale_log2;
 };
 
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(bars.qe_ready), 2 * kRowsT);
         mbar_init(bar(bars.mma_end), 1);
         mbar_fence_init();
-        exact_all = 1;
+        exact_all = a.relu ? 0 : 1;  // the ReLU does not collapse onto the tensor cores
         abort_flag = 0;
     }
     tc_fence_before();
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int w4 = 0; w4 < DI / 4; w4++)
                             d = __dp4a(reinterpret_cast<const int *>(qrow + hh * DI)[w4],
                                        reinterpret_cast<const int *>(raw + c * DI)[w4], d);
-                        acc += (unsigned)a.wI[hh] * (unsigned)d;
+                        acc += (unsigned)a.wI[hh] * (unsigned)(a.relu ? max(d, 0) : d);
                     }
                     const int si = (int)acc;
                     if (!(si > Tint || (si == Tint && j0 + c <= Pp))) keep &= ~(1ull << c);
@@ -612,6 +613,7 @@ esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t
     a.Hkv = s.Hkv;
     a.H_I = s.H_I;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.relu = relu_of(s) ? 1 : 0;
     const long long nqt = (s.Tq + kRowsT - 1) / kRowsT;
     const long long blocks = s.B * s.Hq * ((nqt + 1) / 2);
     if (blocks == 0) return ESA_OK;

@@ -72,6 +72,7 @@ struct TcArgs {
     int32_t *status;
     long long B, Tq, Tk, q_offset, wait_ns;
     int Hq, Hkv, H_I;
+    int relu;  // ReLU on each indexer head's dot product (mask scores on dp4a)
     float scale_log2;
 };
 
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every partial sum of q_eff . kI (|kI| <= 128) must stay below 2^24:
         // each half of the components below 2^23
         fits = fits && absum * 128 < (1ll << 23);
-        exact = __syncthreads_and(fits || r >= rows) != 0;
+        exact = __syncthreads_and((fits || r >= rows) && !a.relu) != 0;  // no collapse under the ReLU
     }
     tc_fence_before();
     __syncthreads();
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int w4 = 0; w4 < DI / 4; w4++)
                         d = __dp4a(reinterpret_cast<const int *>(qrow + hh * DI)[w4],
                                    reinterpret_cast<const int *>(raw + c * DI)[w4], d);
-                    acc += (unsigned)a.wI[hh] * (unsigned)d;
+                    acc += (unsigned)a.wI[hh] * (unsigned)(a.relu ? max(d, 0) : d);
                 }
                 const int si = (int)acc;
                 if (!(si > Tint || (si == Tint && j0 + c <= Pp))) keep &= ~(1u << c);
@@ -493,6 +494,7 @@ esa_status launch_routed_tc(const uint16_t *q, const uint16_t *k, const uint16_t
     a.Hkv = s.Hkv;
     a.H_I = s.H_I;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.relu = relu_of(s) ? 1 : 0;
     long long blocks = s.B * s.Hq * ((s.Tq + kBM - 1) / kBM);
     if (blocks == 0) return ESA_OK;
     if (s.B * s.Tq >= (1ll << 31) || s.B * s.Tk >= (1ll << 31)) return ESA_ERR_UNSUPPORTED;  // TMA coordinates

@@ -89,8 +89,8 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
                                                               const int32_t *__restrict__ wI, int32_t *__restrict__ idx,
                                                               int32_t *__restrict__ cnt, int32_t *__restrict__ thr,
                                                               long long B, long long Tq, long long Tk,
-                                                              long long q_offset, int H_I, int K,
-                                                              const int32_t *__restrict__ only_flagged,
+                                                              long long q_offset, int H_I, int K, int pos_div,
+                                                              int relu, const int32_t *__restrict__ only_flagged,
                                                               int32_t *__restrict__ status) {
     constexpr int W = DI / 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -107,14 +107,15 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
     const long long t0 = tile * kRows;
     const long long row0 = b * Tq + t0;
     const int nrows = (int)min((long long)kRows, Tq - t0);
-    const long long nmax = q_offset + t0 + nrows;  // keys to visit
+    // rows per query position: pos_div (per-head sets: one row per indexer head)
+    const long long nmax = q_offset + (t0 + nrows - 1) / pos_div + 1;  // keys to visit
     // second launch after the tensor-core selection: only the 128-row query
     // tiles that it left (flag 1) are done here
     if (only_flagged && only_flagged[b * ((Tq + 127) / 128) + t0 / 128] == 0) return;
 
     // ---- prologue: row state and indexer queries
     if (tid < kRows) {
-        long long n = tid < nrows ? q_offset + t0 + tid + 1 : 0;
+        long long n = tid < nrows ? q_offset + (t0 + tid) / pos_div + 1 : 0;
         rs.n[tid] = n;
         rs.out[tid] = 0;
         rs.tie[tid] = 0;
@@ -135,8 +136,9 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
     }
     __syncthreads();
     // collapse the indexer heads into q_eff = sum_h w_h qI_h when every
-    // component of every row fits int8 (exact: integer algebra)
-    if (tid == 0) rs.collapsed = 1;
+    // component of every row fits int8 (exact: integer algebra); never with
+    // the ReLU, which acts on each head's own dot product
+    if (tid == 0) rs.collapsed = relu ? 0 : 1;
     __syncthreads();
     {
         bool fits = true;
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
             int d = 0;
 #pragma unroll
             for (int c = 0; c < W; c++) d = __dp4a(qh[c], (int)kw[c], d);
-            acc += (unsigned)wsm[h] * (unsigned)d;
+            acc += (unsigned)wsm[h] * (unsigned)(relu ? max(d, 0) : d);
         }
         return (int)acc;
     };
@@ -448,10 +450,11 @@ esa_status launch_rows_dp4a(const int8_t *qI, const int8_t *kI, const int32_t *w
     void *fn = row_kernel(s.D_I);
     if (!ensure_smem(fn, smem)) return ESA_ERR_CUDA;
     long long B = s.B, Tq = s.Tq, Tk = s.Tk, qo = s.q_offset;
-    int H_I = s.H_I;
-    void *args[] = {(void *)&qI, (void *)&kI, (void *)&wI, (void *)&idx,          (void *)&cnt,
-                    (void *)&thr, (void *)&B, (void *)&Tq, (void *)&Tk,          (void *)&qo,
-                    (void *)&H_I, (void *)&K, (void *)&only_flagged, (void *)&status};
+    int H_I = s.H_I, pos_div = s.pos_div, relu = relu_of(s) ? 1 : 0;
+    void *args[] = {(void *)&qI,  (void *)&kI,      (void *)&wI,   (void *)&idx, (void *)&cnt,
+                    (void *)&thr, (void *)&B,       (void *)&Tq,   (void *)&Tk,  (void *)&qo,
+                    (void *)&H_I, (void *)&K,       (void *)&pos_div, (void *)&relu,
+                    (void *)&only_flagged, (void *)&status};
     cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)tiles), dim3(kThreads), args, smem, st);
     return e == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }

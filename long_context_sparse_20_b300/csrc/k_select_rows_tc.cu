@@ -93,6 +93,8 @@ struct TcSelArgs {
     int32_t *idx, *cnt, *thr, *flags, *status;
     long long B, Tq, Tk, Tkp, q_offset, wait_ns;
     int H_I, K;
+    int pos_div;  // rows per query position (one per indexer head with per-head sets)
+    int relu;     // one indexer head: score = w * max(0, q . k)
 };
 
 // ---- level-1 (log) classes of an exact integer score held in fp32:
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
     const long long t0 = tile * kRowsT;
     const long long row0 = b * a.Tq + t0;
     const int nrows = (int)min((long long)kRowsT, a.Tq - t0);
-    const long long nmax = a.q_offset + t0 + nrows;
+    const long long nmax = a.q_offset + (t0 + nrows - 1) / a.pos_div + 1;
     const int ntk = (int)((nmax + kKT - 1) / kKT);  // key tiles per pass
     const uint32_t sbase = smem_u32(smem);
     unsigned *hist = reinterpret_cast<unsigned *>(smem + L::HIST);
@@ -205,7 +207,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
         for (int c0 = 0; c0 < DI; c0 += 8) {
             long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
             for (int hh = 0; hh < a.H_I; hh++) {
-                const long long wv = a.wI[hh];
+                // with the ReLU the (single) head's weight is applied to the clamped score
+                const long long wv = a.relu ? 1 : a.wI[hh];
                 const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + hh * DI + c0);
 #pragma unroll
                 for (int e = 0; e < 8; e++)
@@ -225,10 +228,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
-        fits = fits && absum * 128 < (1ll << 24);
+        const long long wmul = a.relu ? (a.wI[0] < 0 ? -(long long)a.wI[0] : (long long)a.wI[0]) : 1;
+        fits = fits && absum * 128 * wmul < (1ll << 24);
         if (r < nrows && !fits) atomicAnd(&st.exact_all, 0);
         if (pt == 0) {
-            const int n = r < nrows ? (int)(a.q_offset + t0 + r + 1) : 0;
+            const int n = r < nrows ? (int)(a.q_offset + (t0 + r) / a.pos_div + 1) : 0;
             st.n[r] = n;
             st.open[r] = n > K;  // a prefix of at most K keys is taken whole
             st.T[r] = INT32_MIN;
@@ -326,6 +330,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 const float Tf = (float)st.T[r];
                 const unsigned need = st.need[r];
                 const bool w16 = st.w16[r] != 0;
+                const float wf = a.relu ? (float)a.wI[0] : 1.f;
                 // level 1: running lower bound on the K-th largest score; it starts
                 // below every score (|s| < 2^24) and above the -inf that marks
                 // keys past the prefix, which therefore never count
@@ -345,6 +350,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(st.tfree[buf]));  // the warp's scores are in registers
+                    if (a.relu) {  // w * max(0, q . k): exact, |w| * sum|q| * 128 < 2^24
+#pragma unroll
+                        for (int c = 0; c < kCols; c++) x[c] = __float_as_uint(wf * fmaxf(__uint_as_float(x[c]), 0.f));
+                    }
                     const int j0 = t * kKT + pt * kCols;
                     const int lim = max(0, min(kCols, n_r - j0));  // columns c < lim are in the prefix
                     if (mode == kModeHist) {
@@ -607,6 +616,7 @@ TcPlan plan_tc(const Shape &s, int) {
     TcPlan p{};
     size_t smem = 0;
     if (!tc_kernel(s.D_I, &smem) || tc_disabled()) return p;
+    if (relu_of(s) && s.H_I > 1) return p;  // the ReLU of several heads does not collapse: dp4a
     if (smem + sizeof(TcShared) + 1024 > device_info().smem_optin) return p;
     p.Tkp = (s.Tk + kKT - 1) / kKT * kKT;
     p.ntile = (s.Tq + kRowsT - 1) / kRowsT;
@@ -661,6 +671,8 @@ esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *
     a.wait_ns = wait_limit_ns();
     a.H_I = s.H_I;
     a.K = K;
+    a.pos_div = s.pos_div;
+    a.relu = relu_of(s) ? 1 : 0;
     void *args[] = {(void *)&a};
     if (cudaLaunchKernel(fn, dim3((unsigned)(s.B * p.ntile)), dim3(kThreadsTc), args, smem, st) != cudaSuccess)
         return ESA_ERR_CUDA;

@@ -105,6 +105,8 @@ struct SelArgs {
     unsigned *hdr, *ctrl, *pub;
     int32_t *status;
     long long Tq, Tk, q_offset, wait_ns;
+    int pos_div;  // rows per query position (one per indexer head with per-head sets)
+    int relu;     // ReLU on the (single) indexer head's dot product
     int H_I, K, chunks, rows, extra, stages;
 };
 
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_select_kernel(SelArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long row = blockIdx.x / a.chunks;
     const int ci = blockIdx.x % a.chunks;
-    const long long b = row / a.Tq, t = row % a.Tq;
+    const long long b = row / a.Tq, t = (row % a.Tq) / a.pos_div;
     const long long n = a.q_offset + t + 1;
     const int K = a.K;
     const bool whole = n <= K;  // the whole prefix is kept
@@ -368,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_select_kernel(SelArgs a) {
                 d = __dp4a(q0[1], (int)v.y, d);
                 d = __dp4a(q0[2], (int)v.z, d);
                 d = __dp4a(q0[3], (int)v.w, d);
-                unsigned acc = (unsigned)w0 * (unsigned)d;
+                // with the ReLU (one indexer head) the weight waits for the whole dot product
+                unsigned acc = a.relu ? (unsigned)d : (unsigned)w0 * (unsigned)d;
                 for (int h = 1; h < a.H_I; h++) {
                     const int32_t *qh = sm.q + h * W + j * 4;
                     int e = __dp4a(qh[0], (int)v.x, 0);
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_select_kernel(SelArgs a) {
             }
             const int kk = s * SK + mykey;
             if (kk < span) {
-                const int sv = (int)part[0];
+                const int sv = a.relu ? (int)((unsigned)w0 * (unsigned)max((int)part[0], 0)) : (int)part[0];
                 sc[kk] = sv;
                 atomicAdd(&sm.h1[bin1(sv)], 1u);
                 mn = min(mn, sv);
@@ -658,7 +661,10 @@ SplitPlan plan_split_select(const Shape &s, int K) {
     p.ok = false;
     long long rows = s.B * s.Tq;
     if (rows <= 0) return p;
-    long long nmax = s.q_offset + s.Tq;  // longest prefix
+    long long nmax = s.q_offset + (s.Tq + s.pos_div - 1) / s.pos_div;  // longest prefix
+    // the lane groups sum partial dot products after weighting: a ReLU on
+    // each of several heads' whole dot products is left to the row kernels
+    if (relu_of(s) && s.H_I > 1) return p;
     DevInfo di = device_info();
     void *fn = kernel_ptr(s.D_I);
     // one block per SM (the launch reserves more than half an SM's shared memory)
@@ -705,6 +711,8 @@ esa_status launch_split_select(const int8_t *qI, const int8_t *kI, const int32_t
     a.Tk = s.Tk;
     a.q_offset = s.q_offset;
     a.wait_ns = wait_limit_ns();
+    a.pos_div = s.pos_div;
+    a.relu = relu_of(s) ? 1 : 0;
     a.H_I = s.H_I;
     a.K = K;
     a.chunks = plan.chunks;

@@ -58,6 +58,10 @@ struct AttnArgs {
     int32_t *status;
     long long Tq, Tk, q_offset;
     int Hq, Hkv, K, hg, splits, kps;
+    int nsets;  // index sets per query row (1, or H_I with per-head sets)
+    int hs;     // query heads per index set
+    int seg;    // heads of one key/value head that share one index set
+    int gps;    // head groups per segment
     float scale_log2;
 };
 
@@ -92,8 +96,12 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
     const long long b = row / a.Tq, t = row % a.Tq;
     const long long p = a.q_offset + t;
     const int G = a.Hq / a.Hkv;
-    const int h0 = kvh * G + hgi * GT;  // first query head of this block
-    const int nh = min(GT, G - hgi * GT);
+    // the block's heads lie in one segment: heads of key/value head kvh that
+    // share one index set (all G of them with one set per row)
+    const int sg = hgi / a.gps, sub = hgi % a.gps;
+    const int h0 = kvh * G + sg * a.seg + sub * GT;  // first query head of this block
+    const int nh = min(GT, a.seg - sub * GT);
+    const long long set = a.nsets > 1 ? row * a.nsets + h0 / a.hs : row;  // idx/cnt row of the block's set
 
     if (tid == 0) bad_row = 0;
     // ---- Q tile (GT heads x D), zero rows past the group
@@ -107,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
         cp_async_commit();
     }
     pdl_wait();
-    int c = a.cnt[row];
+    int c = a.cnt[set];
     const int cmax = (int)min((long long)a.K, p + 1);
     __syncthreads();
     if (c < 0 || c > cmax) {
@@ -120,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
 
     // this split's indices, staged in windows of kIdxWin (validated here,
     // then read by the gathers of the following stages)
-    const int32_t *idx_row = a.idx + row * (long long)a.K + k_begin;
+    const int32_t *idx_row = a.idx + set * (long long)a.K + k_begin;
     int win0 = 0;
     auto fill_idx = [&](int base) {
 #pragma unroll 8
@@ -471,10 +479,18 @@ AttnPlan plan_sparse_attn(const Shape &s, int K) {
     // decode-like (few units): split the index list over a cluster, and use
     // smaller head groups until about half the SMs have a block
     int splits = units >= di.sms ? 1 : max_splits;
-    int gt = G <= 16 ? 16 : (G <= 32 ? 32 : 64);
-    while (gt > 16 && units * ((G + gt - 1) / gt) * splits < di.sms / 2) gt /= 2;
+    // segments: the heads of one key/value head that share one index set
+    const bool ph = per_head_of(s);
+    const int hs = ph ? s.Hq / s.H_I : s.Hq;
+    const int seg = ph ? std::min(hs, G) : G;
+    int gt = seg <= 16 ? 16 : (seg <= 32 ? 32 : 64);
+    while (gt > 16 && units * (G / seg) * ((seg + gt - 1) / gt) * splits < di.sms / 2) gt /= 2;
     p.gt = gt;
-    p.hg = (G + gt - 1) / gt;
+    p.nsets = ph ? s.H_I : 1;
+    p.hs = hs;
+    p.seg = seg;
+    p.gps = (seg + gt - 1) / gt;
+    p.hg = (G / seg) * p.gps;
     int kps = (K + splits - 1) / splits;
     kps = (kps + kKeys - 1) / kKeys * kKeys;
     splits = (K + kps - 1) / kps;
@@ -518,6 +534,10 @@ esa_status launch_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16
     a.Hkv = s.Hkv;
     a.K = K;
     a.hg = plan.hg;
+    a.nsets = plan.nsets;
+    a.hs = plan.hs;
+    a.seg = plan.seg;
+    a.gps = plan.gps;
     a.splits = plan.splits;
     a.kps = plan.keys_per_split;
     a.scale_log2 = scale * 1.4426950408889634f;

@@ -22,12 +22,18 @@ def to_dev(inp: dict) -> dict:
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
+def _sets(sh: dict) -> tuple:
+    """() with one index set per query row, (H_I,) with per-head sets."""
+    return (sh["H_I"],) if sh.get("flags", 0) & 2 else ()
+
+
 def gpu_topk(d: dict, sh: dict, K: int, ws=None):
     m = esa()
     shape = m.shape_from(sh)
     ws = ws or m.workspace_for(m.OP_TOPK_SELECT, shape, K)
-    idx = torch.full((sh["B"], sh["Tq"], K), -7, dtype=torch.int32, device="cuda")
-    cnt = torch.full((sh["B"], sh["Tq"]), -7, dtype=torch.int32, device="cuda")
+    sets = _sets(sh)  # per-head index sets: [B, Tq, H_I, K]
+    idx = torch.full((sh["B"], sh["Tq"], *sets, K), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((sh["B"], sh["Tq"], *sets), -7, dtype=torch.int32, device="cuda")
     m.esa_topk_select(d["qI"], d["kI"], d["wI"], shape, K, idx, cnt, ws)
     st = m.esa_read_status(ws)
     assert st == m.OK, m.status_string(st)
@@ -41,8 +47,9 @@ def gpu_attn(d: dict, sh: dict, K: int, idx, cnt, gate=True, want_lse=True, ws=N
     B, Tq, Hq, D = sh["B"], sh["Tq"], sh["Hq"], sh["D"]
     out = torch.full((B, Tq, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
     lse = torch.full((B, Tq, Hq), float("nan"), dtype=torch.float32, device="cuda") if want_lse else None
-    idx_d = torch.as_tensor(np.asarray(idx, dtype=np.int32)).reshape(B, Tq, K).cuda()
-    cnt_d = torch.as_tensor(np.asarray(cnt, dtype=np.int32)).reshape(B, Tq).cuda()
+    sets = _sets(sh)
+    idx_d = torch.as_tensor(np.asarray(idx, dtype=np.int32)).reshape(B, Tq, *sets, K).cuda()
+    cnt_d = torch.as_tensor(np.asarray(cnt, dtype=np.int32)).reshape(B, Tq, *sets).cuda()
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     m.esa_sparse_attn(d["q"], d["k"], d["v"], idx_d, cnt_d, shape, K, scale, d["g"] if gate else None,
                       d["lin"] if gate else None, out, lse, ws)

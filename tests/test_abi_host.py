@@ -88,6 +88,26 @@ def test_host_validation_rejects_before_launch():
         esa.ERR_WORKSPACE
 
 
+def test_host_validation_of_indexer_flags():
+    """Unknown flag bits are invalid; per-head sets need Hq % H_I == 0 and, for
+    attention, heads per set and heads per key/value head dividing one
+    another; the routed call has one threshold form per row, so it refuses
+    per-head sets. All of it is decided before any launch."""
+    import long_context_sparse_20_b300 as esa
+    L = esa._lib
+    fake = ctypes.c_void_p(0x1000)
+    sh = _shape(esa, flags=4)
+    assert L.esa_topk_select(fake, fake, fake, ctypes.byref(sh), 4, fake, fake, fake, 1 << 20, None) == esa.ERR_INVALID
+    for kw, code in [(dict(Hq=6, Hkv=1, H_I=4), esa.ERR_INVALID),            # 6 % 4
+                     (dict(Hq=12, Hkv=3, H_I=2), esa.ERR_UNSUPPORTED)]:      # 6 heads per set, 4 per KV head
+        sh = _shape(esa, flags=esa.PER_HEAD_SETS, **kw)
+        assert L.esa_sparse_attn(fake, fake, fake, fake, fake, ctypes.byref(sh), 4, 0.125, None, None, fake, None,
+                                 fake, 1 << 20, None) == code, kw
+    sh = _shape(esa, flags=esa.PER_HEAD_SETS, Hq=4, Hkv=4, H_I=2)
+    assert L.esa_routed_attn(fake, fake, fake, fake, fake, fake, fake, ctypes.byref(sh), 4, 0.125, None, None, fake,
+                             fake, 1 << 20, None) == esa.ERR_UNSUPPORTED
+
+
 def test_workspace_size_rejects_bad_shapes():
     import long_context_sparse_20_b300 as esa
     assert esa.esa_workspace_size(esa.OP_TOPK_SELECT, _shape(esa, Tq=9), 4) == 0

@@ -305,6 +305,106 @@ def test_routed_values_beyond_fp16():
     assert (err <= 5e-5 * np.maximum(1.0, np.abs(ref[-1]))).all(), err.max()
 
 
+# ------------------------------------------------------------------ indexer options: ReLU, per-head index sets
+RELU, PER_HEAD = 1, 2
+
+
+@pytest.mark.parametrize("flags", [0, RELU, PER_HEAD, RELU | PER_HEAD])
+def test_indexer_score_modes(flags):
+    """Diagnostic scores: weighted sum (or one head's own score) of the
+    int8 dot products, with the ReLU per head when asked; INT32_MIN past the
+    causal prefix."""
+    m = esa()
+    cfg, sh, inp = _case(seed=500 + flags, B=2, Tq=5, Tk=300, q_offset=295, H_I=3, D_I=32, weights="1to4",
+                         flags=flags)
+    d = to_dev(inp)
+    H = sh["H_I"] if flags & PER_HEAD else 1
+    B, Tq, Tk = sh["B"], sh["Tq"], sh["Tk"]
+    scores = torch.full((B, Tq, H, Tk), 7, dtype=torch.int32, device="cuda")
+    shape = m.shape_from(sh)
+    ws = m.workspace_for(m.OP_INDEXER_SCORE, shape, 1)
+    m.esa_indexer_score(d["qI"], d["kI"], d["wI"], shape, scores, ws)
+    assert m.esa_read_status(ws) == m.OK
+    got = scores.cpu().numpy()
+    for b in range(B):
+        for t in range(Tq):
+            n = sh["q_offset"] + t + 1
+            for h in range(H):
+                ref = O.indexer_row(inp["qI"], inp["kI"], inp["wI"], sh, b, t, relu=bool(flags & RELU),
+                                    head=h if flags & PER_HEAD else -1)
+                assert np.array_equal(got[b, t, h, :n], ref), (b, t, h)
+                assert (got[b, t, h, n:] == np.iinfo(np.int32).min).all()
+
+
+MODE_TOPK_CASES = [
+    # decode, split selection: ReLU on one head; per-head sets (4 single-head rows per query)
+    dict(B=2, Tq=1, Tk=20000, q_offset=19999, top_k=1024, D_I=64, H_I=1, flags=RELU),
+    dict(B=2, Tq=1, Tk=20000, q_offset=19999, top_k=1024, D_I=64, H_I=4, flags=PER_HEAD),
+    dict(B=2, Tq=1, Tk=20000, q_offset=19999, top_k=1024, D_I=64, H_I=4, flags=RELU | PER_HEAD),
+    # decode, ReLU on several heads: the row kernel
+    dict(B=1, Tq=1, Tk=9000, q_offset=8999, top_k=512, D_I=32, H_I=3, weights="1to4", flags=RELU),
+    # prefill: tensor-core rows (ReLU on one head, per-head sets), dp4a rows (ReLU on several heads)
+    dict(B=1, Tq=300, Tk=300, top_k=64, D_I=64, H_I=1, flags=RELU),
+    dict(B=2, Tq=200, Tk=200, top_k=50, D_I=32, H_I=4, weights="1to4", flags=RELU),
+    dict(B=1, Tq=150, Tk=700, q_offset=550, top_k=128, D_I=64, H_I=4, flags=PER_HEAD),
+    dict(B=1, Tq=150, Tk=700, q_offset=550, top_k=128, D_I=64, H_I=4, flags=RELU | PER_HEAD),
+]
+
+
+@pytest.mark.parametrize("over", MODE_TOPK_CASES, ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
+def test_topk_modes(over):
+    cfg, sh, inp = _case(seed=511, **over)
+    K = cfg["top_k"]
+    gi, gc = gpu_topk(to_dev(inp), sh, K)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    assert_idx_equal(gi, gc, oi.reshape(-1, K), oc.reshape(-1))
+
+
+def test_topk_relu_weight_sign():
+    """ReLU on one head with a negative weight: the scores are w * max(0, q.k)
+    (not max(0, w * q.k)), on the tensor cores and in decode."""
+    for over in (dict(B=1, Tq=200, Tk=200, top_k=40), dict(B=2, Tq=1, Tk=12000, q_offset=11999, top_k=300)):
+        cfg, sh, inp = _case(seed=512, D_I=64, H_I=1, flags=RELU, **over)
+        inp["wI"] = torch.tensor([-3], dtype=torch.int32)
+        K = cfg["top_k"]
+        gi, gc = gpu_topk(to_dev(inp), sh, K)
+        oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+        assert_idx_equal(gi, gc, oi.reshape(-1, K), oc.reshape(-1))
+
+
+PER_HEAD_ATTN_CASES = [
+    dict(B=1, Tq=90, Tk=90, Hq=16, Hkv=2, D=128, H_I=16, D_I=32, top_k=30, flags=PER_HEAD),  # a set per query head
+    dict(B=1, Tq=90, Tk=90, Hq=16, Hkv=2, D=128, H_I=4, D_I=32, top_k=30, flags=RELU | PER_HEAD),  # 4 heads per set
+    dict(B=2, Tq=60, Tk=60, Hq=8, Hkv=4, D=64, H_I=2, D_I=16, top_k=20, flags=PER_HEAD),  # a set spans 2 KV heads
+    dict(B=1, Tq=1, Tk=9000, q_offset=8999, Hq=32, Hkv=1, D=128, H_I=4, D_I=64, top_k=2048, flags=PER_HEAD),  # decode
+]
+
+
+@pytest.mark.parametrize("over", PER_HEAD_ATTN_CASES, ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
+def test_attention_per_head_sets(over):
+    """Query head h attends to the index set of indexer head h // (Hq // H_I)."""
+    cfg, sh, inp = _case(seed=513, **over)
+    K = cfg["top_k"]
+    d = to_dev(inp)
+    gi, gc = gpu_topk(d, sh, K)
+    oi, oc, ref, ref_lse = O.gated_sparse_attention(inp, sh, K)
+    assert_idx_equal(gi, gc, oi.reshape(-1, K), oc.reshape(-1))
+    st, out, lse = gpu_attn(d, sh, K, gi, gc)
+    assert st == 0
+    assert_close(out, ref)
+    assert_close(lse, ref_lse, what="lse")
+
+
+def test_routed_relu():
+    """Routed heads with the ReLU indexer: the sparse heads' masks come from
+    the clamped per-head scores (dp4a), the thresholds from the row selection."""
+    cfg, sh, inp = _case(seed=514, routed=True, B=1, Tq=200, Tk=200, Hq=4, Hkv=2, D=128, top_k=30, D_I=64, H_I=2,
+                         weights="1to4", flags=RELU)
+    inp["route"] = torch.tensor([[1, 0, 1, 1]], dtype=torch.uint8)
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, 30)
+    assert_close(gpu_routed(to_dev(inp), sh, 30), ref)
+
+
 # ------------------------------------------------------------------ the five workloads at full size
 def _full(name):
     cfg = E.CONFIGS[name]
@@ -365,6 +465,23 @@ def test_chunked_prefill_full():
     oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
     assert_idx_equal(gi, gc, oi, oc, rows=rows)
     assert (gc == K).all()
+    st, out, _ = gpu_attn(d, sh, K, gi, gc)
+    assert st == 0
+    assert_close(out[rows], ref)
+
+
+def test_per_head_prefill_full():
+    """One ReLU'd index set per query head (16 sets per query row) at
+    S=8192: sampled rows plus edge rows, every head."""
+    cfg, sh, inp = _full("per_head_prefill")
+    K = cfg["top_k"]
+    d = to_dev(inp)
+    gi, gc = gpu_topk(d, sh, K)
+    H = sh["H_I"]
+    rows = sample_rows(sh["B"], sh["Tq"], K, 192, seed=4)
+    oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
+    sel = (rows[:, None] * H + np.arange(H)[None, :]).reshape(-1)
+    assert_idx_equal(gi[sel], gc[sel], oi.reshape(-1, K), oc.reshape(-1))
     st, out, _ = gpu_attn(d, sh, K, gi, gc)
     assert st == 0
     assert_close(out[rows], ref)
