@@ -40,7 +40,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 _GAMMA_U = np.uint64(GAMMA)
 
 # Tensor ids: every tensor of a workload draws from its own stream.
-TID = dict(qI=1, kI=2, wI=3, q=4, k=5, v=6, g=7, lin=8, route=9, needles=10)
+TID = dict(qI=1, kI=2, wI=3, q=4, k=5, v=6, g=7, lin=8, route=9, needles=10, router=11)
 
 _CHUNK = 1 << 22
 _THREADS = max(1, min(16, os.cpu_count() or 1))
@@ -247,6 +247,23 @@ def make_inputs(cfg: dict, seed: int | None = None, p_sparse_bits: bool = True) 
     out["k"] = bf16_tensor(k.reshape(-1), (B, Tk, Hkv, D))
     out["kI"] = torch.from_numpy(kI)
     out["needles"] = npos
+    return out
+
+
+def router_weights(cfg: dict, hidden: int = 64, seed: int | None = None) -> dict:
+    """Seeded weights of the 2-layer attention router (no trained weights
+    exist): W1 fp32 [hidden, Hkv*D] ~ N(0, 1/(Hkv*D)), b1 [hidden] ~ N(0, 1/4),
+    W2 fp32 [2*Hq, hidden] ~ N(0, 1/hidden), b2 [2*Hq] ~ N(0, 1/4), from one
+    SplitMix64 N(0,1) stream (fp64, rounded to fp32) in that order."""
+    seed = cfg["seed"] if seed is None else seed
+    C, Hq = cfg["Hkv"] * cfg["D"], cfg["Hq"]
+    sizes = [hidden * C, hidden, 2 * Hq * hidden, 2 * Hq]
+    z = _normal_f64(seed, TID["router"], 0, sum(sizes))
+    out, o = {}, 0
+    for name, n, sd, shp in (("W1", sizes[0], C ** -0.5, (hidden, C)), ("b1", sizes[1], 0.5, (hidden,)),
+                             ("W2", sizes[2], hidden ** -0.5, (2 * Hq, hidden)), ("b2", sizes[3], 0.5, (2 * Hq,))):
+        out[name] = torch.from_numpy((z[o:o + n] * sd).astype(np.float32).reshape(shp))
+        o += n
     return out
 
 

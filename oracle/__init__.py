@@ -58,6 +58,8 @@ def _bind(path: str):
     lib.oracle_attention_rows.restype = c_int
     lib.oracle_attention_rows.argtypes = [vp, vp, vp, vp, vp, c_int, c_long, c_long, c_long, c_long, c_int, c_int,
                                           c_int, ctypes.c_double, vp, vp, vp, vp, c_long, vp, vp, c_int]
+    lib.oracle_route_heads.restype = c_int
+    lib.oracle_route_heads.argtypes = [vp, c_long, c_long, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp]
     lib.oracle_threshold_row.restype = c_int
     lib.oracle_threshold_row.argtypes = [vp, c_long, c_int, vp, vp]
     return lib
@@ -179,6 +181,22 @@ def gated_sparse_attention(inp: dict, shape: dict, K: int, rows=None, gate=True,
                          g=inp["g"] if gate else None, lin=inp["lin"] if gate else None,
                          route=inp.get("route"), rows=rows, L=L)
     return idx, cnt, out, lse
+
+
+def route_heads(k, shape: dict, W1, b1, W2, b2, L=None):
+    """(route uint8 [B, Hq], margin fp64 [B, Hq]) of the attention router:
+    mean key state over the cache -> ReLU(W1 x + b1) -> W2 h + b2, sparse iff
+    the sparse logit >= the full one; margin = sparse - full logit."""
+    L = L or lib()
+    B, Hq = shape["B"], shape["Hq"]
+    ka = _np(k, np.uint16)
+    w1, bb1, w2, bb2 = (_np(a, np.float32) for a in (W1, b1, W2, b2))
+    F = w1.shape[0]
+    route = np.empty((B, Hq), dtype=np.uint8)
+    margin = np.empty((B, Hq), dtype=np.float64)
+    L.oracle_route_heads(_ptr(ka), B, shape["Tk"], shape["Hkv"], shape["D"], Hq, F, _ptr(w1), _ptr(bb1), _ptr(w2),
+                         _ptr(bb2), _ptr(route), _ptr(margin))
+    return route, margin
 
 
 def threshold(scores: np.ndarray, K: int, L=None):

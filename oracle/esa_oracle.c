@@ -288,6 +288,51 @@ int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *
                                       rows, n_rows, out, lse, n_threads);
 }
 
+/*
+ * Attention router (Elastic Attention page, section 2.2: a 2-layer MLP on the
+ * current key hidden states decides, per attention head, full or sparse).
+ * Reading taken: per sequence b the key states are averaged over the Tk
+ * cached positions and concatenated over key/value heads,
+ *   x[c] = (1/Tk) sum_j k[b, j, c / D, c % D],      c < Hkv*D,
+ * then hid[f] = max(0, b1[f] + sum_c W1[f, c] x[c]) for f < F, and for
+ * query head h the logits z_o = b2[2h+o] + sum_f W2[2h+o, f] hid[f]
+ * (o = 0: full, o = 1: sparse); route[b, h] = 1 (sparse) iff z_1 >= z_0.
+ * W1 fp32 [F, Hkv*D], b1 [F], W2 fp32 [2*Hq, F], b2 [2*Hq]; k bf16 bits.
+ * All sums in fp64. margin[b*Hq + h] = z_1 - z_0 (for the test's tie band).
+ */
+int oracle_route_heads(const uint16_t *k, long B, long Tk, int Hkv, int D, int Hq, int F,
+                       const float *W1, const float *b1, const float *W2, const float *b2,
+                       uint8_t *route, double *margin) {
+    const long C = (long)Hkv * D;
+    double *x = (double *)malloc(sizeof(double) * (size_t)C);
+    double *hid = (double *)malloc(sizeof(double) * (size_t)F);
+    for (long b = 0; b < B; b++) {
+        for (long c = 0; c < C; c++) {
+            double acc = 0.0;
+            for (long j = 0; j < Tk; j++) acc += bf16_to_double(k[(b * Tk + j) * C + c]);
+            x[c] = Tk > 0 ? acc / (double)Tk : 0.0;
+        }
+        for (int f = 0; f < F; f++) {
+            double acc = (double)b1[f];
+            for (long c = 0; c < C; c++) acc += (double)W1[(long)f * C + c] * x[c];
+            hid[f] = acc > 0.0 ? acc : 0.0;
+        }
+        for (int h = 0; h < Hq; h++) {
+            double z[2];
+            for (int o = 0; o < 2; o++) {
+                double acc = (double)b2[2 * h + o];
+                for (int f = 0; f < F; f++) acc += (double)W2[(long)(2 * h + o) * F + f] * hid[f];
+                z[o] = acc;
+            }
+            route[b * Hq + h] = (uint8_t)(z[1] >= z[0] ? 1 : 0);
+            if (margin) margin[b * Hq + h] = z[1] - z[0];
+        }
+    }
+    free(x);
+    free(hid);
+    return 0;
+}
+
 /* Threshold form of a row's index set, used to explain parity failures:
  * T = the K-th largest score (or INT32_MIN when p+1 <= K) and the number of
  * positions with score == T that the set holds. Returns 0. */

@@ -399,9 +399,71 @@ def pin_per_head_attention_uses_its_set(L):
         for h in range(2 * s, 2 * s + 2):
             assert np.array_equal(out[:, h], o1[:, h]) and np.array_equal(lse[:, h], l1[:, h]), (s, h)
 
+
+# ------------------------------------------------------------------ attention router
+ROUTER_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "router_tiny.txt")
+
+
+def pin_router_golden(L):
+    """The hand-worked router example of tests/golden/router_tiny.txt."""
+    gv = {}
+    for line in open(ROUTER_GOLDEN):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            key, *rest = line.split()
+            gv[key] = [float(x) for x in rest]
+    k = torch.tensor(gv["k"], dtype=torch.float32).to(torch.bfloat16).reshape(1, 2, 1, 2)
+    sh = dict(B=1, Tk=2, Hkv=1, D=2, Hq=2)
+    W1 = np.array(gv["W1"], dtype=np.float32).reshape(2, 2)
+    W2 = np.array(gv["W2"], dtype=np.float32).reshape(4, 2)
+    route, margin = O.route_heads(k, sh, W1, np.array(gv["b1"], np.float32), W2, np.array(gv["b2"], np.float32), L=L)
+    assert route.reshape(-1).tolist() == [int(x) for x in gv["route"]], route
+    assert np.allclose(margin.reshape(-1), gv["margin"], atol=0, rtol=0), margin
+
+
+def _router_case(seed, B=2, Tk=37, Hkv=2, D=16, Hq=4, F=8):
+    rng = np.random.default_rng(seed)
+    k = torch.from_numpy(rng.standard_normal((B, Tk, Hkv, D)).astype(np.float32) + 0.5).to(torch.bfloat16)
+    C = Hkv * D
+    W = dict(W1=rng.standard_normal((F, C)).astype(np.float32), b1=rng.standard_normal(F).astype(np.float32),
+             W2=rng.standard_normal((2 * Hq, F)).astype(np.float32), b2=rng.standard_normal(2 * Hq).astype(np.float32))
+    return k, dict(B=B, Tk=Tk, Hkv=Hkv, D=D, Hq=Hq), W
+
+
+def pin_router_numpy(L):
+    """numpy: mean over positions, matrix products, elementwise maximum."""
+    for seed in (1, 2, 3):
+        k, sh, W = _router_case(seed)
+        route, margin = O.route_heads(k, sh, W["W1"], W["b1"], W["W2"], W["b2"], L=L)
+        x = k.to(torch.float64).numpy().reshape(sh["B"], sh["Tk"], -1).mean(axis=1)
+        hid = np.maximum(x @ W["W1"].astype(np.float64).T + W["b1"], 0.0)
+        z = (hid @ W["W2"].astype(np.float64).T + W["b2"]).reshape(sh["B"], sh["Hq"], 2)
+        assert np.allclose(margin, z[..., 1] - z[..., 0], rtol=1e-12, atol=1e-12)
+        assert np.array_equal(route, (z[..., 1] >= z[..., 0]).astype(np.uint8))
+
+
+def pin_router_closed_forms(L):
+    """W1 = 0: hid = max(0, b1) whatever the keys; equal full and sparse rows
+    tie and go sparse; permuting the cached positions changes nothing."""
+    k, sh, W = _router_case(7)
+    W0 = dict(W, W1=np.zeros_like(W["W1"]))
+    r0, m0 = O.route_heads(k, sh, W0["W1"], W0["b1"], W0["W2"], W0["b2"], L=L)
+    hid = np.maximum(W["b1"].astype(np.float64), 0.0)
+    z = (W["W2"].astype(np.float64) @ hid + W["b2"]).reshape(sh["Hq"], 2)
+    assert np.allclose(m0, np.broadcast_to(z[:, 1] - z[:, 0], m0.shape), rtol=1e-12, atol=1e-12)
+    Wt = dict(W)
+    Wt["W2"] = np.repeat(W["W2"][0::2], 2, axis=0)
+    Wt["b2"] = np.repeat(W["b2"][0::2], 2)
+    rt, mt = O.route_heads(k, sh, Wt["W1"], Wt["b1"], Wt["W2"], Wt["b2"], L=L)
+    assert (mt == 0).all() and (rt == 1).all()
+    perm = torch.from_numpy(np.random.default_rng(8).permutation(sh["Tk"]))
+    r1, m1 = O.route_heads(k, sh, W["W1"], W["b1"], W["W2"], W["b2"], L=L)
+    r2, m2 = O.route_heads(k[:, perm].contiguous(), sh, W["W1"], W["b1"], W["W2"], W["b2"], L=L)
+    assert np.allclose(m1, m2, rtol=1e-12, atol=1e-12) and np.array_equal(r1, r2)
+
 ALL_PINS = [pin_indexer_golden, pin_indexer_numpy, pin_indexer_onehot, pin_indexer_bound,
             pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special, pin_topk_needles,
             pin_attention_full_is_sdpa, pin_attention_sparse_is_masked_sdpa, pin_attention_closed_forms,
             pin_empty_set, pin_gate, pin_routing, pin_needles_closed_form,
             pin_indexer_modes_golden, pin_relu_special_and_numpy, pin_per_head_sets_are_sliced_queries,
-            pin_per_head_attention_uses_its_set]
+            pin_per_head_attention_uses_its_set, pin_router_golden, pin_router_numpy, pin_router_closed_forms]

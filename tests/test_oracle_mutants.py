@@ -31,6 +31,11 @@ MUTANTS = {
     "per-head score weighted": ("if (head >= 0) s += dot;", "if (head >= 0) s += (int64_t)wI[h] * dot;"),
     "per-head set scored by every head": ("if (head >= 0 && h != head) continue;", ";"),
     "query head reads the wrong set": ("long set = r * nsets + h / (Hq / nsets);", "long set = r * nsets + h % nsets;"),
+    "router sums instead of averaging": ("x[c] = Tk > 0 ? acc / (double)Tk : 0.0;", "x[c] = acc;"),
+    "router without its ReLU": ("hid[f] = acc > 0.0 ? acc : 0.0;", "hid[f] = acc;"),
+    "router decision flipped": ("route[b * Hq + h] = (uint8_t)(z[1] >= z[0] ? 1 : 0);", "route[b * Hq + h] = (uint8_t)(z[0] >= z[1] ? 1 : 0);"),
+    "router ties go full": ("route[b * Hq + h] = (uint8_t)(z[1] >= z[0] ? 1 : 0);", "route[b * Hq + h] = (uint8_t)(z[1] > z[0] ? 1 : 0);"),
+    "router reads the first position only": ("for (long j = 0; j < Tk; j++) acc += bf16_to_double(k[(b * Tk + j) * C + c]);", "for (long j = 0; j < 1; j++) acc += bf16_to_double(k[(b * Tk + j) * C + c]) * (double)Tk;"),
 }
 
 
