@@ -238,6 +238,19 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
             nsparse = B * Hq - nfull
             flops = 4.0 * D * (nfull * causal_pairs + nsparse * sel_pairs)
             entry.update({"full_heads": nfull, "sparse_heads": nsparse, "kernels_ms": {"routed_attn": ms}})
+            # the attention router on the same keys (seeded weights, hidden 64):
+            # bound by one read of k
+            W = {n: t.to(dev) for n, t in E.router_weights(cfg).items()}
+            wsr = esa.workspace_for(esa.OP_ROUTE_HEADS, shape, 1, dev)
+            rt = torch.empty(B, Hq, dtype=torch.uint8, device=dev)
+            ms_r = timed(lambda: esa.esa_route_heads(d["k"], W["W1"], W["b1"], W["W2"], W["b2"], shape, rt, None, wsr,
+                                                     st))
+            assert esa.esa_read_status(wsr, st) == 0
+            rbytes = B * sh["Tk"] * sh["Hkv"] * D * 2 + sum(t.numel() * 4 for t in W.values()) + B * Hq
+            hbm_peak = _load_peaks()[0]
+            entry["router"] = {"ms": ms_r, "algorithmic_bytes": rbytes, "GB_per_s": rbytes / (ms_r / 1e3) / 1e9,
+                               "frac_of_hbm": rbytes / (ms_r / 1e3) / 1e9 / hbm_peak, "peak_kind": kind,
+                               "sparse_heads_routed": int(rt.sum().item())}
         else:
             wsel = esa.workspace_for(esa.OP_TOPK_SELECT, shape, K, dev)
             watt = esa.workspace_for(esa.OP_SPARSE_ATTN, shape, K, dev)

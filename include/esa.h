@@ -124,6 +124,7 @@ typedef struct esa_shape {
 #define ESA_OP_SPARSE_ATTN 2
 #define ESA_OP_GATED_MIX 3
 #define ESA_OP_ROUTED_ATTN 4
+#define ESA_OP_ROUTE_HEADS 5
 
 /* Bytes of workspace that `op` needs for shape `s` and `top_k` (0 when the
  * op needs none beyond the status word, which every op may write; the
@@ -194,6 +195,24 @@ ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const u
                            const int8_t *kI, const int32_t *wI, const uint8_t *route, const esa_shape *s, int top_k,
                            float scale, const float *g, const uint16_t *lin, float *out, void *ws, size_t ws_bytes,
                            void *stream);
+
+/* Attention router (Elastic Attention page, section 2.2: a lightweight
+ * 2-layer MLP on the current key hidden states decides, per attention head,
+ * full or sparse attention; its decisions are the routing metadata of
+ * esa_routed_attn). Per sequence b, with C = Hkv*D:
+ *   x[c]   = (1/Tk) * sum_{j<Tk} k[b, j, c/D, c%D]         (mean key state)
+ *   hid[f] = max(0, b1[f] + sum_c W1[f, c] * x[c])          f < hidden
+ *   z_o    = b2[2h+o] + sum_f W2[2h+o, f] * hid[f]           o = 0 full, 1 sparse
+ *   route[b, h] = 1 (sparse) iff z_1 >= z_0, else 0 (full); margin[b, h] = z_1 - z_0.
+ * k bf16 [B, Tk, Hkv, D]; W1 fp32 [hidden, C]; b1 fp32 [hidden]; W2 fp32
+ * [2*Hq, hidden]; b2 fp32 [2*Hq]; route uint8 [B, Hq]; margin fp32 [B, Hq]
+ * or NULL. hidden in 1..4096 and (C + hidden) * 4 bytes of shared memory per
+ * block. Sums in fp32 in a fixed order: the same inputs give the same bits
+ * on every call. Device memory owned by the caller; workspace
+ * esa_workspace_size(ESA_OP_ROUTE_HEADS, s, hidden) bytes. */
+ESA_API esa_status esa_route_heads(const uint16_t *k, const float *W1, const float *b1, const float *W2,
+                                   const float *b2, const esa_shape *s, int hidden, uint8_t *route, float *margin,
+                                   void *ws, size_t ws_bytes, void *stream);
 
 /* Top-K selection without a caller workspace. The pages have no counterpart
  * to this call: it is a convenience of this library.

@@ -23,7 +23,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_INDEX, ERR_WORKSPACE, ERR_INTERNAL = range(8)
-OP_INDEXER_SCORE, OP_TOPK_SELECT, OP_SPARSE_ATTN, OP_GATED_MIX, OP_ROUTED_ATTN = range(5)
+OP_INDEXER_SCORE, OP_TOPK_SELECT, OP_SPARSE_ATTN, OP_GATED_MIX, OP_ROUTED_ATTN, OP_ROUTE_HEADS = range(6)
 INDEXER_RELU, PER_HEAD_SETS = 1, 2  # esa_shape.flags
 
 
@@ -52,6 +52,7 @@ _SIGS = {
     "esa_routed_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp,
                                _vp, _sz, _vp]),
     "esa_topk_select_noalloc": (_i32, [_vp, _vp, _vp, _sp, ctypes.c_int, _vp, _vp, _vp, _vp]),
+    "esa_route_heads": (_i32, [_vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, _vp, _vp, _vp, _sz, _vp]),
     "esa_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "esa_status_string": (ctypes.c_char_p, [_i32]),
 }
@@ -164,6 +165,12 @@ def esa_routed_attn(q, k, v, qI, kI, wI, route, shape: esa_shape, top_k: int, sc
     _check(_lib.esa_routed_attn(_p(_bits(q)), _p(_bits(k)), _p(_bits(v)), _p(qI), _p(kI), _p(wI), _p(route),
                                 ctypes.byref(shape), top_k, float(scale), _p(g), _p(_bits(lin)), _p(out), ws.ptr,
                                 ws.nbytes, _stream(stream, q)), "esa_routed_attn")
+
+
+def esa_route_heads(k, W1, b1, W2, b2, shape: esa_shape, route, margin, ws: Workspace, stream=None):
+    hidden = int(W1.shape[0])
+    _check(_lib.esa_route_heads(_p(_bits(k)), _p(W1), _p(b1), _p(W2), _p(b2), ctypes.byref(shape), hidden, _p(route),
+                                _p(margin), ws.ptr, ws.nbytes, _stream(stream, k)), "esa_route_heads")
 
 
 def esa_read_status(ws: Workspace, stream=None) -> int:

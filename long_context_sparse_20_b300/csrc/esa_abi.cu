@@ -175,6 +175,10 @@ extern "C" {
 size_t esa_workspace_size(int op, const esa_shape *s, int top_k) {
     bool attn = op == ESA_OP_SPARSE_ATTN || op == ESA_OP_ROUTED_ATTN || op == ESA_OP_GATED_MIX;
     bool index = op == ESA_OP_INDEXER_SCORE || op == ESA_OP_TOPK_SELECT || op == ESA_OP_ROUTED_ATTN;
+    if (op == ESA_OP_ROUTE_HEADS) {
+        if (check_shape(s, true, false) != ESA_OK) return 0;
+        return ws_route_heads(to_shape(s));
+    }
     if (op < 0 || op > 4 || check_shape(s, attn, index) != ESA_OK) return 0;
     if ((op == ESA_OP_TOPK_SELECT || op == ESA_OP_SPARSE_ATTN || op == ESA_OP_ROUTED_ATTN) && top_k <= 0) return 0;
     Shape x = to_shape(s);
@@ -269,6 +273,22 @@ esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t 
     if (x.B * x.Tq == 0) return ESA_OK;
     if ((e = check_ws(ws, ws_bytes, ws_routed(x, top_k)))) return e;
     return launch_routed_attn(q, k, v, qI, kI, wI, route, x, top_k, scale, g, lin, out, ws, (cudaStream_t)stream);
+}
+
+esa_status esa_route_heads(const uint16_t *k, const float *W1, const float *b1, const float *W2, const float *b2,
+                           const esa_shape *s, int hidden, uint8_t *route, float *margin, void *ws, size_t ws_bytes,
+                           void *stream) {
+    esa_status e = check_shape(s, true, false);
+    if (e) return e;
+    if (!k || !W1 || !b1 || !W2 || !b2 || !route) return ESA_ERR_INVALID;
+    if (hidden <= 0 || hidden > 4096) return ESA_ERR_INVALID;
+    if (!aligned16(k)) return ESA_ERR_INVALID;
+    if (s->B > 65535) return ESA_ERR_UNSUPPORTED;
+    const Shape x = to_shape(s);
+    if ((size_t)(x.Hkv * x.D + hidden) * sizeof(float) > device_info().smem_optin) return ESA_ERR_UNSUPPORTED;
+    if (x.B == 0) return ESA_OK;
+    if ((e = check_ws(ws, ws_bytes, ws_route_heads(x)))) return e;
+    return launch_route_heads(k, W1, b1, W2, b2, x, hidden, route, margin, ws, (cudaStream_t)stream);
 }
 
 esa_status esa_read_status(void *ws, void *stream, int32_t *dev_status) {

@@ -140,6 +140,11 @@ esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t
                             const Shape &s, float scale, const float *g, const uint16_t *lin, float *out,
                             void *pp_ws, int32_t *status, cudaStream_t st);
 
+// ---- attention router (full or sparse per head) --------------------------
+size_t ws_route_heads(const Shape &s);
+esa_status launch_route_heads(const uint16_t *k, const float *W1, const float *b1, const float *W2, const float *b2,
+                              const Shape &s, int hidden, uint8_t *route, float *margin, void *ws, cudaStream_t st);
+
 // Wait limit for inter-block waits, in ns (ESA_WAIT_LIMIT_NS overrides) and
 // the count of extra arrivals a barrier waits for (ESA_DEBUG_EXTRA_ARRIVALS;
 // 0 normally — a positive value makes every barrier wait run out, which the

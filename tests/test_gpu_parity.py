@@ -405,6 +405,58 @@ def test_routed_relu():
     assert_close(gpu_routed(to_dev(inp), sh, 30), ref)
 
 
+# ------------------------------------------------------------------ attention router
+def _gpu_route(d_k, sh, W):
+    m = esa()
+    shape = m.shape_from(sh)
+    ws = m.workspace_for(m.OP_ROUTE_HEADS, shape, 1)
+    route = torch.full((sh["B"], sh["Hq"]), 7, dtype=torch.uint8, device="cuda")
+    margin = torch.full((sh["B"], sh["Hq"]), float("nan"), dtype=torch.float32, device="cuda")
+    Wd = {n: t.cuda() for n, t in W.items()}
+    m.esa_route_heads(d_k, Wd["W1"], Wd["b1"], Wd["W2"], Wd["b2"], shape, route, margin, ws)
+    assert m.esa_read_status(ws) == m.OK
+    return route.cpu().numpy(), margin.cpu().numpy()
+
+
+def _check_route(route, margin, oroute, omargin):
+    """Margins within the fp32 error of the sums; route bits equal wherever
+    the oracle's margin is outside that band (inside it both bits are valid)."""
+    band = 1e-4 * (1.0 + np.abs(omargin))
+    assert (np.abs(margin - omargin) <= band).all(), np.abs(margin - omargin).max()
+    decided = np.abs(omargin) > band
+    assert np.array_equal(route[decided], oroute[decided])
+    assert decided.mean() > 0.9
+
+
+@pytest.mark.parametrize("name", ["small", "routed_prefill"])
+def test_route_heads_matches_oracle(name):
+    if name == "small":
+        cfg, sh, inp = _case(seed=515, routed=True, B=2, Tq=300, Tk=300, Hq=8, Hkv=2, D=64)
+        inp["k"] = (inp["k"].float() + 0.4).to(torch.bfloat16)  # a mean key state away from 0
+        W = E.router_weights(cfg, hidden=32)
+    else:
+        cfg, sh, inp = _full("routed_prefill")
+        W = E.router_weights(cfg)
+    route, margin = _gpu_route(inp["k"].cuda(), sh, W)
+    oroute, omargin = O.route_heads(inp["k"], sh, W["W1"], W["b1"], W["W2"], W["b2"])
+    _check_route(route, margin, oroute, omargin)
+    r2, m2 = _gpu_route(inp["k"].cuda(), sh, W)
+    assert np.array_equal(route, r2) and np.array_equal(margin, m2)  # fixed summation order
+
+
+def test_router_drives_routed_attention():
+    """The router's bits are the routed launch's metadata: router -> routed
+    attention, compared with the oracle run on the same bits."""
+    cfg, sh, inp = _case(seed=516, routed=True, B=2, Tq=160, Tk=160, Hq=8, Hkv=8, D=64, top_k=24, D_I=32)
+    W = E.router_weights(cfg, hidden=16)
+    d = to_dev(inp)
+    route, _ = _gpu_route(d["k"], sh, W)
+    d["route"] = torch.from_numpy(route).cuda()
+    inp["route"] = torch.from_numpy(route)
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, 24)
+    assert_close(gpu_routed(d, sh, 24), ref)
+
+
 # ------------------------------------------------------------------ the five workloads at full size
 def _full(name):
     cfg = E.CONFIGS[name]
