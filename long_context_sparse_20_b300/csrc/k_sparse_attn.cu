@@ -65,7 +65,13 @@ struct AttnArgs {
     float scale_log2;
 };
 
-template <int D, int GT>
+// KS (key split; 16-head tiles, one split per index list): warp w takes keys
+// 16w..16w+15 of every 64-key stage for all 16 heads, with its own online
+// softmax over every output column, and the four warps merge (m, l, O)
+// through shared memory at the end: no warp recomputes another's scores.
+// Otherwise the warps that share a head tile score the whole stage and
+// split P V's output columns (the cluster-split decode path).
+template <int D, int GT, bool KS>
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
     constexpr int RS = Cfg<D>::RS;
     constexpr int HT = GT / 16;       // head tiles of 16 heads
@@ -174,6 +180,161 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
         int r = ht * 16 + (lane & 15), col = kk * 16 + (lane >> 4) * 8;
         ldmatrix_x4(smem_u32(Qs + r * RS + col), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
     }
+
+    if constexpr (KS) {
+        static_assert(GT == 16, "key split: one 16-head tile per block");
+        constexpr int DN = D / 8;  // output n-tiles: every column
+        float ok[DN][4];
+#pragma unroll
+        for (int i = 0; i < DN; i++) ok[i][0] = ok[i][1] = ok[i][2] = ok[i][3] = 0.f;
+        float km[2] = {-INFINITY, -INFINITY}, kl[2] = {0.f, 0.f};
+        const int kb = warp * 16;  // this warp's keys within a stage
+        for (int s = 0; s < nstages; s++) {
+            if (s + 1 < nstages) {
+                if ((s + 1) * kKeys - win0 >= kIdxWin) fill_idx((s + 1) * kKeys);
+                load_stage((s + 1) & 1, (s + 1) * kKeys);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            __syncthreads();
+            const uint16_t *Kt = KVs + (s & 1) * 2 * Cfg<D>::TILE;
+            const uint16_t *Vt = Kt + Cfg<D>::TILE;
+            const int kvalid = min(kKeys, nkeys - s * kKeys);
+            float sc[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++) {
+                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < DK; kk += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    const int key = kb + nt * 8 + (lane & 7), col = kk * 16 + (lane >> 3) * 8;
+                    ldmatrix_x4(smem_u32(Kt + key * RS + col), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[nt], qf[kk], b0, b1);
+                    mma_bf16_16816(sc[nt], qf[kk + 1], b2, b3);
+                }
+            }
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++) {
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int key = kb + nt * 8 + 2 * c4 + (e & 1);
+                    const float x = key < kvalid ? sc[nt][e] * a.scale_log2 : -INFINITY;
+                    sc[nt][e] = x;
+                    mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                }
+            }
+            float corr[2];
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                const float mnew = fmaxf(km[r], mx[r]);
+                const float muse = mnew == -INFINITY ? 0.f : mnew;
+                corr[r] = exp2f(km[r] - muse);
+                km[r] = mnew;
+                mx[r] = muse;
+            }
+            float rs[2] = {0.f, 0.f};
+            uint32_t ah[4], al[4];  // P (16 heads x 16 keys) as bf16 hi + lo, A-fragment order
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++) {
+                const float p0 = exp2f(sc[nt][0] - mx[0]), p1 = exp2f(sc[nt][1] - mx[0]);
+                const float p2 = exp2f(sc[nt][2] - mx[1]), p3 = exp2f(sc[nt][3] - mx[1]);
+                rs[0] += p0 + p1;
+                rs[1] += p2 + p3;
+                ah[2 * nt] = pack_bf16(p0, p1);
+                ah[2 * nt + 1] = pack_bf16(p2, p3);
+                al[2 * nt] = pack_bf16(p0 - bf16lo(ah[2 * nt]), p1 - bf16hi(ah[2 * nt]));
+                al[2 * nt + 1] = pack_bf16(p2 - bf16lo(ah[2 * nt + 1]), p3 - bf16hi(ah[2 * nt + 1]));
+            }
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 1);
+                rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 2);
+                kl[r] = kl[r] * corr[r] + rs[r];
+            }
+#pragma unroll
+            for (int dn = 0; dn < DN; dn++) {
+                ok[dn][0] *= corr[0];
+                ok[dn][1] *= corr[0];
+                ok[dn][2] *= corr[1];
+                ok[dn][3] *= corr[1];
+            }
+#pragma unroll
+            for (int dn = 0; dn < DN / 2; dn++) {
+                uint32_t b0, b1, b2, b3;
+                const int key = kb + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int col = dn * 16 + (lane >> 4) * 8;
+                ldmatrix_x4_trans(smem_u32(Vt + key * RS + col), b0, b1, b2, b3);
+                mma_bf16_16816(ok[2 * dn], ah, b0, b1);
+                mma_bf16_16816(ok[2 * dn + 1], ah, b2, b3);
+                mma_bf16_16816(ok[2 * dn], al, b0, b1);
+                mma_bf16_16816(ok[2 * dn + 1], al, b2, b3);
+            }
+            __syncthreads();
+        }
+        // merge the four warps' (m, l, O) through the (now idle) stage buffers
+        if (bad_row) {
+            if (tid == 0) set_status(a.status, ESA_ERR_BAD_INDEX);
+            return;
+        }
+        float *Om = reinterpret_cast<float *>(KVs);  // [4 warps][16 heads][D]
+        float *Mw = Om + 4 * 16 * D, *Lw = Mw + 4 * 16;  // [4][16] each
+#pragma unroll
+        for (int rr = 0; rr < 2; rr++) {
+            const int hr = g8 + rr * 8;
+#pragma unroll
+            for (int dn = 0; dn < DN; dn++)
+                *reinterpret_cast<float2 *>(Om + (warp * 16 + hr) * D + dn * 8 + 2 * c4) =
+                    make_float2(ok[dn][2 * rr], ok[dn][2 * rr + 1]);
+            if (c4 == 0) {
+                Mw[warp * 16 + hr] = km[rr];
+                Lw[warp * 16 + hr] = kl[rr];
+            }
+        }
+        __syncthreads();
+        const bool gated = a.g != nullptr && a.lin != nullptr;
+        constexpr int TPR = kThreads / 16;  // threads per head row
+        constexpr int CPT = D / TPR;        // columns per thread
+        const int hr = tid / TPR, c0 = (tid % TPR) * CPT;
+        if (hr < nh) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < 4; w++) M = fmaxf(M, Mw[w * 16 + hr]);
+            float sw[4], L = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; w++) {
+                sw[w] = Mw[w * 16 + hr] == -INFINITY ? 0.f : exp2f(Mw[w * 16 + hr] - M);
+                L += sw[w] * Lw[w * 16 + hr];
+            }
+            const int h = h0 + hr;
+            const float gh = gated ? a.g[h] : 1.f, inv = L > 0.f ? 1.f / L : 0.f;
+            const long long base = (row * a.Hq + h) * (long long)D;
+#pragma unroll
+            for (int c = 0; c < CPT; c += 2) {
+                float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; w++) {
+                    const float2 t = *reinterpret_cast<const float2 *>(Om + (w * 16 + hr) * D + c0 + c);
+                    v0 = fmaf(sw[w], t.x, v0);
+                    v1 = fmaf(sw[w], t.y, v1);
+                }
+                v0 = L > 0.f ? v0 * inv : 0.f;
+                v1 = L > 0.f ? v1 * inv : 0.f;
+                if (gated) {
+                    const uint32_t lw = *reinterpret_cast<const uint32_t *>(a.lin + base + c0 + c);
+                    v0 = fmaf(gh, v0, (1.0f - gh) * bf16lo(lw));
+                    v1 = fmaf(gh, v1, (1.0f - gh) * bf16hi(lw));
+                }
+                *reinterpret_cast<float2 *>(a.out + base + c0 + c) = make_float2(v0, v1);
+            }
+            if (a.lse && c0 == 0)
+                a.lse[row * a.Hq + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        }
+        return;
+    } else {
 
     float o[DNW][4];
 #pragma unroll
@@ -390,6 +551,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
         if (a.lse && d4 == 0)
             a.lse[row * a.Hq + h] = L > 0.f ? (Mf[i] + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
+    }  // !KS
 }
 
 template <int D, int GT>
@@ -404,17 +566,22 @@ size_t recv_smem(int D, int GT, int S) {
     return (MM * S * D + 3 * MM * S + S + 2 * MM) * 4;
 }
 
-void *attn_kernel(int D, int GT, size_t *smem) {
-    if (D == 64) {
-        if (GT == 16) { *smem = attn_smem<64, 16>(); return (void *)sparse_attn_kernel<64, 16>; }
-        if (GT == 32) { *smem = attn_smem<64, 32>(); return (void *)sparse_attn_kernel<64, 32>; }
-        *smem = attn_smem<64, 64>();
-        return (void *)sparse_attn_kernel<64, 64>;
+void *attn_kernel(int D, int GT, size_t *smem, bool ks = false) {
+    if (ks) {  // key split: 16-head tiles, one split per index list
+        if (D == 64) { *smem = attn_smem<64, 16>(); return (void *)sparse_attn_kernel<64, 16, true>; }
+        *smem = attn_smem<128, 16>();
+        return (void *)sparse_attn_kernel<128, 16, true>;
     }
-    if (GT == 16) { *smem = attn_smem<128, 16>(); return (void *)sparse_attn_kernel<128, 16>; }
-    if (GT == 32) { *smem = attn_smem<128, 32>(); return (void *)sparse_attn_kernel<128, 32>; }
+    if (D == 64) {
+        if (GT == 16) { *smem = attn_smem<64, 16>(); return (void *)sparse_attn_kernel<64, 16, false>; }
+        if (GT == 32) { *smem = attn_smem<64, 32>(); return (void *)sparse_attn_kernel<64, 32, false>; }
+        *smem = attn_smem<64, 64>();
+        return (void *)sparse_attn_kernel<64, 64, false>;
+    }
+    if (GT == 16) { *smem = attn_smem<128, 16>(); return (void *)sparse_attn_kernel<128, 16, false>; }
+    if (GT == 32) { *smem = attn_smem<128, 32>(); return (void *)sparse_attn_kernel<128, 32, false>; }
     *smem = attn_smem<128, 64>();
-    return (void *)sparse_attn_kernel<128, 64>;
+    return (void *)sparse_attn_kernel<128, 64, false>;
 }
 
 // Shared-memory opt-in and non-portable cluster sizes, once per kernel and device.
@@ -505,6 +672,7 @@ AttnPlan plan_sparse_attn(const Shape &s, int K) {
     }
     p.smem = base + recv_smem(s.D, gt, splits);
     p.splits = splits;
+    p.ks = splits == 1 && gt == 16;  // each block owns its whole index list: split the keys over the warps
     p.keys_per_split = kps;
     p.grid = units * p.hg * splits;
     p.ws_bytes = kStatusBytes;
@@ -542,7 +710,7 @@ esa_status launch_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16
     a.kps = plan.keys_per_split;
     a.scale_log2 = scale * 1.4426950408889634f;
     size_t base = 0;
-    void *fn = attn_kernel(s.D, plan.gt, &base);
+    void *fn = attn_kernel(s.D, plan.gt, &base, plan.ks);
     const size_t smem = plan.smem;
     if (!prepare_attn(fn, smem)) return ESA_ERR_CUDA;
     void *args[] = {(void *)&a};
