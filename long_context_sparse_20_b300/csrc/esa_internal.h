@@ -103,7 +103,7 @@ struct AttnPlan {
     int hs;      // query heads per index set
     int seg;     // heads of one key/value head sharing one index set
     int gps;     // head groups per segment
-    bool ks;     // key-split kernel (one split, 16-head tiles)
+    int var;     // kernel variant: 0 column split, 1 key split (16-head tiles), 2 keys as rows (<= 8 heads)
     int splits;  // key splits per (row, kv head, head group)
     int keys_per_split;
     long long grid;

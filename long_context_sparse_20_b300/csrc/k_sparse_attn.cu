@@ -65,16 +65,23 @@ struct AttnArgs {
     float scale_log2;
 };
 
-// KS (key split; 16-head tiles, one split per index list): warp w takes keys
-// 16w..16w+15 of every 64-key stage for all 16 heads, with its own online
-// softmax over every output column, and the four warps merge (m, l, O)
-// through shared memory at the end: no warp recomputes another's scores.
-// Otherwise the warps that share a head tile score the whole stage and
-// split P V's output columns (the cluster-split decode path).
-template <int D, int GT, bool KS>
+// Variants (one split per index list for the key-split ones):
+//  kColSplit  the warps that share a head tile score the whole stage and
+//             split P V's output columns (the cluster-split decode path);
+//  kKeySplit  (16-head tiles) warp w takes keys 16w..16w+15 of every 64-key
+//             stage for all 16 heads with its own online softmax over every
+//             output column; the four warps merge (m, l, O) through shared
+//             memory at the end: no warp recomputes another's scores;
+//  kKeyRows   (at most 8 heads) the same split with the keys as the MMA
+//             rows: S^T = K Q^T (16 keys x 8 heads) and O^T = V^T P^T (D x 8
+//             heads), P^T's fragments by movmatrix transposes — no padded
+//             head rows when a key/value head serves 8 query heads or fewer.
+enum { kColSplit = 0, kKeySplit = 1, kKeyRows = 2 };
+template <int D, int GT, int VAR>
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
+    constexpr bool KS = VAR == kKeySplit;
     constexpr int RS = Cfg<D>::RS;
-    constexpr int HT = GT / 16;       // head tiles of 16 heads
+    constexpr int HT = GT >= 16 ? GT / 16 : 1;  // head tiles of 16 heads
     constexpr int WPH = 4 / HT;       // warps per head tile: they split the output columns
     constexpr int NT = kKeys / 8;     // n-tiles of 8 keys (every warp scores the whole stage)
     constexpr int DK = D / 16;        // k-steps over the head dim
@@ -174,6 +181,155 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
     cp_async_wait<0>();  // Q tile (and maybe stage 0)
     __syncthreads();
 
+    if constexpr (VAR == kKeyRows) {
+        static_assert(GT == 8, "keys as rows: 8 heads per block");
+        constexpr int MT = D / 16;  // O^T m-tiles (16 output columns each)
+        // Q^T as the B operand (k = head dim, n = head): lane holds
+        // Q[g8][16kk + 2c4 ..] (qb[kk][0]) and Q[g8][16kk + 8 + 2c4 ..] (qb[kk][1])
+        uint32_t qb[DK][2];
+#pragma unroll
+        for (int k2 = 0; k2 < DK / 2; k2++)
+            ldmatrix_x4(smem_u32(Qs + (lane & 7) * RS + k2 * 32 + (lane >> 3) * 8), qb[2 * k2][0], qb[2 * k2][1],
+                        qb[2 * k2 + 1][0], qb[2 * k2 + 1][1]);
+        float ot[MT][4];  // O^T: (column 16mt + g8 (+8), heads 2c4, 2c4+1)
+#pragma unroll
+        for (int i = 0; i < MT; i++) ot[i][0] = ot[i][1] = ot[i][2] = ot[i][3] = 0.f;
+        float km[2] = {-INFINITY, -INFINITY}, kl[2] = {0.f, 0.f};  // heads 2c4, 2c4+1
+        const int kb = warp * 16;  // this warp's keys within a stage
+        for (int s = 0; s < nstages; s++) {
+            if (s + 1 < nstages) {
+                if ((s + 1) * kKeys - win0 >= kIdxWin) fill_idx((s + 1) * kKeys);
+                load_stage((s + 1) & 1, (s + 1) * kKeys);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            __syncthreads();
+            const uint16_t *Kt = KVs + (s & 1) * 2 * Cfg<D>::TILE;
+            const uint16_t *Vt = Kt + Cfg<D>::TILE;
+            const int kvalid = min(kKeys, nkeys - s * kKeys);
+            // S^T (keys kb+g8, kb+g8+8) x (heads 2c4, 2c4+1)
+            float st[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < DK; kk++) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(smem_u32(Kt + (kb + (lane & 15)) * RS + kk * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+                const uint32_t af[4] = {a0, a1, a2, a3};
+                mma_bf16_16816(st, af, qb[kk][0], qb[kk][1]);
+            }
+            const bool in0 = kb + g8 < kvalid, in1 = kb + g8 + 8 < kvalid;
+            st[0] = in0 ? st[0] * a.scale_log2 : -INFINITY;
+            st[1] = in0 ? st[1] * a.scale_log2 : -INFINITY;
+            st[2] = in1 ? st[2] * a.scale_log2 : -INFINITY;
+            st[3] = in1 ? st[3] * a.scale_log2 : -INFINITY;
+            float mx[2] = {fmaxf(st[0], st[2]), fmaxf(st[1], st[3])};
+            float corr[2];
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+#pragma unroll
+                for (int d = 4; d < 32; d <<= 1) mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], d));
+                const float mnew = fmaxf(km[e], mx[e]);
+                const float muse = mnew == -INFINITY ? 0.f : mnew;
+                corr[e] = exp2f(km[e] - muse);
+                km[e] = mnew;
+                mx[e] = muse;
+            }
+            const float p0 = exp2f(st[0] - mx[0]), p1 = exp2f(st[1] - mx[1]);
+            const float p2 = exp2f(st[2] - mx[0]), p3 = exp2f(st[3] - mx[1]);
+            float rs[2] = {p0 + p2, p1 + p3};
+#pragma unroll
+            for (int e = 0; e < 2; e++) {
+#pragma unroll
+                for (int d = 4; d < 32; d <<= 1) rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], d);
+                kl[e] = kl[e] * corr[e] + rs[e];
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; mt++) {
+                ot[mt][0] *= corr[0];
+                ot[mt][1] *= corr[1];
+                ot[mt][2] *= corr[0];
+                ot[mt][3] *= corr[1];
+            }
+            // P^T as the B operand (k = key, n = head), bf16 hi + lo: the two
+            // 8x8 (key, head) blocks of P transposed in registers
+            const uint32_t ph0 = pack_bf16(p0, p1), ph1 = pack_bf16(p2, p3);
+            const uint32_t pl0 = pack_bf16(p0 - bf16lo(ph0), p1 - bf16hi(ph0));
+            const uint32_t pl1 = pack_bf16(p2 - bf16lo(ph1), p3 - bf16hi(ph1));
+            const uint32_t bh0 = movmatrix_trans(ph0), bh1 = movmatrix_trans(ph1);
+            const uint32_t bl0 = movmatrix_trans(pl0), bl1 = movmatrix_trans(pl1);
+#pragma unroll
+            for (int mt = 0; mt < MT; mt++) {
+                uint32_t a0, a1, a2, a3;  // V^T: (columns 16mt.., keys kb..)
+                ldmatrix_x4_trans(smem_u32(Vt + (kb + (lane & 7) + ((lane >> 4) & 1) * 8) * RS + mt * 16 +
+                                           ((lane >> 3) & 1) * 8),
+                                  a0, a1, a2, a3);
+                const uint32_t af[4] = {a0, a1, a2, a3};
+                mma_bf16_16816(ot[mt], af, bh0, bh1);
+                mma_bf16_16816(ot[mt], af, bl0, bl1);
+            }
+            __syncthreads();
+        }
+        if (bad_row) {
+            if (tid == 0) set_status(a.status, ESA_ERR_BAD_INDEX);
+            return;
+        }
+        // merge the four warps' (m, l, O) through the idle stage buffers
+        float *Om = reinterpret_cast<float *>(KVs);  // [4 warps][8 heads][D]
+        float *Mw = Om + 4 * 8 * D, *Lw = Mw + 4 * 8;  // [4][8] each
+#pragma unroll
+        for (int mt = 0; mt < MT; mt++) {
+            Om[(warp * 8 + 2 * c4) * D + mt * 16 + g8] = ot[mt][0];
+            Om[(warp * 8 + 2 * c4 + 1) * D + mt * 16 + g8] = ot[mt][1];
+            Om[(warp * 8 + 2 * c4) * D + mt * 16 + g8 + 8] = ot[mt][2];
+            Om[(warp * 8 + 2 * c4 + 1) * D + mt * 16 + g8 + 8] = ot[mt][3];
+        }
+        if (g8 == 0) {
+            Mw[warp * 8 + 2 * c4] = km[0];
+            Mw[warp * 8 + 2 * c4 + 1] = km[1];
+            Lw[warp * 8 + 2 * c4] = kl[0];
+            Lw[warp * 8 + 2 * c4 + 1] = kl[1];
+        }
+        __syncthreads();
+        const bool gated = a.g != nullptr && a.lin != nullptr;
+        constexpr int TPR = kThreads / 8;  // threads per head
+        constexpr int CPT = D / TPR;       // columns per thread
+        const int hr = tid / TPR, c0 = (tid % TPR) * CPT;
+        if (hr < nh) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < 4; w++) M = fmaxf(M, Mw[w * 8 + hr]);
+            float sw[4], L = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; w++) {
+                sw[w] = Mw[w * 8 + hr] == -INFINITY ? 0.f : exp2f(Mw[w * 8 + hr] - M);
+                L += sw[w] * Lw[w * 8 + hr];
+            }
+            const int h = h0 + hr;
+            const float gh = gated ? a.g[h] : 1.f, inv = L > 0.f ? 1.f / L : 0.f;
+            const long long base = (row * a.Hq + h) * (long long)D;
+#pragma unroll
+            for (int c = 0; c < CPT; c += 2) {
+                float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; w++) {
+                    const float2 t = *reinterpret_cast<const float2 *>(Om + (w * 8 + hr) * D + c0 + c);
+                    v0 = fmaf(sw[w], t.x, v0);
+                    v1 = fmaf(sw[w], t.y, v1);
+                }
+                v0 = L > 0.f ? v0 * inv : 0.f;
+                v1 = L > 0.f ? v1 * inv : 0.f;
+                if (gated) {
+                    const uint32_t lw = *reinterpret_cast<const uint32_t *>(a.lin + base + c0 + c);
+                    v0 = fmaf(gh, v0, (1.0f - gh) * bf16lo(lw));
+                    v1 = fmaf(gh, v1, (1.0f - gh) * bf16hi(lw));
+                }
+                *reinterpret_cast<float2 *>(a.out + base + c0 + c) = make_float2(v0, v1);
+            }
+            if (a.lse && c0 == 0)
+                a.lse[row * a.Hq + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        }
+        return;
+    } else {
     uint32_t qf[DK][4];
 #pragma unroll
     for (int kk = 0; kk < DK; kk++) {
@@ -552,6 +708,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
             a.lse[row * a.Hq + h] = L > 0.f ? (Mf[i] + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
     }  // !KS
+    }  // !kKeyRows
 }
 
 template <int D, int GT>
@@ -566,22 +723,27 @@ size_t recv_smem(int D, int GT, int S) {
     return (MM * S * D + 3 * MM * S + S + 2 * MM) * 4;
 }
 
-void *attn_kernel(int D, int GT, size_t *smem, bool ks = false) {
-    if (ks) {  // key split: 16-head tiles, one split per index list
-        if (D == 64) { *smem = attn_smem<64, 16>(); return (void *)sparse_attn_kernel<64, 16, true>; }
+void *attn_kernel(int D, int GT, size_t *smem, int var = kColSplit) {
+    if (var == kKeyRows) {  // keys as MMA rows: 8-head blocks, one split per index list
+        if (D == 64) { *smem = attn_smem<64, 8>(); return (void *)sparse_attn_kernel<64, 8, kKeyRows>; }
+        *smem = attn_smem<128, 8>();
+        return (void *)sparse_attn_kernel<128, 8, kKeyRows>;
+    }
+    if (var == kKeySplit) {  // key split: 16-head tiles, one split per index list
+        if (D == 64) { *smem = attn_smem<64, 16>(); return (void *)sparse_attn_kernel<64, 16, kKeySplit>; }
         *smem = attn_smem<128, 16>();
-        return (void *)sparse_attn_kernel<128, 16, true>;
+        return (void *)sparse_attn_kernel<128, 16, kKeySplit>;
     }
     if (D == 64) {
-        if (GT == 16) { *smem = attn_smem<64, 16>(); return (void *)sparse_attn_kernel<64, 16, false>; }
-        if (GT == 32) { *smem = attn_smem<64, 32>(); return (void *)sparse_attn_kernel<64, 32, false>; }
+        if (GT == 16) { *smem = attn_smem<64, 16>(); return (void *)sparse_attn_kernel<64, 16, kColSplit>; }
+        if (GT == 32) { *smem = attn_smem<64, 32>(); return (void *)sparse_attn_kernel<64, 32, kColSplit>; }
         *smem = attn_smem<64, 64>();
-        return (void *)sparse_attn_kernel<64, 64, false>;
+        return (void *)sparse_attn_kernel<64, 64, kColSplit>;
     }
-    if (GT == 16) { *smem = attn_smem<128, 16>(); return (void *)sparse_attn_kernel<128, 16, false>; }
-    if (GT == 32) { *smem = attn_smem<128, 32>(); return (void *)sparse_attn_kernel<128, 32, false>; }
+    if (GT == 16) { *smem = attn_smem<128, 16>(); return (void *)sparse_attn_kernel<128, 16, kColSplit>; }
+    if (GT == 32) { *smem = attn_smem<128, 32>(); return (void *)sparse_attn_kernel<128, 32, kColSplit>; }
     *smem = attn_smem<128, 64>();
-    return (void *)sparse_attn_kernel<128, 64, false>;
+    return (void *)sparse_attn_kernel<128, 64, kColSplit>;
 }
 
 // Shared-memory opt-in and non-portable cluster sizes, once per kernel and device.
@@ -672,7 +834,19 @@ AttnPlan plan_sparse_attn(const Shape &s, int K) {
     }
     p.smem = base + recv_smem(s.D, gt, splits);
     p.splits = splits;
-    p.ks = splits == 1 && gt == 16;  // each block owns its whole index list: split the keys over the warps
+    // each block owns its whole index list: split the keys over the warps,
+    // with the keys as the MMA rows when a segment has at most 8 heads
+    p.var = kColSplit;
+    if (splits == 1 && seg <= 8) {
+        p.var = kKeyRows;
+        p.gt = 8;
+        p.gps = 1;
+        p.hg = G / seg;
+        attn_kernel(s.D, 8, &base, kKeyRows);
+        p.smem = base;
+    } else if (splits == 1 && gt == 16) {
+        p.var = kKeySplit;
+    }
     p.keys_per_split = kps;
     p.grid = units * p.hg * splits;
     p.ws_bytes = kStatusBytes;
@@ -710,7 +884,7 @@ esa_status launch_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16
     a.kps = plan.keys_per_split;
     a.scale_log2 = scale * 1.4426950408889634f;
     size_t base = 0;
-    void *fn = attn_kernel(s.D, plan.gt, &base, plan.ks);
+    void *fn = attn_kernel(s.D, plan.gt, &base, plan.var);
     const size_t smem = plan.smem;
     if (!prepare_attn(fn, smem)) return ESA_ERR_CUDA;
     void *args[] = {(void *)&a};
