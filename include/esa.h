@@ -206,8 +206,7 @@ ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const u
  *   route[b, h] = 1 (sparse) iff z_1 >= z_0, else 0 (full); margin[b, h] = z_1 - z_0.
  * k bf16 [B, Tk, Hkv, D]; W1 fp32 [hidden, C]; b1 fp32 [hidden]; W2 fp32
  * [2*Hq, hidden]; b2 fp32 [2*Hq]; route uint8 [B, Hq]; margin fp32 [B, Hq]
- * or NULL. hidden in 1..4096 and (C + hidden) * 4 bytes of shared memory per
- * block. Sums in fp32 in a fixed order: the same inputs give the same bits
+ * or NULL. hidden in 1..4096. Sums in fp32 in a fixed order: the same inputs give the same bits
  * on every call. Device memory owned by the caller; workspace
  * esa_workspace_size(ESA_OP_ROUTE_HEADS, s, hidden) bytes. */
 ESA_API esa_status esa_route_heads(const uint16_t *k, const float *W1, const float *b1, const float *W2,

@@ -285,7 +285,6 @@ esa_status esa_route_heads(const uint16_t *k, const float *W1, const float *b1, 
     if (!aligned16(k)) return ESA_ERR_INVALID;
     if (s->B > 65535) return ESA_ERR_UNSUPPORTED;
     const Shape x = to_shape(s);
-    if ((size_t)(x.Hkv * x.D + hidden) * sizeof(float) > device_info().smem_optin) return ESA_ERR_UNSUPPORTED;
     if (x.B == 0) return ESA_OK;
     if ((e = check_ws(ws, ws_bytes, ws_route_heads(x)))) return e;
     return launch_route_heads(k, W1, b1, W2, b2, x, hidden, route, margin, ws, (cudaStream_t)stream);

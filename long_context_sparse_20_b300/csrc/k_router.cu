@@ -10,14 +10,15 @@
 // values), hid = max(0, b1 + W1 x), z_o = b2[2h+o] + W2[2h+o] . hid
 // (o = 0 full, o = 1 sparse), route[b, h] = 1 iff z_1 >= z_0.
 //
-// Two launches, every sum in fp32 in a fixed order (deterministic):
+// Four launches, every sum in fp32 in a fixed order (deterministic):
 //   route_pool_kernel  streams k once (16-byte loads, a warp reads 512
 //                      contiguous bytes per position); block (column block,
 //                      position chunk, sequence) writes its chunk's partial
 //                      column sums to the workspace;
-//   route_mlp_kernel   one block per sequence: sums the chunks in order,
-//                      divides by Tk, then the two layers with one warp per
-//                      output and a fixed shuffle tree.
+//   route_mean_kernel, route_hidden_kernel, route_out_kernel
+//                      the chunks summed in order per column (divided by
+//                      Tk), then the two layers with one warp per output
+//                      and a fixed shuffle tree.
 #include <algorithm>
 
 #include "esa_device.cuh"
@@ -70,50 +71,58 @@ __device__ __forceinline__ float warp_sum_fixed(float v) {
     return v;
 }
 
-__global__ void __launch_bounds__(256) route_mlp_kernel(const float *__restrict__ partial, long long Tk, int C,
-                                                        int chunks, const float *__restrict__ W1,
-                                                        const float *__restrict__ b1, const float *__restrict__ W2,
+// x[b, c] = (sum of the position chunks' partial sums, in chunk order) / Tk
+__global__ void __launch_bounds__(256) route_mean_kernel(const float *__restrict__ partial, float *__restrict__ x,
+                                                         long long Tk, int C, int chunks) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    const long long b = blockIdx.y;
+    if (c >= C) return;
+    float s = 0.f;
+    for (int ch = 0; ch < chunks; ch++) s += partial[(b * chunks + ch) * (long long)C + c];
+    x[b * C + c] = Tk > 0 ? s * (1.f / (float)Tk) : 0.f;
+}
+
+// hid[b, f] = max(0, b1[f] + W1[f] . x[b]): one warp per hidden unit, lanes
+// striding over the inputs, a fixed shuffle tree
+__global__ void __launch_bounds__(256) route_hidden_kernel(const float *__restrict__ x, const float *__restrict__ W1,
+                                                           const float *__restrict__ b1, float *__restrict__ hid, int C,
+                                                           int F) {
+    const int lane = threadIdx.x & 31, f = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const long long b = blockIdx.y;
+    if (f >= F) return;
+    const float *w = W1 + (long long)f * C, *xb = x + b * C;
+    float s = 0.f;
+    for (int c = lane; c < C; c += 32) s = fmaf(w[c], xb[c], s);
+    s = warp_sum_fixed(s) + b1[f];
+    if (lane == 0) hid[b * F + f] = fmaxf(s, 0.f);
+}
+
+// z_o = b2[2h+o] + W2[2h+o] . hid[b]; route = z_1 >= z_0 (one warp per head)
+__global__ void __launch_bounds__(256) route_out_kernel(const float *__restrict__ hid, const float *__restrict__ W2,
                                                         const float *__restrict__ b2, int F, int Hq,
                                                         uint8_t *__restrict__ route, float *__restrict__ margin) {
-    extern __shared__ float sm[];
-    float *x = sm;       // [C]
-    float *hid = sm + C;  // [F]
-    const long long b = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x / 32;
-    const float inv = Tk > 0 ? 1.f / (float)Tk : 0.f;
-    for (int c = tid; c < C; c += blockDim.x) {
-        float s = 0.f;
-        for (int ch = 0; ch < chunks; ch++) s += partial[(b * chunks + ch) * (long long)C + c];
-        x[c] = s * inv;
-    }
-    __syncthreads();
-    for (int f = warp; f < F; f += nw) {
-        const float *w = W1 + (long long)f * C;
-        float s = 0.f;
-        for (int c = lane; c < C; c += 32) s = fmaf(w[c], x[c], s);
-        s = warp_sum_fixed(s) + b1[f];
-        if (lane == 0) hid[f] = fmaxf(s, 0.f);
-    }
-    __syncthreads();
-    for (int h = warp; h < Hq; h += nw) {
-        float z[2];
+    const int lane = threadIdx.x & 31, h = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const long long b = blockIdx.y;
+    if (h >= Hq) return;
+    const float *hb = hid + b * F;
+    float z[2];
 #pragma unroll
-        for (int o = 0; o < 2; o++) {
-            const float *w = W2 + (long long)(2 * h + o) * F;
-            float s = 0.f;
-            for (int f = lane; f < F; f += 32) s = fmaf(w[f], hid[f], s);
-            z[o] = warp_sum_fixed(s) + b2[2 * h + o];
-        }
-        if (lane == 0) {
-            route[b * Hq + h] = z[1] >= z[0] ? 1 : 0;
-            if (margin) margin[b * Hq + h] = z[1] - z[0];
-        }
+    for (int o = 0; o < 2; o++) {
+        const float *w = W2 + (long long)(2 * h + o) * F;
+        float s = 0.f;
+        for (int f = lane; f < F; f += 32) s = fmaf(w[f], hb[f], s);
+        z[o] = warp_sum_fixed(s) + b2[2 * h + o];
+    }
+    if (lane == 0) {
+        route[b * Hq + h] = z[1] >= z[0] ? 1 : 0;
+        if (margin) margin[b * Hq + h] = z[1] - z[0];
     }
 }
 
 struct RoutePlan {
     int chunks;
     long long chunk_len;
+    size_t x_off;  // workspace: [status][partial sums][x: B x C][hid: B x 4096]
     size_t ws_bytes;
 };
 
@@ -127,7 +136,8 @@ RoutePlan plan_route(const Shape &s) {
     chunks = std::max(1ll, std::min(chunks, (s.Tk + 63) / 64));
     p.chunks = (int)chunks;
     p.chunk_len = (s.Tk + chunks - 1) / chunks;
-    p.ws_bytes = kStatusBytes + align256((size_t)s.B * chunks * C * sizeof(float));
+    p.x_off = kStatusBytes + align256((size_t)s.B * chunks * C * sizeof(float));
+    p.ws_bytes = p.x_off + align256((size_t)s.B * C * sizeof(float)) + align256((size_t)s.B * 4096 * sizeof(float));
     return p;
 }
 
@@ -143,10 +153,12 @@ esa_status launch_route_heads(const uint16_t *k, const float *W1, const float *b
     dim3 g1((unsigned)((C + kColsPerBlock - 1) / kColsPerBlock), (unsigned)p.chunks, (unsigned)s.B);
     route_pool_kernel<<<g1, kPoolThreads, 0, st>>>(k, partial, s.Tk, C, p.chunks, p.chunk_len);
     if (cudaGetLastError() != cudaSuccess) return ESA_ERR_CUDA;
-    const size_t smem = (size_t)(C + hidden) * sizeof(float);
-    if (!ensure_smem((const void *)route_mlp_kernel, smem)) return ESA_ERR_CUDA;
-    route_mlp_kernel<<<(unsigned)s.B, 256, smem, st>>>(partial, s.Tk, C, p.chunks, W1, b1, W2, b2, hidden, s.Hq, route,
-                                                       margin);
+    float *x = reinterpret_cast<float *>(static_cast<char *>(ws) + p.x_off);
+    float *hid = x + align256((size_t)s.B * C * sizeof(float)) / sizeof(float);
+    route_mean_kernel<<<dim3((unsigned)((C + 255) / 256), (unsigned)s.B), 256, 0, st>>>(partial, x, s.Tk, C, p.chunks);
+    route_hidden_kernel<<<dim3((unsigned)((hidden + 7) / 8), (unsigned)s.B), 256, 0, st>>>(x, W1, b1, hid, C, hidden);
+    route_out_kernel<<<dim3((unsigned)((s.Hq + 7) / 8), (unsigned)s.B), 256, 0, st>>>(hid, W2, b2, hidden, s.Hq, route,
+                                                                                    margin);
     return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }
 
