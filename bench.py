@@ -47,6 +47,22 @@ def _load_peaks():
     return 6400.0, 1800.0, "fallback"
 
 
+def max_over_ranks(values, world: int, device) -> list:
+    """Per-rank timings reduced to their maximum over all ranks (the whole
+    job ends when its slowest rank does); the identity on one rank."""
+    if world <= 1:
+        return list(values)
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -452,14 +468,10 @@ def esa_arm(args):
         for w in (d["ws_sel"], d["ws_att"]):
             assert esa.esa_read_status(w) == 0
 
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms, e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = tt.tolist()
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], world, dev)
     ms_step = total_ms / args.steps
     tok_per_step = B * world
-    value = tok_per_step / (ms_step / 1e3)
+    value = job_rate(B, world, ms_step)
 
     sel_bytes, att_bytes = decode_bytes(sh, K)
     sel_avg, att_avg = statistics.mean(sel_ms), statistics.mean(att_ms)
@@ -498,7 +510,7 @@ def esa_arm(args):
                               "frac": (sel_bytes + att_bytes) / (ms_step / 1e3) / 1e9 / peak_gbs,
                               "algorithmic_bytes": sel_bytes + att_bytes},
             "gpu_launches": 2 * args.steps,
-            "e2e": {"value": tok_per_step / (e2e_ms / args.steps / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_rate(B, world, e2e_ms / args.steps), "unit": "tok/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps, "timing": e2e_timing},
             "clocks": clocks,
             "cpu_baseline": cpu,
