@@ -60,6 +60,9 @@ def _bind(path: str):
                                           c_int, ctypes.c_double, vp, vp, vp, vp, c_long, vp, vp, c_int]
     lib.oracle_route_heads.restype = c_int
     lib.oracle_route_heads.argtypes = [vp, c_long, c_long, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp]
+    lib.oracle_kda.restype = c_int
+    lib.oracle_kda.argtypes = [vp, vp, vp, vp, vp, vp, c_long, c_long, c_int, c_int, c_int, ctypes.c_double, vp, vp,
+                               c_int]
     lib.oracle_threshold_row.restype = c_int
     lib.oracle_threshold_row.argtypes = [vp, c_long, c_int, vp, vp]
     return lib
@@ -197,6 +200,29 @@ def route_heads(k, shape: dict, W1, b1, W2, b2, L=None):
     L.oracle_route_heads(_ptr(ka), B, shape["Tk"], shape["Hkv"], shape["D"], Hq, F, _ptr(w1), _ptr(bb1), _ptr(w2),
                          _ptr(bb2), _ptr(route), _ptr(margin))
     return route, margin
+
+
+def kda(q, k, v, alpha, beta, state_in=None, scale: float | None = None, L=None):
+    """(o fp64 [B, T, H, Dv], final state fp64 [B, H, Dk, Dv]) of the KDA
+    linear-attention branch: per (sequence, head) the state forgets with
+    alpha_t per key channel, then takes v_t under key k_t with strength beta_t
+    (delta rule), and o_t = scale * S_t^T q_t. q, k bf16 [B, T, H, Dk]; v bf16
+    [B, T, H, Dv]; alpha fp32 [B, T, H, Dk]; beta fp32 [B, T, H]; state_in
+    fp32 [B, H, Dk, Dv] or None (zero). scale defaults to 1/sqrt(Dk)."""
+    L = L or lib()
+    qa, ka, va = _np(q, np.uint16), _np(k, np.uint16), _np(v, np.uint16)
+    B, T, H, Dk = qa.shape
+    Dv = va.shape[-1]
+    aa, ba = _np(alpha, np.float32), _np(beta, np.float32)
+    assert ka.shape == qa.shape and va.shape == (B, T, H, Dv) and aa.shape == qa.shape and ba.shape == (B, T, H)
+    sa = _np(state_in, np.float32)
+    assert sa is None or sa.shape == (B, H, Dk, Dv)
+    o = np.empty((B, T, H, Dv), dtype=np.float64)
+    st = np.empty((B, H, Dk, Dv), dtype=np.float64)
+    sc = 1.0 / math.sqrt(Dk) if scale is None else float(scale)
+    L.oracle_kda(_ptr(qa), _ptr(ka), _ptr(va), _ptr(aa), _ptr(ba), _ptr(sa), B, T, H, Dk, Dv, sc, _ptr(o), _ptr(st),
+                 threads())
+    return o, st
 
 
 def threshold(scores: np.ndarray, K: int, L=None):

@@ -17,6 +17,12 @@
  *    (sparse_attention: indexer_score, topk, gather, softmax(Q K_sel^T/sqrt(d)) V_sel).
  *  - "Elastic Attention：动态路由优化大模型长文本处理", sections 2.2 and 3.1
  *    (per-head routing: a head runs either full or sparse attention).
+ *  - The linear branch: the Gated DSA page, sections 一, 二.3 and 三, names it
+ *    KDA, a gated linear attention kept in most layers that folds the history
+ *    into a recurrent state, and mixes its output with the sparse attention
+ *    output; the page prints no formula, so oracle_kda follows the published
+ *    Kimi Delta Attention recurrence (a delta-rule state update with one
+ *    forgetting factor per key channel).
  *
  * Readings taken where the pages are silent (each is restated in the tests):
  *  the prefix of query position p is keys 0..p inclusive; the indexer is a
@@ -330,6 +336,64 @@ int oracle_route_heads(const uint16_t *k, long B, long Tk, int Hkv, int D, int H
     }
     free(x);
     free(hid);
+    return 0;
+}
+
+/* The linear-attention branch (KDA) whose output is the linear_output of the
+ * gate mix. Per sequence b and head h, a state S of Dk x Dv values (row i: key
+ * channel i; column c: value channel c) starts from state_in (fp32
+ * [B, H, Dk, Dv]) or from zero, and for t = 0 .. T-1:
+ *   forget:  S[i][c] *= alpha_t[i]                (one factor per key channel)
+ *   read:    u[c]  = sum_i k_t[i] S[i][c]          (what S returns for k_t)
+ *   write:   S[i][c] += beta_t k_t[i] (v_t[c] - u[c])   (delta rule)
+ *   output:  o_t[c] = scale * sum_i q_t[i] S[i][c]
+ * q, k bf16 [B, T, H, Dk]; v bf16 [B, T, H, Dv]; alpha fp32 [B, T, H, Dk];
+ * beta fp32 [B, T, H]; o fp64 [B, T, H, Dv]; the final S goes to state_out
+ * (fp64 [B, H, Dk, Dv]) when it is not NULL. Returns 0. */
+int oracle_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
+               const float *state_in, long B, long T, int H, int Dk, int Dv, double scale, double *o,
+               double *state_out, int n_threads) {
+    const long BH = B * H;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#else
+    (void)n_threads;
+#endif
+    for (long bh = 0; bh < BH; bh++) {
+        const long b = bh / H;
+        const int h = (int)(bh % H);
+        double *S = (double *)malloc(sizeof(double) * (size_t)Dk * (size_t)Dv);
+        double *u = (double *)malloc(sizeof(double) * (size_t)Dv);
+        for (int i = 0; i < Dk; i++)
+            for (int c = 0; c < Dv; c++)
+                S[i * Dv + c] = state_in ? (double)state_in[(bh * Dk + i) * Dv + c] : 0.0;
+        for (long t = 0; t < T; t++) {
+            const long row = (b * T + t) * H + h;
+            const uint16_t *kt = k + row * Dk, *qt = q + row * Dk, *vt = v + row * Dv;
+            const float *at = alpha + row * Dk;
+            const double bt = (double)beta[row];
+            for (int i = 0; i < Dk; i++)
+                for (int c = 0; c < Dv; c++) S[i * Dv + c] *= (double)at[i];
+            for (int c = 0; c < Dv; c++) {
+                double acc = 0.0;
+                for (int i = 0; i < Dk; i++) acc += bf16_to_double(kt[i]) * S[i * Dv + c];
+                u[c] = acc;
+            }
+            for (int i = 0; i < Dk; i++)
+                for (int c = 0; c < Dv; c++)
+                    S[i * Dv + c] += bt * bf16_to_double(kt[i]) * (bf16_to_double(vt[c]) - u[c]);
+            for (int c = 0; c < Dv; c++) {
+                double acc = 0.0;
+                for (int i = 0; i < Dk; i++) acc += bf16_to_double(qt[i]) * S[i * Dv + c];
+                o[row * Dv + c] = scale * acc;
+            }
+        }
+        if (state_out)
+            for (long e = 0; e < (long)Dk * Dv; e++) state_out[bh * Dk * Dv + e] = S[e];
+        free(S);
+        free(u);
+    }
     return 0;
 }
 

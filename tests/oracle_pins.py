@@ -8,7 +8,11 @@ AssertionError when the oracle disagrees with:
   * library routines (numpy int64 einsum, numpy lexsort, torch fp64
     scaled_dot_product_attention with a causal or explicit mask);
   * closed forms and invariants (t=0 gives v_0, V=1 gives 1, softmax sums to
-    one, permutation invariance, gate end points and affinity, needles).
+    one, permutation invariance, gate end points and affinity, needles);
+  * for the KDA linear branch: the hand-worked tests/golden/kda_tiny.txt, the
+    full transition-matrix form, the delta rule's retrieval invariant, basis
+    keys (per-row moving averages), orthonormal keys without forgetting
+    (causal linear attention) and state chaining.
 """
 from __future__ import annotations
 
@@ -461,9 +465,156 @@ def pin_router_closed_forms(L):
     r2, m2 = O.route_heads(k[:, perm].contiguous(), sh, W["W1"], W["b1"], W["W2"], W["b2"], L=L)
     assert np.allclose(m1, m2, rtol=1e-12, atol=1e-12) and np.array_equal(r1, r2)
 
+KDA_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "kda_tiny.txt")
+
+
+def _bf(x) -> torch.Tensor:
+    return torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def pin_kda_golden(L):
+    """The two hand-worked KDA examples of tests/golden/kda_tiny.txt."""
+    gv = {}
+    for line in open(KDA_GOLDEN):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            key, *rest = line.split()
+            gv[key] = [float(x) for x in rest]
+    o, st = O.kda(_bf(gv["c1_q"]).reshape(1, 2, 1, 2), _bf(gv["c1_k"]).reshape(1, 2, 1, 2),
+                  _bf(gv["c1_v"]).reshape(1, 2, 1, 1), np.float32(gv["c1_alpha"]).reshape(1, 2, 1, 2),
+                  np.float32(gv["c1_beta"]).reshape(1, 2, 1), scale=1.0, L=L)
+    assert o.reshape(-1).tolist() == gv["c1_o"], o
+    assert st.reshape(-1).tolist() == gv["c1_state"], st
+    o, st = O.kda(_bf(gv["c2_q"]).reshape(1, 1, 1, 2), _bf(gv["c2_k"]).reshape(1, 1, 1, 2),
+                  _bf(gv["c2_v"]).reshape(1, 1, 1, 2), np.float32(gv["c2_alpha"]).reshape(1, 1, 1, 2),
+                  np.float32(gv["c2_beta"]).reshape(1, 1, 1), state_in=np.float32(gv["c2_state_in"]).reshape(1, 1, 2, 2),
+                  scale=0.5, L=L)
+    assert o.reshape(-1).tolist() == gv["c2_o"], o
+    assert st.reshape(-1).tolist() == gv["c2_state"], st
+
+
+def _kda_case(seed, B=2, T=12, H=3, Dk=8, Dv=5, state=True):
+    rng = np.random.default_rng(seed)
+    q = _bf(rng.standard_normal((B, T, H, Dk)) / math.sqrt(Dk))
+    k = rng.standard_normal((B, T, H, Dk))
+    k = _bf(k / np.linalg.norm(k, axis=-1, keepdims=True))
+    v = _bf(rng.standard_normal((B, T, H, Dv)))
+    alpha = rng.uniform(0.5, 1.0, (B, T, H, Dk)).astype(np.float32)
+    beta = rng.uniform(0.0, 1.0, (B, T, H)).astype(np.float32)
+    s0 = rng.standard_normal((B, H, Dk, Dv)).astype(np.float32) if state else None
+    return q, k, v, alpha, beta, s0
+
+
+def _f64(x):
+    return (x.to(torch.float64).numpy() if isinstance(x, torch.Tensor) else np.asarray(x, dtype=np.float64))
+
+
+def pin_kda_transition_matrices(L):
+    """numpy matrix form: S_t = (I - beta_t k_t k_t^T) diag(alpha_t) S_{t-1} +
+    beta_t k_t v_t^T, o_t = scale S_t^T q_t, with the transition built as a
+    full Dk x Dk matrix per step (Dk != Dv, several heads and sequences)."""
+    for seed in (1, 2):
+        q, k, v, alpha, beta, s0 = _kda_case(seed)
+        o, st = O.kda(q, k, v, alpha, beta, state_in=s0, scale=0.7, L=L)
+        qd, kd, vd, ad, bd = (_f64(x) for x in (q, k, v, alpha, beta))
+        B, T, H, Dk = qd.shape
+        for b in range(B):
+            for h in range(H):
+                S = _f64(s0[b, h])
+                for t in range(T):
+                    kk = kd[b, t, h][:, None]
+                    A = (np.eye(Dk) - bd[b, t, h] * (kk @ kk.T)) @ np.diag(ad[b, t, h])
+                    S = A @ S + bd[b, t, h] * kk @ vd[b, t, h][None, :]
+                    assert np.allclose(o[b, t, h], 0.7 * S.T @ qd[b, t, h], rtol=1e-12, atol=1e-12)
+                assert np.allclose(st[b, h], S, rtol=1e-12, atol=1e-12)
+
+
+def pin_kda_retrieval(L):
+    """Delta-rule invariant: with beta_t = 1 and a unit key, the state returns
+    v_t for k_t right after step t, whatever the forgetting factors and the
+    history; so q_t = k_t and scale = 1 give o_t = v_t. The keys are four
+    entries of +-1/2 (exactly unit in bf16)."""
+    rng = np.random.default_rng(5)
+    B, T, H, Dk, Dv = 2, 16, 2, 8, 6
+    q, _, v, alpha, beta, s0 = _kda_case(5, B, T, H, Dk, Dv)
+    kk = np.zeros((B, T, H, Dk))
+    for idx in np.ndindex(B, T, H):
+        pos = rng.choice(Dk, 4, replace=False)
+        kk[idx][pos] = rng.choice([-0.5, 0.5], 4)
+    hit = rng.random((B, T, H)) < 0.5
+    beta = np.where(hit, 1.0, beta).astype(np.float32)
+    k = _bf(kk)
+    qn = torch.where(torch.from_numpy(hit)[..., None], k, q)
+    o, _ = O.kda(qn, k, v, alpha, beta, state_in=s0, scale=1.0, L=L)
+    assert np.allclose(o[hit], _f64(v)[hit], rtol=0, atol=1e-12), np.abs(o[hit] - _f64(v)[hit]).max()
+    assert not np.allclose(o[~hit], _f64(v)[~hit], atol=1e-3)
+
+
+def pin_kda_basis_keys(L):
+    """Keys that are basis vectors e_j make each state row an exponential
+    moving average: every row i decays by alpha_t[i]; row j = key(t) becomes
+    (1 - beta_t) row + beta_t v_t; o_t = scale sum_i q_t[i] row_i. Keys repeat,
+    the initial state is random and Dk != Dv."""
+    rng = np.random.default_rng(9)
+    B, T, H, Dk, Dv = 2, 14, 2, 6, 4
+    q, _, v, alpha, beta, s0 = _kda_case(9, B, T, H, Dk, Dv)
+    j = rng.integers(0, Dk, (B, T, H))
+    k = torch.nn.functional.one_hot(torch.from_numpy(j), Dk).to(torch.bfloat16)
+    o, st = O.kda(q, k, v, alpha, beta, state_in=s0, scale=0.25, L=L)
+    qd, vd = _f64(q), _f64(v)
+    for b in range(B):
+        for h in range(H):
+            rows = _f64(s0[b, h]).copy()
+            for t in range(T):
+                rows *= alpha[b, t, h].astype(np.float64)[:, None]
+                jj = j[b, t, h]
+                bt = float(beta[b, t, h])
+                rows[jj] = (1.0 - bt) * rows[jj] + bt * vd[b, t, h]
+                assert np.allclose(o[b, t, h], 0.25 * (qd[b, t, h][:, None] * rows).sum(0), rtol=1e-12, atol=1e-12)
+            assert np.allclose(st[b, h], rows, rtol=1e-12, atol=1e-12)
+
+
+def pin_kda_linear_attention(L):
+    """No forgetting (alpha = 1), zero initial state and orthonormal keys (rows
+    of a 16 x 16 Hadamard matrix / 4, exact in bf16): nothing stored is ever
+    erased, so o_t = scale sum_{j<=t} beta_j (q_t . k_j) v_j — causal linear
+    attention (torch einsum under a lower-triangular mask)."""
+    rng = np.random.default_rng(13)
+    Hd = np.array([[1.0]])
+    while Hd.shape[0] < 16:
+        Hd = np.block([[Hd, Hd], [Hd, -Hd]])
+    B, T, H, Dk, Dv = 2, 16, 2, 16, 7
+    q, _, v, _, beta, _ = _kda_case(13, B, T, H, Dk, Dv, state=False)
+    kk = np.stack([np.stack([Hd[rng.permutation(16)[:T]] / 4.0 for _ in range(H)], axis=1) for _ in range(B)])
+    k = _bf(kk)
+    alpha = np.ones((B, T, H, Dk), dtype=np.float32)
+    o, _ = O.kda(q, k, v, alpha, beta, scale=0.3, L=L)
+    qt, kt, vt = (x.to(torch.float64) for x in (q, k, v))
+    att = torch.einsum("bthd,bshd->bhts", qt, kt) * torch.from_numpy(beta.astype(np.float64)).permute(0, 2, 1)[:, :, None, :]
+    att = att * torch.tril(torch.ones(T, T, dtype=torch.float64))
+    ref = 0.3 * torch.einsum("bhts,bshc->bthc", att, vt)
+    assert np.allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_kda_chaining(L):
+    """Running T steps at once equals running the first T1 and then the rest
+    from the carried state (chunked prefill, decode); T = 0 hands the initial
+    state straight back."""
+    q, k, v, alpha, beta, s0 = _kda_case(17, T=20)
+    o, st = O.kda(q, k, v, alpha, beta, state_in=s0, L=L)
+    o1, st1 = O.kda(q[:, :7], k[:, :7], v[:, :7], alpha[:, :7], beta[:, :7], state_in=s0, L=L)
+    o2, st2 = O.kda(q[:, 7:], k[:, 7:], v[:, 7:], alpha[:, 7:], beta[:, 7:], state_in=st1.astype(np.float32), L=L)
+    assert np.allclose(o[:, :7], o1, rtol=0, atol=0)
+    assert np.allclose(o[:, 7:], o2, rtol=1e-6, atol=1e-6) and np.allclose(st, st2, rtol=1e-6, atol=1e-6)
+    _, st0 = O.kda(q[:, :0], k[:, :0], v[:, :0], alpha[:, :0], beta[:, :0], state_in=s0, L=L)
+    assert np.array_equal(st0, s0.astype(np.float64))
+
+
 ALL_PINS = [pin_indexer_golden, pin_indexer_numpy, pin_indexer_onehot, pin_indexer_bound,
             pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special, pin_topk_needles,
             pin_attention_full_is_sdpa, pin_attention_sparse_is_masked_sdpa, pin_attention_closed_forms,
             pin_empty_set, pin_gate, pin_routing, pin_needles_closed_form,
             pin_indexer_modes_golden, pin_relu_special_and_numpy, pin_per_head_sets_are_sliced_queries,
-            pin_per_head_attention_uses_its_set, pin_router_golden, pin_router_numpy, pin_router_closed_forms]
+            pin_per_head_attention_uses_its_set, pin_router_golden, pin_router_numpy, pin_router_closed_forms,
+            pin_kda_golden, pin_kda_transition_matrices, pin_kda_retrieval, pin_kda_basis_keys,
+            pin_kda_linear_attention, pin_kda_chaining]

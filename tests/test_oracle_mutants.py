@@ -35,6 +35,20 @@ MUTANTS = {
     "router without its ReLU": ("hid[f] = acc > 0.0 ? acc : 0.0;", "hid[f] = acc;"),
     "router decision flipped": ("route[b * Hq + h] = (uint8_t)(z[1] >= z[0] ? 1 : 0);", "route[b * Hq + h] = (uint8_t)(z[0] >= z[1] ? 1 : 0);"),
     "router ties go full": ("route[b * Hq + h] = (uint8_t)(z[1] >= z[0] ? 1 : 0);", "route[b * Hq + h] = (uint8_t)(z[1] > z[0] ? 1 : 0);"),
+    "KDA forgets along value channels": ("for (int c = 0; c < Dv; c++) S[i * Dv + c] *= (double)at[i];",
+                                         "for (int c = 0; c < Dv; c++) S[i * Dv + c] *= (double)at[c % Dk];"),
+    "KDA forgetting left out": ("for (int c = 0; c < Dv; c++) S[i * Dv + c] *= (double)at[i];", ";"),
+    "KDA erase without beta": ("S[i * Dv + c] += bt * bf16_to_double(kt[i]) * (bf16_to_double(vt[c]) - u[c]);",
+                               "S[i * Dv + c] += bf16_to_double(kt[i]) * (bt * bf16_to_double(vt[c]) - u[c]);"),
+    "KDA adds instead of erasing": ("(bf16_to_double(vt[c]) - u[c])", "(bf16_to_double(vt[c]) + u[c])"),
+    "KDA reads out with the key": ("acc += bf16_to_double(qt[i]) * S[i * Dv + c];", "acc += bf16_to_double(kt[i]) * S[i * Dv + c];"),
+    "KDA output scale dropped": ("o[row * Dv + c] = scale * acc;", "o[row * Dv + c] = acc;"),
+    "KDA initial state transposed": ("(double)state_in[(bh * Dk + i) * Dv + c]", "(double)state_in[(bh * Dv + c) * Dk + i]"),
+    "KDA final state not kept": ("state_out[bh * Dk * Dv + e] = S[e];", "state_out[bh * Dk * Dv + e] = 0.0;"),
+    "KDA heads mixed up": ("const long row = (b * T + t) * H + h;", "const long row = (b * T + t) * H + (H - 1 - h);"),
+    "KDA reads out before the write": (
+        "acc += bf16_to_double(qt[i]) * S[i * Dv + c];",
+        "acc += bf16_to_double(qt[i]) * (S[i * Dv + c] - bt * bf16_to_double(kt[i]) * (bf16_to_double(vt[c]) - u[c]));"),
     "router reads the first position only": ("for (long j = 0; j < Tk; j++) acc += bf16_to_double(k[(b * Tk + j) * C + c]);", "for (long j = 0; j < 1; j++) acc += bf16_to_double(k[(b * Tk + j) * C + c]) * (double)Tk;"),
 }
 
