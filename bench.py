@@ -289,10 +289,109 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
     return res
 
 
+def kda_section(dev, esa, E, reps: int = 3, T: int = 32768) -> dict:
+    """The KDA linear branch (the gate mix's lin input) at the decode shape
+    (8 sequences x 32 heads, one step, 128 x 128 fp32 state per head updated
+    in place) and the long-prefill shape (1 x T steps x 16 heads, zero initial
+    state), timed with CUDA events on the launching stream.
+
+    decode: bound by HBM — each step reads and writes the whole state; 16
+    state buffers rotate (256 MiB > the 126 MB L2); the 16 launches are one
+    CUDA graph, replayed (the per-launch host cost would otherwise hide the
+    ~5 us kernel). Algorithmic bytes: state read + write, the step's q, k, v,
+    alpha, beta, and o (fp32) + lin (bf16).
+    prefill: bound by the fp32 pipes — 7 flops per state element per step
+    (forget 1, read 2, write 2, output 2); peak = 148 SMs x 128 fp32 lanes x
+    2 flops x the maximum SM clock."""
+    peak_gbs, _, kind = _load_peaks()
+    sm_mhz = 2032.0
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        sm_mhz = float(json.load(open(p)).get("sm_max_mhz", sm_mhz))
+    alu_peak = 148 * 128 * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s
+    st = torch.cuda.current_stream(dev)
+    res = {}
+
+    B, H, D, NB = 8, 32, 128, 16
+    x = {k: v.to(dev) for k, v in E.kda_inputs(B, 1, H, D, D, 2002, state=True).items()}
+    states = [x["state"].clone() for _ in range(NB)]
+    o = torch.empty(B, 1, H, D, dtype=torch.float32, device=dev)
+    lin = torch.empty(B, 1, H, D, dtype=torch.bfloat16, device=dev)
+
+    def launch(i):
+        esa.esa_kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=states[i], o=o, lin=lin,
+                    state_out=states[i])
+
+    for i in range(NB):
+        launch(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(NB):
+            launch(i)
+    g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(10):
+            g.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (10 * NB)
+        best = us if best is None else min(best, us)
+    nbytes = 2 * B * H * D * D * 4 + B * H * (2 * D * 2 + D * 2 + D * 4 + 4) + B * H * D * (4 + 2)
+    res["decode"] = {"workload": f"KDA decode: B={B} x 1 step, H={H}, Dk=Dv={D}, state in place",
+                     "us": best, "algorithmic_bytes": nbytes, "GB_per_s": nbytes / (best / 1e6) / 1e9,
+                     "frac_of_hbm": nbytes / (best / 1e6) / 1e9 / peak_gbs, "peak_gbs": peak_gbs, "peak_kind": kind,
+                     "l2": f"{NB} state buffers in rotation ({NB * B * H * D * D * 4 / 2**20:.0f} MiB > 126 MB L2)",
+                     "timing": "CUDA graph of 16 launches, replayed 10 times; best of 3"}
+    del x, states, o, lin, g
+    torch.cuda.empty_cache()
+
+    B, H = 1, 16
+    x = {k: v.to(dev) for k, v in E.kda_inputs(B, T, H, D, D, 2003).items()}
+    o = torch.empty(B, T, H, D, dtype=torch.float32, device=dev)
+    lin = torch.empty(B, T, H, D, dtype=torch.bfloat16, device=dev)
+    so = torch.empty(B, H, D, D, dtype=torch.float32, device=dev)
+
+    def run():
+        esa.esa_kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], o=o, lin=lin, state_out=so)
+
+    run()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        run()
+        e1.record(st)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    flops = 7.0 * B * H * T * D * D
+    res["long_prefill"] = {"workload": f"KDA prefill: B={B} x {T} steps, H={H}, Dk=Dv={D}, zero initial state",
+                           "ms": best, "tok_per_s": B * T / (best / 1e3), "algorithmic_flops": flops,
+                           "achieved_tflops": flops / (best / 1e3) / 1e12, "bound": "alu",
+                           "alu_peak_tflops": alu_peak, "frac_of_alu": flops / (best / 1e3) / 1e12 / alu_peak,
+                           "alu_peak_from": f"148 SMs x 128 fp32 lanes x 2 flops x {sm_mhz:.0f} MHz"}
+    del x, o, lin, so
+    torch.cuda.empty_cache()
+    return res
+
+
 def esa_arm(args):
     world, rank, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.kda_only:  # profiling aid: the KDA linear branch alone
+        sys.path.insert(0, ROOT)
+        import esa_inputs as E
+        import long_context_sparse_20_b300 as esa
+        if rank == 0:
+            print(json.dumps({"linear_branch": kda_section(dev, esa, E, T=args.kda_steps)}), flush=True)
+        return
     if args.prefill_only:  # profiling aid: the prefill workloads alone
         sys.path.insert(0, ROOT)
         import esa_inputs as E
@@ -481,9 +580,11 @@ def esa_arm(args):
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     traffic = _traffic_for("split_select" if dom_is_sel else "sparse_attn", SELECT_SRC if dom_is_sel else ATTN_SRC)
 
-    prefill = None
+    prefill = kda = None
     if rank == 0 and not args.no_prefill:
         prefill = prefill_section(dev, esa, E, seq=args.prefill_seq)
+    if rank == 0 and not args.no_kda:
+        kda = kda_section(dev, esa, E, T=args.kda_steps)
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
@@ -515,6 +616,7 @@ def esa_arm(args):
             "clocks": clocks,
             "cpu_baseline": cpu,
             "prefill": prefill,
+            "linear_branch": kda,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -536,6 +638,9 @@ def main():
     ap.add_argument("--prefill-seq", type=int, default=0, help="override the prefill sequence length (profiling)")
     ap.add_argument("--prefill-names", default="long_prefill,chunked_prefill,per_head_prefill,routed_prefill",
                     help="comma-separated prefill workloads for --prefill-only (profiling)")
+    ap.add_argument("--no-kda", action="store_true", help="skip the KDA linear branch's timings")
+    ap.add_argument("--kda-only", action="store_true", help="time the KDA linear branch alone (profiling)")
+    ap.add_argument("--kda-steps", type=int, default=32768, help="KDA prefill steps (profiling of small cases)")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)

@@ -40,7 +40,8 @@ _M2 = np.uint64(0x94D049BB133111EB)
 _GAMMA_U = np.uint64(GAMMA)
 
 # Tensor ids: every tensor of a workload draws from its own stream.
-TID = dict(qI=1, kI=2, wI=3, q=4, k=5, v=6, g=7, lin=8, route=9, needles=10, router=11)
+TID = dict(qI=1, kI=2, wI=3, q=4, k=5, v=6, g=7, lin=8, route=9, needles=10, router=11,
+           kda_q=12, kda_k=13, kda_v=14, kda_alpha=15, kda_beta=16, kda_state=17)
 
 _CHUNK = 1 << 22
 _THREADS = max(1, min(16, os.cpu_count() or 1))
@@ -264,6 +265,37 @@ def router_weights(cfg: dict, hidden: int = 64, seed: int | None = None) -> dict
                              ("W2", sizes[2], hidden ** -0.5, (2 * Hq, hidden)), ("b2", sizes[3], 0.5, (2 * Hq,))):
         out[name] = torch.from_numpy((z[o:o + n] * sd).astype(np.float32).reshape(shp))
         o += n
+    return out
+
+
+def kda_inputs(B: int, T: int, H: int, Dk: int, Dv: int, seed: int, state: bool = False) -> dict:
+    """Seeded inputs of the KDA linear-attention branch (CPU tensors), shaped
+    like the model's: q, k bf16 [B, T, H, Dk] are N(0,1) vectors scaled to
+    unit length in fp64, then rounded to fp32 and bf16 (the model normalises
+    its queries and keys); v bf16 [B, T, H, Dv] ~ N(0,1); alpha fp32
+    [B, T, H, Dk] uniform in [0.9, 1) as 0.9 + 0.1 * (w >> 11) * 2**-53;
+    beta fp32 [B, T, H] = 1 / (1 + exp(-z)), z ~ N(0,1); with ``state`` also
+    an initial state fp32 [B, H, Dk, Dv] ~ 0.1 N(0,1)."""
+    n = B * T * H * Dk
+
+    def unit(tid):
+        z = _chunked(n, lambda s, c: _normal_f64(seed, TID[tid], s, c), np.empty(n, dtype=np.float64))
+        z = z.reshape(B, T, H, Dk)
+        z /= np.linalg.norm(z, axis=-1, keepdims=True)
+        return torch.from_numpy(z.astype(np.float32)).to(torch.bfloat16)
+
+    def uniform(s, c):
+        return 0.9 + 0.1 * (words(seed, TID["kda_alpha"], s, c) >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+
+    out = dict(q=unit("kda_q"), k=unit("kda_k"),
+               v=bf16_tensor(normal_bf16_bits(seed, TID["kda_v"], B * T * H * Dv), (B, T, H, Dv)))
+    alpha = _chunked(n, uniform, np.empty(n, dtype=np.float64))
+    out["alpha"] = torch.from_numpy(alpha.astype(np.float32).reshape(B, T, H, Dk))
+    zb = _normal_f64(seed, TID["kda_beta"], 0, B * T * H)
+    out["beta"] = torch.from_numpy((1.0 / (1.0 + np.exp(-zb))).astype(np.float32).reshape(B, T, H))
+    if state:
+        zs = _normal_f64(seed, TID["kda_state"], 0, B * H * Dk * Dv)
+        out["state"] = torch.from_numpy((0.1 * zs).astype(np.float32).reshape(B, H, Dk, Dv))
     return out
 
 

@@ -12,7 +12,9 @@
  *   4. a per-head gate mixes that output with a linear-attention branch,
  *      final = g*attn + (1-g)*linear_output (first page, sections 二.3, 四.1);
  *   5. optionally a per-head route sends each head to full causal attention or
- *      to the sparse path inside one launch ("Elastic Attention…", 2.2, 3.1).
+ *      to the sparse path inside one launch ("Elastic Attention…", 2.2, 3.1);
+ *      the route itself comes from a small MLP router (esa_route_heads);
+ *   6. the linear branch that step 4 mixes in: KDA (esa_kda).
  *
  * Conventions shared by every call
  *   - Pointers named as tensors are DEVICE pointers owned by the caller; all
@@ -212,6 +214,37 @@ ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const u
 ESA_API esa_status esa_route_heads(const uint16_t *k, const float *W1, const float *b1, const float *W2,
                                    const float *b2, const esa_shape *s, int hidden, uint8_t *route, float *margin,
                                    void *ws, size_t ws_bytes, void *stream);
+
+/* The linear-attention branch (KDA) whose output is the gate mix's `lin`.
+ * The Gated DSA page (sections 一, 二.3 and 三) keeps KDA, a gated linear
+ * attention that folds the history into a recurrent state, beside the sparse
+ * attention and mixes the two outputs; it prints no formula, and this call
+ * computes the published Kimi Delta Attention recurrence. Per sequence b and
+ * head h, a state S of Dk x Dv values (row i: key channel i) starts from
+ * state_in (or zero when state_in is NULL) and for t = 0 .. T-1:
+ *   S[i][c] *= alpha[b,t,h,i]                         (forgetting, per key channel)
+ *   u[c]     = sum_i k[b,t,h,i] S[i][c]
+ *   S[i][c] += beta[b,t,h] k[b,t,h,i] (v[b,t,h,c] - u[c])   (delta rule)
+ *   o[b,t,h,c] = scale * sum_i q[b,t,h,i] S[i][c]
+ * The final S goes to state_out (NULL: dropped). Chunked prefill and decode
+ * carry the state across calls (state_out may be the same buffer as
+ * state_in); T = 0 copies state_in to state_out.
+ *   q, k   bf16 [B, T, H, Dk]      (the model normally gives unit-norm keys)
+ *   v      bf16 [B, T, H, Dv]
+ *   alpha  fp32 [B, T, H, Dk]      forgetting factors, normally in (0, 1]
+ *   beta   fp32 [B, T, H]          write strengths, normally in [0, 1]
+ *   state_in, state_out  fp32 [B, H, Dk, Dv]
+ *   o      fp32 [B, T, H, Dv] or NULL
+ *   lin    bf16 [B, T, H, Dv] or NULL: o rounded to bf16, the input of
+ *          esa_gated_mix / esa_sparse_attn when H = Hq and Dv = D
+ * Dk in {64, 128}; Dv a multiple of 16 in 16..512 (else ESA_ERR_UNSUPPORTED);
+ * B, H <= 65535. q, k, v, alpha, state_in, state_out and o 16-byte aligned,
+ * lin 8-byte, beta 4-byte (else ESA_ERR_INVALID). o and lin must not overlap
+ * any input. fp32 arithmetic in a fixed order (deterministic); no workspace,
+ * and no device-side error is possible. */
+ESA_API esa_status esa_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                           const float *beta, const float *state_in, int64_t B, int64_t T, int32_t H, int32_t Dk,
+                           int32_t Dv, float scale, float *o, uint16_t *lin, float *state_out, void *stream);
 
 /* Top-K selection without a caller workspace. The pages have no counterpart
  * to this call: it is a convenience of this library.

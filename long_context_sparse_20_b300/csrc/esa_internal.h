@@ -146,6 +146,11 @@ size_t ws_route_heads(const Shape &s);
 esa_status launch_route_heads(const uint16_t *k, const float *W1, const float *b1, const float *W2, const float *b2,
                               const Shape &s, int hidden, uint8_t *route, float *margin, void *ws, cudaStream_t st);
 
+// ---- KDA linear-attention branch ----------------------------------------
+esa_status launch_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
+                      const float *state_in, long long B, long long T, int H, int Dk, int Dv, float scale, float *o,
+                      uint16_t *lin, float *state_out, cudaStream_t st);
+
 // Wait limit for inter-block waits, in ns (ESA_WAIT_LIMIT_NS overrides) and
 // the count of extra arrivals a barrier waits for (ESA_DEBUG_EXTRA_ARRIVALS;
 // 0 normally — a positive value makes every barrier wait run out, which the

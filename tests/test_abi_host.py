@@ -120,3 +120,24 @@ def test_status_strings():
     assert esa.status_string(esa.ERR_TIMEOUT) == "device wait timed out"
     assert esa.status_string(esa.OK) == "ok"
     assert esa.status_string(123) == "unknown status"
+
+
+def test_host_validation_of_kda():
+    import long_context_sparse_20_b300 as esa
+    L = esa._lib
+    f = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails (or returns) first
+    mis = ctypes.c_void_p(0x1008)
+
+    def call(q=f, k=f, v=f, a=f, b=f, s_in=None, B=1, T=4, H=2, Dk=128, Dv=128, o=f, lin=None, s_out=None):
+        return L.esa_kda(q, k, v, a, b, s_in, B, T, H, Dk, Dv, 0.1, o, lin, s_out, None)
+
+    assert call(Dk=96) == esa.ERR_UNSUPPORTED
+    assert call(Dv=24) == esa.ERR_UNSUPPORTED and call(Dv=1024) == esa.ERR_UNSUPPORTED
+    assert call(H=0) == esa.ERR_INVALID and call(T=-1) == esa.ERR_INVALID
+    assert call(B=70000) == esa.ERR_UNSUPPORTED
+    assert call(q=None) == esa.ERR_INVALID and call(b=None) == esa.ERR_INVALID
+    assert call(k=mis) == esa.ERR_INVALID and call(o=mis) == esa.ERR_INVALID and call(s_out=mis) == esa.ERR_INVALID
+    assert call(lin=ctypes.c_void_p(0x1004)) == esa.ERR_INVALID
+    # nothing to do: no launch
+    assert call(B=0) == esa.OK
+    assert call(q=None, k=None, v=None, a=None, b=None, T=0) == esa.OK
