@@ -29,6 +29,8 @@
 //     64-byte rows (state_out may alias state_in: each block owns its tile).
 // Every sum is fp32 in a fixed order, so results are deterministic.
 #include <algorithm>
+#include <mutex>
+#include <set>
 
 #include "esa_device.cuh"
 #include "esa_internal.h"
@@ -41,6 +43,7 @@ constexpr int kNS = 8;  // lanes per value column
 constexpr int kKdaWarps = 4;
 constexpr int kKdaThreads = kKdaWarps * 32;
 constexpr int kColsB = kKdaThreads / kNS;  // value columns per block (16)
+constexpr int kDecodeSteps = 4;            // calls with at most this many steps stream the state once per step
 
 template <int DK, int CT>
 struct KdaLayout {
@@ -53,8 +56,8 @@ struct KdaLayout {
     static constexpr int IN = (BETA + CT * 4 + 15) / 16 * 16;
     static constexpr int TILE = DK * kColsB * 4;  // the state tile, staged in one buffer
     static constexpr int BUF = IN > TILE ? IN : TILE;
-    static constexpr int OUT = 2 * BUF;  // fp32 [2][CT][kColsB]
-    static constexpr int TOTAL = OUT + 2 * CT * kColsB * 4;
+    static constexpr int PART = 2 * BUF;  // fp32 [CT][kColsB][kNS]: per-lane shares of q . s
+    static constexpr int TOTAL = PART + CT * kKdaThreads * 4;
 };
 
 // A row of DK elements of `es` bytes is split into 16-byte pieces; lane slice s
@@ -103,23 +106,72 @@ __device__ __forceinline__ void kda_issue(uint32_t sb, const KdaArgs &a, long lo
     for (int i = tid; i < n; i += kKdaThreads) cp_async4(sb + L::BETA + i * 4, a.beta + row0 + (long long)i * a.H);
 }
 
-template <int DK, int CT>
-__device__ __forceinline__ void kda_store(const float *ob, const KdaArgs &a, long long b, int h, int c0, long long t0,
-                                          int n, int tid) {
-    for (int i = tid; i < n * (kColsB / 4); i += kKdaThreads) {
-        const int tt = i / (kColsB / 4), q4 = i % (kColsB / 4);
-        const float4 x = *reinterpret_cast<const float4 *>(ob + tt * kColsB + q4 * 4);
-        const long long e = ((b * a.T + t0 + tt) * a.H + h) * (long long)a.Dv + c0 + q4 * 4;
-        if (a.o) *reinterpret_cast<float4 *>(a.o + e) = x;
-        if (a.lin) *reinterpret_cast<uint2 *>(a.lin + e) = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
-    }
-}
-
 __device__ __forceinline__ float sum8(float x) {  // over the 8 lanes of a column; every lane gets the same bits
     x += __shfl_xor_sync(0xffffffffu, x, 1);
     x += __shfl_xor_sync(0xffffffffu, x, 2);
     x += __shfl_xor_sync(0xffffffffu, x, 4);
     return x;
+}
+
+// One step's operands for a lane: its R key channels of k_t, q_t and alpha_t,
+// and v_t of its column, beta_t.
+template <int R>
+struct StepIn {
+    float k[R], q[R], a[R], v, b;
+};
+
+template <int DK, int CT>
+__device__ __forceinline__ void load_step(const unsigned char *in, int tt, int s, int cl, StepIn<DK / kNS> &x) {
+    using L = KdaLayout<DK, CT>;
+    constexpr int R = DK / kNS;
+    const unsigned char *rq = in + L::Q + tt * DK * 2 + s * 16, *rk = in + L::K + tt * DK * 2 + s * 16;
+    const unsigned char *ra = in + L::A + tt * DK * 4 + s * 16;
+#pragma unroll
+    for (int j = 0; j < R / 8; j++) {
+        const uint4 wk = *reinterpret_cast<const uint4 *>(rk + j * kNS * 16);
+        const uint4 wq = *reinterpret_cast<const uint4 *>(rq + j * kNS * 16);
+        const uint32_t ks[4] = {wk.x, wk.y, wk.z, wk.w}, qs[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            x.k[j * 8 + 2 * e] = bf16lo(ks[e]);
+            x.k[j * 8 + 2 * e + 1] = bf16hi(ks[e]);
+            x.q[j * 8 + 2 * e] = bf16lo(qs[e]);
+            x.q[j * 8 + 2 * e + 1] = bf16hi(qs[e]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < R / 4; j++) {
+        const float4 av = *reinterpret_cast<const float4 *>(ra + j * kNS * 16);
+        x.a[j * 4] = av.x;
+        x.a[j * 4 + 1] = av.y;
+        x.a[j * 4 + 2] = av.z;
+        x.a[j * 4 + 3] = av.w;
+    }
+    x.v = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(in + L::V)[tt * kColsB + cl] << 16);
+    x.b = reinterpret_cast<const float *>(in + L::BETA)[tt];
+}
+
+// One step for this lane's R key channels of its column: forget, read
+// u = k_t . s (summed over the column's 8 lanes), write beta_t (v_t - u) along
+// k_t, and store this lane's share of q_t . s. The products k*alpha and
+// alpha*s do not wait for the previous step's sum.
+template <int R>
+__device__ __forceinline__ void kda_step(const StepIn<R> &x, float (&st)[R], float *share) {
+    float p[4] = {0.f, 0.f, 0.f, 0.f}, sa[R];
+#pragma unroll
+    for (int m = 0; m < R; m++) {
+        p[m & 3] = fmaf(x.k[m] * x.a[m], st[m], p[m & 3]);
+        sa[m] = st[m] * x.a[m];
+    }
+    const float u = sum8((p[0] + p[1]) + (p[2] + p[3]));
+    const float d = x.b * (x.v - u);
+    float ov[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < R; m++) {
+        st[m] = fmaf(x.k[m], d, sa[m]);
+        ov[m & 3] = fmaf(x.q[m], st[m], ov[m & 3]);
+    }
+    *share = (ov[0] + ov[1]) + (ov[2] + ov[3]);
 }
 
 template <int DK, int CT>
@@ -153,6 +205,7 @@ __global__ void __launch_bounds__(kKdaThreads) kda_kernel(const KdaArgs a) {
     for (int m = 0; m < R; m++) st[m] = tile[(s * R + m) * kColsB + cl];
     __syncthreads();
 
+    float *part = reinterpret_cast<float *>(smem + L::PART);
     for (int c = 0; c < nch; c++) {
         const long long t0 = (long long)c * CT;
         const int n = (int)min((long long)CT, a.T - t0);
@@ -162,64 +215,32 @@ __global__ void __launch_bounds__(kKdaThreads) kda_kernel(const KdaArgs a) {
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
-        if (c > 0)
-            kda_store<DK, CT>(reinterpret_cast<const float *>(smem + L::OUT) + ((c - 1) & 1) * CT * kColsB, a, b, h,
-                              c0, t0 - CT, CT, tid);
         const unsigned char *in = smem + (c & 1) * L::BUF;
-        float *ob = reinterpret_cast<float *>(smem + L::OUT) + (c & 1) * CT * kColsB;
-        for (int tt = 0; tt < n; tt++) {
-            float kf[R], qf[R], af[R];
-            const unsigned char *rq = in + L::Q + tt * DK * 2 + s * 16, *rk = in + L::K + tt * DK * 2 + s * 16;
-            const unsigned char *ra = in + L::A + tt * DK * 4 + s * 16;
-#pragma unroll
-            for (int j = 0; j < R / 8; j++) {
-                const uint4 wk = *reinterpret_cast<const uint4 *>(rk + j * kNS * 16);
-                const uint4 wq = *reinterpret_cast<const uint4 *>(rq + j * kNS * 16);
-                const uint32_t ks[4] = {wk.x, wk.y, wk.z, wk.w}, qs[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    kf[j * 8 + 2 * e] = bf16lo(ks[e]);
-                    kf[j * 8 + 2 * e + 1] = bf16hi(ks[e]);
-                    qf[j * 8 + 2 * e] = bf16lo(qs[e]);
-                    qf[j * 8 + 2 * e + 1] = bf16hi(qs[e]);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < R / 4; j++) {
-                const float4 av = *reinterpret_cast<const float4 *>(ra + j * kNS * 16);
-                af[j * 4] = av.x;
-                af[j * 4 + 1] = av.y;
-                af[j * 4 + 2] = av.z;
-                af[j * 4 + 3] = av.w;
-            }
-            const float vc = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(in + L::V)[tt * kColsB + cl]
-                                             << 16);
-            const float bt = reinterpret_cast<const float *>(in + L::BETA)[tt];
-            // forget, then read what the column returns for k_t
-            float p[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int m = 0; m < R; m++) {
-                st[m] *= af[m];
-                p[m & 3] = fmaf(kf[m], st[m], p[m & 3]);
-            }
-            const float u = sum8((p[0] + p[1]) + (p[2] + p[3]));
-            // write beta_t (v_t - u) along k_t, then read out with q_t
-            const float d = bt * (vc - u);
-            float ov[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int m = 0; m < R; m++) {
-                st[m] = fmaf(kf[m], d, st[m]);
-                ov[m & 3] = fmaf(qf[m], st[m], ov[m & 3]);
-            }
-            const float o = sum8((ov[0] + ov[1]) + (ov[2] + ov[3]));
-            if (s == 0) ob[tt * kColsB + cl] = o * a.scale;
+        // two operand sets alternate: the next step's operands are read while
+        // this step's chain runs
+        StepIn<R> x0, x1;
+        load_step<DK, CT>(in, 0, s, cl, x0);
+        for (int tt = 0; tt < n; tt += 2) {
+            load_step<DK, CT>(in, min(tt + 1, n - 1), s, cl, x1);
+            kda_step<R>(x0, st, part + tt * kKdaThreads + cl * kNS + s);
+            if (tt + 1 >= n) break;
+            load_step<DK, CT>(in, min(tt + 2, n - 1), s, cl, x0);
+            kda_step<R>(x1, st, part + (tt + 1) * kKdaThreads + cl * kNS + s);
         }
-        __syncthreads();  // buffer c&1 is read; the next chunk may refill it
-    }
-    if (nch > 0) {
-        const long long t0 = (long long)(nch - 1) * CT;
-        kda_store<DK, CT>(reinterpret_cast<const float *>(smem + L::OUT) + ((nch - 1) & 1) * CT * kColsB, a, b, h, c0,
-                          t0, (int)(a.T - t0), tid);
+        __syncthreads();  // the shares are complete; buffer c&1 is read and may be refilled
+        // o_t[c] = scale * (the 8 shares, in lane order); 16 consecutive threads
+        // write one step's 16 columns
+        for (int i = tid; i < n * kColsB; i += kKdaThreads) {
+            const int tt = i / kColsB, col = i % kColsB;
+            const float *pp = part + tt * kKdaThreads + col * kNS;
+            float o = pp[0];
+#pragma unroll
+            for (int j = 1; j < kNS; j++) o += pp[j];
+            o *= a.scale;
+            const long long e = ((b * a.T + t0 + tt) * a.H + h) * (long long)a.Dv + c0 + col;
+            if (a.o) a.o[e] = o;
+            if (a.lin) a.lin[e] = (uint16_t)(pack_bf16(o, 0.f) & 0xffffu);
+        }
     }
     if (a.state_out) {
         cp_async_wait<0>();
@@ -236,11 +257,142 @@ __global__ void __launch_bounds__(kKdaThreads) kda_kernel(const KdaArgs a) {
     }
 }
 
+// A few steps (decode): the state streams through registers once. Block =
+// 128 threads = 16 columns of one (sequence, head); thread (rg = tid / 4,
+// cg = tid % 4) holds rows rg + 32 j and columns 4 cg .. 4 cg + 3 as float4,
+// so each warp load reads 8 rows x 64 contiguous bytes. Per step, with
+// S' = alpha * S (per row):
+//   u[c] = sum_i (alpha_i k_i) S[i][c],  z[c] = sum_i (alpha_i q_i) S[i][c],
+// summed over the thread's rows, then over the warp's 8 row groups (shuffles)
+// and the 4 warps (shared memory, in warp order); then
+//   d[c] = beta (v[c] - u[c]),  o[c] = scale (z[c] + (q . k) d[c]),
+//   S[i][c] = alpha_i S[i][c] + k_i d[c].
+constexpr int kDecRowGroups = kKdaThreads / 4;
+
+template <int DK>
+__global__ void __launch_bounds__(kKdaThreads) kda_decode_kernel(const KdaArgs a) {
+    constexpr int RJ = DK / kDecRowGroups;  // rows per thread
+    __shared__ float red[kKdaWarps][2 * kColsB + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rg = tid >> 2, cg = tid & 3;
+    const int c0 = blockIdx.x * kColsB, h = blockIdx.y;
+    const long long b = blockIdx.z;
+    const long long sbase = (b * a.H + h) * (long long)DK * a.Dv + c0 + cg * 4;
+    float4 S[RJ];
+#pragma unroll
+    for (int j = 0; j < RJ; j++)
+        S[j] = a.state_in ? *reinterpret_cast<const float4 *>(a.state_in + sbase + (long long)(rg + kDecRowGroups * j) * a.Dv)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long t = 0; t < a.T; t++) {
+        const long long row = (b * a.T + t) * a.H + h;
+        float al[RJ], kk[RJ];
+        float u[4] = {0.f, 0.f, 0.f, 0.f}, z[4] = {0.f, 0.f, 0.f, 0.f}, qk = 0.f;
+#pragma unroll
+        for (int j = 0; j < RJ; j++) {
+            const int i = rg + kDecRowGroups * j;
+            al[j] = a.alpha[row * DK + i];
+            kk[j] = __uint_as_float((uint32_t)a.k[row * DK + i] << 16);
+            const float qq = __uint_as_float((uint32_t)a.q[row * DK + i] << 16);
+            const float ak = al[j] * kk[j], aq = al[j] * qq;
+            if (cg == 0) qk = fmaf(qq, kk[j], qk);
+            u[0] = fmaf(ak, S[j].x, u[0]);
+            u[1] = fmaf(ak, S[j].y, u[1]);
+            u[2] = fmaf(ak, S[j].z, u[2]);
+            u[3] = fmaf(ak, S[j].w, u[3]);
+            z[0] = fmaf(aq, S[j].x, z[0]);
+            z[1] = fmaf(aq, S[j].y, z[1]);
+            z[2] = fmaf(aq, S[j].z, z[2]);
+            z[3] = fmaf(aq, S[j].w, z[3]);
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                u[e] += __shfl_xor_sync(0xffffffffu, u[e], off);
+                z[e] += __shfl_xor_sync(0xffffffffu, z[e], off);
+            }
+            qk += __shfl_xor_sync(0xffffffffu, qk, off);
+        }
+        if (lane < 4) {
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                red[warp][cg * 4 + e] = u[e];
+                red[warp][kColsB + cg * 4 + e] = z[e];
+            }
+            if (lane == 0) red[warp][2 * kColsB] = qk;
+        }
+        __syncthreads();
+        float U[4], Z[4];
+        qk = red[0][2 * kColsB];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            U[e] = red[0][cg * 4 + e];
+            Z[e] = red[0][kColsB + cg * 4 + e];
+        }
+#pragma unroll
+        for (int w = 1; w < kKdaWarps; w++) {
+            qk += red[w][2 * kColsB];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                U[e] += red[w][cg * 4 + e];
+                Z[e] += red[w][kColsB + cg * 4 + e];
+            }
+        }
+        __syncthreads();  // red is rewritten by the next step
+        const float bt = a.beta[row];
+        const uint2 vw = *reinterpret_cast<const uint2 *>(a.v + row * a.Dv + c0 + cg * 4);
+        const float vv[4] = {bf16lo(vw.x), bf16hi(vw.x), bf16lo(vw.y), bf16hi(vw.y)};
+        float d[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) d[e] = bt * (vv[e] - U[e]);
+        if (rg == 0) {
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) o[e] = a.scale * fmaf(qk, d[e], Z[e]);
+            const long long oe = row * a.Dv + c0 + cg * 4;
+            if (a.o) *reinterpret_cast<float4 *>(a.o + oe) = make_float4(o[0], o[1], o[2], o[3]);
+            if (a.lin) *reinterpret_cast<uint2 *>(a.lin + oe) = make_uint2(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]));
+        }
+#pragma unroll
+        for (int j = 0; j < RJ; j++) {
+            S[j].x = fmaf(kk[j], d[0], al[j] * S[j].x);
+            S[j].y = fmaf(kk[j], d[1], al[j] * S[j].y);
+            S[j].z = fmaf(kk[j], d[2], al[j] * S[j].z);
+            S[j].w = fmaf(kk[j], d[3], al[j] * S[j].w);
+        }
+    }
+    if (a.state_out) {
+#pragma unroll
+        for (int j = 0; j < RJ; j++)
+            *reinterpret_cast<float4 *>(a.state_out + sbase + (long long)(rg + kDecRowGroups * j) * a.Dv) = S[j];
+    }
+}
+
+// the largest shared-memory carveout
+bool kda_configure(const void *fn, size_t smem) {
+    static std::mutex mu;
+    static std::set<std::pair<int, const void *>> done;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (done.count({dev, fn})) return true;
+    }
+    if (!ensure_smem(fn, smem) ||
+        cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    done.insert({dev, fn});
+    return true;
+}
+
 template <int DK, int CT>
 esa_status launch_kda_t(const KdaArgs &a, long long B, cudaStream_t st) {
     using L = KdaLayout<DK, CT>;
     const void *fn = reinterpret_cast<const void *>(&kda_kernel<DK, CT>);
-    if (!ensure_smem(fn, L::TOTAL)) return ESA_ERR_CUDA;
+    if (!kda_configure(fn, L::TOTAL)) return ESA_ERR_CUDA;
     dim3 grid((unsigned)(a.Dv / kColsB), (unsigned)a.H, (unsigned)B);
     kda_kernel<DK, CT><<<grid, kKdaThreads, L::TOTAL, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
@@ -252,10 +404,18 @@ esa_status launch_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
                       const float *state_in, long long B, long long T, int H, int Dk, int Dv, float scale, float *o,
                       uint16_t *lin, float *state_out, cudaStream_t st) {
     const KdaArgs a{q, k, v, alpha, beta, state_in, o, state_out, lin, T, H, Dv, scale};
-    // decode-sized calls stage few steps: a smaller block footprint, more blocks per SM
-    const bool small = T <= 4;
-    if (Dk == 128) return small ? launch_kda_t<128, 4>(a, B, st) : launch_kda_t<128, 32>(a, B, st);
-    if (Dk == 64) return small ? launch_kda_t<64, 4>(a, B, st) : launch_kda_t<64, 32>(a, B, st);
+    if (T <= kDecodeSteps) {  // a few steps: one streaming pass over the state
+        dim3 grid((unsigned)(Dv / kColsB), (unsigned)H, (unsigned)B);
+        if (Dk == 128)
+            kda_decode_kernel<128><<<grid, kKdaThreads, 0, st>>>(a);
+        else if (Dk == 64)
+            kda_decode_kernel<64><<<grid, kKdaThreads, 0, st>>>(a);
+        else
+            return ESA_ERR_UNSUPPORTED;
+        return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
+    }
+    if (Dk == 128) return launch_kda_t<128, 32>(a, B, st);
+    if (Dk == 64) return launch_kda_t<64, 32>(a, B, st);
     return ESA_ERR_UNSUPPORTED;
 }
 
