@@ -39,32 +39,39 @@ namespace esa {
 
 namespace {
 
-constexpr int kNS = 8;  // lanes per value column
 constexpr int kKdaWarps = 4;
 constexpr int kKdaThreads = kKdaWarps * 32;
-constexpr int kColsB = kKdaThreads / kNS;  // value columns per block (16)
-constexpr int kDecodeSteps = 4;            // calls with at most this many steps stream the state once per step
+constexpr int kCT = 32;          // steps staged per chunk
+constexpr int kDecCols = 16;     // value columns per decode block
+constexpr int kDecodeSteps = 4;  // calls with at most this many steps stream the state once per step
 
-template <int DK, int CT>
+// NS lanes share CC value columns, R = DK / NS key channels each; a block
+// holds COLS = 128 / NS * CC columns of one head.
+template <int DK, int NS, int CC>
 struct KdaLayout {
-    static constexpr int R = DK / kNS;  // key channels per lane
-    static constexpr int Q = 0;         // bf16 [CT][DK], pieces permuted (below)
-    static constexpr int K = Q + CT * DK * 2;
-    static constexpr int A = K + CT * DK * 2;         // fp32 [CT][DK], pieces permuted
-    static constexpr int V = A + CT * DK * 4;         // bf16 [CT][kColsB]
-    static constexpr int BETA = V + CT * kColsB * 2;  // fp32 [CT]
-    static constexpr int IN = (BETA + CT * 4 + 15) / 16 * 16;
-    static constexpr int TILE = DK * kColsB * 4;  // the state tile, staged in one buffer
+    static constexpr int R = DK / NS;
+    static constexpr int COLS = kKdaThreads / NS * CC;
+    static constexpr int Q = 0;  // bf16 [kCT][DK], pieces permuted (below)
+    static constexpr int K = Q + kCT * DK * 2;
+    static constexpr int A = K + kCT * DK * 2;       // fp32 [kCT][DK], pieces permuted
+    static constexpr int V = A + kCT * DK * 4;       // bf16 [kCT][COLS]
+    static constexpr int BETA = V + kCT * COLS * 2;  // fp32 [kCT]
+    static constexpr int IN = (BETA + kCT * 4 + 15) / 16 * 16;
+    static constexpr int TILE = DK * COLS * 4;  // the state tile, staged in one buffer
     static constexpr int BUF = IN > TILE ? IN : TILE;
-    static constexpr int PART = 2 * BUF;  // fp32 [CT][kColsB][kNS]: per-lane shares of q . s
-    static constexpr int TOTAL = PART + CT * kKdaThreads * 4;
+    static constexpr int PART = 2 * BUF;  // fp32 [kCT][COLS][NS]: per-lane shares of q . s
+    static constexpr int TOTAL = PART + kCT * COLS * NS * 4;
+    static_assert(R % 8 == 0 && COLS % 8 == 0, "whole 16-byte pieces per lane and per v row");
 };
 
 // A row of DK elements of `es` bytes is split into 16-byte pieces; lane slice s
 // owns key channels s*R .. s*R+R-1, i.e. pieces s*PPL .. s*PPL+PPL-1. Piece p
-// is stored at (p % PPL) * 128 + (p / PPL) * 16, so that for each of its PPL
-// pieces the 8 slices read 128 consecutive bytes.
-__device__ __forceinline__ uint32_t piece_off(int p, int ppl) { return (p % ppl) * (kNS * 16) + (p / ppl) * 16; }
+// is stored at (p % PPL) * NS * 16 + (p / PPL) * 16, so that for each of its
+// PPL pieces the NS slices read NS * 16 consecutive bytes.
+template <int NS>
+__device__ __forceinline__ uint32_t piece_off(int p, int ppl) {
+    return (p % ppl) * (NS * 16) + (p / ppl) * 16;
+}
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
@@ -80,56 +87,51 @@ struct KdaArgs {
     float scale;
 };
 
-template <int DK, int CT>
+template <int DK, int NS, int CC>
 __device__ __forceinline__ void kda_issue(uint32_t sb, const KdaArgs &a, long long b, int h, int c0, long long t0,
                                           int n, int tid) {
-    using L = KdaLayout<DK, CT>;
+    using L = KdaLayout<DK, NS, CC>;
     constexpr int PQ = DK * 2 / 16, PA = DK * 4 / 16;  // 16-byte pieces per q/k row, per alpha row
+    constexpr int PV = L::COLS * 2 / 16;                // per row of the block's v values
     const long long row0 = (b * a.T + t0) * a.H + h;
     for (int i = tid; i < n * PQ; i += kKdaThreads) {
         const int tt = i / PQ, p = i % PQ;
         const long long row = row0 + (long long)tt * a.H;
-        const uint32_t off = tt * DK * 2 + piece_off(p, PQ / kNS);
+        const uint32_t off = tt * DK * 2 + piece_off<NS>(p, PQ / NS);
         cp_async16(sb + L::Q + off, a.q + row * DK + p * 8);
         cp_async16(sb + L::K + off, a.k + row * DK + p * 8);
     }
     for (int i = tid; i < n * PA; i += kKdaThreads) {
         const int tt = i / PA, p = i % PA;
         const long long row = row0 + (long long)tt * a.H;
-        cp_async16(sb + L::A + tt * DK * 4 + piece_off(p, PA / kNS), a.alpha + row * DK + p * 4);
+        cp_async16(sb + L::A + tt * DK * 4 + piece_off<NS>(p, PA / NS), a.alpha + row * DK + p * 4);
     }
-    for (int i = tid; i < n * 2; i += kKdaThreads) {  // the block's 16 v values: two pieces
-        const int tt = i / 2, p = i % 2;
+    for (int i = tid; i < n * PV; i += kKdaThreads) {
+        const int tt = i / PV, p = i % PV;
         const long long row = row0 + (long long)tt * a.H;
-        cp_async16(sb + L::V + tt * kColsB * 2 + p * 16, a.v + row * a.Dv + c0 + p * 8);
+        cp_async16(sb + L::V + tt * L::COLS * 2 + p * 16, a.v + row * a.Dv + c0 + p * 8);
     }
     for (int i = tid; i < n; i += kKdaThreads) cp_async4(sb + L::BETA + i * 4, a.beta + row0 + (long long)i * a.H);
 }
 
-__device__ __forceinline__ float sum8(float x) {  // over the 8 lanes of a column; every lane gets the same bits
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    return x;
-}
-
 // One step's operands for a lane: its R key channels of k_t, q_t and alpha_t,
-// and v_t of its column, beta_t.
-template <int R>
+// v_t of its CC columns, beta_t.
+template <int R, int CC>
 struct StepIn {
-    float k[R], q[R], a[R], v, b;
+    float k[R], q[R], a[R], v[CC], b;
 };
 
-template <int DK, int CT>
-__device__ __forceinline__ void load_step(const unsigned char *in, int tt, int s, int cl, StepIn<DK / kNS> &x) {
-    using L = KdaLayout<DK, CT>;
-    constexpr int R = DK / kNS;
+template <int DK, int NS, int CC>
+__device__ __forceinline__ void load_step(const unsigned char *in, int tt, int s, int cl,
+                                          StepIn<DK / NS, CC> &x) {
+    using L = KdaLayout<DK, NS, CC>;
+    constexpr int R = L::R;
     const unsigned char *rq = in + L::Q + tt * DK * 2 + s * 16, *rk = in + L::K + tt * DK * 2 + s * 16;
     const unsigned char *ra = in + L::A + tt * DK * 4 + s * 16;
 #pragma unroll
     for (int j = 0; j < R / 8; j++) {
-        const uint4 wk = *reinterpret_cast<const uint4 *>(rk + j * kNS * 16);
-        const uint4 wq = *reinterpret_cast<const uint4 *>(rq + j * kNS * 16);
+        const uint4 wk = *reinterpret_cast<const uint4 *>(rk + j * NS * 16);
+        const uint4 wq = *reinterpret_cast<const uint4 *>(rq + j * NS * 16);
         const uint32_t ks[4] = {wk.x, wk.y, wk.z, wk.w}, qs[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
         for (int e = 0; e < 4; e++) {
@@ -141,101 +143,122 @@ __device__ __forceinline__ void load_step(const unsigned char *in, int tt, int s
     }
 #pragma unroll
     for (int j = 0; j < R / 4; j++) {
-        const float4 av = *reinterpret_cast<const float4 *>(ra + j * kNS * 16);
+        const float4 av = *reinterpret_cast<const float4 *>(ra + j * NS * 16);
         x.a[j * 4] = av.x;
         x.a[j * 4 + 1] = av.y;
         x.a[j * 4 + 2] = av.z;
         x.a[j * 4 + 3] = av.w;
     }
-    x.v = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(in + L::V)[tt * kColsB + cl] << 16);
+#pragma unroll
+    for (int cc = 0; cc < CC; cc++)
+        x.v[cc] = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(in + L::V)[tt * L::COLS + cl * CC + cc]
+                                  << 16);
     x.b = reinterpret_cast<const float *>(in + L::BETA)[tt];
 }
 
-// One step for this lane's R key channels of its column: forget, read
-// u = k_t . s (summed over the column's 8 lanes), write beta_t (v_t - u) along
-// k_t, and store this lane's share of q_t . s. The products k*alpha and
-// alpha*s do not wait for the previous step's sum.
-template <int R>
-__device__ __forceinline__ void kda_step(const StepIn<R> &x, float (&st)[R], float *share) {
-    float p[4] = {0.f, 0.f, 0.f, 0.f}, sa[R];
+// One step for this lane's R key channels of its CC columns: forget, read
+// u = k_t . s (summed over the columns' NS lanes; the CC sums interleave),
+// write beta_t (v_t - u) along k_t, and store this lane's share of q_t . s for
+// each column (share[cc * NS]). The products k*alpha and alpha*s do not wait
+// for the previous step's sums.
+template <int R, int NS, int CC>
+__device__ __forceinline__ void kda_step(const StepIn<R, CC> &x, float (&st)[CC][R], float *share) {
+    float ka[R], u[CC], sa[CC][R];
 #pragma unroll
-    for (int m = 0; m < R; m++) {
-        p[m & 3] = fmaf(x.k[m] * x.a[m], st[m], p[m & 3]);
-        sa[m] = st[m] * x.a[m];
-    }
-    const float u = sum8((p[0] + p[1]) + (p[2] + p[3]));
-    const float d = x.b * (x.v - u);
-    float ov[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int m = 0; m < R; m++) ka[m] = x.k[m] * x.a[m];
 #pragma unroll
-    for (int m = 0; m < R; m++) {
-        st[m] = fmaf(x.k[m], d, sa[m]);
-        ov[m & 3] = fmaf(x.q[m], st[m], ov[m & 3]);
+    for (int cc = 0; cc < CC; cc++) {
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < R; m++) {
+            p[m & 3] = fmaf(ka[m], st[cc][m], p[m & 3]);
+            sa[cc][m] = st[cc][m] * x.a[m];
+        }
+        u[cc] = (p[0] + p[1]) + (p[2] + p[3]);
     }
-    *share = (ov[0] + ov[1]) + (ov[2] + ov[3]);
+#pragma unroll
+    for (int off = 1; off < NS; off <<= 1)
+#pragma unroll
+        for (int cc = 0; cc < CC; cc++) u[cc] += __shfl_xor_sync(0xffffffffu, u[cc], off);
+#pragma unroll
+    for (int cc = 0; cc < CC; cc++) {
+        const float d = x.b * (x.v[cc] - u[cc]);
+        float ov[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < R; m++) {
+            st[cc][m] = fmaf(x.k[m], d, sa[cc][m]);
+            ov[m & 3] = fmaf(x.q[m], st[cc][m], ov[m & 3]);
+        }
+        share[cc * NS] = (ov[0] + ov[1]) + (ov[2] + ov[3]);
+    }
 }
 
-template <int DK, int CT>
+template <int DK, int NS, int CC>
 __global__ void __launch_bounds__(kKdaThreads) kda_kernel(const KdaArgs a) {
-    using L = KdaLayout<DK, CT>;
-    constexpr int R = L::R;
+    using L = KdaLayout<DK, NS, CC>;
+    constexpr int R = L::R, COLS = L::COLS;
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31;
-    const int cl = (tid >> 5) * (32 / kNS) + lane / kNS;  // block column 0..15
-    const int s = lane % kNS;                             // key channels s*R .. s*R+R-1
-    const int c0 = blockIdx.x * kColsB, h = blockIdx.y;
+    const int cl = (tid >> 5) * (32 / NS) + lane / NS;  // block columns cl*CC .. cl*CC+CC-1
+    const int s = lane % NS;                            // key channels s*R .. s*R+R-1
+    const int c0 = blockIdx.x * COLS, h = blockIdx.y;
     const long long b = blockIdx.z;
     const uint32_t sb = smem_u32(smem);
-    const int nch = (int)((a.T + CT - 1) / CT);
+    const int nch = (int)((a.T + kCT - 1) / kCT);
 
-    if (nch > 0) kda_issue<DK, CT>(sb, a, b, h, c0, 0, (int)min((long long)CT, a.T), tid);
+    if (nch > 0) kda_issue<DK, NS, CC>(sb, a, b, h, c0, 0, (int)min((long long)kCT, a.T), tid);
     cp_async_commit();
 
-    // the state tile [DK][16] through buffer 1 (no copy targets it yet)
+    // the state tile [DK][COLS] through buffer 1 (no copy targets it yet)
     float *tile = reinterpret_cast<float *>(smem + L::BUF);
     const long long sbase = (b * a.H + h) * (long long)DK * a.Dv + c0;
-    for (int i = tid; i < DK * (kColsB / 4); i += kKdaThreads) {
-        const int r = i / (kColsB / 4), q4 = i % (kColsB / 4);
+    for (int i = tid; i < DK * (COLS / 4); i += kKdaThreads) {
+        const int r = i / (COLS / 4), q4 = i % (COLS / 4);
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (a.state_in) x = *reinterpret_cast<const float4 *>(a.state_in + sbase + (long long)r * a.Dv + q4 * 4);
-        *reinterpret_cast<float4 *>(tile + r * kColsB + q4 * 4) = x;
+        *reinterpret_cast<float4 *>(tile + r * COLS + q4 * 4) = x;
     }
     __syncthreads();
-    float st[R];
+    float st[CC][R];
 #pragma unroll
-    for (int m = 0; m < R; m++) st[m] = tile[(s * R + m) * kColsB + cl];
+    for (int cc = 0; cc < CC; cc++)
+#pragma unroll
+        for (int m = 0; m < R; m++) st[cc][m] = tile[(s * R + m) * COLS + cl * CC + cc];
     __syncthreads();
 
     float *part = reinterpret_cast<float *>(smem + L::PART);
     for (int c = 0; c < nch; c++) {
-        const long long t0 = (long long)c * CT;
-        const int n = (int)min((long long)CT, a.T - t0);
+        const long long t0 = (long long)c * kCT;
+        const int n = (int)min((long long)kCT, a.T - t0);
         if (c + 1 < nch)
-            kda_issue<DK, CT>(sb + ((c + 1) & 1) * L::BUF, a, b, h, c0, t0 + CT,
-                              (int)min((long long)CT, a.T - t0 - CT), tid);
+            kda_issue<DK, NS, CC>(sb + ((c + 1) & 1) * L::BUF, a, b, h, c0, t0 + kCT,
+                              (int)min((long long)kCT, a.T - t0 - kCT), tid);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
         const unsigned char *in = smem + (c & 1) * L::BUF;
         // two operand sets alternate: the next step's operands are read while
         // this step's chain runs
-        StepIn<R> x0, x1;
-        load_step<DK, CT>(in, 0, s, cl, x0);
+        // shares [kCT][COLS][NS]: this lane's column cl*CC+cc at (cl*CC+cc)*NS + s
+        float *my = part + cl * CC * NS + s;
+        StepIn<R, CC> x0, x1;
+        load_step<DK, NS, CC>(in, 0, s, cl, x0);
         for (int tt = 0; tt < n; tt += 2) {
-            load_step<DK, CT>(in, min(tt + 1, n - 1), s, cl, x1);
-            kda_step<R>(x0, st, part + tt * kKdaThreads + cl * kNS + s);
+            load_step<DK, NS, CC>(in, min(tt + 1, n - 1), s, cl, x1);
+            kda_step<R, NS, CC>(x0, st, my + tt * COLS * NS);
             if (tt + 1 >= n) break;
-            load_step<DK, CT>(in, min(tt + 2, n - 1), s, cl, x0);
-            kda_step<R>(x1, st, part + (tt + 1) * kKdaThreads + cl * kNS + s);
+            load_step<DK, NS, CC>(in, min(tt + 2, n - 1), s, cl, x0);
+            kda_step<R, NS, CC>(x1, st, my + (tt + 1) * COLS * NS);
         }
         __syncthreads();  // the shares are complete; buffer c&1 is read and may be refilled
-        // o_t[c] = scale * (the 8 shares, in lane order); 16 consecutive threads
-        // write one step's 16 columns
-        for (int i = tid; i < n * kColsB; i += kKdaThreads) {
-            const int tt = i / kColsB, col = i % kColsB;
-            const float *pp = part + tt * kKdaThreads + col * kNS;
+        // o_t[c] = scale * (the NS shares, in lane order); COLS consecutive
+        // threads write one step's columns
+        for (int i = tid; i < n * COLS; i += kKdaThreads) {
+            const int tt = i / COLS, col = i % COLS;
+            const float *pp = part + (tt * COLS + col) * NS;
             float o = pp[0];
 #pragma unroll
-            for (int j = 1; j < kNS; j++) o += pp[j];
+            for (int j = 1; j < NS; j++) o += pp[j];
             o *= a.scale;
             const long long e = ((b * a.T + t0 + tt) * a.H + h) * (long long)a.Dv + c0 + col;
             if (a.o) a.o[e] = o;
@@ -247,12 +270,14 @@ __global__ void __launch_bounds__(kKdaThreads) kda_kernel(const KdaArgs a) {
         __syncthreads();
         float *t2 = reinterpret_cast<float *>(smem);
 #pragma unroll
-        for (int m = 0; m < R; m++) t2[(s * R + m) * kColsB + cl] = st[m];
+        for (int cc = 0; cc < CC; cc++)
+#pragma unroll
+            for (int m = 0; m < R; m++) t2[(s * R + m) * COLS + cl * CC + cc] = st[cc][m];
         __syncthreads();
-        for (int i = tid; i < DK * (kColsB / 4); i += kKdaThreads) {
-            const int r = i / (kColsB / 4), q4 = i % (kColsB / 4);
+        for (int i = tid; i < DK * (COLS / 4); i += kKdaThreads) {
+            const int r = i / (COLS / 4), q4 = i % (COLS / 4);
             *reinterpret_cast<float4 *>(a.state_out + sbase + (long long)r * a.Dv + q4 * 4) =
-                *reinterpret_cast<const float4 *>(t2 + r * kColsB + q4 * 4);
+                *reinterpret_cast<const float4 *>(t2 + r * COLS + q4 * 4);
         }
     }
 }
@@ -272,10 +297,10 @@ constexpr int kDecRowGroups = kKdaThreads / 4;
 template <int DK>
 __global__ void __launch_bounds__(kKdaThreads) kda_decode_kernel(const KdaArgs a) {
     constexpr int RJ = DK / kDecRowGroups;  // rows per thread
-    __shared__ float red[kKdaWarps][2 * kColsB + 1];
+    __shared__ float red[kKdaWarps][2 * kDecCols + 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rg = tid >> 2, cg = tid & 3;
-    const int c0 = blockIdx.x * kColsB, h = blockIdx.y;
+    const int c0 = blockIdx.x * kDecCols, h = blockIdx.y;
     const long long b = blockIdx.z;
     const long long sbase = (b * a.H + h) * (long long)DK * a.Dv + c0 + cg * 4;
     float4 S[RJ];
@@ -317,25 +342,25 @@ __global__ void __launch_bounds__(kKdaThreads) kda_decode_kernel(const KdaArgs a
 #pragma unroll
             for (int e = 0; e < 4; e++) {
                 red[warp][cg * 4 + e] = u[e];
-                red[warp][kColsB + cg * 4 + e] = z[e];
+                red[warp][kDecCols + cg * 4 + e] = z[e];
             }
-            if (lane == 0) red[warp][2 * kColsB] = qk;
+            if (lane == 0) red[warp][2 * kDecCols] = qk;
         }
         __syncthreads();
         float U[4], Z[4];
-        qk = red[0][2 * kColsB];
+        qk = red[0][2 * kDecCols];
 #pragma unroll
         for (int e = 0; e < 4; e++) {
             U[e] = red[0][cg * 4 + e];
-            Z[e] = red[0][kColsB + cg * 4 + e];
+            Z[e] = red[0][kDecCols + cg * 4 + e];
         }
 #pragma unroll
         for (int w = 1; w < kKdaWarps; w++) {
-            qk += red[w][2 * kColsB];
+            qk += red[w][2 * kDecCols];
 #pragma unroll
             for (int e = 0; e < 4; e++) {
                 U[e] += red[w][cg * 4 + e];
-                Z[e] += red[w][kColsB + cg * 4 + e];
+                Z[e] += red[w][kDecCols + cg * 4 + e];
             }
         }
         __syncthreads();  // red is rewritten by the next step
@@ -388,13 +413,13 @@ bool kda_configure(const void *fn, size_t smem) {
     return true;
 }
 
-template <int DK, int CT>
+template <int DK, int NS, int CC>
 esa_status launch_kda_t(const KdaArgs &a, long long B, cudaStream_t st) {
-    using L = KdaLayout<DK, CT>;
-    const void *fn = reinterpret_cast<const void *>(&kda_kernel<DK, CT>);
+    using L = KdaLayout<DK, NS, CC>;
+    const void *fn = reinterpret_cast<const void *>(&kda_kernel<DK, NS, CC>);
     if (!kda_configure(fn, L::TOTAL)) return ESA_ERR_CUDA;
-    dim3 grid((unsigned)(a.Dv / kColsB), (unsigned)a.H, (unsigned)B);
-    kda_kernel<DK, CT><<<grid, kKdaThreads, L::TOTAL, st>>>(a);
+    dim3 grid((unsigned)(a.Dv / L::COLS), (unsigned)a.H, (unsigned)B);
+    kda_kernel<DK, NS, CC><<<grid, kKdaThreads, L::TOTAL, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }
 
@@ -405,7 +430,7 @@ esa_status launch_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
                       uint16_t *lin, float *state_out, cudaStream_t st) {
     const KdaArgs a{q, k, v, alpha, beta, state_in, o, state_out, lin, T, H, Dv, scale};
     if (T <= kDecodeSteps) {  // a few steps: one streaming pass over the state
-        dim3 grid((unsigned)(Dv / kColsB), (unsigned)H, (unsigned)B);
+        dim3 grid((unsigned)(Dv / kDecCols), (unsigned)H, (unsigned)B);
         if (Dk == 128)
             kda_decode_kernel<128><<<grid, kKdaThreads, 0, st>>>(a);
         else if (Dk == 64)
@@ -414,8 +439,10 @@ esa_status launch_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
             return ESA_ERR_UNSUPPORTED;
         return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
     }
-    if (Dk == 128) return launch_kda_t<128, 32>(a, B, st);
-    if (Dk == 64) return launch_kda_t<64, 32>(a, B, st);
+    // 8 key channels per lane: at Dk = 128, 16 lanes hold two columns each
+    // (the operands a lane loads serve both); at Dk = 64, 8 lanes one column
+    if (Dk == 128) return launch_kda_t<128, 16, 2>(a, B, st);
+    if (Dk == 64) return launch_kda_t<64, 8, 1>(a, B, st);
     return ESA_ERR_UNSUPPORTED;
 }
 
