@@ -596,6 +596,23 @@ def pin_kda_linear_attention(L):
     assert np.allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
 
 
+def pin_kda_extreme_gates(L):
+    """alpha_t = 0 wipes the state before the write, so
+    o_t = scale * beta_t * (q_t . k_t) * v_t whatever came before; beta = 0
+    writes nothing, so with alpha = 1 every output reads the initial state:
+    o_t = scale * S_0^T q_t."""
+    q, k, v, alpha, beta, s0 = _kda_case(21, T=9)
+    a0 = alpha.copy()
+    a0[:, 4] = 0.0
+    o, _ = O.kda(q, k, v, a0, beta, state_in=s0, scale=0.5, L=L)
+    qd, kd, vd = _f64(q), _f64(k), _f64(v)
+    ref = 0.5 * beta[:, 4].astype(np.float64)[..., None] * (qd[:, 4] * kd[:, 4]).sum(-1)[..., None] * vd[:, 4]
+    assert np.allclose(o[:, 4], ref, rtol=1e-12, atol=1e-12)
+    o1, st1 = O.kda(q, k, v, np.ones_like(alpha), np.zeros_like(beta), state_in=s0, scale=0.5, L=L)
+    ref1 = 0.5 * np.einsum("bhic,bthi->bthc", s0.astype(np.float64), qd)
+    assert np.allclose(o1, ref1, rtol=1e-12, atol=1e-12) and np.array_equal(st1, s0.astype(np.float64))
+
+
 def pin_kda_chaining(L):
     """Running T steps at once equals running the first T1 and then the rest
     from the carried state (chunked prefill, decode); T = 0 hands the initial
@@ -617,4 +634,4 @@ ALL_PINS = [pin_indexer_golden, pin_indexer_numpy, pin_indexer_onehot, pin_index
             pin_indexer_modes_golden, pin_relu_special_and_numpy, pin_per_head_sets_are_sliced_queries,
             pin_per_head_attention_uses_its_set, pin_router_golden, pin_router_numpy, pin_router_closed_forms,
             pin_kda_golden, pin_kda_transition_matrices, pin_kda_retrieval, pin_kda_basis_keys,
-            pin_kda_linear_attention, pin_kda_chaining]
+            pin_kda_linear_attention, pin_kda_chaining, pin_kda_extreme_gates]

@@ -55,7 +55,7 @@ def _check(o, lin, so, ro, rs):
 
 KDA_CASES = [
     dict(B=1, T=1, H=2, Dk=128, Dv=128, state=True),   # one decode step
-    dict(B=2, T=4, H=2, Dk=64, Dv=128, state=True),    # few steps (small staging)
+    dict(B=2, T=4, H=2, Dk=64, Dv=128, state=True),    # few steps (the streaming kernel)
     dict(B=2, T=37, H=3, Dk=64, Dv=64, state=False),   # one ragged chunk
     dict(B=1, T=5, H=1, Dk=128, Dv=48, state=True),    # three column blocks
     dict(B=1, T=100, H=2, Dk=128, Dv=64, state=True),  # several chunks, ragged tail
@@ -107,6 +107,29 @@ def test_kda_empty_and_state_only():
     # zero initial state when none is given
     ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"])
     o, lin, so = _gpu(x)
+    _check(o, lin, so, ro, rs)
+
+
+@pytest.mark.parametrize("T", [3, 70])
+def test_kda_extreme_gates(T):
+    """Gates at their ends on both kernels (a few steps and many): alpha = 0
+    (the state is wiped), alpha = 1 (nothing forgotten), beta = 0 (no
+    write) and beta = 1 (full replacement) mixed over steps, heads and
+    channels."""
+    x = _inputs(2, T, 3, 128, 64, 90 + T, True)
+    rng = np.random.default_rng(T)
+    a = x["alpha"].numpy().copy()
+    pick = rng.random(a.shape)
+    a[pick < 0.1] = 0.0
+    a[pick > 0.8] = 1.0
+    x["alpha"] = torch.from_numpy(a)
+    bt = x["beta"].numpy().copy()
+    pb = rng.random(bt.shape)
+    bt[pb < 0.2] = 0.0
+    bt[pb > 0.8] = 1.0
+    x["beta"] = torch.from_numpy(bt)
+    ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
+    o, lin, so = _gpu(x, state_in=x["state"])
     _check(o, lin, so, ro, rs)
 
 
