@@ -167,6 +167,48 @@ def run_cpu_baseline(cfg: dict, inp: dict, seconds: float = 10.0):
     return rows * reps / el, threads, f"{reps} full decode steps ({rows} rows each), {el:.1f} s"
 
 
+def run_cpu_baseline_1thread(cfg: dict, inp: dict, seconds: float = 5.0):
+    """The same on one host thread: decode steps row by row, for about `seconds`."""
+    sys.path.insert(0, ROOT)
+    import esa_inputs as E
+    import oracle as O
+    sh = E.shape_of(cfg)
+    K = cfg["top_k"]
+    old = os.environ.get("ESA_ORACLE_THREADS")
+    os.environ["ESA_ORACLE_THREADS"] = "1"
+    try:
+        rows, n, t0 = sh["B"] * sh["Tq"], 0, time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            O.gated_sparse_attention(inp, sh, K, rows=[n % rows])
+            n += 1
+        el = time.perf_counter() - t0
+    finally:
+        if old is None:
+            del os.environ["ESA_ORACLE_THREADS"]
+        else:
+            os.environ["ESA_ORACLE_THREADS"] = old
+    return n / el, f"{n} decode rows one at a time, {el:.1f} s"
+
+
+def oracle_row_sample(host: dict, sh: dict, K: int, n_rows: int = 16, seed: int = 0) -> dict:
+    """The oracle, as it stands, on a seeded uniform sample of a prefill
+    workload's query rows (all host threads), extrapolated to the whole
+    forward: est = rows / n_sample * t_sample (unbiased: a row's cost depends
+    only on its position, drawn uniformly)."""
+    sys.path.insert(0, ROOT)
+    import oracle as O
+    O.lib()
+    total = sh["B"] * sh["Tq"]
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(total, size=min(n_rows, total), replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    O.gated_sparse_attention(host, sh, K, rows=rows)
+    el = time.perf_counter() - t0
+    est = el * total / len(rows)
+    return {"tok_per_s": total / est, "unit": "tok/s", "cores": min(O.threads(), len(rows)),
+            "kind": "oracle, extrapolated", "sample": f"{len(rows)} seeded uniform rows of {total}, {el:.2f} s"}
+
+
 def reference_arm(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -200,7 +242,8 @@ def reference_arm(args):
 
 
 def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
-                    names=("long_prefill", "chunked_prefill", "per_head_prefill", "routed_prefill")) -> dict:
+                    names=("long_prefill", "chunked_prefill", "per_head_prefill", "routed_prefill"),
+                    oracle_rows: int = 0) -> dict:
     """The two prefill workloads, one forward each (after one untimed warm-up),
     timed with CUDA events on the launching stream. Inputs (hundreds of MB to
     GBs) exceed the 126 MB L2. Algorithmic flops count what the method
@@ -283,13 +326,15 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
         entry.update({"ms": ms, "tok_per_s": B * S / (ms / 1e3), "algorithmic_tflops": flops / (ms / 1e3) / 1e12,
                       "tensor_peak_tflops": tf_peak, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tf_peak,
                       "peak_kind": kind})
+        if oracle_rows:
+            entry["cpu_baseline"] = oracle_row_sample(host, sh, K, n_rows=oracle_rows)
         res[name] = entry
         del d, host, out
         torch.cuda.empty_cache()
     return res
 
 
-def kda_section(dev, esa, E, reps: int = 3, T: int = 32768) -> dict:
+def kda_section(dev, esa, E, reps: int = 3, T: int = 32768, oracle: bool = False) -> dict:
     """The KDA linear branch (the gate mix's lin input) at the decode shape
     (8 sequences x 32 heads, one step, 128 x 128 fp32 state per head updated
     in place) and the long-prefill shape (1 x T steps x 16 heads, zero initial
@@ -302,7 +347,10 @@ def kda_section(dev, esa, E, reps: int = 3, T: int = 32768) -> dict:
     alpha, beta, and o (fp32) + lin (bf16).
     prefill: bound by the fp32 pipes — 7 flops per state element per step
     (forget 1, read 2, write 2, output 2); peak = 148 SMs x 128 fp32 lanes x
-    2 flops x the maximum SM clock."""
+    2 flops x the maximum SM clock.
+    With `oracle`, the oracle as it stands is timed beside each: whole decode
+    steps repeated for ~2 s; the prefill on one head in full, extrapolated to
+    every head over the host threads (heads are independent)."""
     peak_gbs, _, kind = _load_peaks()
     sm_mhz = 2032.0
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -312,8 +360,13 @@ def kda_section(dev, esa, E, reps: int = 3, T: int = 32768) -> dict:
     st = torch.cuda.current_stream(dev)
     res = {}
 
+    if oracle:
+        sys.path.insert(0, ROOT)
+        import oracle as O
+        O.lib()
     B, H, D, NB = 8, 32, 128, 16
-    x = {k: v.to(dev) for k, v in E.kda_inputs(B, 1, H, D, D, 2002, state=True).items()}
+    xh = E.kda_inputs(B, 1, H, D, D, 2002, state=True)
+    x = {k: v.to(dev) for k, v in xh.items()}
     states = [x["state"].clone() for _ in range(NB)]
     o = torch.empty(B, 1, H, D, dtype=torch.float32, device=dev)
     lin = torch.empty(B, 1, H, D, dtype=torch.bfloat16, device=dev)
@@ -347,11 +400,20 @@ def kda_section(dev, esa, E, reps: int = 3, T: int = 32768) -> dict:
                      "frac_of_hbm": nbytes / (best / 1e6) / 1e9 / peak_gbs, "peak_gbs": peak_gbs, "peak_kind": kind,
                      "l2": f"{NB} state buffers in rotation ({NB * B * H * D * D * 4 / 2**20:.0f} MiB > 126 MB L2)",
                      "timing": "CUDA graph of 16 launches, replayed 10 times; best of 3"}
+    if oracle:
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 2.0:
+            O.kda(xh["q"], xh["k"], xh["v"], xh["alpha"], xh["beta"], state_in=xh["state"])
+            n += 1
+        el = time.perf_counter() - t0
+        res["decode"]["cpu_baseline"] = {"us": el / n * 1e6, "tok_per_s": B * n / el, "cores": min(O.threads(), B * H),
+                                         "kind": "oracle", "sample": f"{n} whole decode steps, {el:.1f} s"}
     del x, states, o, lin, g
     torch.cuda.empty_cache()
 
     B, H = 1, 16
-    x = {k: v.to(dev) for k, v in E.kda_inputs(B, T, H, D, D, 2003).items()}
+    xh = E.kda_inputs(B, T, H, D, D, 2003)
+    x = {k: v.to(dev) for k, v in xh.items()}
     o = torch.empty(B, T, H, D, dtype=torch.float32, device=dev)
     lin = torch.empty(B, T, H, D, dtype=torch.bfloat16, device=dev)
     so = torch.empty(B, H, D, D, dtype=torch.float32, device=dev)
@@ -376,6 +438,16 @@ def kda_section(dev, esa, E, reps: int = 3, T: int = 32768) -> dict:
                            "achieved_tflops": flops / (best / 1e3) / 1e12, "bound": "alu",
                            "alu_peak_tflops": alu_peak, "frac_of_alu": flops / (best / 1e3) / 1e12 / alu_peak,
                            "alu_peak_from": f"148 SMs x 128 fp32 lanes x 2 flops x {sm_mhz:.0f} MHz"}
+    if oracle:
+        one = {k: v[:, :, :1].contiguous() for k, v in xh.items()}
+        t0 = time.perf_counter()
+        O.kda(one["q"], one["k"], one["v"], one["alpha"], one["beta"])
+        el = time.perf_counter() - t0
+        cores = min(O.threads(), B * H)
+        est = el * B * H / cores
+        res["long_prefill"]["cpu_baseline"] = {"ms": est * 1e3, "tok_per_s": B * T / est, "cores": cores,
+                                               "kind": "oracle, extrapolated",
+                                               "sample": f"one head of {B * H}, {T} steps, {el:.1f} s"}
     del x, o, lin, so
     torch.cuda.empty_cache()
     return res
@@ -582,14 +654,17 @@ def esa_arm(args):
 
     prefill = kda = None
     if rank == 0 and not args.no_prefill:
-        prefill = prefill_section(dev, esa, E, seq=args.prefill_seq)
+        prefill = prefill_section(dev, esa, E, seq=args.prefill_seq,
+                                  oracle_rows=0 if args.no_cpu_baseline else args.oracle_rows)
     if rank == 0 and not args.no_kda:
-        kda = kda_section(dev, esa, E, T=args.kda_steps)
+        kda = kda_section(dev, esa, E, T=args.kda_steps, oracle=not args.no_cpu_baseline)
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             v, cores, sample = run_cpu_baseline(cfg, host, seconds=args.cpu_seconds)
-            cpu = {"value": v, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample}
+            v1, sample1 = run_cpu_baseline_1thread(cfg, host, seconds=args.cpu_seconds / 2)
+            cpu = {"value": v, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample,
+                   "one_thread": {"value": v1, "unit": "tok/s", "cores": 1, "sample": sample1}}
         line = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
@@ -639,6 +714,8 @@ def main():
     ap.add_argument("--prefill-names", default="long_prefill,chunked_prefill,per_head_prefill,routed_prefill",
                     help="comma-separated prefill workloads for --prefill-only (profiling)")
     ap.add_argument("--no-kda", action="store_true", help="skip the KDA linear branch's timings")
+    ap.add_argument("--oracle-rows", type=int, default=64,
+                    help="query rows per prefill workload on which the oracle is timed (extrapolated)")
     ap.add_argument("--kda-only", action="store_true", help="time the KDA linear branch alone (profiling)")
     ap.add_argument("--kda-steps", type=int, default=32768, help="KDA prefill steps (profiling of small cases)")
     args = ap.parse_args()
