@@ -193,6 +193,58 @@ __device__ __forceinline__ void kda_step(const StepIn<R, CC> &x, float (&st)[CC]
     }
 }
 
+// Two steps t, t+1 with one lane-sum tree. From the state s before step t,
+//   u_t     = (k_t a_t) . s
+//   u_{t+1} = k_{t+1} . (a_{t+1} * (a_t * s + k_t d_t))
+//           = (k_{t+1} a_{t+1} a_t) . s + d_t ((k_{t+1} a_{t+1}) . k_t),
+// so the lane shares of (k_t a_t).s and (k_{t+1} a_{t+1} a_t).s for each
+// column and of the column-free (k_{t+1} a_{t+1}).k_t are summed over the NS
+// lanes together: one shuffle chain per two steps instead of two.
+template <int R, int NS, int CC>
+__device__ __forceinline__ void kda_step2(const StepIn<R, CC> &x0, const StepIn<R, CC> &x1, float (&st)[CC][R],
+                                          float *share0, float *share1) {
+    float kk1[R], red[2 * CC + 1];
+#pragma unroll
+    for (int m = 0; m < R; m++) kk1[m] = x1.k[m] * x1.a[m];
+    {
+        float pa[2] = {0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < R; m++) pa[m & 1] = fmaf(kk1[m], x0.k[m], pa[m & 1]);
+        red[2 * CC] = pa[0] + pa[1];
+    }
+#pragma unroll
+    for (int cc = 0; cc < CC; cc++) {
+        float p0[2] = {0.f, 0.f}, p1[2] = {0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < R; m++) {
+            p0[m & 1] = fmaf(x0.k[m] * x0.a[m], st[cc][m], p0[m & 1]);
+            p1[m & 1] = fmaf(kk1[m] * x0.a[m], st[cc][m], p1[m & 1]);
+        }
+        red[cc] = p0[0] + p0[1];
+        red[CC + cc] = p1[0] + p1[1];
+    }
+#pragma unroll
+    for (int off = 1; off < NS; off <<= 1)
+#pragma unroll
+        for (int i = 0; i < 2 * CC + 1; i++) red[i] += __shfl_xor_sync(0xffffffffu, red[i], off);
+#pragma unroll
+    for (int cc = 0; cc < CC; cc++) {
+        const float d0 = x0.b * (x0.v[cc] - red[cc]);
+        const float d1 = x1.b * (x1.v[cc] - fmaf(red[2 * CC], d0, red[CC + cc]));
+        float o0[2] = {0.f, 0.f}, o1[2] = {0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < R; m++) {
+            float v = fmaf(x0.k[m], d0, st[cc][m] * x0.a[m]);
+            o0[m & 1] = fmaf(x0.q[m], v, o0[m & 1]);
+            v = fmaf(x1.k[m], d1, v * x1.a[m]);
+            o1[m & 1] = fmaf(x1.q[m], v, o1[m & 1]);
+            st[cc][m] = v;
+        }
+        share0[cc * NS] = o0[0] + o0[1];
+        share1[cc * NS] = o1[0] + o1[1];
+    }
+}
+
 template <int DK, int NS, int CC>
 __global__ void __launch_bounds__(kKdaThreads) kda_kernel(const KdaArgs a) {
     using L = KdaLayout<DK, NS, CC>;
@@ -237,19 +289,31 @@ __global__ void __launch_bounds__(kKdaThreads) kda_kernel(const KdaArgs a) {
         cp_async_wait<1>();
         __syncthreads();
         const unsigned char *in = smem + (c & 1) * L::BUF;
-        // two operand sets alternate: the next step's operands are read while
-        // this step's chain runs
         // shares [kCT][COLS][NS]: this lane's column cl*CC+cc at (cl*CC+cc)*NS + s
         float *my = part + cl * CC * NS + s;
-        StepIn<R, CC> x0, x1;
-        load_step<DK, NS, CC>(in, 0, s, cl, x0);
-        for (int tt = 0; tt < n; tt += 2) {
-            load_step<DK, NS, CC>(in, min(tt + 1, n - 1), s, cl, x1);
-            kda_step<R, NS, CC>(x0, st, my + tt * COLS * NS);
-            if (tt + 1 >= n) break;
-            load_step<DK, NS, CC>(in, min(tt + 2, n - 1), s, cl, x0);
-            kda_step<R, NS, CC>(x1, st, my + (tt + 1) * COLS * NS);
+        // steps in pairs; two operand-set pairs alternate so that the next
+        // pair's operands are read while this pair's chain runs; an odd last
+        // step runs alone
+        StepIn<R, CC> xa0, xa1, xb0, xb1;
+        load_step<DK, NS, CC>(in, 0, s, cl, xa0);
+        load_step<DK, NS, CC>(in, min(1, n - 1), s, cl, xa1);
+        int tt = 0;
+        while (tt + 1 < n) {
+            load_step<DK, NS, CC>(in, min(tt + 2, n - 1), s, cl, xb0);
+            load_step<DK, NS, CC>(in, min(tt + 3, n - 1), s, cl, xb1);
+            kda_step2<R, NS, CC>(xa0, xa1, st, my + tt * COLS * NS, my + (tt + 1) * COLS * NS);
+            tt += 2;
+            if (tt + 1 >= n) {
+                if (tt < n) kda_step<R, NS, CC>(xb0, st, my + tt * COLS * NS);
+                tt = n;
+                break;
+            }
+            load_step<DK, NS, CC>(in, min(tt + 2, n - 1), s, cl, xa0);
+            load_step<DK, NS, CC>(in, min(tt + 3, n - 1), s, cl, xa1);
+            kda_step2<R, NS, CC>(xb0, xb1, st, my + tt * COLS * NS, my + (tt + 1) * COLS * NS);
+            tt += 2;
         }
+        if (tt < n) kda_step<R, NS, CC>(xa0, st, my + tt * COLS * NS);
         __syncthreads();  // the shares are complete; buffer c&1 is read and may be refilled
         // o_t[c] = scale * (the NS shares, in lane order); COLS consecutive
         // threads write one step's columns

@@ -73,21 +73,28 @@ def test_kda_small(c):
 
 
 def test_kda_state_carried_across_calls():
-    """Chunked prefill: 100 steps in one call, or 45 then 55 with the state
-    updated in place, give the same bits (the state is carried in fp32), and
-    both match the oracle."""
+    """Chunked prefill: 100 steps in one call, or 64 then 36 with the state
+    updated in place, give the same bits (the state is carried in fp32 and
+    the split falls on the kernel's 32-step staging, so every step is
+    computed alike); a split at 45 (steps paired differently) matches the
+    oracle; both match the oracle."""
     x = _inputs(2, 100, 2, 128, 128, 71, True)
     ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
     o, lin, so = _gpu(x, state_in=x["state"])
     _check(o, lin, so, ro, rs)
-    st = x["state"].clone().cuda()
-    parts = []
-    for a, b in ((0, 45), (45, 100)):
-        xs = {k: (v[:, a:b].contiguous() if k != "state" else v) for k, v in x.items()}
-        po, _, _ = _gpu(xs, state_in=st, inplace=True, lin=False)
-        parts.append(po)
-    assert torch.equal(torch.cat(parts, dim=1), o)
-    assert torch.equal(st.cpu(), so)
+    for cut, exact in ((64, True), (45, False)):
+        st = x["state"].clone().cuda()
+        parts = []
+        for a, b in ((0, cut), (cut, 100)):
+            xs = {k: (v[:, a:b].contiguous() if k != "state" else v) for k, v in x.items()}
+            po, _, _ = _gpu(xs, state_in=st, inplace=True, lin=False)
+            parts.append(po)
+        oc = torch.cat(parts, dim=1)
+        if exact:
+            assert torch.equal(oc, o)
+            assert torch.equal(st.cpu(), so)
+        else:
+            _check(oc, None, st.cpu(), ro, rs)
 
 
 def test_kda_empty_and_state_only():
