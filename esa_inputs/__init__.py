@@ -21,6 +21,10 @@ Generator (its definition, so that anyone can re-derive every value):
 * gate value: ``fp32(1 / (1 + exp(-z)))`` with ``z`` N(0,1) in fp64; the gate
   reaches the method already squashed into (0,1).
 * needles: distinct positions ``w mod (L-1)`` taken in counter order.
+* KDA linear branch: q and k are N(0,1) vectors (fp64) scaled to unit length,
+  then rounded to fp32 and bf16; v bf16 N(0,1); forgetting factors
+  ``0.9 + 0.1 * (w >> 11) * 2**-53`` in fp64, rounded to fp32; write
+  strengths ``fp32(1 / (1 + exp(-z)))``; initial state ``fp32(0.1 * z)``.
 """
 from __future__ import annotations
 
