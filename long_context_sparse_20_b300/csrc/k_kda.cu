@@ -12,21 +12,25 @@
 //
 // The recurrence is sequential in t but independent per value column c:
 // column c of S is a Dk-vector s with s = alpha_t * s, then
-// s += beta_t (v_t[c] - k_t . s) k_t. So the kernel spreads the columns over
-// the chip and holds each column in registers for the whole sequence:
-//   - 8 lanes per column, each holding Dk/8 key channels; a step is Dk/8
-//     multiplies and 3 Dk/8 FMAs per lane, plus two 3-level shuffle sums
-//     (k . s, on the step-to-step chain, and q . s, off it);
-//   - block = 4 warps = 16 columns of one (sequence, head); grid (Dv/16, H, B);
-//   - the inputs of CT steps (the head's q, k and alpha rows, the block's 16
-//     v values, beta) are staged in shared memory with cp.async, double
-//     buffered, laid out so that the 8 lanes of a column read 8 consecutive
-//     16-byte pieces (no bank conflicts; the 4 columns of a warp read the
-//     same pieces);
-//   - a chunk's outputs are staged in shared memory and stored as 64-byte rows
-//     (fp32 o and/or its bf16 rounding, the gate mix's lin input);
-//   - the state tile is read and written once, through shared memory, in
-//     64-byte rows (state_out may alias state_in: each block owns its tile).
+// s += beta_t (v_t[c] - k_t . s) k_t. Two kernels:
+//   kda_kernel (many steps) holds the state in registers for the whole
+//   sequence: NS lanes share CC columns, each lane R = Dk/NS key channels of
+//   them (Dk = 128: 16 lanes x 8 channels x 2 columns; Dk = 64: 8 x 8 x 1);
+//   a block of 4 warps holds 16 columns of one (sequence, head), grid
+//   (Dv/16, H, B).
+//   - The inputs of 32 steps (the head's q, k and alpha rows, the block's v
+//     values, beta) are staged in shared memory with cp.async, double
+//     buffered, laid out so that the NS lanes of a column group read
+//     consecutive 16-byte pieces (no bank conflicts).
+//   - Steps go in pairs: both steps' reads are written against the state
+//     before the pair (kda_step2), so one shuffle tree over the NS lanes
+//     serves two steps; the lanes' shares of q . s go to shared memory and a
+//     chunk's outputs are summed in lane order and stored once (fp32 o and/or
+//     its bf16 rounding, the gate mix's lin input).
+//   - The state tile is read and written once, through shared memory, in
+//     whole rows (state_out may alias state_in: each block owns its tile).
+//   kda_decode_kernel (at most 4 steps) streams the state through registers
+//   once per step in float4 rows (below).
 // Every sum is fp32 in a fixed order, so results are deterministic.
 #include <algorithm>
 #include <mutex>
