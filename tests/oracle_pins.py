@@ -596,6 +596,36 @@ def pin_kda_linear_attention(L):
     assert np.allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
 
 
+def pin_kda_chunked_form(L):
+    """The chunked (matrix) form of the recurrence, chunk by chunk of C steps
+    with g_t = prod_{tau <= t} alpha_tau inside the chunk: reads of the
+    chunk-start state W = (K*G) S, Z = (Q*G) S; intra-chunk couplings
+    A = strictly-lower((K*G)(K/G)^T), B = lower((Q*G)(K/G)^T); writes
+    D = (I + diag(beta) A)^{-1} diag(beta) (V - W); outputs scale (Z + B D);
+    state g_last * S + ((K/G) * g_last)^T D. Equal to the step-by-step
+    recurrence (C = 4, a ragged last chunk, an initial state, Dk != Dv)."""
+    q, k, v, alpha, beta, s0 = _kda_case(31, B=2, T=13, H=2, Dk=8, Dv=5)
+    o, st = O.kda(q, k, v, alpha, beta, state_in=s0, scale=0.6, L=L)
+    qd, kd, vd, ad = (_f64(x) for x in (q, k, v, alpha))
+    bd = beta.astype(np.float64)
+    B, T, H, _ = qd.shape
+    C = 4
+    for b in range(B):
+        for h in range(H):
+            S = s0[b, h].astype(np.float64)
+            for c0 in range(0, T, C):
+                sl = slice(c0, min(T, c0 + C))
+                Kc, Qc, Vc, Ac, bc = kd[b, sl, h], qd[b, sl, h], vd[b, sl, h], ad[b, sl, h], bd[b, sl, h]
+                G = np.cumprod(Ac, axis=0)
+                Kt, Qt, Ki = Kc * G, Qc * G, Kc / G
+                A = np.tril(Kt @ Ki.T, -1)
+                Bm = np.tril(Qt @ Ki.T)
+                D = np.linalg.solve(np.eye(len(bc)) + bc[:, None] * A, bc[:, None] * (Vc - Kt @ S))
+                assert np.allclose(o[b, sl, h], 0.6 * (Qt @ S + Bm @ D), rtol=1e-10, atol=1e-10)
+                S = G[-1][:, None] * S + (Ki * G[-1]).T @ D
+            assert np.allclose(st[b, h], S, rtol=1e-10, atol=1e-10)
+
+
 def pin_kda_extreme_gates(L):
     """alpha_t = 0 wipes the state before the write, so
     o_t = scale * beta_t * (q_t . k_t) * v_t whatever came before; beta = 0
@@ -634,4 +664,4 @@ ALL_PINS = [pin_indexer_golden, pin_indexer_numpy, pin_indexer_onehot, pin_index
             pin_indexer_modes_golden, pin_relu_special_and_numpy, pin_per_head_sets_are_sliced_queries,
             pin_per_head_attention_uses_its_set, pin_router_golden, pin_router_numpy, pin_router_closed_forms,
             pin_kda_golden, pin_kda_transition_matrices, pin_kda_retrieval, pin_kda_basis_keys,
-            pin_kda_linear_attention, pin_kda_chaining, pin_kda_extreme_gates]
+            pin_kda_linear_attention, pin_kda_chaining, pin_kda_extreme_gates, pin_kda_chunked_form]
