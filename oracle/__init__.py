@@ -63,8 +63,9 @@ def _bind(path: str):
     lib.oracle_kda.restype = c_int
     lib.oracle_kda.argtypes = [vp, vp, vp, vp, vp, vp, c_long, c_long, c_int, c_int, c_int, ctypes.c_double, vp, vp,
                                c_int]
-    lib.oracle_threshold_row.restype = c_int
-    lib.oracle_threshold_row.argtypes = [vp, c_long, c_int, vp, vp]
+    lib.oracle_threshold_rows.restype = c_int
+    lib.oracle_threshold_rows.argtypes = [vp, vp, vp, c_long, c_long, c_long, c_long, c_int, c_int, c_int, c_int, vp,
+                                          c_long, vp, c_int]
     return lib
 
 
@@ -225,12 +226,20 @@ def kda(q, k, v, alpha, beta, state_in=None, scale: float | None = None, L=None)
     return o, st
 
 
-def threshold(scores: np.ndarray, K: int, L=None):
-    """(T, ties_taken) of a score row: the K-th largest score and how many
-    positions scoring exactly T the index set holds."""
+def threshold(qI, kI, wI, shape: dict, K: int, rows=None, L=None) -> np.ndarray:
+    """int32 [n_rows, 2] threshold form (T, P) of each listed row's index set
+    (one set per row): key j <= p is selected iff s_j > T, or s_j == T and
+    j <= P; T = INT32_MIN and P = p when the prefix holds at most K keys."""
     L = L or lib()
-    s = np.ascontiguousarray(scores, dtype=np.int32)
-    T = ctypes.c_int32()
-    tt = ctypes.c_long()
-    L.oracle_threshold_row(_ptr(s), len(s), K, ctypes.byref(T), ctypes.byref(tt))
-    return int(T.value), int(tt.value)
+    qa, ka, wa = _np(qI, np.int8), _np(kI, np.int8), _np(wI, np.int32)
+    rr = _rows(shape["B"], shape["Tq"], rows)
+    flags = int(shape.get("flags", 0))
+    if flags & PER_HEAD:
+        raise ValueError("the threshold form describes one index set per row")
+    thr = np.empty((len(rr), 2), dtype=np.int32)
+    rc = L.oracle_threshold_rows(_ptr(qa), _ptr(ka), _ptr(wa), shape["B"], shape["Tq"], shape["Tk"],
+                                 shape["q_offset"], shape["H_I"], shape["D_I"], K, flags, _ptr(rr), len(rr), _ptr(thr),
+                                 threads())
+    if rc != 0:
+        raise ValueError("oracle_threshold_rows: a score does not fit in int32")
+    return thr

@@ -397,25 +397,55 @@ int oracle_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const fl
     return 0;
 }
 
-/* Threshold form of a row's index set, used to explain parity failures:
- * T = the K-th largest score (or INT32_MIN when p+1 <= K) and the number of
- * positions with score == T that the set holds. Returns 0. */
-int oracle_threshold_row(const int32_t *scores, long n, int K, int32_t *T, long *ties_taken) {
-    if (n <= K) {
-        *T = INT32_MIN;
-        *ties_taken = 0;
-        return 0;
+/*
+ * Threshold form of the index sets of a list of query rows (flat row id
+ * r = b*Tq + t; one index set per row, scored as in oracle_indexer_row_mode
+ * with head = -1). The top-K set of a row under the tie rule "lower position
+ * wins" is described by two integers:
+ *   T = the score of the K-th position in (score descending, position
+ *       ascending) order, and P = that K-th position itself;
+ *   key j <= p is in the set iff s_j > T, or s_j == T and j <= P
+ * (the positions scoring T that the set holds are exactly the lowest ones,
+ * and the K-th of the order is the last of them). When the prefix holds at
+ * most K keys the set is the whole prefix: T = INT32_MIN, P = p. The routed
+ * attention (Elastic Attention page, section 3.1: sparse heads inside the
+ * fused kernel) rebuilds its sparse heads' sets from this form.
+ * thr is [n_rows][2] = (T, P). Returns 0, or -1 on int32 overflow.
+ */
+int oracle_threshold_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
+                          long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
+                          int K, int flags, const int64_t *rows, long n_rows,
+                          int32_t *thr, int n_threads) {
+    const int relu = flags & 1;
+    int bad = 0;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#endif
+    for (long r = 0; r < n_rows; r++) {
+        const long b = rows[r] / Tq, t = rows[r] % Tq;
+        const long p = q_offset + t, n = p + 1;  /* keys 0..p */
+        if (n <= K) {
+            thr[2 * r] = INT32_MIN;
+            thr[2 * r + 1] = (int32_t)p;
+            continue;
+        }
+        int32_t *sc = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+        scored_pos *order = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
+        if (oracle_indexer_row_mode(qI, kI, wI, B, Tq, Tk, q_offset, H_I, D_I, b, t, relu, -1, sc) != n) {
+            bad |= 1;
+        } else {
+            for (long j = 0; j < n; j++) {
+                order[j].s = sc[j];
+                order[j].j = (int32_t)j;
+            }
+            qsort(order, (size_t)n, sizeof(scored_pos), by_score_then_position);
+            const scored_pos kth = order[K - 1];
+            thr[2 * r] = kth.s;
+            thr[2 * r + 1] = kth.j;
+        }
+        free(sc);
+        free(order);
     }
-    scored_pos *order = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
-    for (long j = 0; j < n; j++) {
-        order[j].s = scores[j];
-        order[j].j = (int32_t)j;
-    }
-    qsort(order, (size_t)n, sizeof(scored_pos), by_score_then_position);
-    *T = order[K - 1].s;
-    long tt = 0;
-    for (long i = 0; i < K; i++) tt += (order[i].s == *T);
-    *ties_taken = tt;
-    free(order);
-    return 0;
+    return bad ? -1 : 0;
 }

@@ -148,6 +148,43 @@ def pin_topk_bruteforce(L, seed=9):
             assert (idx[r, cnt[r]:] == -1).all()
 
 
+def pin_threshold_form(L, seed=23):
+    """The threshold form (T, P) of a row's set: the hand-worked rows of the
+    golden file, then on tie-heavy rows the set it describes
+    ({j : s_j > T or (s_j == T and j <= P)}) equals the brute-force counting
+    set, T equals the K-th largest score (numpy sort) and s_P == T; whole
+    prefixes give (INT32_MIN, p)."""
+    gv = _golden()
+    qI = np.array(gv["qI"], dtype=np.int8).reshape(1, 3, 2, 3)
+    kI = np.array(gv["kI"], dtype=np.int8).reshape(1, 3, 3)
+    w = np.array(gv["w"], dtype=np.int32)
+    sh = dict(B=1, Tq=3, Tk=3, q_offset=0, Hq=1, Hkv=1, D=64, H_I=2, D_I=3)
+    for K in (1, 2):
+        thr = O.threshold(qI, kI, w, sh, K, L=L)
+        assert thr.reshape(-1).tolist() == gv[f"thr{K}"], (K, thr)
+    rng = np.random.default_rng(seed)
+    imin = np.iinfo(np.int32).min
+    for trial in range(6):
+        B, Tq, Tk, qo, DI = 2, 6, 30, 24, 4
+        qI = rng.integers(-2, 2, (B, Tq, 1, DI), dtype=np.int8)  # small range: many ties
+        kI = rng.integers(-2, 2, (B, Tk, DI), dtype=np.int8)
+        w = np.ones(1, dtype=np.int32)
+        sh = dict(B=B, Tq=Tq, Tk=Tk, q_offset=qo, Hq=1, Hkv=1, D=64, H_I=1, D_I=DI)
+        K = [1, 2, 5, 24, 25, 31][trial]
+        thr = O.threshold(qI, kI, w, sh, K, L=L)
+        for r in range(B * Tq):
+            b, t = divmod(r, Tq)
+            s = O.indexer_row(qI, kI, w, sh, b, t, L=L)
+            T, P = int(thr[r, 0]), int(thr[r, 1])
+            n = len(s)
+            if n <= K:
+                assert (T, P) == (imin, n - 1), (trial, r, T, P)
+                continue
+            assert T == int(np.sort(s)[::-1][K - 1]) and int(s[P]) == T, (trial, r, T, P)
+            described = [j for j in range(n) if s[j] > T or (s[j] == T and j <= P)]
+            assert described == _topk_bruteforce(s, K), (trial, r)
+
+
 def pin_topk_lexsort(L, seed=13):
     cfg, sh, inp = _small(seed=seed, Tq=48, Tk=48, H_I=2, D_I=16, top_k=20, weights="1to4")
     K = 20
@@ -658,7 +695,7 @@ def pin_kda_chaining(L):
 
 
 ALL_PINS = [pin_indexer_golden, pin_indexer_numpy, pin_indexer_onehot, pin_indexer_bound,
-            pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special, pin_topk_needles,
+            pin_topk_bruteforce, pin_threshold_form, pin_topk_lexsort, pin_topk_special, pin_topk_needles,
             pin_attention_full_is_sdpa, pin_attention_sparse_is_masked_sdpa, pin_attention_closed_forms,
             pin_empty_set, pin_gate, pin_routing, pin_needles_closed_form,
             pin_indexer_modes_golden, pin_relu_special_and_numpy, pin_per_head_sets_are_sliced_queries,
