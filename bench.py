@@ -1,22 +1,21 @@
 """Benchmark of the gated fine-grained sparse attention hot path on B300.
 
 One step = one decode pass of the whole path for every sequence of the batch:
-indexer scores over the full 131,072-key cache, exact top-2048 selection
-(esa_topk_select), gathered sparse attention with the gate mix fused
-(esa_sparse_attn). Workload: 8 sequences, 1 new token each, 32 query heads
-sharing 1 KV head, head dim 128, indexer 1 head x 64 (int8), synthetic seeded
-inputs. Multi-GPU runs are replicas (each rank its own batch, no collective
-on the data path): scaling "weak", value = tokens of all ranks / max time.
+indexer scores over the full 131,072-key cache, exact top-2048 selection,
+gathered sparse attention with the gate mix fused. Workload: 8 sequences, 1
+new token each, 32 query heads sharing 1 KV head, head dim 128, indexer
+1 head x 64 (int8), synthetic seeded inputs. Multi-GPU runs are replicas
+(each rank its own batch, no collective on the data path): scaling "weak",
+value = tokens of all ranks / max time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl esa|reference] [--no-prefill]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl esa|reference]
 
-The JSON line's "prefill" object adds one forward of each prefill workload
-(long_prefill and chunked_prefill: Top-K selection + gathered attention;
-routed_prefill: the routed launch) with tokens/s and algorithmic TFLOP/s
-against the bf16 peak.
-  python bench.py --workload long_prefill|routed_prefill|million_decode|tiny_prefill
-
-Prints one JSON line.
+Rank 0 also times every other workload (the 1M-token decode, the tiny,
+long, chunked, per-head and routed prefills, the attention router and the
+KDA linear branch), each next to the oracle on the host cores. The stdout
+JSON line is compact: its "configs" map holds one short entry per workload
+(time, rate, roofline fraction, oracle rate); the full per-workload detail
+goes to stderr as a second JSON line.
 """
 from __future__ import annotations
 
@@ -133,17 +132,32 @@ def _traffic_for(kernel: str, src_files: list[str]):
 
 
 SELECT_SRC = ["long_context_sparse_20_b300/csrc/k_select_split.cu", "long_context_sparse_20_b300/csrc/esa_device.cuh"]
+FUSED_SRC = SELECT_SRC
 ATTN_SRC = ["long_context_sparse_20_b300/csrc/k_sparse_attn.cu", "long_context_sparse_20_b300/csrc/esa_device.cuh"]
 
 
 def decode_bytes(sh: dict, K: int):
-    """Algorithmic HBM bytes of one decode step, per kernel (DESIGN: roofline)."""
+    """Algorithmic HBM bytes of one decode step, per kernel: the selection
+    streams every indexer key once and writes the index list; the attention
+    reads the index list, gathers one K and one V row per selected key and
+    KV head, and reads q and lin and writes the fp32 output."""
     B, L, Hq, Hkv, D, HI, DI = (sh[k] for k in ("B", "Tk", "Hq", "Hkv", "D", "H_I", "D_I"))
     sel = B * L * DI + B * HI * DI + B * K * 4 + B * 4            # kI stream, qI, idx + cnt written
     k_sel = min(K, L)
     attn = B * k_sel * Hkv * D * 2 * 2 + B * k_sel * 4 + B * 4      # gathered K and V rows, idx + cnt read
     attn += B * Hq * D * 2 * 2 + B * Hq * D * 4 + Hq * 4            # q, lin in; out (fp32) out; g
     return sel, attn
+
+
+def fused_step_bytes(sh: dict, K: int) -> int:
+    """Algorithmic HBM bytes of one fused decode step: every indexer key
+    streamed once, the indexer queries, one K and one V row per selected key
+    and KV head, q and lin read, the fp32 output written, the gate. The index
+    list, the scores and the attention partials stay on chip (the partials
+    pass through L2 once)."""
+    B, L, Hq, Hkv, D, HI, DI = (sh[k] for k in ("B", "Tk", "Hq", "Hkv", "D", "H_I", "D_I"))
+    k_sel = min(K, L)
+    return (B * L * DI + B * HI * DI + B * k_sel * Hkv * D * 2 * 2 + B * Hq * D * (2 + 2 + 4) + Hq * 4)
 
 
 def run_cpu_baseline(cfg: dict, inp: dict, seconds: float = 10.0):
@@ -205,8 +219,22 @@ def oracle_row_sample(host: dict, sh: dict, K: int, n_rows: int = 16, seed: int 
     O.gated_sparse_attention(host, sh, K, rows=rows)
     el = time.perf_counter() - t0
     est = el * total / len(rows)
+    whole = len(rows) == total
     return {"tok_per_s": total / est, "unit": "tok/s", "cores": min(O.threads(), len(rows)),
-            "kind": "oracle, extrapolated", "sample": f"{len(rows)} seeded uniform rows of {total}, {el:.2f} s"}
+            "kind": "oracle" if whole else "oracle, extrapolated",
+            "sample": f"all {total} rows, {el:.2f} s" if whole else f"{len(rows)} seeded uniform rows of {total}, {el:.2f} s"}
+
+
+def decode_label(name: str, sh: dict, K: int) -> str:
+    """The workload string of a decode configuration, the same in both arms."""
+    return (f"{name}: B={sh['B']} x 1 new token, cache {sh['Tk']}, Hq={sh['Hq']}, Hkv={sh['Hkv']}, D={sh['D']}, "
+            f"indexer {sh['H_I']}x{sh['D_I']} int8, top_k={K}")
+
+
+def run_config(name: str, sh: dict, K: int, world: int) -> dict:
+    """The JSON line's "config" object, identical in both arms."""
+    return {"workload": decode_label(name, sh, K), "global_batch": sh["B"] * world, "seq_len": sh["Tk"],
+            "parallelism": f"replicas x{world}"}
 
 
 def reference_arm(args):
@@ -233,8 +261,7 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tok/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "B": sh["B"], "cache_len": sh["Tk"], "Hq": sh["Hq"],
-                       "Hkv": sh["Hkv"], "D": sh["D"], "D_I": sh["D_I"], "top_k": K},
+            "config": run_config(args.workload, sh, K, 1),
             "cpu_baseline": {"value": val, "unit": "tok/s", "cores": 1, "kind": "oracle",
                              "sample": f"{args.steps} steps of one query row each (rows taken in turn)"},
             "e2e": {"value": val, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -242,11 +269,11 @@ def reference_arm(args):
 
 
 def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
-                    names=("long_prefill", "chunked_prefill", "per_head_prefill", "routed_prefill"),
+                    names=("tiny_prefill", "long_prefill", "chunked_prefill", "per_head_prefill", "routed_prefill"),
                     oracle_rows: int = 0) -> dict:
-    """The two prefill workloads, one forward each (after one untimed warm-up),
-    timed with CUDA events on the launching stream. Inputs (hundreds of MB to
-    GBs) exceed the 126 MB L2. Algorithmic flops count what the method
+    """The prefill workloads, one forward each (after one untimed warm-up),
+    timed with CUDA events on the launching stream. Inputs exceed the 126 MB
+    L2 except for the tiny prefill's (a few MB: launch-bound at any rate). Algorithmic flops count what the method
     computes: causal pairs for full heads, selected pairs (min(K, p+1) per
     row) for sparse heads, 4*D flops per pair (Q.K and P.V)."""
     _, tf_peak, kind = _load_peaks()
@@ -327,7 +354,8 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
                       "tensor_peak_tflops": tf_peak, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tf_peak,
                       "peak_kind": kind})
         if oracle_rows:
-            entry["cpu_baseline"] = oracle_row_sample(host, sh, K, n_rows=oracle_rows)
+            entry["cpu_baseline"] = oracle_row_sample(host, sh, K, n_rows=min(oracle_rows, B * S) if B * S > 4096
+                                                      else B * S)
         res[name] = entry
         del d, host, out
         torch.cuda.empty_cache()
@@ -453,56 +481,61 @@ def kda_section(dev, esa, E, reps: int = 3, T: int = 32768, oracle: bool = False
     return res
 
 
-def esa_arm(args):
-    world, rank, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if args.kda_only:  # profiling aid: the KDA linear branch alone
-        sys.path.insert(0, ROOT)
-        import esa_inputs as E
-        import long_context_sparse_20_b300 as esa
-        if rank == 0:
-            print(json.dumps({"linear_branch": kda_section(dev, esa, E, T=args.kda_steps)}), flush=True)
-        return
-    if args.prefill_only:  # profiling aid: the prefill workloads alone
-        sys.path.insert(0, ROOT)
-        import esa_inputs as E
-        import long_context_sparse_20_b300 as esa
-        if rank == 0:
-            print(json.dumps({"prefill": prefill_section(dev, esa, E, seq=args.prefill_seq,
-                                                         names=args.prefill_names.split(","))}), flush=True)
-        return
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    sys.path.insert(0, ROOT)
-    import esa_inputs as E
-    import long_context_sparse_20_b300 as esa
+def decode_section(dev, esa, E, name: str, args, world: int, e2e: bool) -> dict:
+    """Time decode steps of workload `name` (inputs resident in HBM).
 
-    cfg = dict(E.CONFIGS[args.workload])
+    NSETS rotating copies of the whole decode state (their kI caches exceed
+    the 126 MB L2). The K = args.steps timed steps are captured once into a
+    CUDA graph (host launch overhead would otherwise starve the GPU),
+    replayed once untimed, then `args.repeats` times timed, each replay
+    bracketed by a barrier and a synchronize with CUDA events on the
+    launching stream; the step time is the median replay over K (the max
+    over ranks of each replay first). The timed graph holds kernels only: an
+    event between the kernels of a step would cut the programmatic
+    (early-launch) edge between them; a second graph of the same steps with
+    an event around each kernel gives the per-kernel durations (the
+    roofline's launch time). With `e2e`, the same steps also run end to end
+    through host buffers."""
+    cfg = dict(E.CONFIGS[name])
     assert cfg["Tq"] == 1, "the step benchmark runs decode workloads"
     sh = E.shape_of(cfg)
     K = cfg["top_k"]
     B, L, Hq, Hkv, D, HI, DI = (sh[k] for k in ("B", "Tk", "Hq", "Hkv", "D", "H_I", "D_I"))
+    rank = _dist()[1]
     host = E.make_inputs(cfg, seed=cfg["seed"] + 1000 * rank)
     shape = esa.shape_from(sh)
     scale = 1.0 / math.sqrt(D)
 
-    # NSETS rotating copies of the whole decode state, each with its outputs
+    # the decode step: esa_topk_select + esa_sparse_attn (two public calls,
+    # each kernel timed apart for the roofline), or the one-call
+    # esa_gated_sparse_attn (--gated; a single launch with ESA_DECODE_PATH=fused)
+    fused = args.gated or os.environ.get("ESA_DECODE_PATH") == "fused"
     sets = []
     for _ in range(args.sets):
         d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
-        d["idx"] = torch.empty(B, 1, K, dtype=torch.int32, device=dev)
-        d["cnt"] = torch.empty(B, 1, dtype=torch.int32, device=dev)
         d["out"] = torch.empty(B, 1, Hq, D, dtype=torch.float32, device=dev)
-        d["ws_sel"] = esa.workspace_for(esa.OP_TOPK_SELECT, shape, K, dev)
-        d["ws_att"] = esa.workspace_for(esa.OP_SPARSE_ATTN, shape, K, dev)
+        if fused:
+            d["ws"] = esa.workspace_for(esa.OP_GATED_SPARSE_ATTN, shape, K, dev)
+        else:
+            d["idx"] = torch.empty(B, 1, K, dtype=torch.int32, device=dev)
+            d["cnt"] = torch.empty(B, 1, dtype=torch.int32, device=dev)
+            d["ws_sel"] = esa.workspace_for(esa.OP_TOPK_SELECT, shape, K, dev)
+            d["ws_att"] = esa.workspace_for(esa.OP_SPARSE_ATTN, shape, K, dev)
         sets.append(d)
+    single = fused and os.environ.get("ESA_DECODE_PATH") == "fused"  # one cooperative launch per step
+    launches_per_step = 1 if single else 2
 
     def step(d, ev=None):
         st = torch.cuda.current_stream(dev)
         if ev:
             ev[0].record(st)
+        if fused:  # the whole path in one call
+            esa.esa_gated_sparse_attn(d["q"], d["k"], d["v"], d["qI"], d["kI"], d["wI"], shape, K, scale, d["g"],
+                                      d["lin"], d["out"], None, None, None, d["ws"], st)
+            if ev:
+                ev[1].record(st)
+                ev[2].record(st)
+            return
         esa.esa_topk_select(d["qI"], d["kI"], d["wI"], shape, K, d["idx"], d["cnt"], d["ws_sel"], st)
         if ev:
             ev[1].record(st)
@@ -511,27 +544,23 @@ def esa_arm(args):
         if ev:
             ev[2].record(st)
 
+    def check_status():
+        for d in sets:
+            for w in ((d["ws"],) if fused else (d["ws_sel"], d["ws_att"])):
+                assert esa.esa_read_status(w) == 0
+
     for i in range(max(3, args.warmup)):
         step(sets[i % len(sets)])
     torch.cuda.synchronize()
-    for d in sets:
-        for w in (d["ws_sel"], d["ws_att"]):
-            assert esa.esa_read_status(w) == 0
+    check_status()
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    # The K timed steps are captured once into a CUDA graph, so that host
-    # launch overhead does not starve the GPU; the graph is replayed once
-    # untimed, then once timed. The timed graph holds kernels only: an event
-    # between the two kernels of a step would cut the programmatic
-    # (early-launch) dependency between them. A second graph of the same K
-    # steps with an event around each kernel is replayed after the timed run
-    # for the per-kernel durations (the roofline's launch time).
     evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] for _ in range(args.steps)]
-    timing = "cuda-graph"
+    timing = f"median of {args.repeats} timed replays of a {args.steps}-step CUDA graph"
 
     def capture(with_events):
         gr = torch.cuda.CUDAGraph()
@@ -546,7 +575,7 @@ def esa_arm(args):
         run = capture(False)
         run_breakdown = capture(True)
     except Exception as exc:  # capture unsupported: time eager launches
-        timing = f"eager ({type(exc).__name__})"
+        timing = f"median of {args.repeats} timed runs of {args.steps} eager steps ({type(exc).__name__})"
         torch.cuda.synchronize()
 
         def run():
@@ -556,32 +585,72 @@ def esa_arm(args):
         def run_breakdown():
             for i in range(args.steps):
                 step(sets[i % len(sets)], evs[i])
-    with Clocks(local) as clk:
-        barrier()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record()
-        run()
-        t1.record()
-        barrier()
+    replays = []
+    with Clocks(torch.cuda.current_device()) as clk:
+        for _ in range(args.repeats):
+            barrier()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            run()
+            t1.record()
+            barrier()
+            replays.append(t0.elapsed_time(t1))
     clocks = clk.summary()
-    total_ms = t0.elapsed_time(t1)
+    replays = max_over_ranks(replays, world, dev)
+    ms_step = statistics.median(replays) / args.steps
     run_breakdown()
     torch.cuda.synchronize()
-    sel_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    att_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    for d in sets:
-        for w in (d["ws_sel"], d["ws_att"]):
-            assert esa.esa_read_status(w) == 0
+    sel_avg = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    att_avg = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    check_status()
+
+    peak_gbs, _, peak_kind = _load_peaks()
+    if fused:
+        # the single launch keeps the index list on chip; two launches
+        # write it and read it back
+        step_bytes = fused_step_bytes(sh, K) if single else sum(decode_bytes(sh, K))
+        sel_bytes, att_bytes = step_bytes, 0
+        dom_name = "decode_step (single launch)" if single else "esa_gated_sparse_attn (select + attention)"
+        dom_ms, dom_bytes = sel_avg, step_bytes
+        traffic = _traffic_for("decode_step", FUSED_SRC)
+        kernels = {"decode_step": sel_avg * 1e3}
+    else:
+        sel_bytes, att_bytes = decode_bytes(sh, K)
+        dom_is_sel = sel_avg >= att_avg
+        dom_name = "split_select" if dom_is_sel else "sparse_attn"
+        dom_ms, dom_bytes = (sel_avg, sel_bytes) if dom_is_sel else (att_avg, att_bytes)
+        traffic = _traffic_for(dom_name, SELECT_SRC if dom_is_sel else ATTN_SRC)
+        kernels = {"split_select": sel_avg * 1e3, "sparse_attn": att_avg * 1e3}
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    res = {
+        "name": name, "sh": sh, "K": K, "host": host, "cfg": cfg, "ms_per_step": ms_step,
+        "replay_ms": replays, "timing": timing, "clocks": clocks, "launches_per_step": launches_per_step,
+        "l2": f"{args.sets} rotating input sets (kI caches {args.sets * B * L * DI / 2**20:.0f} MiB"
+              f"{' > 126 MB L2' if args.sets * B * L * DI > 126e6 else ', within L2'})",
+        "roofline": {"bound": "hbm", "kernel": dom_name,
+                     "achieved": achieved, "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
+                     "peak_kind": peak_kind, "traffic": traffic, "algorithmic_bytes": dom_bytes,
+                     "avg_launch_us": dom_ms * 1e3},
+        "kernels_us": kernels,
+        "step_roofline": {"achieved": (sel_bytes + att_bytes) / (ms_step / 1e3) / 1e9, "peak": peak_gbs,
+                          "frac": (sel_bytes + att_bytes) / (ms_step / 1e3) / 1e9 / peak_gbs,
+                          "algorithmic_bytes": sel_bytes + att_bytes},
+    }
+    if not e2e:
+        del sets
+        torch.cuda.empty_cache()
+        return res
 
     # ---- end to end through host buffers: per step copy the new token's
     # inputs in (q, qI, lin, and its K/V/kI rows, written into the caches at
     # position L-1) and the output back. The inputs travel as ONE copy from a
     # pinned staging buffer into a device staging buffer whose typed views
     # are the step's q, qI and lin; three device copies place the new cache
-    # rows. Each input set's whole step (copy in, row placement, the two
-    # library calls, copy out) is captured once into a CUDA graph and
-    # replayed per step.
+    # rows. Each input set's whole step (copy in, row placement, the library
+    # calls, copy out) is captured once into a CUDA graph and replayed per
+    # step. A decode step's inputs depend on the previous step's output, so
+    # the steps are serialised on one stream.
     parts = [host["q"], host["qI"], host["lin"], host["k"][:, L - 1:L], host["v"][:, L - 1:L], host["kI"][:, L - 1:L]]
     parts = [t.contiguous() for t in parts]
     nbytes = [t.numel() * t.element_size() for t in parts]
@@ -628,72 +697,143 @@ def esa_arm(args):
         e2e_run = e2e_steps
     for i in range(3):
         e2e_run[i % len(e2e_run)]()
-    barrier()
-    a0 = time.perf_counter()
-    for i in range(args.steps):
-        e2e_run[i % len(e2e_run)]()
-    torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - a0) * 1e3
-    barrier()
-    for d in sets:
-        for w in (d["ws_sel"], d["ws_att"]):
-            assert esa.esa_read_status(w) == 0
+    e2e_reps = []
+    for _ in range(args.repeats):
+        barrier()
+        a0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_run[i % len(e2e_run)]()
+        torch.cuda.synchronize()
+        e2e_reps.append((time.perf_counter() - a0) * 1e3)
+        barrier()
+    check_status()
+    e2e_reps = max_over_ranks(e2e_reps, world, dev)
+    e2e_ms = statistics.median(e2e_reps) / args.steps
+    res["e2e"] = {"value": job_rate(B, world, e2e_ms), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                  "timing": f"{e2e_timing}, median of {args.repeats} runs of {args.steps} steps (host clock)"}
+    del sets, e2e_run, e2e_steps
+    torch.cuda.empty_cache()
+    return res
 
-    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], world, dev)
-    ms_step = total_ms / args.steps
-    tok_per_step = B * world
+
+def _r(x, n=4):
+    """A number rounded to n significant digits (keeps the JSON line short)."""
+    if x is None or not isinstance(x, (int, float)) or x == 0 or not math.isfinite(x):
+        return x
+    return float(f"{x:.{n}g}")
+
+
+def summarise(dec: dict, mdec: dict | None, prefill: dict | None, kda: dict | None, cpu: dict | None,
+              mcpu: dict | None) -> dict:
+    """One short entry per workload: time, rate, roofline fraction, oracle rate."""
+    out = {}
+    if prefill and "tiny_prefill" in prefill:
+        p = prefill["tiny_prefill"]
+        out["1_tiny_prefill"] = {"ms": _r(p["ms"]), "tok_s": _r(p["tok_per_s"]), "bound": "launch",
+                                 "cpu_tok_s": _r((p.get("cpu_baseline") or {}).get("tok_per_s"))}
+    for key, d, c in (("2_decode", dec, cpu), ("5_million_decode", mdec, mcpu)):
+        if d:
+            out[key] = {"us": _r(d["ms_per_step"] * 1e3), "tok_s": _r(d["sh"]["B"] / d["ms_per_step"] * 1e3),
+                        "hbm_frac": _r(d["step_roofline"]["frac"], 3),
+                        "top_kernel_frac": _r(d["roofline"]["frac"], 3),
+                        "cpu_tok_s": _r((c or {}).get("value"))}
+    for key, name in (("3_long_prefill", "long_prefill"), ("4_routed_prefill", "routed_prefill"),
+                      ("chunked_prefill", "chunked_prefill"), ("per_head_prefill", "per_head_prefill")):
+        if prefill and name in prefill:
+            p = prefill[name]
+            e = {"ms": _r(p["ms"]), "tok_s": _r(p["tok_per_s"]), "bf16_frac": _r(p["frac_of_bf16_peak"], 3)}
+            e.update({k: _r(v) for k, v in p["kernels_ms"].items()})
+            e["cpu_tok_s"] = _r((p.get("cpu_baseline") or {}).get("tok_per_s"))
+            out[key] = e
+            if "router" in p:
+                out["router"] = {"ms": _r(p["router"]["ms"]), "hbm_frac": _r(p["router"]["frac_of_hbm"], 3)}
+    if kda:
+        if "decode" in kda:
+            k = kda["decode"]
+            out["kda_decode"] = {"us": _r(k["us"]), "hbm_frac": _r(k["frac_of_hbm"], 3),
+                                 "cpu_tok_s": _r((k.get("cpu_baseline") or {}).get("tok_per_s"))}
+        if "long_prefill" in kda:
+            k = kda["long_prefill"]
+            out["kda_prefill"] = {"ms": _r(k["ms"]), "alu_frac": _r(k["frac_of_alu"], 3),
+                                  "cpu_tok_s": _r((k.get("cpu_baseline") or {}).get("tok_per_s"))}
+    return out
+
+
+def esa_arm(args):
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if args.kda_only:  # profiling aid: the KDA linear branch alone
+        sys.path.insert(0, ROOT)
+        import esa_inputs as E
+        import long_context_sparse_20_b300 as esa
+        if rank == 0:
+            print(json.dumps({"linear_branch": kda_section(dev, esa, E, T=args.kda_steps)}), flush=True)
+        return
+    if args.prefill_only:  # profiling aid: the prefill workloads alone
+        sys.path.insert(0, ROOT)
+        import esa_inputs as E
+        import long_context_sparse_20_b300 as esa
+        if rank == 0:
+            print(json.dumps({"prefill": prefill_section(dev, esa, E, seq=args.prefill_seq,
+                                                         names=args.prefill_names.split(","))}), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sys.path.insert(0, ROOT)
+    import esa_inputs as E
+    import long_context_sparse_20_b300 as esa
+
+    dec = decode_section(dev, esa, E, args.workload, args, world, e2e=True)
+    sh, K, B = dec["sh"], dec["K"], dec["sh"]["B"]
+    ms_step = dec["ms_per_step"]
     value = job_rate(B, world, ms_step)
 
-    sel_bytes, att_bytes = decode_bytes(sh, K)
-    sel_avg, att_avg = statistics.mean(sel_ms), statistics.mean(att_ms)
-    peak_gbs, _, peak_kind = _load_peaks()
-    dom_is_sel = sel_avg >= att_avg
-    dom_ms, dom_bytes = (sel_avg, sel_bytes) if dom_is_sel else (att_avg, att_bytes)
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    traffic = _traffic_for("split_select" if dom_is_sel else "sparse_attn", SELECT_SRC if dom_is_sel else ATTN_SRC)
-
-    prefill = kda = None
+    mdec = prefill = kda = cpu = mcpu = None
+    other = "million_decode" if args.workload != "million_decode" else "decode"
+    if rank == 0 and not args.no_extra_decode:
+        mdec = decode_section(dev, esa, E, other, args, 1, e2e=False)
     if rank == 0 and not args.no_prefill:
         prefill = prefill_section(dev, esa, E, seq=args.prefill_seq,
                                   oracle_rows=0 if args.no_cpu_baseline else args.oracle_rows)
     if rank == 0 and not args.no_kda:
         kda = kda_section(dev, esa, E, T=args.kda_steps, oracle=not args.no_cpu_baseline)
     if rank == 0:
-        cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            v, cores, sample = run_cpu_baseline(cfg, host, seconds=args.cpu_seconds)
-            v1, sample1 = run_cpu_baseline_1thread(cfg, host, seconds=args.cpu_seconds / 2)
+            v, cores, sample = run_cpu_baseline(dec["cfg"], dec["host"], seconds=args.cpu_seconds)
+            v1, sample1 = run_cpu_baseline_1thread(dec["cfg"], dec["host"], seconds=args.cpu_seconds / 2)
             cpu = {"value": v, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample,
                    "one_thread": {"value": v1, "unit": "tok/s", "cores": 1, "sample": sample1}}
+            if mdec:
+                v, cores, sample = run_cpu_baseline(mdec["cfg"], mdec["host"], seconds=args.cpu_seconds / 2)
+                mcpu = {"value": v, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample}
+        configs = summarise(dec if args.workload == "decode" else mdec, mdec if args.workload == "decode" else dec,
+                            prefill, kda, cpu if args.workload == "decode" else mcpu,
+                            mcpu if args.workload == "decode" else cpu)
+        roof = {k: (_r(v) if isinstance(v, float) else v) for k, v in dec["roofline"].items()}
         line = {
             "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
+            "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": _r(ms_step * 1e3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded counter-based generator)",
-            "config": {"workload": f"{args.workload}: B={B} x 1 new token, cache {L}, Hq={Hq}, Hkv={Hkv}, D={D}, "
-                                   f"indexer {HI}x{DI} int8, top_k={K}",
-                       "global_batch": B * world, "seq_len": L, "parallelism": f"replicas x{world}",
-                       "l2": f"{args.sets} rotating input sets (kI caches {args.sets * B * L * DI / 2**20:.0f} MiB"
-                             f"{' > 126 MB L2' if args.sets * B * L * DI > 126e6 else ', within L2'})",
-                       "timing": timing},
-            "roofline": {"bound": "hbm", "kernel": "split_select" if dom_is_sel else "sparse_attn",
-                         "achieved": achieved, "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
-                         "peak_kind": peak_kind, "traffic": traffic, "algorithmic_bytes": dom_bytes,
-                         "avg_launch_us": dom_ms * 1e3,
-                         "launch_time_from": "replay of the timed graph with an event around each kernel"},
-            "kernels_us": {"split_select": sel_avg * 1e3, "sparse_attn": att_avg * 1e3},
-            "step_roofline": {"achieved": (sel_bytes + att_bytes) / (ms_step / 1e3) / 1e9, "peak": peak_gbs,
-                              "frac": (sel_bytes + att_bytes) / (ms_step / 1e3) / 1e9 / peak_gbs,
-                              "algorithmic_bytes": sel_bytes + att_bytes},
-            "gpu_launches": 2 * args.steps,
-            "e2e": {"value": job_rate(B, world, e2e_ms / args.steps), "unit": "tok/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps, "timing": e2e_timing},
-            "clocks": clocks,
-            "cpu_baseline": cpu,
-            "prefill": prefill,
-            "linear_branch": kda,
+            "data": "synthetic (seeded)",
+            "config": run_config(args.workload, sh, K, world),
+            "timing": f"{dec['timing']}; {dec['l2']}",
+            "roofline": roof,
+            "step_roofline_frac": _r(dec["step_roofline"]["frac"], 3),
+            "gpu_launches": dec["launches_per_step"] * args.steps,
+            "e2e": {k: (_r(v) if isinstance(v, float) else v) for k, v in dec["e2e"].items() if k != "timing"},
+            "clocks": dec["clocks"],
+            "cpu_baseline": ({k: (_r(v) if isinstance(v, float) else v) for k, v in cpu.items() if k != "one_thread"}
+                             if cpu else None),
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
+        detail = {"decode": {k: v for k, v in dec.items() if k not in ("host", "cfg")},
+                  "other_decode": {k: v for k, v in mdec.items() if k not in ("host", "cfg")} if mdec else None,
+                  "cpu_baseline": cpu, "other_cpu_baseline": mcpu, "prefill": prefill, "linear_branch": kda}
+        print(json.dumps({"detail": detail}, default=str), file=sys.stderr, flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -701,8 +841,9 @@ def esa_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--repeats", type=int, default=7, help="timed replays of the K-step graph (median taken)")
     ap.add_argument("--impl", default="esa", choices=["esa", "reference"])
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -711,9 +852,13 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill workloads' timings")
     ap.add_argument("--prefill-only", action="store_true", help="time the prefill workloads only (profiling)")
     ap.add_argument("--prefill-seq", type=int, default=0, help="override the prefill sequence length (profiling)")
-    ap.add_argument("--prefill-names", default="long_prefill,chunked_prefill,per_head_prefill,routed_prefill",
+    ap.add_argument("--prefill-names", default="tiny_prefill,long_prefill,chunked_prefill,per_head_prefill,routed_prefill",
                     help="comma-separated prefill workloads for --prefill-only (profiling)")
     ap.add_argument("--no-kda", action="store_true", help="skip the KDA linear branch's timings")
+    ap.add_argument("--no-extra-decode", action="store_true", help="skip the second decode workload")
+    ap.add_argument("--gated", action="store_true",
+                    help="decode step as the one-call esa_gated_sparse_attn instead of esa_topk_select + "
+                         "esa_sparse_attn")
     ap.add_argument("--oracle-rows", type=int, default=64,
                     help="query rows per prefill workload on which the oracle is timed (extrapolated)")
     ap.add_argument("--kda-only", action="store_true", help="time the KDA linear branch alone (profiling)")

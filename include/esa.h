@@ -34,6 +34,15 @@
  *     call (they clear what they use), except after a device error, after
  *     which it must be re-initialised. Calls that share a workspace must not
  *     overlap in time (use one stream per workspace).
+ *   - Decode-like selections (esa_topk_select, esa_gated_sparse_attn and
+ *     esa_topk_select_noalloc on few rows with long prefixes) keep a small
+ *     state between calls (a call counter, barrier counters, histograms),
+ *     each call clearing what the next one needs. Such calls may share one
+ *     workspace (sized for the largest) across shapes. A workspace that any
+ *     other call used since (another op, or a prefill-like shape) must be
+ *     re-initialised with esa_workspace_init before the next decode-like
+ *     selection: their scratch may overlap that state. Stale state makes
+ *     results wrong (or sets a status), never an out-of-bounds access.
  *
  * Shapes (esa_shape):
  *   B sequences; Tq query rows per sequence; Tk key positions per sequence;
@@ -127,6 +136,8 @@ typedef struct esa_shape {
 #define ESA_OP_GATED_MIX 3
 #define ESA_OP_ROUTED_ATTN 4
 #define ESA_OP_ROUTE_HEADS 5
+#define ESA_OP_TOPK_THRESHOLD 6
+#define ESA_OP_GATED_SPARSE_ATTN 7
 
 /* Bytes of workspace that `op` needs for shape `s` and `top_k` (0 when the
  * op needs none beyond the status word, which every op may write; the
@@ -177,6 +188,32 @@ ESA_API esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const u
                            const int32_t *cnt, const esa_shape *s, int top_k, float scale, const float *g,
                            const uint16_t *lin, float *out, float *lse, void *ws, size_t ws_bytes, void *stream);
 
+/* The whole gated sparse path in one call: the Gated DSA pseudo-code's
+ * gated_sparse_attention(query, history_keys, history_values, top_k) (first
+ * page, section 四.1; sections 二.1-二.3): indexer scores, per-row top-K,
+ * attention over the gathered keys, gate mix. Computes exactly what
+ * esa_topk_select followed by esa_sparse_attn computes (same index sets,
+ * outputs within the same tolerance of the exact result), and writes the
+ * index sets to idx/cnt when they are given (both or neither; layouts as
+ * esa_topk_select's).
+ * It runs the selection kernel and the gathered-attention kernel back to
+ * back on `stream` (the attention launched early on the programmatic
+ * edge). With the environment variable ESA_DECODE_PATH=fused, decode-like
+ * shapes (few rows, long prefixes: B*Tq up to half the SMs, one index set
+ * per row, D in {64, 128}, (Hq/Hkv rounded up to 16) * Hkv up to 128
+ * query-head rows) take ONE cooperative launch instead: each block scores
+ * its span of the cache, the row's blocks agree on the threshold, each
+ * block attends over its own selected keys, and their partial softmax
+ * results are merged inside the same launch. Both give the same index sets
+ * and outputs within the same tolerance; the two launches are the default
+ * because they measured faster on B300. Workspace:
+ * esa_workspace_size(ESA_OP_GATED_SPARSE_ATTN, s, top_k) bytes. g, lin, lse
+ * nullable as in esa_sparse_attn; idx, cnt nullable. */
+ESA_API esa_status esa_gated_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
+                                         const int8_t *kI, const int32_t *wI, const esa_shape *s, int top_k,
+                                         float scale, const float *g, const uint16_t *lin, float *out, float *lse,
+                                         int32_t *idx, int32_t *cnt, void *ws, size_t ws_bytes, void *stream);
+
 /* Gate mix on its own (Gated DSA page, sections 二.3 and 四.1 step 5):
  *   out[b,t,h,:] = g[h]*attn[b,t,h,:] + (1-g[h])*lin[b,t,h,:]
  * for heads with head_mask[b,h] != 0 (all heads when head_mask is NULL);
@@ -197,6 +234,23 @@ ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const u
                            const int8_t *kI, const int32_t *wI, const uint8_t *route, const esa_shape *s, int top_k,
                            float scale, const float *g, const uint16_t *lin, float *out, void *ws, size_t ws_bytes,
                            void *stream);
+
+/* The threshold form of every query row's Top-K set: the selection step of
+ * esa_routed_attn, whose sparse heads rebuild their index set from it inside
+ * the fused attention launch (Elastic Attention page, section 3.1; the set
+ * itself is the Gated DSA page's top-K, section 二.1). For each row, with s_j
+ * the indexer score of esa_indexer_score and n = p+1:
+ *   n <= top_k:  thr[b,t,0] = INT32_MIN, thr[b,t,1] = p   (the whole prefix);
+ *   otherwise:   order the positions 0..p by (score descending, position
+ *                ascending); thr[b,t,0] = T, the score of the top_k-th of
+ *                that order, and thr[b,t,1] = P, its position.
+ * Key j <= p is in the row's set iff s_j > T, or s_j == T and j <= P: the
+ * same set as esa_topk_select's idx row. thr int32 [B, Tq, 2]. One index
+ * set per row only (ESA_PER_HEAD_SETS returns ESA_ERR_UNSUPPORTED).
+ * Workspace esa_workspace_size(ESA_OP_TOPK_THRESHOLD, s, top_k) bytes;
+ * the same kernels and workspace layout as the routed call's selection. */
+ESA_API esa_status esa_topk_threshold(const int8_t *qI, const int8_t *kI, const int32_t *wI, const esa_shape *s,
+                                      int top_k, int32_t *thr, void *ws, size_t ws_bytes, void *stream);
 
 /* Attention router (Elastic Attention page, section 2.2: a lightweight
  * 2-layer MLP on the current key hidden states decides, per attention head,
@@ -261,8 +315,13 @@ ESA_API esa_status esa_kda(const uint16_t *q, const uint16_t *k, const uint16_t 
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture on the device.
  *   - Shapes whose scratch would exceed ESA_NOALLOC_SCRATCH_BYTES return
- *     ESA_ERR_UNSUPPORTED (decode with up to 8 query rows and prefill of any
- *     size fit).
+ *     ESA_ERR_UNSUPPORTED. The limit counts selection rows: B*Tq, times H_I
+ *     with ESA_PER_HEAD_SETS. A decode batch whose selection spreads over
+ *     the SMs (at most half as many rows as SMs) fits with up to about 26
+ *     selection rows on a 148-SM GPU (per-block published counts, ~4.9 MB,
+ *     plus ~128 KB of control state per row); shapes that take the
+ *     row-tiled selection (prefill, long batches) need only the status word
+ *     and fit at any size.
  *   - Every call shares the one array: it clears the parts that must start
  *     at zero on `stream` before launching, and calls whose GPU work overlaps
  *     in time (different streams, or several host threads) race on it.

@@ -23,7 +23,8 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_INDEX, ERR_WORKSPACE, ERR_INTERNAL = range(8)
-OP_INDEXER_SCORE, OP_TOPK_SELECT, OP_SPARSE_ATTN, OP_GATED_MIX, OP_ROUTED_ATTN, OP_ROUTE_HEADS = range(6)
+(OP_INDEXER_SCORE, OP_TOPK_SELECT, OP_SPARSE_ATTN, OP_GATED_MIX, OP_ROUTED_ATTN, OP_ROUTE_HEADS, OP_TOPK_THRESHOLD,
+ OP_GATED_SPARSE_ATTN) = range(8)
 INDEXER_RELU, PER_HEAD_SETS = 1, 2  # esa_shape.flags
 
 
@@ -49,8 +50,11 @@ _SIGS = {
     "esa_sparse_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
                                _sz, _vp]),
     "esa_gated_mix": (_i32, [_vp, _vp, _vp, _vp, _sp, _vp, _vp]),
+    "esa_gated_sparse_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp,
+                                     _vp, _vp, _vp, _vp, _sz, _vp]),
     "esa_routed_attn": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, ctypes.c_float, _vp, _vp, _vp,
                                _vp, _sz, _vp]),
+    "esa_topk_threshold": (_i32, [_vp, _vp, _vp, _sp, ctypes.c_int, _vp, _vp, _sz, _vp]),
     "esa_topk_select_noalloc": (_i32, [_vp, _vp, _vp, _sp, ctypes.c_int, _vp, _vp, _vp, _vp]),
     "esa_route_heads": (_i32, [_vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, _vp, _vp, _vp, _sz, _vp]),
     "esa_kda": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int64, ctypes.c_int64, _i32, _i32, _i32, ctypes.c_float,
@@ -135,6 +139,12 @@ def esa_topk_select(qI, kI, wI, shape: esa_shape, top_k: int, idx, cnt, ws: Work
                                 ws.nbytes, _stream(stream, qI)), "esa_topk_select")
 
 
+def esa_topk_threshold(qI, kI, wI, shape: esa_shape, top_k: int, thr, ws: Workspace, stream=None):
+    """thr int32 [B, Tq, 2]: the threshold form (T, P) of every row's Top-K set."""
+    _check(_lib.esa_topk_threshold(_p(qI), _p(kI), _p(wI), ctypes.byref(shape), top_k, _p(thr), ws.ptr, ws.nbytes,
+                                   _stream(stream, qI)), "esa_topk_threshold")
+
+
 def esa_topk_select_noalloc(qI, kI, wI, shape: esa_shape, top_k: int, idx, cnt, dev_status=None, stream=None):
     """esa_topk_select without a workspace: for callers that may not allocate
     device memory (the library's own fixed scratch array is used)."""
@@ -155,6 +165,15 @@ def esa_sparse_attn(q, k, v, idx, cnt, shape: esa_shape, top_k: int, scale: floa
     _check(_lib.esa_sparse_attn(_p(_bits(q)), _p(_bits(k)), _p(_bits(v)), _p(idx), _p(cnt), ctypes.byref(shape),
                                 top_k, float(scale), _p(g), _p(_bits(lin)), _p(out), _p(lse), ws.ptr, ws.nbytes,
                                 _stream(stream, q)), "esa_sparse_attn")
+
+
+def esa_gated_sparse_attn(q, k, v, qI, kI, wI, shape: esa_shape, top_k: int, scale: float, g, lin, out, lse=None,
+                          idx=None, cnt=None, ws: Workspace = None, stream=None):
+    """The whole path (indexer, top-K, gathered attention, gate mix) in one
+    call; one launch for decode-like shapes. idx/cnt optional outputs."""
+    _check(_lib.esa_gated_sparse_attn(_p(_bits(q)), _p(_bits(k)), _p(_bits(v)), _p(qI), _p(kI), _p(wI),
+                                      ctypes.byref(shape), top_k, float(scale), _p(g), _p(_bits(lin)), _p(out), _p(lse),
+                                      _p(idx), _p(cnt), ws.ptr, ws.nbytes, _stream(stream, q)), "esa_gated_sparse_attn")
 
 
 def esa_gated_mix(attn, lin, g, head_mask, shape: esa_shape, out, stream=None):

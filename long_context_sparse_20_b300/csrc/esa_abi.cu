@@ -3,7 +3,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -168,6 +170,34 @@ size_t topk_ws(const Shape &s, int K) {
     return w < kStatusBytes ? kStatusBytes : w;
 }
 
+// The single-launch decode step (selection, attention and merge in one
+// cooperative kernel) is taken only when ESA_DECODE_PATH=fused: measured on
+// B300 it is slower than the selection kernel followed by the gathered
+// attention kernel (launched early on the programmatic edge), so the two
+// launches are the default. Both give the same index sets and outputs
+// within the same tolerance.
+bool decode_single_launch() {
+    const char *e = getenv("ESA_DECODE_PATH");
+    return e && strcmp(e, "fused") == 0;
+}
+
+// Offset of the two-launch path's idx/cnt room: past the selection's own
+// workspace and past any shape's persistent selection state.
+size_t gated_scratch_off(const Shape &x, int K) {
+    return align256(std::max(topk_ws(x, K), split_state_max_bytes()));
+}
+
+// Workspace of esa_gated_sparse_attn: the fused step's, or for the two
+// launches the selection's workspace plus room for idx/cnt when the caller
+// passes none.
+size_t gated_ws(const Shape &x, int K) {
+    DecodePlan dp = decode_single_launch() ? plan_decode_step(x, K) : DecodePlan{};
+    if (dp.ok) return dp.ws_bytes;
+    const Shape r = selection_rows(x);
+    const size_t sets = (size_t)(r.B * r.Tq);
+    return gated_scratch_off(x, K) + align256(sets * K * 4) + align256(sets * 4);
+}
+
 }  // namespace
 
 extern "C" {
@@ -175,6 +205,15 @@ extern "C" {
 size_t esa_workspace_size(int op, const esa_shape *s, int top_k) {
     bool attn = op == ESA_OP_SPARSE_ATTN || op == ESA_OP_ROUTED_ATTN || op == ESA_OP_GATED_MIX;
     bool index = op == ESA_OP_INDEXER_SCORE || op == ESA_OP_TOPK_SELECT || op == ESA_OP_ROUTED_ATTN;
+    if (op == ESA_OP_TOPK_THRESHOLD) {
+        if (check_shape(s, false, true) != ESA_OK || top_k <= 0 || (s->flags & ESA_PER_HEAD_SETS)) return 0;
+        const size_t w = ws_row_select(to_shape(s), top_k);
+        return w < kStatusBytes ? kStatusBytes : w;
+    }
+    if (op == ESA_OP_GATED_SPARSE_ATTN) {
+        if (check_shape(s, true, true) != ESA_OK || top_k <= 0) return 0;
+        return gated_ws(to_shape(s), top_k);
+    }
     if (op == ESA_OP_ROUTE_HEADS) {
         if (check_shape(s, true, false) != ESA_OK) return 0;
         return ws_route_heads(to_shape(s));
@@ -222,8 +261,23 @@ esa_status esa_topk_select(const int8_t *qI, const int8_t *kI, const int32_t *wI
     if (!w) return ESA_ERR_CUDA;
     SplitPlan sp = plan_split_select(x, top_k);
     if ((e = check_ws(ws, ws_bytes, sp.ok ? sp.ws_bytes : ws_row_select(x, top_k)))) return e;
-    if (sp.ok) return launch_split_select(qI, kI, w, x, top_k, idx, cnt, ws, sp, (cudaStream_t)stream);
+    if (sp.ok) return launch_split_select(qI, kI, w, x, top_k, idx, cnt, ws, ws_bytes, sp, (cudaStream_t)stream);
     return launch_row_select(qI, kI, w, x, top_k, idx, cnt, nullptr, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+esa_status esa_topk_threshold(const int8_t *qI, const int8_t *kI, const int32_t *wI, const esa_shape *s, int top_k,
+                              int32_t *thr, void *ws, size_t ws_bytes, void *stream) {
+    esa_status e = check_shape(s, false, true);
+    if (e) return e;
+    if (!qI || !kI || !wI || !thr) return ESA_ERR_INVALID;
+    if (top_k <= 0 || top_k > 65536) return ESA_ERR_INVALID;
+    if (!aligned16(qI) || !aligned16(kI)) return ESA_ERR_INVALID;
+    if (s->flags & ESA_PER_HEAD_SETS) return ESA_ERR_UNSUPPORTED;  // one threshold form per row
+    const Shape x = to_shape(s);
+    if (x.B * x.Tq == 0) return ESA_OK;
+    if ((e = check_ws(ws, ws_bytes, ws_row_select(x, top_k)))) return e;
+    // the routed call's own selection step: no index list, the threshold form only
+    return launch_row_select(qI, kI, wI, x, top_k, nullptr, nullptr, thr, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,
@@ -242,6 +296,46 @@ esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t 
     AttnPlan p = plan_sparse_attn(x, top_k);
     if ((e = check_ws(ws, ws_bytes, p.ws_bytes))) return e;
     return launch_sparse_attn(q, k, v, idx, cnt, x, top_k, scale, g, lin, out, lse, ws, p, (cudaStream_t)stream);
+}
+
+esa_status esa_gated_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
+                                 const int8_t *kI, const int32_t *wI, const esa_shape *s, int top_k, float scale,
+                                 const float *g, const uint16_t *lin, float *out, float *lse, int32_t *idx,
+                                 int32_t *cnt, void *ws, size_t ws_bytes, void *stream) {
+    esa_status e = check_shape(s, true, true);
+    if (e) return e;
+    if (!q || !k || !v || !qI || !kI || !wI || !out) return ESA_ERR_INVALID;
+    if ((g == nullptr) != (lin == nullptr) || (idx == nullptr) != (cnt == nullptr)) return ESA_ERR_INVALID;
+    if (top_k <= 0 || top_k > 65536) return ESA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(qI) || !aligned16(kI) || !aligned16(out) ||
+        (lin && !aligned16(lin)))
+        return ESA_ERR_INVALID;
+    if (!(scale > 0.f) || scale != scale) return ESA_ERR_INVALID;
+    const Shape x = to_shape(s);
+    if (x.B * x.Tq == 0) return ESA_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    DecodePlan dp = decode_single_launch() ? plan_decode_step(x, top_k) : DecodePlan{};
+    if (dp.ok) {
+        if ((e = check_ws(ws, ws_bytes, dp.ws_bytes))) return e;
+        return launch_decode_step(q, k, v, qI, kI, wI, x, top_k, scale, g, lin, out, lse, idx, cnt, ws, dp, st);
+    }
+    // two launches: the selection into idx/cnt (or workspace room), then the
+    // attention over the gathered keys
+    if ((e = check_ws(ws, ws_bytes, gated_ws(x, top_k)))) return e;
+    const Shape r = selection_rows(x);
+    const size_t sel_bytes = align256(topk_ws(x, top_k));
+    const size_t scr = gated_scratch_off(x, top_k);
+    char *base = static_cast<char *>(ws);
+    int32_t *ii = idx ? idx : reinterpret_cast<int32_t *>(base + scr);
+    int32_t *cc = cnt ? cnt : reinterpret_cast<int32_t *>(base + scr + align256((size_t)(r.B * r.Tq) * top_k * 4));
+    const int32_t *w = per_head_of(r) ? unit_weight() : wI;
+    if (!w) return ESA_ERR_CUDA;
+    SplitPlan sp = plan_split_select(r, top_k);
+    e = sp.ok ? launch_split_select(qI, kI, w, r, top_k, ii, cc, ws, scr, sp, st)
+              : launch_row_select(qI, kI, w, r, top_k, ii, cc, nullptr, ws, sel_bytes, st);
+    if (e != ESA_OK) return e;
+    AttnPlan ap = plan_sparse_attn(x, top_k);
+    return launch_sparse_attn(q, k, v, ii, cc, x, top_k, scale, g, lin, out, lse, ws, ap, st);
 }
 
 esa_status esa_gated_mix(const float *attn, const uint16_t *lin, const float *g, const uint8_t *head_mask,

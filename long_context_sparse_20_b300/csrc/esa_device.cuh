@@ -135,6 +135,14 @@ __device__ __forceinline__ void mma_bf16_16816(float *d, const uint32_t *a, uint
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// D(16x8 f32) += A(16x8 bf16, row) * B(8x8 bf16, col); a0 holds row g, a1 row
+// g+8 (columns 2t, 2t+1), b0 rows 2t, 2t+1 of column g (g = lane/4, t = lane%4)
+__device__ __forceinline__ void mma_bf16_1688(float *d, uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
 // D(16x8 s32) += A(16x32 s8, row) * B(32x8 s8, col) — exact integer arithmetic
 __device__ __forceinline__ void mma_s8_16832(int *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
     asm volatile(

@@ -74,11 +74,37 @@ struct SplitPlan {
     size_t pub_off;     // per-block publications (written before read; no zeroing)
     size_t ctrl_off;    // per-row control state, two parities (zero before first use)
     size_t ctrl_bytes;
+    int ctrl_rows_max;  // the most rows any split plan on this device uses
     size_t ws_bytes;
 };
 SplitPlan plan_split_select(const Shape &s, int K);
+// ws_bytes: the workspace's size (bounds the control state a call may clear)
 esa_status launch_split_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
-                               int32_t *idx, int32_t *cnt, void *ws, const SplitPlan &plan, cudaStream_t st);
+                               int32_t *idx, int32_t *cnt, void *ws, size_t ws_bytes, const SplitPlan &plan,
+                               cudaStream_t st);
+// Bytes of persistent selection state (status, header, publications, the
+// control rows of the most rows any split plan uses): scratch that other
+// calls write fresh lies past this, so workspaces can be shared.
+size_t split_state_max_bytes();
+
+// The fused decode step: the split selection, then attention over each
+// block's own selected keys, the row's partials merged after a second
+// barrier, and the gate mix — one cooperative launch (few rows, long
+// prefixes, one index set per row). idx/cnt may be null.
+struct DecodePlan {
+    bool ok;
+    SplitPlan sel;     // the selection's plan (its stages and smem are the fused kernel's)
+    int MPK, MTT, KG;  // m-tiles per key/value head, m-tiles, key groups of 8 per stage
+    int sel_cap;       // entries of the block's selected-key list
+    size_t off_q, off_sel, off_aux;  // dynamic shared memory offsets
+    size_t part_off, ml_off;         // workspace: per-block partial outputs, (max, sum)
+    size_t ws_bytes;
+};
+DecodePlan plan_decode_step(const Shape &s, int K);
+esa_status launch_decode_step(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
+                              const int8_t *kI, const int32_t *wI, const Shape &s, int K, float scale, const float *g,
+                              const uint16_t *lin, float *out, float *lse, int32_t *idx, int32_t *cnt, void *ws,
+                              const DecodePlan &plan, cudaStream_t st);
 
 // Row-tiled selection of many query rows. Writes idx/cnt when idx !=
 // nullptr and the threshold form (T, P) of every row to thr (int32 pairs

@@ -81,7 +81,8 @@ extern "C" ESA_API esa_status esa_topk_select_noalloc(const int8_t *qI, const in
     if (cudaMemsetAsync(scratch, 0, clear, st) != cudaSuccess) return ESA_ERR_CUDA;
     if (sp.ok && cudaMemsetAsync(static_cast<char *>(scratch) + sp.ctrl_off, 0, sp.ctrl_bytes, st) != cudaSuccess)
         return ESA_ERR_CUDA;
-    esa_status e = sp.ok ? launch_split_select(qI, kI, wI, x, top_k, idx, cnt, scratch, sp, st)
+    esa_status e = sp.ok ? launch_split_select(qI, kI, wI, x, top_k, idx, cnt, scratch,
+                                               (size_t)ESA_NOALLOC_SCRATCH_BYTES, sp, st)
                          : launch_row_select(qI, kI, wI, x, top_k, idx, cnt, nullptr, scratch,
                                              (size_t)ESA_NOALLOC_SCRATCH_BYTES, st);
     if (e != ESA_OK) return e;

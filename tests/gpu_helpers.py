@@ -40,6 +40,25 @@ def gpu_topk(d: dict, sh: dict, K: int, ws=None):
     return idx.reshape(-1, K).cpu().numpy(), cnt.reshape(-1).cpu().numpy()
 
 
+def gpu_threshold(d: dict, sh: dict, K: int, ws=None):
+    """The threshold form (T, P) of every row's set, int32 [rows, 2], from the
+    routed call's selection step (esa_topk_threshold)."""
+    m = esa()
+    shape = m.shape_from(sh)
+    ws = ws or m.workspace_for(m.OP_TOPK_THRESHOLD, shape, K)
+    thr = torch.full((sh["B"], sh["Tq"], 2), -7, dtype=torch.int32, device="cuda")
+    m.esa_topk_threshold(d["qI"], d["kI"], d["wI"], shape, K, thr, ws)
+    st = m.esa_read_status(ws)
+    assert st == m.OK, m.status_string(st)
+    return thr.reshape(-1, 2).cpu().numpy()
+
+
+def assert_thr_equal(got, ref):
+    bad = np.nonzero((got != ref).any(axis=1))[0]
+    assert len(bad) == 0, f"{len(bad)} rows differ; first row {bad[0] if len(bad) else None}: " \
+                          f"{got[bad[0]] if len(bad) else None} vs {ref[bad[0]] if len(bad) else None}"
+
+
 def gpu_attn(d: dict, sh: dict, K: int, idx, cnt, gate=True, want_lse=True, ws=None, scale=None):
     m = esa()
     shape = m.shape_from(sh)
@@ -71,10 +90,12 @@ def gpu_routed(d: dict, sh: dict, K: int, gate=True):
 
 
 def sample_rows(B: int, Tq: int, K: int, n: int, seed: int = 0) -> np.ndarray:
-    """A seeded uniform sample of flat rows plus the edge rows of every
-    sequence (0, 1, K-2, K-1, K, Tq-1)."""
+    """A seeded uniform sample of n flat rows per sequence plus the edge rows
+    of every sequence (0, 1, K-2, K-1, K, Tq-1)."""
     rng = np.random.default_rng(seed)
-    rows = set(rng.choice(B * Tq, size=min(n, B * Tq), replace=False).tolist())
+    rows = set()
+    for b in range(B):
+        rows |= set((b * Tq + rng.choice(Tq, size=min(n, Tq), replace=False)).tolist())
     for b in range(B):
         for t in (0, 1, K - 2, K - 1, K, Tq - 1):
             if 0 <= t < Tq:

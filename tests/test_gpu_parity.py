@@ -3,7 +3,8 @@
 Index sets and counts must match bit-exactly; fp32 outputs within 2e-3
 max-abs (bf16 inputs, fp32 accumulation). Small cases span several tiles
 and ragged tails; the five workloads run at full size, compared on all rows
-(decode) or on seeded row samples plus edge rows (prefill)."""
+(decode; index sets of every prefill workload) or on seeded row samples
+plus edge rows (prefill outputs)."""
 import math
 import os
 
@@ -13,8 +14,8 @@ import torch
 
 import esa_inputs as E
 import oracle as O
-from gpu_helpers import (ATOL, assert_close, assert_idx_equal, esa, gpu_attn, gpu_routed, gpu_topk, sample_rows,
-                         to_dev)
+from gpu_helpers import (ATOL, assert_close, assert_idx_equal, assert_thr_equal, esa, gpu_attn, gpu_routed,
+                         gpu_threshold, gpu_topk, sample_rows, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +52,49 @@ def test_topk_small(over):
     gi, gc = gpu_topk(to_dev(inp), sh, K)
     oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
     assert_idx_equal(gi, gc, oi, oc)
+
+
+THR_CASES = [
+    dict(B=1, Tq=300, Tk=300, top_k=64, D_I=32),
+    dict(B=2, Tq=200, Tk=200, top_k=100, D_I=64, H_I=4, weights="1to4"),
+    dict(B=1, Tq=130, Tk=130, top_k=1, D_I=16),
+    dict(B=2, Tq=70, Tk=600, q_offset=530, top_k=128, D_I=64),
+    dict(B=1, Tq=257, Tk=257, top_k=256, D_I=128, H_I=2, weights="1to4"),  # dp4a kernel (D_I = 128)
+]
+
+
+@pytest.mark.parametrize("over", THR_CASES, ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
+def test_topk_threshold_small(over):
+    """The routed call's selection step, (T, P) per row, bit-exact against the
+    oracle's threshold form, and the set it describes equal to the idx row
+    of esa_topk_select."""
+    cfg, sh, inp = _case(seed=111, **over)
+    K = cfg["top_k"]
+    d = to_dev(inp)
+    thr = gpu_threshold(d, sh, K)
+    assert_thr_equal(thr, O.threshold(inp["qI"], inp["kI"], inp["wI"], sh, K))
+    gi, gc = gpu_topk(d, sh, K)
+    for r in range(0, sh["B"] * sh["Tq"], 7):
+        b, t = divmod(r, sh["Tq"])
+        s = O.indexer_row(inp["qI"], inp["kI"], inp["wI"], sh, b, t)
+        T, P = thr[r]
+        j = np.arange(len(s))
+        described = j[(s > T) | ((s == T) & (j <= P))]
+        assert described.tolist() == gi[r, :gc[r]].tolist(), r
+
+
+def test_topk_threshold_ties():
+    """All scores equal, and tie-heavy small-range scores: the last tie taken
+    (P) must be exactly the oracle's."""
+    cfg, sh, inp = _case(seed=112, B=1, Tq=260, Tk=260, top_k=50, D_I=64)
+    inp["kI"] = torch.zeros_like(inp["kI"])
+    d = to_dev(inp)
+    assert_thr_equal(gpu_threshold(d, sh, 50), O.threshold(inp["qI"], inp["kI"], inp["wI"], sh, 50))
+    g = torch.Generator().manual_seed(5)
+    inp["qI"] = torch.randint(-1, 2, inp["qI"].shape, dtype=torch.int8, generator=g)
+    inp["kI"] = torch.randint(-1, 2, inp["kI"].shape, dtype=torch.int8, generator=g)
+    d = to_dev(inp)
+    assert_thr_equal(gpu_threshold(d, sh, 50), O.threshold(inp["qI"], inp["kI"], inp["wI"], sh, 50))
 
 
 @pytest.mark.parametrize("decode", [False, True])
@@ -493,14 +537,16 @@ def test_decode_full(name):
 
 
 def test_long_prefill_full():
+    """Index sets on all 32768 rows; outputs on 1024 seeded rows plus edges."""
     cfg, sh, inp = _full("long_prefill")
     K = cfg["top_k"]
     d = to_dev(inp)
     gi, gc = gpu_topk(d, sh, K)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    assert_idx_equal(gi, gc, oi, oc)
+    assert (gc == np.minimum(K, np.arange(sh["Tq"]) + 1)).all()
     rows = sample_rows(sh["B"], sh["Tq"], K, 1024, seed=1)
     oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
-    assert_idx_equal(gi, gc, oi, oc, rows=rows)
-    assert (gc == np.minimum(K, np.arange(sh["Tq"]) + 1)).all()
     st, out, _ = gpu_attn(d, sh, K, gi, gc)
     assert st == 0
     assert_close(out[rows], ref)
@@ -508,15 +554,17 @@ def test_long_prefill_full():
 
 def test_chunked_prefill_full():
     """A 16384-token chunk at the end of a 131072-token cache (queries at
-    positions 114688..131071): sampled rows plus the chunk's edge rows."""
+    positions 114688..131071): index sets on all rows, outputs on 512 seeded
+    rows plus the chunk's edge rows."""
     cfg, sh, inp = _full("chunked_prefill")
     K = cfg["top_k"]
     d = to_dev(inp)
     gi, gc = gpu_topk(d, sh, K)
-    rows = sample_rows(sh["B"], sh["Tq"], K, 384, seed=3)
-    oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
-    assert_idx_equal(gi, gc, oi, oc, rows=rows)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    assert_idx_equal(gi, gc, oi, oc)
     assert (gc == K).all()
+    rows = sample_rows(sh["B"], sh["Tq"], K, 512, seed=3)
+    oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
     st, out, _ = gpu_attn(d, sh, K, gi, gc)
     assert st == 0
     assert_close(out[rows], ref)
@@ -524,26 +572,32 @@ def test_chunked_prefill_full():
 
 def test_per_head_prefill_full():
     """One ReLU'd index set per query head (16 sets per query row) at
-    S=8192: sampled rows plus edge rows, every head."""
+    S=8192: every set of every row; outputs on 512 seeded rows plus edge
+    rows, every head."""
     cfg, sh, inp = _full("per_head_prefill")
     K = cfg["top_k"]
     d = to_dev(inp)
     gi, gc = gpu_topk(d, sh, K)
-    H = sh["H_I"]
-    rows = sample_rows(sh["B"], sh["Tq"], K, 192, seed=4)
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    assert_idx_equal(gi, gc, oi.reshape(-1, K), oc.reshape(-1))
+    rows = sample_rows(sh["B"], sh["Tq"], K, 512, seed=4)
     oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
-    sel = (rows[:, None] * H + np.arange(H)[None, :]).reshape(-1)
-    assert_idx_equal(gi[sel], gc[sel], oi.reshape(-1, K), oc.reshape(-1))
     st, out, _ = gpu_attn(d, sh, K, gi, gc)
     assert st == 0
     assert_close(out[rows], ref)
 
 
 def test_routed_prefill_full():
+    """The routed call's selection, its threshold form (T, P), on all 131072
+    rows, bit-exact; outputs of every head on 512 seeded rows per sequence
+    plus edge rows."""
     cfg, sh, inp = _full("routed_prefill")
     K = cfg["top_k"]
-    rows = sample_rows(sh["B"], sh["Tq"], K, 256, seed=2)
-    out = gpu_routed(to_dev(inp), sh, K)
+    d = to_dev(inp)
+    thr = gpu_threshold(d, sh, K)
+    assert_thr_equal(thr, O.threshold(inp["qI"], inp["kI"], inp["wI"], sh, K))
+    rows = sample_rows(sh["B"], sh["Tq"], K, 512, seed=2)
+    out = gpu_routed(d, sh, K)
     _, _, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
     assert_close(out[rows], ref)
 
