@@ -151,6 +151,10 @@ struct Smem {
     // followed by the scores of the block's span (int32)
 };
 
+// Bytes of the Smem header in dynamic shared memory (the scores that follow
+// start on a 128-byte boundary: 16-byte vector reads).
+constexpr size_t kSmemHdr = (sizeof(Smem) + 127) & ~size_t(127);
+
 // Block-wide: among bins [0,nb) of the global histogram h, find v with
 // sum_{u>v} h[u] < need <= sum_{u>=v} h[u]. Result in sm.bin / sm.above
 // (sm.bin = -1 if there is none). Every thread reads its own contiguous 16
@@ -732,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_select_kernel(SelArgs a) {
     const int NS = a.stages;
     unsigned char *ring = smem_raw;
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw + NS * SB);
-    int32_t *sc = reinterpret_cast<int32_t *>(smem_raw + NS * SB + sizeof(Smem));
+    int32_t *sc = reinterpret_cast<int32_t *>(smem_raw + NS * SB + kSmemHdr);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long row = blockIdx.x / a.chunks;
@@ -962,9 +966,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_select_kernel(SelArgs a) {
             // their published suffix counts (S(v) = #{bin >= v})
             T = (int)vlo;
             const int x = vstar - kWinLo;  // in [0, kWin-1)
-            if constexpr (D > 0) {
-                // the fused step issues these loads now and reads them only
-                // after its keys above T are listed and their gathers issued
+            {
+                // issued now, read only after this block's own counts (phase
+                // C) or its keys above T and their gathers (the fused step)
                 if (tid < ci) {
                     const unsigned *pq = a.pub + ((size_t)row * a.chunks + tid) * kPubWords;
                     pend.have = true;
@@ -974,17 +978,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_select_kernel(SelArgs a) {
                     pend.tot = __ldcg(pq + 2);
                     pend.s0 = __ldcg(pq + 4 + x);
                     pend.s1 = __ldcg(pq + 5 + x);
-                }
-            } else {
-                for (int c = tid; c < ci; c += kThreads) {
-                    const unsigned *pq = a.pub + ((size_t)row * a.chunks + c) * kPubWords;
-                    const int clo = (int)__ldcg(pq), chi = (int)__ldcg(pq + 1);
-                    const unsigned ctot = __ldcg(pq + 2);
-                    const unsigned s0 = __ldcg(pq + 4 + x), s1 = __ldcg(pq + 5 + x);
-                    const unsigned S0 = vstar <= clo ? ctot : (vstar > chi ? 0u : s0);
-                    const unsigned S1 = vstar + 1 <= clo ? ctot : (vstar + 1 > chi ? 0u : s1);
-                    gt_b += S1;
-                    eq_b += S0 - S1;
                 }
             }
         } else {
@@ -1056,83 +1049,116 @@ __global__ void __launch_bounds__(kThreads, 1) split_select_kernel(SelArgs a) {
     }
 
     // ---- phase C: ordered write of this span's selected positions (the
-    // fused step lists its keys and writes idx in its own tail instead)
+    // fused step lists its keys and writes idx in its own tail instead).
+    // Each thread holds 16 consecutive scores in registers; one block-wide
+    // scan of (keys above T, keys at T) gives every thread its output slot:
+    // above T always, at T while the row's first K - #(above T) ties (in
+    // position order) are not all taken.
     if (D == 0 && ok) {
         const unsigned need_ties = (unsigned)K - above;  // ties at T to take, >= 1
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            gt_b += __shfl_xor_sync(0xffffffffu, gt_b, d);
-            eq_b += __shfl_xor_sync(0xffffffffu, eq_b, d);
-        }
-        __syncthreads();
-        if (lane == 0) {
-            sm.red[warp] = gt_b;
-            sm.red[32 + warp] = eq_b;
-        }
-        // per-warp counts over contiguous segments of the span. Almost every
-        // 32-key chunk lies wholly below T: one ballot on s >= T skips it.
-        const int seg = ((span + kWarps * 32 - 1) / (kWarps * 32)) * 32;
-        const int s0 = warp * seg, s1 = min(span, s0 + seg);
-        unsigned wgt = 0, weq = 0;
-#pragma unroll 4
-        for (int j0 = s0; j0 < s1; j0 += 32) {
-            const int j = j0 + lane;
-            const int sv = j < s1 ? sc[j] : INT32_MIN;
-            const unsigned gem = __ballot_sync(0xffffffffu, sv >= T);
-            if (gem) {
-                const unsigned eqm = __ballot_sync(0xffffffffu, sv == T);
-                wgt += __popc(gem & ~eqm);
-                weq += __popc(eqm);
-            }
-        }
-        if (lane == 0) {
-            sm.wsum[0][warp] = wgt;
-            sm.wsum[1][warp] = weq;
-        }
-        __syncthreads();
+        // earlier spans' counts above T and at T (loads issued before)
+        unsigned gtp = gt_b, eqp = eq_b;
+        unsigned carry_gt = 0, carry_eq = 0;  // keys of earlier rounds of this span
         unsigned gt_before = 0, eq_before = 0;
-        for (int w2 = 0; w2 < kWarps; w2++) {
-            gt_before += sm.red[w2];
-            eq_before += sm.red[32 + w2];
-        }
-        // output base of this span and of this warp's segment
-        unsigned out = gt_before + min(eq_before, need_ties);
-        unsigned tie = eq_before;
-        for (int w2 = 0; w2 < warp; w2++) {
-            unsigned e = sm.wsum[1][w2];
-            unsigned take = tie >= need_ties ? 0u : min(e, need_ties - tie);
-            out += sm.wsum[0][w2] + take;
-            tie += e;
-        }
-        // ordered write: same chunks, same skip
-        const unsigned lt = lanemask_lt();
-        if (wgt + weq > 0u) {
-#pragma unroll 4
-            for (int j0 = s0; j0 < s1; j0 += 32) {
-                const int j = j0 + lane;
-                const int sv = j < s1 ? sc[j] : INT32_MIN;
-                const unsigned gem = __ballot_sync(0xffffffffu, sv >= T);
-                if (gem == 0u) continue;
-                const unsigned eqm = __ballot_sync(0xffffffffu, sv == T);
-                const unsigned gtm = gem & ~eqm;
-                // ties taken in this chunk: its first min(#ties, need - taken so far)
-                const unsigned ne = __popc(eqm);
-                const unsigned take = tie >= need_ties ? 0u : min(ne, need_ties - tie);
-                unsigned tmask = 0u;
-                if (take == ne) {
-                    tmask = eqm;
-                } else if (take > 0u) {  // the lowest `take` ties (warp-uniform branch)
-                    tmask = __ballot_sync(0xffffffffu, ((eqm >> lane) & 1u) && __popc(eqm & lt) < take);
+        const int nchunk = (span + 15) / 16;
+        for (int c0 = 0; c0 < nchunk; c0 += kThreads) {
+            const int c = c0 + tid, j0 = c * 16;
+            int v[16];
+            if (c < nchunk) {
+                const int4 *p4 = reinterpret_cast<const int4 *>(sc + j0);
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int4 w4 = p4[q];
+                    v[4 * q] = w4.x;
+                    v[4 * q + 1] = w4.y;
+                    v[4 * q + 2] = w4.z;
+                    v[4 * q + 3] = w4.w;
                 }
-                const unsigned selm = gtm | tmask;
-                if ((selm >> lane) & 1u) {
-                    const unsigned pos = out + __popc(selm & lt);
-                    if (pos < (unsigned)K) idx_row[pos] = (int32_t)(lo + j);
-                    else set_status(a.status, ESA_ERR_INTERNAL);
-                }
-                out += __popc(selm);
-                tie += ne;
             }
+            unsigned ng = 0, ne = 0;
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                if (c >= nchunk || j0 + i >= span) v[i] = INT32_MIN;  // past the span: never taken
+                ng += v[i] > T;
+                ne += v[i] == T;
+            }
+            // inclusive scan of (ng, ne) over the warp, then over the warps
+            unsigned ig = ng, ie = ne;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const unsigned ug = __shfl_up_sync(0xffffffffu, ig, d), ue = __shfl_up_sync(0xffffffffu, ie, d);
+                if (lane >= d) {
+                    ig += ug;
+                    ie += ue;
+                }
+            }
+            if (c0 == 0 && pend.have) {  // the earlier spans' counts, now that their loads have landed
+                const unsigned S0 = pend.vstar <= pend.clo ? pend.tot : (pend.vstar > pend.chi ? 0u : pend.s0);
+                const unsigned S1 =
+                    pend.vstar + 1 <= pend.clo ? pend.tot : (pend.vstar + 1 > pend.chi ? 0u : pend.s1);
+                gtp += S1;
+                eqp += S0 - S1;
+            }
+            if (c0 == 0) {
+#pragma unroll
+                for (int d = 16; d > 0; d >>= 1) {
+                    gtp += __shfl_xor_sync(0xffffffffu, gtp, d);
+                    eqp += __shfl_xor_sync(0xffffffffu, eqp, d);
+                }
+            }
+            __syncthreads();  // sm.red / sm.wsum free (the previous round's readers are done)
+            if (lane == 31) {
+                sm.wsum[0][warp] = ig;
+                sm.wsum[1][warp] = ie;
+            }
+            if (c0 == 0 && lane == 0) {
+                sm.red[warp] = gtp;
+                sm.red[32 + warp] = eqp;
+            }
+            __syncthreads();
+            // every warp scans the warp totals (lanes < kWarps) alike
+            const unsigned wg = lane < kWarps ? sm.wsum[0][lane] : 0u, we = lane < kWarps ? sm.wsum[1][lane] : 0u;
+            unsigned sg = wg, se = we;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const unsigned ug = __shfl_up_sync(0xffffffffu, sg, d), ue = __shfl_up_sync(0xffffffffu, se, d);
+                if (lane >= d) {
+                    sg += ug;
+                    se += ue;
+                }
+            }
+            if (c0 == 0) {
+                unsigned rg = lane < kWarps ? sm.red[lane] : 0u, re = lane < kWarps ? sm.red[32 + lane] : 0u;
+#pragma unroll
+                for (int d = 16; d > 0; d >>= 1) {
+                    rg += __shfl_xor_sync(0xffffffffu, rg, d);
+                    re += __shfl_xor_sync(0xffffffffu, re, d);
+                }
+                gt_before = rg;
+                eq_before = re;
+            }
+            const unsigned tot_g = __shfl_sync(0xffffffffu, sg, 31), tot_e = __shfl_sync(0xffffffffu, se, 31);
+            const unsigned pre_g = carry_gt + __shfl_sync(0xffffffffu, sg - wg, warp) + (ig - ng);
+            const unsigned pre_e = carry_eq + __shfl_sync(0xffffffffu, se - we, warp) + (ie - ne);
+            // ties at T taken before this thread's keys, and by them
+            const unsigned tie0 = eq_before + pre_e;
+            const unsigned take_before = min(tie0, need_ties) - min(eq_before, need_ties);
+            unsigned tk = tie0 >= need_ties ? 0u : min(ne, need_ties - tie0);
+            unsigned out = gt_before + min(eq_before, need_ties) + pre_g + take_before;
+            if (ng + tk > 0) {
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const bool take = v[i] > T || (v[i] == T && tk > 0);
+                    if (v[i] == T && tk > 0) tk--;
+                    if (take) {
+                        if (out < (unsigned)K) idx_row[out] = (int32_t)(lo + j0 + i);
+                        else set_status(a.status, ESA_ERR_INTERNAL);
+                        out++;
+                    }
+                }
+            }
+            carry_gt += tot_g;
+            carry_eq += tot_e;
         }
         if (ci == 0 && tid == 0) a.cnt[row] = K;
     }
@@ -1186,7 +1212,7 @@ size_t stage_bytes(int DI) { return (size_t)kThreads * DI; }
 // levels' bins and for `min_ring` bytes of later use (0 if that does not
 // fit); `extra` bytes of shared memory follow the scores.
 int stages_for(long long len, int DI, size_t extra = 0, size_t min_ring = 0) {
-    size_t fixed = sizeof(Smem) + scores_bytes(len) + extra;
+    size_t fixed = kSmemHdr + scores_bytes(len) + extra;
     if (fixed >= kSmemBudget) return 0;
     size_t sb = stage_bytes(DI);
     size_t want = std::max<size_t>(std::max<size_t>(kRingBytes / sb, kMinStages), (min_ring + sb - 1) / sb);
@@ -1196,7 +1222,7 @@ int stages_for(long long len, int DI, size_t extra = 0, size_t min_ring = 0) {
 }
 
 size_t smem_for(long long len, int DI, int stages, size_t extra = 0) {
-    return (size_t)stages * stage_bytes(DI) + sizeof(Smem) + scores_bytes(len) + extra;
+    return (size_t)stages * stage_bytes(DI) + kSmemHdr + scores_bytes(len) + extra;
 }
 
 }  // namespace
@@ -1317,7 +1343,7 @@ DecodePlan plan_decode_step(const Shape &s, int K) {
     const int stages = stages_for(len, s.D_I, extra, min_ring);
     if (stages == 0) return p;
     // the Q tile (cp.async and ldmatrix rows) starts on a 128-byte boundary
-    const size_t base = ((size_t)stages * stage_bytes(s.D_I) + sizeof(Smem) + scores_bytes(len) + 127) & ~size_t(127);
+    const size_t base = ((size_t)stages * stage_bytes(s.D_I) + kSmemHdr + scores_bytes(len) + 127) & ~size_t(127);
     void *fn = fused_kernel_ptr(s.D_I, s.D);
     const size_t smem = base + q_bytes + sel_bytes + aux_bytes;
     if (occupancy(fn, kThreads, smem) < 1) return p;
