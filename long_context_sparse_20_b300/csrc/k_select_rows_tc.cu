@@ -25,9 +25,22 @@
 //              so that a tile is one contiguous 16-KiB block) into a ring
 //   warp 17    one thread issues the MMAs into four 128-column buffers
 // Passes over the keys; the scores are recomputed by every pass:
-//   1      a log histogram per row (4 classes per octave); keys below a
-//          running lower bound on the row's K-th largest score are not
-//          counted, so most keys cost one comparison;
+//   sample (query tiles whose prefixes span 128 key tiles or more) a log
+//          histogram (4 classes per octave) of every 8th or 16th key tile;
+//          it brackets each row's K-th largest score: the scores between
+//          the sample's (r - d)-th and (r + d)-th largest, r = K m / n the
+//          K-th score's expected rank among the m sampled of n keys and
+//          d = 4 sqrt(r) + 8; a second pass over the same tiles bins the
+//          sample inside that log-bin bracket (512 bins) and narrows its
+//          edges to those two ranks;
+//   bracket every key: counted above the bracket, counted below it, or
+//          binned inside it (512 16-bit bins); the counts verify the bracket
+//          (fewer than K keys above it, at least K above its floor, the
+//          bins summing to the keys inside) and a row whose bracket misses
+//          falls back to the passes below;
+//   1      (without a sample, or on fallback) a log histogram per row;
+//          keys below a running lower bound on the row's K-th largest score
+//          are not counted, so most keys cost one comparison;
 //   2 ..   256 bins over the bucket that holds the K-th score, until the
 //          threshold T is exact (one pass while that bucket spans at most
 //          256 integers);
@@ -59,9 +72,12 @@ constexpr int kHS = kNB + 1;  // row stride of the histograms (words)
 constexpr int kLog0 = 100;    // level-1 bin of the score 0
 constexpr int kRing = 65536;  // bytes of key-tile ring
 constexpr int kMaxStages = 8;
-constexpr int kMaxLevels = 6;
+constexpr int kMaxLevels = 8;
+constexpr int kSampleMinTiles = 128;  // sample only prefixes of at least this many key tiles
 
-enum { kModeStart = -1, kModeHist = 0, kModeFinal = 1, kModeDone = 2 };
+enum { kModeStart = -1, kModeHist = 0, kModeFinal = 1, kModeDone = 2, kModeSample = 3 };
+// what a row's histogram pass does
+enum { kKindLog = 0, kKindBucket = 1, kKindBracket = 2 };
 
 template <int DI>
 struct TcLay {
@@ -82,8 +98,13 @@ struct TcShared {
     unsigned above[kRowsT];  // keys above the current bucket
     int open[kRowsT];        // threshold not exact yet
     int w16[kRowsT];         // level >= 2: 512 16-bit bins
+    int kind[kRowsT];        // kKindLog, kKindBucket or kKindBracket
+    unsigned cab[kRowsT], cbe[kRowsT];  // bracket pass: keys above / below the bracket
     uint32_t tmem_base;
     int mode, level, exact_all;
+    int stride, toff;  // sample pass: key tiles toff, toff + stride, ...
+    int sround;        // sample passes done (the log histogram, then the bracket refinement)
+    unsigned rhi[kRowsT], rlo[kRowsT];  // sample ranks that bound the K-th score
 };
 
 struct TcSelArgs {
@@ -145,10 +166,65 @@ __device__ __forceinline__ float rescan1(const volatile unsigned *h, int top, un
     return -INFINITY;
 }
 
+// Shared-memory counter update under a predicate, without a branch: the
+// per-element histogram updates of the passes below stay in straight-line
+// code whatever the other rows of the warp do (the address is formed for
+// every element and used only where the predicate holds).
+__device__ __forceinline__ void red_smem_if(const unsigned *p, unsigned v, bool pred) {
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q red.shared.add.u32 [%0], %1;\n}\n" ::"r"(smem_u32(p)),
+        "r"(v), "r"((unsigned)pred)
+        : "memory");
+}
+
 // bins of a level >= 2 histogram: 256 x 32-bit counters, or 512 x 16-bit
 // counters (two per word) when the bucket holds fewer than 2^16 keys
 __device__ __forceinline__ unsigned bin_count(const unsigned *h, int b, bool w16) {
     return w16 ? (h[b >> 1] >> ((b & 1) * 16)) & 0xFFFFu : h[b];
+}
+
+// One warp, one row's histogram hh (bpl bins per lane; wide: 512 16-bit
+// bins): the bin v where the count of keys in bins above v stays below
+// `need` and reaches it with bin v. Returns -1 in `found` when the
+// histogram holds fewer than `need` keys; `total` = all keys counted.
+__device__ __forceinline__ void warp_crossing(const unsigned *hh, bool wide, unsigned need, int lane, int &found,
+                                              unsigned &above_in, unsigned &in_bin, unsigned &total) {
+    const int bpl = wide ? 16 : 8;  // bins per lane
+    const int b0 = lane * bpl;
+    unsigned seg = 0;
+    for (int v = 0; v < bpl; v++) seg += bin_count(hh, b0 + v, wide);
+    unsigned xs = seg;  // keys in the bins of lanes >= lane
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned y = __shfl_down_sync(0xffffffffu, xs, d);
+        if (lane + d < 32) xs += y;
+    }
+    total = __shfl_sync(0xffffffffu, xs, 0);
+    const unsigned excl = xs - seg;
+    int f = -1;
+    unsigned ab = 0, ib = 0;
+    if (excl < need && need <= xs) {
+        unsigned acc = excl;
+        for (int v = b0 + bpl - 1; v >= b0; v--) {
+            const unsigned hv = bin_count(hh, v, wide);
+            if (acc + hv >= need) {
+                f = v;
+                ab = acc;
+                ib = hv;
+                break;
+            }
+            acc += hv;
+        }
+    }
+    const unsigned fl = __ballot_sync(0xffffffffu, f >= 0);
+    found = -1;
+    above_in = in_bin = 0;
+    if (fl != 0u) {
+        const int src = __ffs(fl) - 1;
+        found = __shfl_sync(0xffffffffu, f, src);
+        above_in = __shfl_sync(0xffffffffu, ab, src);
+        in_bin = __shfl_sync(0xffffffffu, ib, src);
+    }
 }
 
 template <int DI>
@@ -241,6 +317,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
             st.above[r] = 0u;
             st.w16[r] = 0;
             st.lo[r] = st.hi[r] = st.sh[r] = 0;
+            st.kind[r] = kKindLog;
         }
         fence_async_smem();  // q_eff is read by the tensor cores
     }
@@ -262,9 +339,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 for (int i = 0; i < kRowsT; i++) any |= st.open[i];
                 const int m = st.mode;
                 int next = m == kModeFinal ? kModeDone : (any ? kModeHist : kModeFinal);
+                if (m == kModeStart && any && ntk >= kSampleMinTiles) next = kModeSample;
+                if (m == kModeSample && any && st.sround < 2) next = kModeSample;
                 if (abort_flag) next = kModeDone;
-                if (next == kModeHist) {
-                    st.level = m == kModeHist ? st.level + 1 : 1;
+                if (next == kModeSample) {
+                    if (m == kModeStart) {
+                        st.stride = ntk >= 2 * kSampleMinTiles ? 16 : 8;
+                        st.toff = st.stride / 2;
+                        st.level = 0;
+                        st.sround = 0;
+                    }
+                    st.sround++;
+                } else if (next == kModeHist) {
+                    st.level = st.level + 1;
                     if (st.level > kMaxLevels) {  // consistency check; never reached
                         set_status(a.status, ESA_ERR_INTERNAL);
                         next = kModeDone;
@@ -273,16 +360,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 st.mode = next;
             }
             __syncthreads();
-            const int mode = st.mode, level = st.level;
+            const int mode = st.mode;
             if (mode == kModeDone) break;
+            // key tiles of this pass: all of the prefix's, or the sample's
+            const int tstep = mode == kModeSample ? st.stride : 1, toff = mode == kModeSample ? st.toff : 0;
+            const int ntp = mode == kModeSample ? (ntk - toff + tstep - 1) / tstep : ntk;
 
             if (warp == kProdWarp) {
                 // ---------------------------------------------- key tiles
                 if (lane == 0) {
                     const uint64_t pol = l2_evict_last_policy();
                     const char *src = reinterpret_cast<const char *>(a.kh) + (size_t)(b * a.Tkp) * DI * 2;
-                    for (int t = 0; t < ntk; t++) {
-                        const int g = g0 + t, slot = g % S;
+                    for (int it = 0; it < ntp; it++) {
+                        const int t = toff + it * tstep;
+                        const int g = g0 + it, slot = g % S;
                         if (g >= S && !wait_or_abort(bar(st.sfree[slot]), (uint32_t)(g / S - 1) & 1u, a.wait_ns,
                                                      &abort_flag, a.status))
                             break;
@@ -296,8 +387,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 // ---------------------------------------------- MMA issue
                 if (lane == 0) {
                     constexpr uint32_t id = idesc(kKT, 0u, 0u);  // fp16 x fp16 -> fp32, N = 128
-                    for (int t = 0; t < ntk; t++) {
-                        const int g = g0 + t, slot = g % S, buf = g % kTBufs;
+                    for (int it = 0; it < ntp; it++) {
+                        const int g = g0 + it, slot = g % S, buf = g % kTBufs;
                         if (!wait_or_abort(bar(st.full[slot]), (uint32_t)(g / S) & 1u, a.wait_ns, &abort_flag,
                                            a.status))
                             break;
@@ -320,11 +411,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 const int n_r = st.n[r];
                 const bool open_r = st.open[r] != 0;
                 unsigned *h = hist + r * kHS;
-                if (mode == kModeHist) {
+                if (mode == kModeHist || mode == kModeSample) {
                     for (int i = tid; i < kRowsT * kHS; i += kCons) hist[i] = 0u;
+                    if (tid < kRowsT) st.cab[tid] = st.cbe[tid] = 0u;
                     __syncwarp();
                     asm volatile("bar.sync 5, %0;" ::"n"(kCons) : "memory");  // histograms cleared
                 }
+                const int kind_r = st.kind[r];
+                unsigned ca = 0, cb = 0;  // bracket pass: this part's keys above / below the bracket
                 const int lo = st.lo[r], hi = st.hi[r], sh = st.sh[r];
                 const float flo = (float)lo, fhi = (float)hi;
                 const float Tf = (float)st.T[r];
@@ -339,8 +433,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 unsigned tie_run = 0, out_run = 0;  // final pass: ties seen, positions written
                 int32_t *orow = (a.idx && r < nrows) ? a.idx + (row0 + r) * (long long)K : nullptr;
                 uint2 *xch = reinterpret_cast<uint2 *>(hist);  // final pass: [2][kRowsT][kParts] (g, e)
-                for (int t = 0; t < ntk; t++) {
-                    const int g = g0 + t, buf = g % kTBufs;
+                for (int it = 0; it < ntp; it++) {
+                    const int t = toff + it * tstep;
+                    const int g = g0 + it, buf = g % kTBufs;
                     wait_or_abort(bar(st.tfull[buf]), (uint32_t)(g / kTBufs) & 1u, a.wait_ns, &abort_flag, a.status);
                     __syncwarp();  // tcgen05.ld is warp-collective
                     tc_fence_after();
@@ -356,18 +451,36 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                     }
                     const int j0 = t * kKT + pt * kCols;
                     const int lim = max(0, min(kCols, n_r - j0));  // columns c < lim are in the prefix
-                    if (mode == kModeHist) {
+                    if (mode == kModeSample && kind_r == kKindLog) {
+                        // every sampled key of the prefix, log histogram
                         if (!open_r || lim == 0) continue;
+#pragma unroll
+                        for (int c = 0; c < kCols; c++) red_smem_if(h + log_bin(__uint_as_float(x[c])), 1u, c < lim);
+                    } else if (mode == kModeHist || mode == kModeSample) {
+                        if (!open_r || lim == 0) continue;
+                        if (kind_r == kKindBracket) {
+                            // above, below or inside the bracket [lo, hi]
+#pragma unroll
+                            for (int c = 0; c < kCols; c++) {
+                                const float f = __uint_as_float(x[c]);
+                                const bool in = c < lim, up = f > fhi, dn = f < flo;
+                                ca += in && up;
+                                cb += in && dn;
+                                const int bn = (int)((unsigned)(__float2int_rz(f) - lo) >> sh) & (2 * kNB - 1);
+                                red_smem_if(h + (bn >> 1), 1u << ((bn & 1) * 16), in && !up && !dn);
+                            }
+                            continue;
+                        }
                         if (lim < kCols) {  // keys past the row's prefix never count
 #pragma unroll
                             for (int c = 0; c < kCols; c++)
                                 if (c >= lim) x[c] = 0xff800000u;  // -inf
                         }
-                        if (level == 1) {
+                        if (kind_r == kKindLog) {
 #pragma unroll
                             for (int c = 0; c < kCols; c++) {
                                 const float f = __uint_as_float(x[c]);
-                                if (f >= fb) atomicAdd(h + log_bin(f), 1u);
+                                red_smem_if(h + log_bin(f), 1u, f >= fb);
                             }
                             // raise the bound: every tile until it is positive, then every 8th
                             if (fb <= 0.f || ++since_scan == 8) {
@@ -378,11 +491,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
 #pragma unroll
                             for (int c = 0; c < kCols; c++) {
                                 const float f = __uint_as_float(x[c]);
-                                if (f >= flo && f <= fhi) {
-                                    const int bn = (__float2int_rz(f) - lo) >> sh;
-                                    if (w16) atomicAdd(h + (bn >> 1), 1u << ((bn & 1) * 16));
-                                    else atomicAdd(h + bn, 1u);
-                                }
+                                const int bn = (int)((unsigned)(__float2int_rz(f) - lo) >> sh) & (2 * kNB - 1);
+                                red_smem_if(w16 ? h + (bn >> 1) : h + (bn & (kNB - 1)), w16 ? 1u << ((bn & 1) * 16) : 1u,
+                                            f >= flo && f <= fhi);
                             }
                         }
                     } else {
@@ -443,58 +554,118 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 if (mode == kModeFinal && r < nrows && pt == 0 && !abort_flag &&
                     out_run != (unsigned)min(K, n_r))  // consistency check; never reached
                     set_status(a.status, ESA_ERR_INTERNAL);
+                if ((mode == kModeHist || mode == kModeSample) && open_r && kind_r == kKindBracket) {
+                    atomicAdd(&st.cab[r], ca);
+                    atomicAdd(&st.cbe[r], cb);
+                }
             }
-            g0 += ntk;
+            g0 += ntp;
             __syncthreads();  // pass drained: every MMA read, every histogram count in
-            if (mode == kModeHist && warp < kConsWarps && !abort_flag) {
+            if ((mode == kModeHist || mode == kModeSample) && warp < kConsWarps && !abort_flag) {
                 // ---------------------------------------------- next bucket
-                // warp w resolves rows w, w+16, ...: lane l sums bins bpl*l .. +bpl-1
+                // warp w resolves rows w, w+16, ...
                 for (int rr = warp; rr < kRowsT; rr += kConsWarps) {
                     if (!st.open[rr]) continue;
-                    const unsigned need = (unsigned)K - st.above[rr];
                     const unsigned *hh = hist + rr * kHS;
-                    const bool wide = level > 1 && st.w16[rr] != 0;  // 512 16-bit bins
-                    const int bpl = wide ? 16 : 8;                    // bins per lane
-                    const int b0 = lane * bpl;
-                    unsigned seg = 0;
-                    for (int v = 0; v < bpl; v++) seg += bin_count(hh, b0 + v, wide);
-                    unsigned xs = seg;  // keys in the bins of lanes >= lane
-#pragma unroll
-                    for (int d = 1; d < 32; d <<= 1) {
-                        const unsigned y = __shfl_down_sync(0xffffffffu, xs, d);
-                        if (lane + d < 32) xs += y;
-                    }
-                    const unsigned excl = xs - seg;
-                    int found = -1;
-                    unsigned above_in = 0, in_bin = 0;
-                    if (excl < need && need <= xs) {
-                        unsigned acc = excl;
-                        for (int v = b0 + bpl - 1; v >= b0; v--) {
-                            const unsigned hv = bin_count(hh, v, wide);
-                            if (acc + hv >= need) {
-                                found = v;
-                                above_in = acc;
-                                in_bin = hv;
-                                break;
-                            }
-                            acc += hv;
+                    int found;
+                    unsigned above_in, in_bin, total;
+                    if (mode == kModeSample && st.kind[rr] == kKindBracket) {
+                        // second sample pass: the sample's keys above, below and in
+                        // 512 bins of the log-bin bracket; narrow the bracket to
+                        // the bins that hold the sample ranks rhi and rlo
+                        const unsigned up = st.cab[rr], r_hi = st.rhi[rr], r_lo = st.rlo[rr];
+                        int lo2 = st.lo[rr], hi2 = st.hi[rr];
+                        const int sh2 = st.sh[rr];
+                        if (up < r_hi) {
+                            int bh;
+                            warp_crossing(hh, true, r_hi - up, lane, bh, above_in, in_bin, total);
+                            if (bh >= 0) hi2 = (int)min((long long)hi2, (long long)lo2 + ((long long)(bh + 1) << sh2) - 1);
                         }
+                        if (r_lo > up) {
+                            int bl;
+                            warp_crossing(hh, true, r_lo - up, lane, bl, above_in, in_bin, total);
+                            if (bl >= 0) lo2 = lo2 + (bl << sh2);
+                        }
+                        if (lane == 0) {
+                            int s2 = 0;
+                            while ((((long long)hi2 - lo2) >> s2) >= 2 * kNB) s2++;
+                            st.lo[rr] = lo2;
+                            st.hi[rr] = hi2;
+                            st.sh[rr] = s2;
+                        }
+                        continue;
                     }
-                    const unsigned fl = __ballot_sync(0xffffffffu, found >= 0);
-                    if (fl == 0u) {  // consistency check; never reached
+                    if (mode == kModeSample) {
+                        // bracket the K-th score from the sample: the sample ranks
+                        // r -+ d, r = K m / n the expected rank, d = 4 sqrt(r) + 8
+                        warp_crossing(hh, false, 0xffffffffu, lane, found, above_in, in_bin, total);
+                        const unsigned m = total, n = (unsigned)st.n[rr];
+                        const unsigned rx = max(1u, (unsigned)(((unsigned long long)K * m + n / 2) / n));
+                        const unsigned dd = (unsigned)(4.f * sqrtf((float)rx)) + 8u;
+                        const unsigned r_hi = rx > dd ? rx - dd : 1u, r_lo = rx + dd;
+                        int bhi, blo;
+                        warp_crossing(hh, false, r_hi, lane, bhi, above_in, in_bin, total);
+                        int vlo = -(1 << 24), vhi = 1 << 24;  // |s| < 2^24 (the exactness bound)
+                        if (bhi >= 0) {
+                            int l2, h2;
+                            bin_range1(bhi, l2, h2);
+                            vhi = h2;
+                        }
+                        if (r_lo <= m) {
+                            warp_crossing(hh, false, r_lo, lane, blo, above_in, in_bin, total);
+                            if (blo >= 0) {
+                                int l2, h2;
+                                bin_range1(blo, l2, h2);
+                                vlo = l2;
+                            }
+                        }
+                        if (lane == 0) {
+                            int s2 = 0;
+                            while ((((long long)vhi - vlo) >> s2) >= 2 * kNB) s2++;
+                            st.kind[rr] = kKindBracket;
+                            st.lo[rr] = vlo;
+                            st.hi[rr] = vhi;
+                            st.sh[rr] = s2;
+                            st.w16[rr] = 1;
+                            st.above[rr] = 0u;
+                            st.rhi[rr] = r_hi;
+                            st.rlo[rr] = r_lo;
+                        }
+                        continue;
+                    }
+                    const int kind = st.kind[rr];
+                    if (kind == kKindBracket) {
+                        // the bracket holds the K-th score iff fewer than K keys lie
+                        // above it and at least K at or above its floor; 16-bit bins
+                        // must sum to the keys inside it (no carry between bins)
+                        const unsigned up = st.cab[rr], dn = st.cbe[rr], n = (unsigned)st.n[rr];
+                        const unsigned inb = n - up - dn;
+                        warp_crossing(hh, true, 0xffffffffu, lane, found, above_in, in_bin, total);
+                        const bool valid = total == inb && up < (unsigned)K && up + inb >= (unsigned)K;
+                        if (!valid) {  // fall back to the full log histogram
+                            if (lane == 0) {
+                                st.kind[rr] = kKindLog;
+                                st.above[rr] = 0u;
+                                st.w16[rr] = 0;
+                            }
+                            continue;
+                        }
+                        if (lane == 0) st.above[rr] = up;
+                        __syncwarp();
+                    }
+                    const unsigned need = (unsigned)K - st.above[rr];
+                    const bool wide = kind != kKindLog && st.w16[rr] != 0;  // 512 16-bit bins
+                    warp_crossing(hh, wide, need, lane, found, above_in, in_bin, total);
+                    if (found < 0) {  // consistency check; never reached
                         if (lane == 0) {
                             set_status(a.status, ESA_ERR_INTERNAL);
                             st.open[rr] = 0;
                         }
                         continue;
                     }
-                    const int src = __ffs(fl) - 1;
-                    found = __shfl_sync(0xffffffffu, found, src);
-                    above_in = __shfl_sync(0xffffffffu, above_in, src);
-                    in_bin = __shfl_sync(0xffffffffu, in_bin, src);
                     if (lane == 0) {
                         int nlo, nhi;
-                        if (level == 1) {
+                        if (kind == kKindLog) {
                             bin_range1(found, nlo, nhi);
                         } else {
                             nlo = st.lo[rr] + (found << st.sh[rr]);
@@ -512,6 +683,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                             const int nb = w ? 2 * kNB : kNB;
                             int s2 = 0;
                             while ((((long long)nhi - nlo) >> s2) >= nb) s2++;
+                            st.kind[rr] = kKindBucket;
                             st.lo[rr] = nlo;
                             st.hi[rr] = nhi;
                             st.sh[rr] = s2;
