@@ -25,8 +25,9 @@
 //              so that a tile is one contiguous 16-KiB block) into a ring
 //   warp 17    one thread issues the MMAs into four 128-column buffers
 // Passes over the keys; the scores are recomputed by every pass:
-//   sample (query tiles whose prefixes span 128 key tiles or more) a log
-//          histogram (4 classes per octave) of every 8th or 16th key tile;
+//   sample (query tiles whose prefixes span 48 key tiles or more) a log
+//          histogram (4 classes per octave) of every 4th, 8th or 16th key
+//          tile (prefixes of 48, 128, 256 key tiles and more);
 //          it brackets each row's K-th largest score: the scores between
 //          the sample's (r - d)-th and (r + d)-th largest, r = K m / n the
 //          K-th score's expected rank among the m sampled of n keys and
@@ -73,7 +74,7 @@ constexpr int kLog0 = 100;    // level-1 bin of the score 0
 constexpr int kRing = 65536;  // bytes of key-tile ring
 constexpr int kMaxStages = 8;
 constexpr int kMaxLevels = 8;
-constexpr int kSampleMinTiles = 128;  // sample only prefixes of at least this many key tiles
+constexpr int kSampleMinTiles = 48;  // sample only prefixes of at least this many key tiles
 
 enum { kModeStart = -1, kModeHist = 0, kModeFinal = 1, kModeDone = 2, kModeSample = 3 };
 // what a row's histogram pass does
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                 if (abort_flag) next = kModeDone;
                 if (next == kModeSample) {
                     if (m == kModeStart) {
-                        st.stride = ntk >= 2 * kSampleMinTiles ? 16 : 8;
+                        st.stride = ntk >= 256 ? 16 : (ntk >= 128 ? 8 : 4);
                         st.toff = st.stride / 2;
                         st.level = 0;
                         st.sround = 0;
