@@ -228,15 +228,15 @@ def kda(q, k, v, alpha, beta, state_in=None, scale: float | None = None, L=None)
 
 def threshold(qI, kI, wI, shape: dict, K: int, rows=None, L=None) -> np.ndarray:
     """int32 [n_rows, 2] threshold form (T, P) of each listed row's index set
-    (one set per row): key j <= p is selected iff s_j > T, or s_j == T and
-    j <= P; T = INT32_MIN and P = p when the prefix holds at most K keys."""
+    ([n_rows, H_I, 2] with per-head sets): key j <= p is selected iff
+    s_j > T, or s_j == T and j <= P; T = INT32_MIN and P = p when the prefix
+    holds at most K keys."""
     L = L or lib()
     qa, ka, wa = _np(qI, np.int8), _np(kI, np.int8), _np(wI, np.int32)
     rr = _rows(shape["B"], shape["Tq"], rows)
     flags = int(shape.get("flags", 0))
-    if flags & PER_HEAD:
-        raise ValueError("the threshold form describes one index set per row")
-    thr = np.empty((len(rr), 2), dtype=np.int32)
+    sets = (shape["H_I"],) if flags & PER_HEAD else ()
+    thr = np.empty((len(rr), *sets, 2), dtype=np.int32)
     rc = L.oracle_threshold_rows(_ptr(qa), _ptr(ka), _ptr(wa), shape["B"], shape["Tq"], shape["Tk"],
                                  shape["q_offset"], shape["H_I"], shape["D_I"], K, flags, _ptr(rr), len(rr), _ptr(thr),
                                  threads())

@@ -410,13 +410,17 @@ int oracle_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const fl
  * most K keys the set is the whole prefix: T = INT32_MIN, P = p. The routed
  * attention (Elastic Attention page, section 3.1: sparse heads inside the
  * fused kernel) rebuilds its sparse heads' sets from this form.
- * thr is [n_rows][2] = (T, P). Returns 0, or -1 on int32 overflow.
+ * flags as in oracle_topk_rows_mode: with per-head sets (bit 1) every
+ * indexer head of a row has its own set, scored by that head alone.
+ * thr is [n_rows][2] = (T, P), or [n_rows][H_I][2] with per-head sets.
+ * Returns 0, or -1 on int32 overflow.
  */
 int oracle_threshold_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
                           long B, long Tq, long Tk, long q_offset, int H_I, int D_I,
                           int K, int flags, const int64_t *rows, long n_rows,
                           int32_t *thr, int n_threads) {
-    const int relu = flags & 1;
+    const int relu = flags & 1, per_head = (flags >> 1) & 1;
+    const int nsets = per_head ? H_I : 1;
     int bad = 0;
 #ifdef _OPENMP
     if (n_threads > 0) omp_set_num_threads(n_threads);
@@ -425,27 +429,31 @@ int oracle_threshold_rows(const int8_t *qI, const int8_t *kI, const int32_t *wI,
     for (long r = 0; r < n_rows; r++) {
         const long b = rows[r] / Tq, t = rows[r] % Tq;
         const long p = q_offset + t, n = p + 1;  /* keys 0..p */
-        if (n <= K) {
-            thr[2 * r] = INT32_MIN;
-            thr[2 * r + 1] = (int32_t)p;
-            continue;
-        }
-        int32_t *sc = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
-        scored_pos *order = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
-        if (oracle_indexer_row_mode(qI, kI, wI, B, Tq, Tk, q_offset, H_I, D_I, b, t, relu, -1, sc) != n) {
-            bad |= 1;
-        } else {
-            for (long j = 0; j < n; j++) {
-                order[j].s = sc[j];
-                order[j].j = (int32_t)j;
+        for (int set = 0; set < nsets; set++) {
+            int32_t *tr = thr + 2 * (r * nsets + set);
+            if (n <= K) {
+                tr[0] = INT32_MIN;
+                tr[1] = (int32_t)p;
+                continue;
             }
-            qsort(order, (size_t)n, sizeof(scored_pos), by_score_then_position);
-            const scored_pos kth = order[K - 1];
-            thr[2 * r] = kth.s;
-            thr[2 * r + 1] = kth.j;
+            int32_t *sc = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+            scored_pos *order = (scored_pos *)malloc(sizeof(scored_pos) * (size_t)n);
+            const int scored_head = per_head ? set : -1; /* the set's own head, or the weighted sum */
+            if (oracle_indexer_row_mode(qI, kI, wI, B, Tq, Tk, q_offset, H_I, D_I, b, t, relu, scored_head, sc) != n) {
+                bad |= 1;
+            } else {
+                for (long j = 0; j < n; j++) {
+                    order[j].s = sc[j];
+                    order[j].j = (int32_t)j;
+                }
+                qsort(order, (size_t)n, sizeof(scored_pos), by_score_then_position);
+                const scored_pos kth = order[K - 1];
+                tr[0] = kth.s;
+                tr[1] = kth.j;
+            }
+            free(sc);
+            free(order);
         }
-        free(sc);
-        free(order);
     }
     return bad ? -1 : 0;
 }

@@ -185,6 +185,21 @@ def pin_threshold_form(L, seed=23):
             assert described == _topk_bruteforce(s, K), (trial, r)
 
 
+def pin_threshold_form_per_head(L, seed=29):
+    """With per-head sets (and the ReLU), each set's threshold form equals
+    the one-set threshold form of the query sliced to that indexer head
+    (weight 1)."""
+    cfg, sh, inp = _small(seed=seed, Tq=40, Tk=40, H_I=3, D_I=16, top_k=9, weights="1to4")
+    for flags in (2, 3):
+        shp = dict(sh, flags=flags)
+        thr = O.threshold(inp["qI"], inp["kI"], inp["wI"], shp, 9, L=L)
+        assert thr.shape == (40, 3, 2)
+        for hh in range(3):
+            one = dict(sh, H_I=1, flags=flags & 1)
+            ref = O.threshold(inp["qI"][:, :, hh:hh + 1].contiguous(), inp["kI"], np.ones(1, np.int32), one, 9, L=L)
+            assert np.array_equal(thr[:, hh], ref), (flags, hh)
+
+
 def pin_topk_lexsort(L, seed=13):
     cfg, sh, inp = _small(seed=seed, Tq=48, Tk=48, H_I=2, D_I=16, top_k=20, weights="1to4")
     K = 20
@@ -695,7 +710,7 @@ def pin_kda_chaining(L):
 
 
 ALL_PINS = [pin_indexer_golden, pin_indexer_numpy, pin_indexer_onehot, pin_indexer_bound,
-            pin_topk_bruteforce, pin_threshold_form, pin_topk_lexsort, pin_topk_special, pin_topk_needles,
+            pin_topk_bruteforce, pin_threshold_form, pin_threshold_form_per_head, pin_topk_lexsort, pin_topk_special, pin_topk_needles,
             pin_attention_full_is_sdpa, pin_attention_sparse_is_masked_sdpa, pin_attention_closed_forms,
             pin_empty_set, pin_gate, pin_routing, pin_needles_closed_form,
             pin_indexer_modes_golden, pin_relu_special_and_numpy, pin_per_head_sets_are_sliced_queries,

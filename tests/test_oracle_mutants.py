@@ -28,8 +28,10 @@ MUTANTS = {
     "full heads skip the diagonal": ("nk = p + 1;\n                for (long j = 0; j < nk; j++)", "nk = p;\n                for (long j = 0; j < nk; j++)"),
     "threshold form from the (K+1)-th position": ("const scored_pos kth = order[K - 1];",
                                                   "const scored_pos kth = order[K];"),
-    "threshold form of a whole prefix off by one": ("thr[2 * r + 1] = (int32_t)p;",
-                                                    "thr[2 * r + 1] = (int32_t)(p + 1);"),
+    "threshold form of a whole prefix off by one": ("tr[1] = (int32_t)p;",
+                                                    "tr[1] = (int32_t)(p + 1);"),
+    "per-head threshold form scored by every head": ("const int scored_head = per_head ? set : -1;",
+                                                      "const int scored_head = -1;"),
     "ReLU not applied": ("if (relu && dot < 0) dot = 0;", ";"),
     "ReLU clamps the weighted sum instead of each head": ("if (relu && dot < 0) dot = 0;", "if (relu && dot < 0 && H_I == 1) dot = 0;"),
     "per-head score weighted": ("if (head >= 0) s += dot;", "if (head >= 0) s += (int64_t)wI[h] * dot;"),
