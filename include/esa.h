@@ -65,8 +65,10 @@
  *                        page's pseudo-code, section 四.1); query head h
  *                        attends to the set of indexer head h / (Hq/H_I),
  *                        which needs Hq % H_I == 0 and, for attention, one of
- *                        Hq/H_I and Hq/Hkv to divide the other. Not for the
- *                        routed call (ESA_ERR_UNSUPPORTED).
+ *                        Hq/H_I and Hq/Hkv to divide the other. The routed
+ *                        call masks each sparse head with its own set (on its
+ *                        warp-specialised kernel, D = 128 with D_I <= 64;
+ *                        other shapes return ESA_ERR_UNSUPPORTED).
  *
  * Tensor layouts:
  *   qI  int8  [B, Tq, H_I, D_I]     indexer queries
@@ -227,7 +229,8 @@ ESA_API esa_status esa_gated_mix(const float *attn, const uint16_t *lin, const f
  * one fused kernel). route[b,h] = 0: exact causal attention over all keys
  * 0..p, output without the gate. route[b,h] = 1: the sparse path — the
  * index set of esa_topk_select (one set per (b,t), shared by all sparse
- * heads), attention over it, then the gate mix with lin when g and lin are
+ * heads; with ESA_PER_HEAD_SETS the set of indexer head h / (Hq/H_I)),
+ * attention over it, then the gate mix with lin when g and lin are
  * given. Every head of the layer runs in one attention launch (on the
  * tensor cores, accumulators in tensor memory). scale is normally 1/sqrt(D). */
 ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
@@ -245,8 +248,9 @@ ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const u
  *                ascending); thr[b,t,0] = T, the score of the top_k-th of
  *                that order, and thr[b,t,1] = P, its position.
  * Key j <= p is in the row's set iff s_j > T, or s_j == T and j <= P: the
- * same set as esa_topk_select's idx row. thr int32 [B, Tq, 2]. One index
- * set per row only (ESA_PER_HEAD_SETS returns ESA_ERR_UNSUPPORTED).
+ * same set as esa_topk_select's idx row. thr int32 [B, Tq, 2], or
+ * [B, Tq, H_I, 2] with ESA_PER_HEAD_SETS (each set scored by its own
+ * indexer head, as esa_topk_select's per-head rows).
  * Workspace esa_workspace_size(ESA_OP_TOPK_THRESHOLD, s, top_k) bytes;
  * the same kernels and workspace layout as the routed call's selection. */
 ESA_API esa_status esa_topk_threshold(const int8_t *qI, const int8_t *kI, const int32_t *wI, const esa_shape *s,

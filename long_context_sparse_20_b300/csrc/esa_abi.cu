@@ -206,8 +206,8 @@ size_t esa_workspace_size(int op, const esa_shape *s, int top_k) {
     bool attn = op == ESA_OP_SPARSE_ATTN || op == ESA_OP_ROUTED_ATTN || op == ESA_OP_GATED_MIX;
     bool index = op == ESA_OP_INDEXER_SCORE || op == ESA_OP_TOPK_SELECT || op == ESA_OP_ROUTED_ATTN;
     if (op == ESA_OP_TOPK_THRESHOLD) {
-        if (check_shape(s, false, true) != ESA_OK || top_k <= 0 || (s->flags & ESA_PER_HEAD_SETS)) return 0;
-        const size_t w = ws_row_select(to_shape(s), top_k);
+        if (check_shape(s, false, true) != ESA_OK || top_k <= 0) return 0;
+        const size_t w = ws_row_select(selection_rows(to_shape(s)), top_k);
         return w < kStatusBytes ? kStatusBytes : w;
     }
     if (op == ESA_OP_GATED_SPARSE_ATTN) {
@@ -272,12 +272,13 @@ esa_status esa_topk_threshold(const int8_t *qI, const int8_t *kI, const int32_t 
     if (!qI || !kI || !wI || !thr) return ESA_ERR_INVALID;
     if (top_k <= 0 || top_k > 65536) return ESA_ERR_INVALID;
     if (!aligned16(qI) || !aligned16(kI)) return ESA_ERR_INVALID;
-    if (s->flags & ESA_PER_HEAD_SETS) return ESA_ERR_UNSUPPORTED;  // one threshold form per row
-    const Shape x = to_shape(s);
+    const Shape x = selection_rows(to_shape(s));  // per-head sets: one row per (query, indexer head)
     if (x.B * x.Tq == 0) return ESA_OK;
     if ((e = check_ws(ws, ws_bytes, ws_row_select(x, top_k)))) return e;
+    const int32_t *w = per_head_of(x) ? unit_weight() : wI;
+    if (!w) return ESA_ERR_CUDA;
     // the routed call's own selection step: no index list, the threshold form only
-    return launch_row_select(qI, kI, wI, x, top_k, nullptr, nullptr, thr, ws, ws_bytes, (cudaStream_t)stream);
+    return launch_row_select(qI, kI, w, x, top_k, nullptr, nullptr, thr, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,
@@ -362,8 +363,9 @@ esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t 
         (lin && !aligned16(lin)))
         return ESA_ERR_INVALID;
     if (!(scale > 0.f) || scale != scale) return ESA_ERR_INVALID;
-    if (s->flags & ESA_PER_HEAD_SETS) return ESA_ERR_UNSUPPORTED;  // one threshold form per row
     Shape x = to_shape(s);
+    // per-head index sets: on the warp-specialised kernel only
+    if (per_head_of(x) && !routed_pp_supported(x)) return ESA_ERR_UNSUPPORTED;
     if (x.B * x.Tq == 0) return ESA_OK;
     if ((e = check_ws(ws, ws_bytes, ws_routed(x, top_k)))) return e;
     return launch_routed_attn(q, k, v, qI, kI, wI, route, x, top_k, scale, g, lin, out, ws, (cudaStream_t)stream);

@@ -21,9 +21,12 @@
 
 namespace esa {
 
-// workspace: [row selection: status word, tensor-core scratch][thr][routed_pp: flag, fp16 values]
+// workspace: [row selection: status word, tensor-core scratch][thr][routed_pp: flag, fp16 values].
+// With per-head index sets the selection runs on the per-head rows (one
+// (T, P) per row and indexer head, [B, Tq, H_I, 2]).
 size_t ws_routed(const Shape &s, int K) {
-    return align256(ws_row_select(s, K)) + align256((size_t)s.B * s.Tq * 2 * 4) +
+    const Shape r = selection_rows(s);
+    return align256(ws_row_select(r, K)) + align256((size_t)r.B * r.Tq * 2 * 4) +
            (routed_pp_supported(s) ? ws_routed_pp(s) : 0);
 }
 
@@ -32,15 +35,19 @@ esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16
                               float scale, const float *g, const uint16_t *lin, float *out, void *ws,
                               cudaStream_t st) {
     char *base = static_cast<char *>(ws);
-    const size_t sel_bytes = align256(ws_row_select(s, K));
+    const Shape r = selection_rows(s);
+    const size_t sel_bytes = align256(ws_row_select(r, K));
     int32_t *thr = reinterpret_cast<int32_t *>(base + sel_bytes);
-    esa_status e = launch_row_select(qI, kI, wI, s, K, nullptr, nullptr, thr, ws, sel_bytes, st);
+    const int32_t *w = per_head_of(s) ? unit_weight() : wI;
+    if (!w) return ESA_ERR_CUDA;
+    esa_status e = launch_row_select(qI, kI, w, r, K, nullptr, nullptr, thr, ws, sel_bytes, st);
     if (e != ESA_OK) return e;
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     if (routed_pp_supported(s)) {
-        void *pp_ws = base + sel_bytes + align256((size_t)s.B * s.Tq * 2 * 4);
+        void *pp_ws = base + sel_bytes + align256((size_t)r.B * r.Tq * 2 * 4);
         return launch_routed_pp(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, pp_ws, status, st);
     }
+    if (per_head_of(s)) return ESA_ERR_UNSUPPORTED;  // the fallback kernel masks with one set per row
     return launch_routed_tc(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, status, st);
 }
 

@@ -73,7 +73,8 @@ struct PpArgs {
     int32_t *status;
     long long B, Tq, Tk, q_offset, wait_ns;
     int Hq, Hkv, H_I;
-    int relu;  // ReLU on each indexer head's dot product (mask scores on dp4a)
+    int relu;  // ReLU on each indexer head's dot product
+    int pset;  // one index set per indexer head: query head h masks with set h / (Hq / H_I), weight 1
     float scale_log2;
 };
 
@@ -118,6 +119,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long b = bid / a.Hq;
     const int kvh = h / (a.Hq / a.Hkv);
     const bool sparse = a.route[b * a.Hq + h] != 0;
+    // the index set this head masks with: its own indexer head's (per-head
+    // sets, weight 1) or the row's one weighted set
+    const int iset = a.pset ? h / (a.Hq / a.H_I) : 0;
+    const int nsets = a.pset ? a.H_I : 1, nih = a.pset ? 1 : a.H_I;
     long long t0x[2];
     int rowsx[2], ntx[2];
     for (int x = 0; x < 2; x++) {
@@ -153,7 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(bars.qe_ready), 2 * kRowsT);
         mbar_init(bar(bars.mma_end), 1);
         mbar_fence_init();
-        exact_all = a.relu ? 0 : 1;  // the ReLU does not collapse onto the tensor cores
+        // a ReLU stays exact on the tensor cores for one indexer head of
+        // non-negative weight (max(0, w d) = w max(0, d)); several heads do
+        // not collapse, so their mask scores come from dp4a
+        exact_all = (a.relu && !(nih == 1 && (a.pset || a.wI[0] >= 0))) ? 0 : 1;
         abort_flag = 0;
     }
     tc_fence_before();
@@ -174,19 +182,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         int Tint = 0, Pp = -1;
         if (sparse) {
             if (r < rows) {
-                Tint = a.thr[2 * (row0 + r)];
-                Pp = a.thr[2 * (row0 + r) + 1];
+                Tint = a.thr[2 * ((row0 + r) * nsets + iset)];
+                Pp = a.thr[2 * ((row0 + r) * nsets + iset) + 1];
             }
             Tf = (float)Tint;
             // collapsed indexer query q_eff = sum_h w_h qI_h (fp16, exact while
             // |q_eff| <= 2048 and every partial sum of q_eff . kI stays below 2^24)
             long long absum = 0;
             bool fits = true;
-            const int8_t *qrow = a.qI + (row0 + (r < rows ? r : 0)) * (long long)a.H_I * DI;
+            const int8_t *qrow = a.qI + ((row0 + (r < rows ? r : 0)) * (long long)a.H_I + iset) * DI;
             for (int c0 = 0; c0 < DI; c0 += 8) {
                 long long acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // 64-bit: any int32 weight
-                for (int hh = 0; hh < a.H_I; hh++) {
-                    const long long wv = a.wI[hh];
+                for (int hh = 0; hh < nih; hh++) {
+                    const long long wv = a.pset ? 1 : a.wI[hh];
                     const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + hh * DI + c0);
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
@@ -233,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t ir[32];
                     tmem_ld32(tmem + lane_base + colSI + half * 32, ir);
                     tmem_wait_ld();
+                    if (a.relu) {  // one head of non-negative weight: exact
+#pragma unroll
+                        for (int c = 0; c < 32; c++) ir[c] = __float_as_uint(fmaxf(__uint_as_float(ir[c]), 0.f));
+                    }
                     const int pl = (int)max(-1ll, min(64ll, (long long)Pp - j0));  // ties kept for c <= pl
                     if (pl < 0 || pl >= 63) {
                         // the tie position is outside this tile: kept iff s >= cut,
@@ -257,16 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const unsigned char *raw = smem + L::RING + slot * L::SLOT + L::SKI;
-                const int8_t *qrow = a.qI + (row0 + (r < rows ? r : 0)) * (long long)a.H_I * DI;
+                const int8_t *qrow = a.qI + ((row0 + (r < rows ? r : 0)) * (long long)a.H_I + iset) * DI;
                 for (int c = 0; c < 64; c++) {
                     unsigned acc = 0;
-                    for (int hh = 0; hh < a.H_I; hh++) {
+                    for (int hh = 0; hh < nih; hh++) {
                         int d = 0;
 #pragma unroll
                         for (int w4 = 0; w4 < DI / 4; w4++)
                             d = __dp4a(reinterpret_cast<const int *>(qrow + hh * DI)[w4],
                                        reinterpret_cast<const int *>(raw + c * DI)[w4], d);
-                        acc += (unsigned)a.wI[hh] * (unsigned)(a.relu ? max(d, 0) : d);
+                        acc += (unsigned)(a.pset ? 1 : a.wI[hh]) * (unsigned)(a.relu ? max(d, 0) : d);
                     }
                     const int si = (int)acc;
                     if (!(si > Tint || (si == Tint && j0 + c <= Pp))) keep &= ~(1ull << c);
@@ -614,6 +626,7 @@ esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t
     a.H_I = s.H_I;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.relu = relu_of(s) ? 1 : 0;
+    a.pset = per_head_of(s) ? 1 : 0;
     const long long nqt = (s.Tq + kRowsT - 1) / kRowsT;
     const long long blocks = s.B * s.Hq * ((nqt + 1) / 2);
     if (blocks == 0) return ESA_OK;

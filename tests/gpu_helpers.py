@@ -46,7 +46,8 @@ def gpu_threshold(d: dict, sh: dict, K: int, ws=None):
     m = esa()
     shape = m.shape_from(sh)
     ws = ws or m.workspace_for(m.OP_TOPK_THRESHOLD, shape, K)
-    thr = torch.full((sh["B"], sh["Tq"], 2), -7, dtype=torch.int32, device="cuda")
+    sets = _sets(sh)  # per-head index sets: [B, Tq, H_I, 2]
+    thr = torch.full((sh["B"], sh["Tq"], *sets, 2), -7, dtype=torch.int32, device="cuda")
     m.esa_topk_threshold(d["qI"], d["kI"], d["wI"], shape, K, thr, ws)
     st = m.esa_read_status(ws)
     assert st == m.OK, m.status_string(st)

@@ -91,8 +91,9 @@ def test_host_validation_rejects_before_launch():
 def test_host_validation_of_indexer_flags():
     """Unknown flag bits are invalid; per-head sets need Hq % H_I == 0 and, for
     attention, heads per set and heads per key/value head dividing one
-    another; the routed call has one threshold form per row, so it refuses
-    per-head sets. All of it is decided before any launch."""
+    another; the routed call takes per-head sets only on its warp-specialised
+    kernel, which does not fit D = 128 with D_I = 128. All of it is decided
+    before any launch."""
     import long_context_sparse_20_b300 as esa
     L = esa._lib
     fake = ctypes.c_void_p(0x1000)
@@ -103,7 +104,7 @@ def test_host_validation_of_indexer_flags():
         sh = _shape(esa, flags=esa.PER_HEAD_SETS, **kw)
         assert L.esa_sparse_attn(fake, fake, fake, fake, fake, ctypes.byref(sh), 4, 0.125, None, None, fake, None,
                                  fake, 1 << 20, None) == code, kw
-    sh = _shape(esa, flags=esa.PER_HEAD_SETS, Hq=4, Hkv=4, H_I=2)
+    sh = _shape(esa, flags=esa.PER_HEAD_SETS, Hq=4, Hkv=4, H_I=2, D=128, D_I=128)
     assert L.esa_routed_attn(fake, fake, fake, fake, fake, fake, fake, ctypes.byref(sh), 4, 0.125, None, None, fake,
                              fake, 1 << 20, None) == esa.ERR_UNSUPPORTED
 

@@ -449,6 +449,46 @@ def test_routed_relu():
     assert_close(gpu_routed(to_dev(inp), sh, 30), ref)
 
 
+ROUTED_PER_HEAD_CASES = [
+    # a set per query head, drawn routes
+    dict(B=1, Tq=300, Tk=300, Hq=8, Hkv=2, D=128, H_I=8, D_I=64, top_k=64, flags=PER_HEAD),
+    # 2 query heads per set, with the ReLU (one head per set: exact on the tensor cores)
+    dict(B=2, Tq=200, Tk=200, Hq=8, Hkv=8, D=128, H_I=4, D_I=32, top_k=40, flags=RELU | PER_HEAD),
+    # D = 64, a set spanning two key/value heads, queries deep in a cache
+    dict(B=1, Tq=130, Tk=700, q_offset=570, Hq=8, Hkv=4, D=64, H_I=2, D_I=16, top_k=100, flags=PER_HEAD),
+]
+
+
+@pytest.mark.parametrize("routes", ["drawn", "all_sparse"])
+@pytest.mark.parametrize("over", ROUTED_PER_HEAD_CASES, ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
+def test_routed_per_head_sets(over, routes):
+    """Routed attention with one index set per indexer head: each sparse
+    head masks with the set of indexer head h // (Hq // H_I), rebuilt from
+    that head's own scores and its threshold form; full heads stay exact
+    causal attention."""
+    cfg, sh, inp = _case(seed=515, routed=True, **over)
+    if routes == "all_sparse":
+        inp["route"] = torch.ones_like(inp["route"])
+    K = cfg["top_k"]
+    d = to_dev(inp)
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, K)
+    assert_close(gpu_routed(d, sh, K), ref)
+    thr = gpu_threshold(d, sh, K).reshape(-1, sh["H_I"], 2)
+    assert_thr_equal(thr.reshape(-1, 2), O.threshold(inp["qI"], inp["kI"], inp["wI"], sh, K).reshape(-1, 2))
+
+
+def test_threshold_per_head_ties():
+    """Per-head threshold forms on tie-heavy scores (small int8 range), with
+    and without the ReLU."""
+    for flags in (PER_HEAD, RELU | PER_HEAD):
+        cfg, sh, inp = _case(seed=516, B=1, Tq=260, Tk=260, H_I=3, D_I=64, top_k=50, flags=flags)
+        g = torch.Generator().manual_seed(6)
+        inp["qI"] = torch.randint(-1, 2, inp["qI"].shape, dtype=torch.int8, generator=g)
+        inp["kI"] = torch.randint(-1, 2, inp["kI"].shape, dtype=torch.int8, generator=g)
+        d = to_dev(inp)
+        assert_thr_equal(gpu_threshold(d, sh, 50), O.threshold(inp["qI"], inp["kI"], inp["wI"], sh, 50).reshape(-1, 2))
+
+
 # ------------------------------------------------------------------ attention router
 def _gpu_route(d_k, sh, W):
     m = esa()
@@ -584,6 +624,23 @@ def test_per_head_prefill_full():
     oi, oc, ref, _ = O.gated_sparse_attention(inp, sh, K, rows=rows)
     st, out, _ = gpu_attn(d, sh, K, gi, gc)
     assert st == 0
+    assert_close(out[rows], ref)
+
+
+def test_per_head_prefill_routed_full():
+    """The per-head workload (S=8192, a ReLU'd set per query head) through
+    the routed launch with every head sparse: the per-head threshold forms on
+    every row and set, bit-exact; outputs on 512 seeded rows plus edge rows,
+    equal to the gathered path's definition."""
+    cfg, sh, inp = _full("per_head_prefill")
+    K = cfg["top_k"]
+    d = to_dev(inp)
+    d["route"] = torch.ones(sh["B"], sh["Hq"], dtype=torch.uint8, device="cuda")
+    thr = gpu_threshold(d, sh, K)
+    assert_thr_equal(thr, O.threshold(inp["qI"], inp["kI"], inp["wI"], sh, K).reshape(-1, 2))
+    rows = sample_rows(sh["B"], sh["Tq"], K, 512, seed=5)
+    out = gpu_routed(d, sh, K)
+    _, _, ref, _ = O.gated_sparse_attention(dict(inp, route=None), sh, K, rows=rows)
     assert_close(out[rows], ref)
 
 
