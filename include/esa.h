@@ -34,15 +34,17 @@
  *     call (they clear what they use), except after a device error, after
  *     which it must be re-initialised. Calls that share a workspace must not
  *     overlap in time (use one stream per workspace).
- *   - Decode-like selections (esa_topk_select, esa_gated_sparse_attn and
- *     esa_topk_select_noalloc on few rows with long prefixes) keep a small
- *     state between calls (a call counter, barrier counters, histograms),
- *     each call clearing what the next one needs. Such calls may share one
- *     workspace (sized for the largest) across shapes. A workspace that any
- *     other call used since (another op, or a prefill-like shape) must be
- *     re-initialised with esa_workspace_init before the next decode-like
- *     selection: their scratch may overlap that state. Stale state makes
- *     results wrong (or sets a status), never an out-of-bounds access.
+ *   - Decode-like calls (esa_topk_select, esa_sparse_attn,
+ *     esa_gated_sparse_attn and esa_topk_select_noalloc on few rows with
+ *     long prefixes) keep a small state between calls (a call counter,
+ *     barrier counters, histograms; the attention's per-block ready
+ *     records), each call clearing what the next one needs. Such calls may
+ *     share one workspace (sized for the largest) across shapes. A
+ *     workspace that any other call used since (another op, or a
+ *     prefill-like shape) must be re-initialised with esa_workspace_init
+ *     before the next decode-like call: their scratch may overlap that
+ *     state. Stale state makes results wrong (or sets a status), never an
+ *     out-of-bounds access.
  *
  * Shapes (esa_shape):
  *   B sequences; Tq query rows per sequence; Tk key positions per sequence;
@@ -185,7 +187,10 @@ ESA_API esa_status esa_topk_select(const int8_t *qI, const int8_t *kI, const int
  * lse may be NULL (g and lin together). A row with cnt = 0 gets out = 0 (or
  * the linear branch share when gated) and lse = -inf. Indices outside
  * 0..p, or cnt outside 0..min(top_k, p+1), set ESA_ERR_BAD_INDEX in the
- * status word; the offending row is left unwritten. */
+ * status word; the offending row is left unwritten. Rows whose index list
+ * is split over several blocks (few rows: decode) exchange partial results
+ * through the workspace and wait for one another with a bounded wait
+ * (ESA_ERR_TIMEOUT when it runs out, the rows left unwritten). */
 ESA_API esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,
                            const int32_t *cnt, const esa_shape *s, int top_k, float scale, const float *g,
                            const uint16_t *lin, float *out, float *lse, void *ws, size_t ws_bytes, void *stream);

@@ -181,21 +181,26 @@ bool decode_single_launch() {
     return e && strcmp(e, "fused") == 0;
 }
 
-// Offset of the two-launch path's idx/cnt room: past the selection's own
-// workspace and past any shape's persistent selection state.
-size_t gated_scratch_off(const Shape &x, int K) {
-    return align256(std::max(topk_ws(x, K), split_state_max_bytes()));
-}
+// The two-launch path's layout: the selection's own workspace and any
+// shape's persistent selection state, the attention's records region (the
+// same offset for every decode-like shape), then idx/cnt room and the
+// attention's partials.
+size_t gated_rec_off(const Shape &x, int K) { return align256(std::max(topk_ws(x, K), split_state_max_bytes())); }
+size_t gated_scratch_off(const Shape &x, int K) { return gated_rec_off(x, K) + dec_rec_bytes(); }
 
 // Workspace of esa_gated_sparse_attn: the fused step's, or for the two
 // launches the selection's workspace plus room for idx/cnt when the caller
 // passes none.
-size_t gated_ws(const Shape &x, int K) {
-    DecodePlan dp = decode_single_launch() ? plan_decode_step(x, K) : DecodePlan{};
-    if (dp.ok) return dp.ws_bytes;
+// The attention's exchange area follows.
+size_t gated_xoff(const Shape &x, int K) {
     const Shape r = selection_rows(x);
     const size_t sets = (size_t)(r.B * r.Tq);
     return gated_scratch_off(x, K) + align256(sets * K * 4) + align256(sets * 4);
+}
+size_t gated_ws(const Shape &x, int K) {
+    DecodePlan dp = decode_single_launch() ? plan_decode_step(x, K) : DecodePlan{};
+    if (dp.ok) return dp.ws_bytes;
+    return gated_xoff(x, K) + align256(plan_sparse_attn(x, K).x_bytes);
 }
 
 }  // namespace
@@ -332,11 +337,12 @@ esa_status esa_gated_sparse_attn(const uint16_t *q, const uint16_t *k, const uin
     const int32_t *w = per_head_of(r) ? unit_weight() : wI;
     if (!w) return ESA_ERR_CUDA;
     SplitPlan sp = plan_split_select(r, top_k);
-    e = sp.ok ? launch_split_select(qI, kI, w, r, top_k, ii, cc, ws, scr, sp, st)
+    e = sp.ok ? launch_split_select(qI, kI, w, r, top_k, ii, cc, ws, gated_rec_off(x, top_k), sp, st)
               : launch_row_select(qI, kI, w, r, top_k, ii, cc, nullptr, ws, sel_bytes, st);
     if (e != ESA_OK) return e;
     AttnPlan ap = plan_sparse_attn(x, top_k);
-    return launch_sparse_attn(q, k, v, ii, cc, x, top_k, scale, g, lin, out, lse, ws, ap, st);
+    return launch_sparse_attn(q, k, v, ii, cc, x, top_k, scale, g, lin, out, lse, ws, ap, st,
+                              base + gated_rec_off(x, top_k), base + gated_xoff(x, top_k));
 }
 
 esa_status esa_gated_mix(const float *attn, const uint16_t *lin, const float *g, const uint8_t *head_mask,

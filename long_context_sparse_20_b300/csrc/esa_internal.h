@@ -129,18 +129,26 @@ struct AttnPlan {
     int hs;      // query heads per index set
     int seg;     // heads of one key/value head sharing one index set
     int gps;     // head groups per segment
-    int var;     // kernel variant: 0 column split, 1 key split (16-head tiles), 2 keys as rows (<= 8 heads)
+    int var;     // kernel variant: 0 column split, 1 key split (16-head tiles), 2 keys as rows (<= 8 heads),
+                 // 3 split index lists (the decode kernel, 8 warps over key slices)
     int splits;  // key splits per (row, kv head, head group)
     int keys_per_split;
     long long grid;
     size_t smem;
-    size_t ws_bytes;
+    size_t rec_bytes;  // the decode kernel's (max, sum) records (dec_rec_bytes; zero between calls)
+    size_t x_bytes;    // the decode kernel's partial outputs
+    size_t ws_bytes;   // status word + records + partials
 };
 AttnPlan plan_sparse_attn(const Shape &s, int K);
+// Bytes of the decode kernel's records region on this device (the same for
+// every shape, so that one region serves alternating shapes).
+size_t dec_rec_bytes();
+// The status word is at ws; the decode kernel's records at xrec and partials
+// at xpart (defaults: ws + kStatusBytes, then + rec_bytes).
 esa_status launch_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,
                               const int32_t *cnt, const Shape &s, int K, float scale, const float *g,
                               const uint16_t *lin, float *out, float *lse, void *ws, const AttnPlan &plan,
-                              cudaStream_t st);
+                              cudaStream_t st, void *xrec = nullptr, void *xpart = nullptr);
 
 // ---- routed (full | sparse per head) attention ---------------------------
 size_t ws_routed(const Shape &s, int K);

@@ -25,8 +25,10 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 #include <set>
+#include <string>
 #include <utility>
 
 #include "esa_device.cuh"
@@ -40,7 +42,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kKeys = 64;  // keys per stage
-constexpr int kMaxSplits = 16;
+constexpr int kMaxSplits = 16;  // at most 32: the decode kernel's merge gives each block one lane
 constexpr int kIdxWin = 512;  // staged indices (a multiple of kKeys; small enough for 3 blocks per SM)
 
 template <int D>
@@ -63,6 +65,12 @@ struct AttnArgs {
     int seg;    // heads of one key/value head that share one index set
     int gps;    // head groups per segment
     float scale_log2;
+    // split index lists (the decode kernel): the blocks' merged partials and
+    // their (max, sum) records in the workspace
+    float *xpart;
+    unsigned long long *xrec;
+    long long wait_ns;
+    int extra;  // extra arrivals the barrier waits for (0; > 0 only to test the timeout path)
 };
 
 // Variants (one split per index list for the key-split ones):
@@ -76,7 +84,7 @@ struct AttnArgs {
 //             rows: S^T = K Q^T (16 keys x 8 heads) and O^T = V^T P^T (D x 8
 //             heads), P^T's fragments by movmatrix transposes — no padded
 //             head rows when a key/value head serves 8 query heads or fewer.
-enum { kColSplit = 0, kKeySplit = 1, kKeyRows = 2 };
+enum { kColSplit = 0, kKeySplit = 1, kKeyRows = 2, kDecode = 3 };
 template <int D, int GT, int VAR>
 __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
     constexpr bool KS = VAR == kKeySplit;
@@ -711,6 +719,443 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(AttnArgs a) {
     }  // !kKeyRows
 }
 
+// Floats of one (row, head group)'s partial outputs: [S blocks][GT heads][D].
+// Its (max, sum) records, [S][GT] 64-bit words, live in a separate region
+// (zero between calls), followed by one word nothing writes (the timeout
+// test waits on it).
+__host__ __device__ inline size_t dec_group_floats(int GT, int D, int S) { return (size_t)S * GT * D; }
+
+// A block's (max, sum) record: max's bits low, sum's high. Zero means "not
+// yet written" (a written record never is: sum >= 1 whenever max is finite,
+// and max = -inf when sum = 0); an all-ones sum marks a block that found an
+// invalid index.
+constexpr unsigned kBadSum = 0xffffffffu;
+__device__ __forceinline__ unsigned long long ml_record(float M, float L) {
+    return (unsigned long long)__float_as_uint(M) | ((unsigned long long)__float_as_uint(L) << 32);
+}
+
+// Decode rows (the index list split over S blocks): 8 warps, and each warp
+// owns a slice of every stage's keys for one 16-head tile, so no score is
+// computed twice. A stage holds 128 keys; with GT = 16 * HT heads, warp w
+// takes head tile w % HT and keys (w / HT) * SL .. + SL of the stage (SL =
+// 16 * HT). A warp keeps its own online softmax over every output column;
+// at the end the warps of a head tile merge through shared memory and each
+// block publishes its merged (max, sum, unnormalised output) per head to the
+// workspace (L2), then a (max, sum) record per head with a release store.
+// Block `split` finalises heads split, split + S, ...: it polls the S
+// records of each (acquire loads, bounded), clears them, and merges the S
+// partials. The launch is cooperative (every block resident; one block per
+// SM by registers), so no thread-block cluster has to fit in one GPC:
+// 16-block clusters at one block per SM fit only 7 at a time here.
+constexpr int kDecThreads = 256;
+constexpr int kDecKeys = 128;  // keys per stage
+
+template <int D>
+struct DecCfg {
+    static constexpr int RS = D + 8;             // padded K/V row stride (bf16 elements)
+    static constexpr int TILE = kDecKeys * RS;   // one K or V stage tile (elements)
+    static constexpr int OS = D + 8;             // padded row stride of a warp's fp32 partial
+    static constexpr size_t STAGE_BYTES = (size_t)2 * TILE * 2;
+    static constexpr size_t MERGE_BYTES = (size_t)8 * 16 * OS * 4 + 2 * 8 * 16 * 4;
+};
+
+template <int D, int GT>
+__global__ void __launch_bounds__(kDecThreads) decode_attn_kernel(AttnArgs a) {
+    constexpr int RS = DecCfg<D>::RS, TILE = DecCfg<D>::TILE, OS = DecCfg<D>::OS;
+    constexpr int HT = GT / 16;         // head tiles
+    constexpr int KQ = 8 / HT;          // key slices per stage
+    constexpr int SL = kDecKeys / KQ;   // keys per warp and stage
+    constexpr int NT = SL / 8;          // score n-tiles of 8 keys
+    constexpr int DK = D / 16;          // k-steps over the head dim
+    constexpr int DN = D / 8;           // output n-tiles (every column)
+    constexpr int CH = D / 8;           // 16-byte chunks per K/V row
+    constexpr int KPR = kDecThreads / CH;  // keys per gather round
+    constexpr int GR = kDecKeys / KPR;     // gather rounds per stage
+    static_assert(HT * KQ == 8 && NT % 2 == 0 && DN % 2 == 0, "tile split");
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint16_t *Qs = reinterpret_cast<uint16_t *>(smem_raw);
+    unsigned char *work = smem_raw + (size_t)GT * RS * 2;  // stage buffers, then the warps' partials
+    uint16_t *KVs = reinterpret_cast<uint16_t *>(work);
+
+    __shared__ int fin_state;  // finalising: 0 ok, 1 an invalid index, 2 a wait ran out
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ht = warp % HT, kq = warp / HT;
+    const int g8 = lane >> 2, c4 = lane & 3;
+
+    long long bid = blockIdx.x;
+    const int split = (int)(bid % a.splits);
+    const long long grp = bid / a.splits;  // (row, key/value head, head group)
+    bid = grp;
+    const int hgi = (int)(bid % a.hg);
+    bid /= a.hg;
+    const int kvh = (int)(bid % a.Hkv);
+    const long long row = bid / a.Hkv;  // b*Tq + t
+    const long long b = row / a.Tq, t = row % a.Tq;
+    const long long p = a.q_offset + t;
+    const int G = a.Hq / a.Hkv;
+    const int sg = hgi / a.gps, sub = hgi % a.gps;
+    const int h0 = kvh * G + sg * a.seg + sub * GT;  // first query head of this block
+    const int nh = min(GT, a.seg - sub * GT);
+    const long long set = a.nsets > 1 ? row * a.nsets + h0 / a.hs : row;
+
+    // ---- Q tile (GT heads x D), zero rows past the group (independent of the selection)
+    {
+        const uint16_t *qrow = a.q + (row * a.Hq + h0) * (long long)D;
+        for (int i = tid; i < GT * CH; i += kDecThreads) {
+            const int hr = i / CH, ch = i % CH;
+            cp_async16_zfill(smem_u32(Qs + hr * RS + ch * 8), qrow + (hr < nh ? hr * D + ch * 8 : 0), hr < nh);
+        }
+        cp_async_commit();
+    }
+    pdl_wait();
+    const int k_begin = split * a.kps;
+    const int lim = max(0, min(a.kps, a.K - k_begin));  // list positions of this split
+    const int32_t *idx_row = a.idx + set * (long long)a.K + k_begin;
+    const uint16_t *kbase = a.k + (b * a.Tk * a.Hkv + kvh) * (long long)D;
+    const uint16_t *vbase = a.v + (b * a.Tk * a.Hkv + kvh) * (long long)D;
+    const long long kstride = (long long)a.Hkv * D;
+    // gathers: thread tid fetches chunk tid % CH of keys tid / CH + r * KPR;
+    // the indices are read first (for stage 0 together with the count)
+    const int ch = tid % CH, k0 = tid / CH;
+    auto load_idx = [&](int kb, int *j) {
+#pragma unroll
+        for (int r = 0; r < GR; r++) {
+            const int pos = kb + k0 + r * KPR;
+            j[r] = pos < lim ? __ldg(idx_row + pos) : -1;
+        }
+    };
+    int j0[GR];
+    load_idx(0, j0);
+    int bad = 0;
+    int c = a.cnt[set];
+    // this block's first output element of the finalising merge: its gate
+    // and linear-branch values are fetched now, off the critical path
+    const bool gated = a.g != nullptr && a.lin != nullptr;
+    const int S = a.splits;
+    const int mine = nh > split ? (nh - split + S - 1) / S : 0;  // heads this block finalises
+    uint2 lw0 = make_uint2(0u, 0u);
+    float gh0 = 1.f;
+    if (gated && tid < mine * (D / 4)) {
+        const int h = h0 + split + (tid / (D / 4)) * S;
+        lw0 = *reinterpret_cast<const uint2 *>(a.lin + (row * a.Hq + h) * (long long)D + (tid % (D / 4)) * 4);
+        gh0 = a.g[h];
+    }
+    const int cmax = (int)min((long long)a.K, p + 1);
+    if (c < 0 || c > cmax) {
+        bad = 1;
+        c = 0;
+    }
+    const int k_end = min(c, k_begin + a.kps);
+    const int nkeys = max(0, k_end - k_begin);
+    auto load_stage = [&](int buf, int kb, int *j) {
+        uint16_t *Kt = KVs + buf * 2 * TILE;
+        uint16_t *Vt = Kt + TILE;
+#pragma unroll
+        for (int r = 0; r < GR; r++) {
+            const int pos = kb + k0 + r * KPR;
+            int jr = pos < nkeys ? j[r] : -1;
+            if (pos < nkeys && (jr < 0 || jr > p)) {
+                bad = 1;
+                jr = -1;
+            }
+            const bool valid = jr >= 0;
+            const long long off = (valid ? jr : 0) * kstride + ch * 8;
+            const int key = k0 + r * KPR;
+            cp_async16_zfill(smem_u32(Kt + key * RS + ch * 8), kbase + off, valid);
+            cp_async16_zfill(smem_u32(Vt + key * RS + ch * 8), vbase + off, valid);
+        }
+        cp_async_commit();
+    };
+
+    const int nst = (nkeys + kDecKeys - 1) / kDecKeys;
+    if (nst > 0) load_stage(0, 0, j0);
+    if (nst > 0) cp_async_wait<1>(); else cp_async_wait<0>();  // the Q tile
+    __syncthreads();
+    // Q fragments are re-read from shared memory at every k-step (registers
+    // for two blocks per SM: a 16-block cluster then needs only 8 SMs of a GPC)
+    const uint32_t qaddr = smem_u32(Qs + (ht * 16 + (lane & 15)) * RS + (lane >> 4) * 8);
+
+    float o[DN][4];
+#pragma unroll
+    for (int i = 0; i < DN; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};  // head rows g8, g8 + 8
+    const int kb = kq * SL;  // this warp's first key within a stage
+
+    for (int s = 0; s < nst; s++) {
+        if (s + 1 < nst) {
+            int jn[GR];
+            load_idx((s + 1) * kDecKeys, jn);
+            load_stage((s + 1) & 1, (s + 1) * kDecKeys, jn);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const uint16_t *Kt = KVs + (s & 1) * 2 * TILE;
+        const uint16_t *Vt = Kt + TILE;
+        const int kvalid = min(kDecKeys, nkeys - s * kDecKeys);
+        if (kb < kvalid) {
+            float sc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < DK; kk += 2) {
+                uint32_t qa[4], qb[4];
+                ldmatrix_x4(qaddr + kk * 32, qa[0], qa[1], qa[2], qa[3]);
+                ldmatrix_x4(qaddr + kk * 32 + 32, qb[0], qb[1], qb[2], qb[3]);
+#pragma unroll
+                for (int nt = 0; nt < NT; nt++) {
+                    uint32_t b0, b1, b2, b3;
+                    const int key = kb + nt * 8 + (lane & 7), col = kk * 16 + (lane >> 3) * 8;
+                    ldmatrix_x4(smem_u32(Kt + key * RS + col), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[nt], qa, b0, b1);
+                    mma_bf16_16816(sc[nt], qb, b2, b3);
+                }
+            }
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int key = kb + nt * 8 + 2 * c4 + (e & 1);
+                    const float x = key < kvalid ? sc[nt][e] * a.scale_log2 : -INFINITY;
+                    sc[nt][e] = x;
+                    mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                }
+            }
+            float corr[2];
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                const float mnew = fmaxf(m_r[r], mx[r]);
+                const float muse = mnew == -INFINITY ? 0.f : mnew;
+                corr[r] = exp2f(m_r[r] - muse);
+                m_r[r] = mnew;
+                mx[r] = muse;
+            }
+            float rs[2] = {0.f, 0.f};
+            uint32_t ph[NT][2], pl[NT][2];  // P as bf16 hi + lo (~16 significant bits)
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                const float p0 = exp2f(sc[nt][0] - mx[0]), p1 = exp2f(sc[nt][1] - mx[0]);
+                const float p2 = exp2f(sc[nt][2] - mx[1]), p3 = exp2f(sc[nt][3] - mx[1]);
+                rs[0] += p0 + p1;
+                rs[1] += p2 + p3;
+                ph[nt][0] = pack_bf16(p0, p1);
+                ph[nt][1] = pack_bf16(p2, p3);
+                pl[nt][0] = pack_bf16(p0 - bf16lo(ph[nt][0]), p1 - bf16hi(ph[nt][0]));
+                pl[nt][1] = pack_bf16(p2 - bf16lo(ph[nt][1]), p3 - bf16hi(ph[nt][1]));
+            }
+#pragma unroll
+            for (int r = 0; r < 2; r++) {
+                rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 1);
+                rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 2);
+                l_r[r] = l_r[r] * corr[r] + rs[r];
+            }
+#pragma unroll
+            for (int dn = 0; dn < DN; dn++) {
+                o[dn][0] *= corr[0];
+                o[dn][1] *= corr[0];
+                o[dn][2] *= corr[1];
+                o[dn][3] *= corr[1];
+            }
+#pragma unroll
+            for (int kk2 = 0; kk2 < NT / 2; kk2++) {
+                const uint32_t ah[4] = {ph[2 * kk2][0], ph[2 * kk2][1], ph[2 * kk2 + 1][0], ph[2 * kk2 + 1][1]};
+                const uint32_t al[4] = {pl[2 * kk2][0], pl[2 * kk2][1], pl[2 * kk2 + 1][0], pl[2 * kk2 + 1][1]};
+#pragma unroll
+                for (int dn = 0; dn < DN / 2; dn++) {
+                    uint32_t b0, b1, b2, b3;
+                    const int key = kb + kk2 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int col = dn * 16 + (lane >> 4) * 8;
+                    ldmatrix_x4_trans(smem_u32(Vt + key * RS + col), b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * dn], ah, b0, b1);
+                    mma_bf16_16816(o[2 * dn + 1], ah, b2, b3);
+                    mma_bf16_16816(o[2 * dn], al, b0, b1);
+                    mma_bf16_16816(o[2 * dn + 1], al, b2, b3);
+                }
+            }
+        }
+        __syncthreads();  // the buffer is free for the stage after next
+    }
+    bad = __syncthreads_or(bad);  // also: every warp is done with the stage buffers
+
+    // ---- the warps' partials -> shared memory
+    float *Wo = reinterpret_cast<float *>(work);  // [8 warps][16 heads][OS]
+    float *Wm = Wo + 8 * 16 * OS, *Wl = Wm + 8 * 16;
+#pragma unroll
+    for (int rr = 0; rr < 2; rr++) {
+        const int hr = g8 + rr * 8;
+#pragma unroll
+        for (int dn = 0; dn < DN; dn++)
+            *reinterpret_cast<float2 *>(Wo + (warp * 16 + hr) * OS + dn * 8 + 2 * c4) =
+                make_float2(o[dn][2 * rr], o[dn][2 * rr + 1]);
+        if (c4 == 0) {
+            Wm[warp * 16 + hr] = m_r[rr];
+            Wl[warp * 16 + hr] = l_r[rr];
+        }
+    }
+    // the group's exchange area (dec_group_floats)
+    float *XP = a.xpart + (size_t)grp * dec_group_floats(GT, D, S);
+    unsigned long long *XR = a.xrec + (size_t)grp * S * GT;
+    const unsigned long long *never = a.xrec + (size_t)gridDim.x * GT;
+    const int MM = (GT + S - 1) / S;  // heads per finalising block, at most
+    const size_t stage_bytes = DecCfg<D>::STAGE_BYTES * (a.kps > kDecKeys ? 2 : 1);
+    float *Wt = reinterpret_cast<float *>(
+        work + (stage_bytes > DecCfg<D>::MERGE_BYTES ? stage_bytes : DecCfg<D>::MERGE_BYTES));  // [MM][S]
+    float *Mf = Wt + MM * S, *Lf = Mf + MM;                                                   // [MM]
+    __syncthreads();
+    // merge each head's key slices (TPH threads per head), store the block's
+    // partial, then (after a barrier: every thread's stores come first) its
+    // record
+    {
+        constexpr int TPH = kDecThreads / GT;  // threads per head
+        constexpr int FPT = D / 4 / TPH;       // float4 columns per thread
+        static_assert(FPT * TPH * 4 == D, "column split");
+        const int hr = tid / TPH, w0 = hr / 16, r16 = hr % 16;  // warps w0 + HT * q hold this head
+        float M = -INFINITY, L = 0.f;
+        if (hr < nh) {
+#pragma unroll
+            for (int q = 0; q < KQ; q++) M = fmaxf(M, Wm[(w0 + HT * q) * 16 + r16]);
+            float sw[KQ];
+#pragma unroll
+            for (int q = 0; q < KQ; q++) {
+                const int w = w0 + HT * q;
+                const float mw = Wm[w * 16 + r16];
+                sw[q] = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                L = fmaf(sw[q], Wl[w * 16 + r16], L);
+            }
+            float *xp = XP + ((size_t)split * GT + hr) * D;
+#pragma unroll
+            for (int f = 0; f < FPT; f++) {
+                const int d4 = (tid % TPH + f * TPH) * 4;
+                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < KQ; q++) {
+                    const float4 v = *reinterpret_cast<const float4 *>(Wo + ((w0 + HT * q) * 16 + r16) * OS + d4);
+                    O.x = fmaf(sw[q], v.x, O.x);
+                    O.y = fmaf(sw[q], v.y, O.y);
+                    O.z = fmaf(sw[q], v.z, O.z);
+                    O.w = fmaf(sw[q], v.w, O.w);
+                }
+                __stcg(reinterpret_cast<float4 *>(xp + d4), O);
+            }
+        }
+        __syncthreads();
+        if (hr < nh && tid % TPH == 0)
+            st_release_u64(XR + (size_t)split * GT + hr,
+                           bad ? ((unsigned long long)kBadSum << 32) : ml_record(M, L));
+    }
+    // finalise: one warp per head, one lane per block's record (S < 32);
+    // with test-only extra arrivals, lane S also waits on a word nothing writes
+    if (tid == 0) fin_state = 0;
+    __syncthreads();
+    for (int i = warp; i < mine; i += kDecThreads / 32) {
+        const int hr = split + i * S;
+        unsigned long long rec = ml_record(-INFINITY, 0.f);
+        bool timed_out = false;
+        if (lane < S || (lane == S && a.extra > 0)) {
+            const unsigned long long *src = lane < S ? XR + (size_t)lane * GT + hr : never;
+            rec = ld_acquire_u64(src);
+            if (rec == 0) {
+                unsigned long long t0, t;
+                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+                unsigned ns = 32;
+                while ((rec = ld_acquire_u64(src)) == 0) {
+                    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+                    if ((long long)(t - t0) > a.wait_ns) {
+                        timed_out = true;
+                        break;
+                    }
+                    __nanosleep(ns);
+                    if (ns < 256) ns <<= 1;
+                }
+            }
+            if (lane < S) XR[(size_t)lane * GT + hr] = 0ull;  // cleared for the next call
+            if (lane == S) rec = ml_record(-INFINITY, 0.f);
+        }
+        const bool badrec = (unsigned)(rec >> 32) == kBadSum;
+        if (__any_sync(0xffffffffu, timed_out)) {
+            if (lane == 0) atomicMax(&fin_state, 2);
+        } else if (__any_sync(0xffffffffu, badrec)) {
+            if (lane == 0) atomicMax(&fin_state, 1);
+        }
+        const float mb = __uint_as_float((unsigned)rec), lb = __uint_as_float((unsigned)(rec >> 32));
+        float Mx = mb;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+        const float Mu = Mx == -INFINITY ? 0.f : Mx;
+        const float w = lane < S ? exp2f(mb - Mu) : 0.f;
+        float Ls = lane < S ? lb * w : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+        if (lane < S) Wt[i * S + lane] = w;
+        if (lane == 0) {
+            Mf[i] = Mx;
+            Lf[i] = Ls;
+        }
+    }
+    __syncthreads();
+    if (fin_state != 0) {
+        if (tid == 0) set_status(a.status, fin_state == 2 ? ESA_ERR_TIMEOUT : ESA_ERR_BAD_INDEX);
+        return;
+    }
+    for (int e = tid; e < mine * (D / 4); e += kDecThreads) {
+        const int i = e / (D / 4), d4 = (e % (D / 4)) * 4;
+        const int hr = split + i * S, h = h0 + hr;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float *xp = XP + (size_t)hr * D + d4;
+        // eight blocks' partials in flight at a time
+        for (int s0 = 0; s0 < S; s0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++)
+                if (s0 + u < S) v[u] = __ldcg(reinterpret_cast<const float4 *>(xp + (size_t)(s0 + u) * GT * D));
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                if (s0 + u < S) {
+                    const float w = Wt[i * S + s0 + u];
+                    O.x = fmaf(v[u].x, w, O.x);
+                    O.y = fmaf(v[u].y, w, O.y);
+                    O.z = fmaf(v[u].z, w, O.z);
+                    O.w = fmaf(v[u].w, w, O.w);
+                }
+            }
+        }
+        const float L = Lf[i];
+        float4 res = L > 0.f ? make_float4(O.x / L, O.y / L, O.z / L, O.w / L) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const long long off = (row * a.Hq + h) * (long long)D + d4;
+        if (gated) {
+            const bool first = e == tid;
+            const float gh = first ? gh0 : a.g[h], gl = 1.0f - gh;
+            const uint2 lw = first ? lw0 : *reinterpret_cast<const uint2 *>(a.lin + off);
+            res.x = fmaf(gh, res.x, gl * bf16lo(lw.x));
+            res.y = fmaf(gh, res.y, gl * bf16hi(lw.x));
+            res.z = fmaf(gh, res.z, gl * bf16lo(lw.y));
+            res.w = fmaf(gh, res.w, gl * bf16hi(lw.y));
+        }
+        *reinterpret_cast<float4 *>(a.out + off) = res;
+        if (a.lse && d4 == 0)
+            a.lse[row * a.Hq + h] = L > 0.f ? (Mf[i] + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
+}
+
+template <int D>
+size_t dec_smem(int GT, int S, int kps) {
+    const size_t work = std::max(DecCfg<D>::STAGE_BYTES * (kps > kDecKeys ? 2 : 1), DecCfg<D>::MERGE_BYTES);
+    const size_t MM = (size_t)(GT + S - 1) / S;
+    return (size_t)GT * DecCfg<D>::RS * 2 + work + (MM * S + 2 * MM) * 4;
+}
+size_t dec_part_bytes(long long groups, int GT, int D, int S) {
+    return align256((size_t)groups * dec_group_floats(GT, D, S) * 4);
+}
+// Records region: every decode-kernel shape on this device indexes it from
+// its start, so one region (zero between calls: each call clears the
+// records it read) serves any sequence of shapes.
+constexpr int kMaxRecBlocksPerSm = 2, kMaxRecHeads = 64;
+size_t dec_rec_entries() { return (size_t)device_info().sms * kMaxRecBlocksPerSm * kMaxRecHeads; }
+
 template <int D, int GT>
 size_t attn_smem() {
     return (size_t)GT * Cfg<D>::RS * 2 + (size_t)2 * 2 * Cfg<D>::TILE * 2;  // Q tile + 2 stages x (K, V)
@@ -765,8 +1210,31 @@ bool prepare_attn(void *fn, size_t smem) {
     return true;
 }
 
+void *dec_kernel(int D, int GT) {
+    if (D == 64) {
+        if (GT == 16) return (void *)decode_attn_kernel<64, 16>;
+        if (GT == 32) return (void *)decode_attn_kernel<64, 32>;
+        return (void *)decode_attn_kernel<64, 64>;
+    }
+    if (GT == 16) return (void *)decode_attn_kernel<128, 16>;
+    if (GT == 32) return (void *)decode_attn_kernel<128, 32>;
+    return (void *)decode_attn_kernel<128, 64>;
+}
+size_t dec_smem_of(int D, int GT, int S, int kps) {
+    return D == 64 ? dec_smem<64>(GT, S, kps) : dec_smem<128>(GT, S, kps);
+}
+// The column-split kernel for split index lists instead of the decode
+// kernel (ESA_DECODE_ATTN=colsplit; read once).
+bool decode_colsplit() {
+    static const bool v = [] {
+        const char *e = getenv("ESA_DECODE_ATTN");
+        return e && std::string(e) == "colsplit";
+    }();
+    return v;
+}
+
 // Whether a cluster of `n` blocks of this kernel can be resident (cached).
-bool cluster_fits(void *fn, size_t smem, int n) {
+bool cluster_fits(void *fn, size_t smem, int n, int threads = kThreads) {
     static std::mutex mu;
     static std::set<std::pair<std::pair<int, void *>, int>> ok, bad;
     int dev = 0;
@@ -780,7 +1248,7 @@ bool cluster_fits(void *fn, size_t smem, int n) {
     if (!prepare_attn(fn, smem)) return false;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)n);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -798,6 +1266,8 @@ bool cluster_fits(void *fn, size_t smem, int n) {
 }
 
 }  // namespace
+
+size_t dec_rec_bytes() { return align256((dec_rec_entries() + 1) * 8); }
 
 AttnPlan plan_sparse_attn(const Shape &s, int K) {
     AttnPlan p{};
@@ -825,13 +1295,35 @@ AttnPlan plan_sparse_attn(const Shape &s, int K) {
     splits = (K + kps - 1) / kps;
     size_t base = 0;
     void *fn = attn_kernel(s.D, gt, &base);
-    // shrink the cluster until the device can hold one
-    while (splits > 1 && !cluster_fits(fn, base + recv_smem(s.D, gt, splits), splits)) {
+    auto fewer = [&]() {
         splits = (splits + 1) / 2;
         kps = (K + splits - 1) / splits;
         kps = (kps + kKeys - 1) / kKeys * kKeys;
         splits = (K + kps - 1) / kps;
+    };
+    if (splits > 1 && !decode_colsplit()) {
+        // the decode kernel: every block resident (a cooperative launch), so
+        // fewer splits until the grid fits the device
+        auto cap = [&]() {
+            return (long long)occupancy(dec_kernel(s.D, gt), kDecThreads, dec_smem_of(s.D, gt, splits, kps)) * di.sms;
+        };
+        while (splits > 1 && (units * p.hg * splits > cap() ||
+                              (size_t)(units * p.hg * splits) * gt >= dec_rec_entries()))
+            fewer();
+        if (splits > 1) {
+            p.var = kDecode;
+            p.splits = splits;
+            p.smem = dec_smem_of(s.D, gt, splits, kps);
+            p.keys_per_split = kps;
+            p.grid = units * p.hg * splits;
+            p.x_bytes = dec_part_bytes(units * p.hg, gt, s.D, splits);
+            p.rec_bytes = dec_rec_bytes();
+            p.ws_bytes = kStatusBytes + p.rec_bytes + p.x_bytes;
+            return p;
+        }
     }
+    // the column-split kernel over a cluster: shrink it until the device can hold one
+    while (splits > 1 && !cluster_fits(fn, base + recv_smem(s.D, gt, splits), splits)) fewer();
     p.smem = base + recv_smem(s.D, gt, splits);
     p.splits = splits;
     // each block owns its whole index list: split the keys over the warps,
@@ -856,7 +1348,7 @@ AttnPlan plan_sparse_attn(const Shape &s, int K) {
 esa_status launch_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *idx,
                               const int32_t *cnt, const Shape &s, int K, float scale, const float *g,
                               const uint16_t *lin, float *out, float *lse, void *ws, const AttnPlan &plan,
-                              cudaStream_t st) {
+                              cudaStream_t st, void *xrec, void *xpart) {
     if (plan.grid == 0) return ESA_OK;
     AttnArgs a{};
     a.q = q;
@@ -883,26 +1375,45 @@ esa_status launch_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16
     a.splits = plan.splits;
     a.kps = plan.keys_per_split;
     a.scale_log2 = scale * 1.4426950408889634f;
+    if (plan.var == kDecode) {
+        char *w = static_cast<char *>(ws);
+        a.xrec = reinterpret_cast<unsigned long long *>(xrec ? xrec : w + kStatusBytes);
+        a.xpart = reinterpret_cast<float *>(xpart ? xpart : w + kStatusBytes + plan.rec_bytes);
+        a.wait_ns = wait_limit_ns();
+        a.extra = debug_extra_arrivals();
+    }
     size_t base = 0;
-    void *fn = attn_kernel(s.D, plan.gt, &base, plan.var);
+    void *fn = plan.var == kDecode ? dec_kernel(s.D, plan.gt) : attn_kernel(s.D, plan.gt, &base, plan.var);
     const size_t smem = plan.smem;
     if (!prepare_attn(fn, smem)) return ESA_ERR_CUDA;
     void *args[] = {(void *)&a};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)plan.grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(plan.var == kDecode ? kDecThreads : kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)plan.splits;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
+    if (plan.var == kDecode) {
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+    } else {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)plan.splits;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess && plan.var == kDecode) {
+        // a cooperative launch without the programmatic edge
+        cudaGetLastError();
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelExC(&cfg, fn, args);
+    }
     return e == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }
 

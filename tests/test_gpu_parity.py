@@ -204,6 +204,8 @@ ATTN_CASES = [
     dict(B=1, Tq=1, Tk=20000, q_offset=19999, Hq=64, Hkv=1, D=128, top_k=2048, D_I=64),  # 64 heads per KV head
     dict(B=3, Tq=1, Tk=4000, q_offset=3999, Hq=8, Hkv=2, D=64, top_k=300, D_I=32),
     dict(B=1, Tq=40, Tk=500, q_offset=460, Hq=48, Hkv=1, D=128, top_k=100, D_I=64),     # chunked, 48 heads
+    dict(B=1, Tq=1, Tk=12000, q_offset=11999, Hq=32, Hkv=1, D=128, top_k=4000, D_I=64),  # decode, two stages
+    dict(B=8, Tq=1, Tk=3000, q_offset=2999, Hq=64, Hkv=1, D=64, top_k=1024, D_I=32),     # decode, 64-head blocks
 ]
 
 
@@ -682,3 +684,50 @@ def test_wait_timeout_reports_status(monkeypatch):
     gi, gc = gpu_topk(d, sh, 512, ws=ws)
     oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, 512)
     assert_idx_equal(gi, gc, oi, oc)
+
+
+def test_decode_attention_wait_timeout_reports_status(monkeypatch):
+    """The decode attention's blocks of one row meet at a bounded counter
+    barrier; made unreachable it runs out: the call returns, the status word
+    says TIMEOUT, the rows stay unwritten, and after re-initialising the
+    workspace the same call is exact."""
+    m = esa()
+    cfg, sh, inp = _case(seed=33, B=2, Tq=1, Tk=9000, q_offset=8999, Hq=32, Hkv=1, D=128, top_k=2048, D_I=64)
+    K = 2048
+    oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+    d = to_dev(inp)
+    ws = m.workspace_for(m.OP_SPARSE_ATTN, m.shape_from(sh), K)
+    monkeypatch.setenv("ESA_DEBUG_EXTRA_ARRIVALS", "1")
+    monkeypatch.setenv("ESA_WAIT_LIMIT_NS", "20000000")
+    st, out, _ = gpu_attn(d, sh, K, oi, oc, ws=ws)
+    assert st == m.ERR_TIMEOUT
+    assert np.isnan(out).all()
+    monkeypatch.delenv("ESA_DEBUG_EXTRA_ARRIVALS")
+    monkeypatch.delenv("ESA_WAIT_LIMIT_NS")
+    m.esa_workspace_init(ws)
+    st, out, lse = gpu_attn(d, sh, K, oi, oc, ws=ws)
+    assert st == 0
+    ref, ref_lse = O.attention(inp["q"], inp["k"], inp["v"], oi, oc, sh, K, g=inp["g"], lin=inp["lin"])
+    assert_close(out, ref)
+    assert_close(lse, ref_lse, what="lse")
+
+
+def test_decode_attention_repeated_calls():
+    """The barrier's counters are cleared by each call: many calls on one
+    workspace (two shapes alternating, sized for the larger) stay exact."""
+    m = esa()
+    cases = []
+    for seed, over in ((34, dict(B=2, Tq=1, Tk=9000, q_offset=8999, Hq=32, Hkv=1, D=128, top_k=2048, D_I=64)),
+                       (35, dict(B=1, Tq=1, Tk=20000, q_offset=19999, Hq=64, Hkv=1, D=128, top_k=1024, D_I=64))):
+        cfg, sh, inp = _case(seed=seed, **over)
+        K = cfg["top_k"]
+        oi, oc = O.topk(inp["qI"], inp["kI"], inp["wI"], sh, K)
+        ref, ref_lse = O.attention(inp["q"], inp["k"], inp["v"], oi, oc, sh, K, g=inp["g"], lin=inp["lin"])
+        cases.append((sh, K, to_dev(inp), oi, oc, ref))
+    n = max(m.esa_workspace_size(m.OP_SPARSE_ATTN, m.shape_from(sh), K) for sh, K, *_ in cases)
+    ws = m.Workspace(n)
+    for it in range(6):
+        sh, K, d, oi, oc, ref = cases[it % 2]
+        st, out, _ = gpu_attn(d, sh, K, oi, oc, ws=ws, want_lse=False)
+        assert st == 0
+        assert_close(out, ref)
