@@ -349,6 +349,13 @@ ESA_API esa_status esa_read_status(void *ws, void *stream, int32_t *dev_status);
 /* A static, human-readable name for a status code. */
 ESA_API const char *esa_status_string(esa_status st);
 
+/* The compute capability the library's kernels were compiled for, as the
+ * CUDA runtime reports it for the current device (cudaFuncAttributes
+ * binaryVersion of one of its kernels: 103 for sm_103a), or -1 when the
+ * runtime cannot load them (no device, or a device they were not built
+ * for). */
+ESA_API int esa_binary_version(void);
+
 #ifdef __cplusplus
 }
 #endif

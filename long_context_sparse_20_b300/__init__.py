@@ -61,6 +61,7 @@ _SIGS = {
                        _vp, _vp, _vp, _vp]),
     "esa_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "esa_status_string": (ctypes.c_char_p, [_i32]),
+    "esa_binary_version": (ctypes.c_int, []),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)

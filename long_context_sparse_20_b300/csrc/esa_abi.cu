@@ -419,6 +419,8 @@ esa_status esa_read_status(void *ws, void *stream, int32_t *dev_status) {
     return ESA_OK;
 }
 
+int esa_binary_version(void) { return mix_binary_version(); }
+
 const char *esa_status_string(esa_status st) {
     switch (st) {
         case ESA_OK: return "ok";

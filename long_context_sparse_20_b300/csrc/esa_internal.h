@@ -53,6 +53,9 @@ int occupancy(const void *fn, int threads, size_t smem);
 constexpr size_t kStatusBytes = 256;
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// binaryVersion of the library's kernels on the current device (-1: not loadable)
+int mix_binary_version();
+
 // ---- gate mix -----------------------------------------------------------
 cudaError_t launch_gated_mix(const float *attn, const uint16_t *lin, const float *g, const uint8_t *head_mask,
                              const Shape &s, float *out, cudaStream_t st);

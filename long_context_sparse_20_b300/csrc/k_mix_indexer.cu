@@ -34,6 +34,15 @@ __global__ void __launch_bounds__(256) gated_mix_kernel(const float4 *__restrict
     }
 }
 
+int mix_binary_version() {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, gated_mix_kernel) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return fa.binaryVersion;
+}
+
 cudaError_t launch_gated_mix(const float *attn, const uint16_t *lin, const float *g, const uint8_t *head_mask,
                              const Shape &s, float *out, cudaStream_t st) {
     long long n4 = s.B * s.Tq * s.Hq * (long long)s.D / 4;
