@@ -661,11 +661,11 @@ def decode_section(dev, esa, E, name: str, args, world: int, e2e: bool) -> dict:
     # inputs in (q, qI, lin, and its K/V/kI rows, written into the caches at
     # position L-1) and the output back. The inputs travel as ONE copy from a
     # pinned staging buffer into a device staging buffer whose typed views
-    # are the step's q, qI and lin; three device copies place the new cache
-    # rows. Each input set's whole step (copy in, row placement, the library
-    # calls, copy out) is captured once into a CUDA graph and replayed per
-    # step. A decode step's inputs depend on the previous step's output, so
-    # the steps are serialised on one stream.
+    # are the step's q, qI and lin; esa_cache_append (one launch) places the
+    # new cache rows. Each input set's whole step (copy in, cache append, the
+    # library calls, copy out) is captured once into a CUDA graph and
+    # replayed per step. A decode step's inputs depend on the previous step's
+    # output, so the steps are serialised on one stream.
     parts = [host["q"], host["qI"], host["lin"], host["k"][:, L - 1:L], host["v"][:, L - 1:L], host["kI"][:, L - 1:L]]
     parts = [t.contiguous() for t in parts]
     nbytes = [t.numel() * t.element_size() for t in parts]
@@ -686,9 +686,7 @@ def decode_section(dev, esa, E, name: str, args, world: int, e2e: bool) -> dict:
 
         def e2e_step():
             d_in.copy_(h_in, non_blocking=True)
-            d["k"][:, L - 1:L].copy_(v[3])
-            d["v"][:, L - 1:L].copy_(v[4])
-            d["kI"][:, L - 1:L].copy_(v[5])
+            esa.esa_cache_append(v[3], v[4], v[5], d["k"], d["v"], d["kI"], shape)
             step(dd)
             h_out.copy_(d["out"], non_blocking=True)
         return e2e_step

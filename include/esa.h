@@ -346,6 +346,20 @@ ESA_API esa_status esa_topk_select_noalloc(const int8_t *qI, const int8_t *kI, c
  * ESA_ERR_CUDA when the synchronisation or the copy failed. */
 ESA_API esa_status esa_read_status(void *ws, void *stream, int32_t *dev_status);
 
+/* Write a step's new key rows into the caches: for b < B and t < Tq,
+ *   k[b, q_offset + t, :, :] = k_new[b, t, :, :]   (k_new, v_new bf16 [B, Tq, Hkv, D])
+ *   v[b, q_offset + t, :, :] = v_new[b, t, :, :]
+ *   kI[b, q_offset + t, :]   = kI_new[b, t, :]     (kI_new int8 [B, Tq, D_I])
+ * with the caches in the layouts above: a decode step appends Tq = 1
+ * position at q_offset = Tk - 1 before its selection reads the cache (the
+ * key cache is the "history_keys" the Gated DSA pseudo-code indexes,
+ * section 四.1). One launch writes all three; a cache whose pointer and new
+ * rows are both NULL is skipped (one without the other is an error). All
+ * pointers 16-byte aligned; new rows must not overlap the caches. Device
+ * memory owned by the caller; no workspace. */
+ESA_API esa_status esa_cache_append(const uint16_t *k_new, const uint16_t *v_new, const int8_t *kI_new, uint16_t *k,
+                                    uint16_t *v, int8_t *kI, const esa_shape *s, void *stream);
+
 /* A static, human-readable name for a status code. */
 ESA_API const char *esa_status_string(esa_status st);
 

@@ -62,6 +62,7 @@ _SIGS = {
     "esa_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "esa_status_string": (ctypes.c_char_p, [_i32]),
     "esa_binary_version": (ctypes.c_int, []),
+    "esa_cache_append": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _sp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -180,6 +181,12 @@ def esa_gated_sparse_attn(q, k, v, qI, kI, wI, shape: esa_shape, top_k: int, sca
 def esa_gated_mix(attn, lin, g, head_mask, shape: esa_shape, out, stream=None):
     _check(_lib.esa_gated_mix(_p(attn), _p(_bits(lin)), _p(g), _p(head_mask), ctypes.byref(shape), _p(out),
                               _stream(stream, attn)), "esa_gated_mix")
+
+
+def esa_cache_append(k_new, v_new, kI_new, k, v, kI, shape: esa_shape, stream=None):
+    ref = next(t for t in (k, v, kI) if t is not None)
+    _check(_lib.esa_cache_append(_p(_bits(k_new)), _p(_bits(v_new)), _p(kI_new), _p(_bits(k)), _p(_bits(v)), _p(kI),
+                                 ctypes.byref(shape), _stream(stream, ref)), "esa_cache_append")
 
 
 def esa_routed_attn(q, k, v, qI, kI, wI, route, shape: esa_shape, top_k: int, scale: float, g, lin, out,

@@ -421,6 +421,24 @@ esa_status esa_read_status(void *ws, void *stream, int32_t *dev_status) {
 
 int esa_binary_version(void) { return mix_binary_version(); }
 
+esa_status esa_cache_append(const uint16_t *k_new, const uint16_t *v_new, const int8_t *kI_new, uint16_t *k,
+                            uint16_t *v, int8_t *kI, const esa_shape *s, void *stream) {
+    if ((k_new == nullptr) != (k == nullptr) || (v_new == nullptr) != (v == nullptr) ||
+        (kI_new == nullptr) != (kI == nullptr))
+        return ESA_ERR_INVALID;
+    const bool kv = k || v;
+    if (!kv && !kI) return ESA_ERR_INVALID;
+    esa_status e = check_shape(s, kv, kI != nullptr);
+    if (e) return e;
+    for (const void *p : {(const void *)k_new, (const void *)v_new, (const void *)kI_new, (const void *)k,
+                          (const void *)v, (const void *)kI})
+        if (p && !aligned16(p)) return ESA_ERR_INVALID;
+    const Shape x = to_shape(s);
+    if (x.B * x.Tq == 0) return ESA_OK;
+    return launch_cache_append(k_new, v_new, kI_new, k, v, kI, x, (cudaStream_t)stream) == cudaSuccess ? ESA_OK
+                                                                                                        : ESA_ERR_CUDA;
+}
+
 const char *esa_status_string(esa_status st) {
     switch (st) {
         case ESA_OK: return "ok";

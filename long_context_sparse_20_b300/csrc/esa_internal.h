@@ -56,6 +56,10 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // binaryVersion of the library's kernels on the current device (-1: not loadable)
 int mix_binary_version();
 
+// ---- cache append (k, v, kI rows of new positions; null pairs skipped) ---
+cudaError_t launch_cache_append(const uint16_t *k_new, const uint16_t *v_new, const int8_t *kI_new, uint16_t *k,
+                                uint16_t *v, int8_t *kI, const Shape &s, cudaStream_t st);
+
 // ---- gate mix -----------------------------------------------------------
 cudaError_t launch_gated_mix(const float *attn, const uint16_t *lin, const float *g, const uint8_t *head_mask,
                              const Shape &s, float *out, cudaStream_t st);

@@ -34,6 +34,34 @@ __global__ void __launch_bounds__(256) gated_mix_kernel(const float4 *__restrict
     }
 }
 
+// The step's new K, V and indexer-key rows into the caches: one block per
+// (sequence, new position), 16-byte copies.
+__global__ void __launch_bounds__(128) cache_append_kernel(const uint4 *__restrict__ kn, const uint4 *__restrict__ vn,
+                                                           const uint4 *__restrict__ kin, uint4 *k, uint4 *v,
+                                                           uint4 *ki, long long Tq, long long Tk, long long q_offset,
+                                                           int kv16, int ki16) {
+    const long long r = blockIdx.x, b = r / Tq, t = r % Tq;
+    const long long dst = b * Tk + q_offset + t;
+    for (int i = threadIdx.x; i < kv16; i += blockDim.x) {
+        if (kn) k[dst * kv16 + i] = kn[r * kv16 + i];
+        if (vn) v[dst * kv16 + i] = vn[r * kv16 + i];
+    }
+    if (kin)
+        for (int i = threadIdx.x; i < ki16; i += blockDim.x) ki[dst * ki16 + i] = kin[r * ki16 + i];
+}
+
+cudaError_t launch_cache_append(const uint16_t *k_new, const uint16_t *v_new, const int8_t *kI_new, uint16_t *k,
+                                uint16_t *v, int8_t *kI, const Shape &s, cudaStream_t st) {
+    const long long rows = s.B * s.Tq;
+    if (rows == 0) return cudaSuccess;
+    const int kv16 = (k || v) ? s.Hkv * s.D * 2 / 16 : 0, ki16 = kI ? s.D_I / 16 : 0;
+    cache_append_kernel<<<(unsigned)rows, 128, 0, st>>>(
+        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
+        reinterpret_cast<const uint4 *>(kI_new), reinterpret_cast<uint4 *>(k), reinterpret_cast<uint4 *>(v),
+        reinterpret_cast<uint4 *>(kI), s.Tq, s.Tk, s.q_offset, kv16, ki16);
+    return cudaGetLastError();
+}
+
 int mix_binary_version() {
     cudaFuncAttributes fa{};
     if (cudaFuncGetAttributes(&fa, gated_mix_kernel) != cudaSuccess) {

@@ -58,6 +58,25 @@ def _shape(esa, **kw):
     return esa.shape_from(d)
 
 
+def test_cache_append_validation():
+    import long_context_sparse_20_b300 as esa
+    L = esa._lib
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    s = _shape(esa, Tq=1, Tk=8, q_offset=7)
+    # a cache without its new rows, and nothing to write
+    assert L.esa_cache_append(None, fake, fake, fake, fake, fake, ctypes.byref(s), None) == esa.ERR_INVALID
+    assert L.esa_cache_append(None, None, None, None, None, None, ctypes.byref(s), None) == esa.ERR_INVALID
+    # misaligned pointer
+    odd = ctypes.c_void_p(0x1008)
+    assert L.esa_cache_append(fake, fake, fake, fake, fake, odd, ctypes.byref(s), None) == esa.ERR_INVALID
+    # positions past the cache
+    bad = _shape(esa, Tq=2, Tk=8, q_offset=7)
+    assert L.esa_cache_append(fake, fake, fake, fake, fake, fake, ctypes.byref(bad), None) == esa.ERR_INVALID
+    # nothing to do: B * Tq = 0 launches nothing
+    empty = _shape(esa, B=0, Tq=1, Tk=8, q_offset=7)
+    assert L.esa_cache_append(fake, fake, fake, fake, fake, fake, ctypes.byref(empty), None) == esa.OK
+
+
 def test_host_validation_rejects_before_launch():
     import long_context_sparse_20_b300 as esa
     L = esa._lib

@@ -731,3 +731,34 @@ def test_decode_attention_repeated_calls():
         st, out, _ = gpu_attn(d, sh, K, oi, oc, ws=ws, want_lse=False)
         assert st == 0
         assert_close(out, ref)
+
+
+# ------------------------------------------------------------------ cache append
+@pytest.mark.parametrize("Tq", [1, 5])
+def test_cache_append_writes_exactly_the_new_rows(Tq):
+    """The new positions' rows land at q_offset..q_offset+Tq-1 of each
+    sequence, bit for bit; every other cache byte is unchanged; a skipped
+    cache (both pointers NULL) is untouched."""
+    m = esa()
+    B, Tk, Hkv, D, DI = 3, 40, 2, 128, 64
+    q_offset = Tk - Tq
+    sh = dict(B=B, Tq=Tq, Tk=Tk, q_offset=q_offset, Hq=4, Hkv=Hkv, D=D, H_I=1, D_I=DI)
+    g = torch.Generator().manual_seed(5)
+    k = torch.randn(B, Tk, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Tk, Hkv, D, generator=g).to(torch.bfloat16)
+    kI = torch.randint(-128, 128, (B, Tk, DI), generator=g, dtype=torch.int8)
+    kn = torch.randn(B, Tq, Hkv, D, generator=g).to(torch.bfloat16)
+    vn = torch.randn(B, Tq, Hkv, D, generator=g).to(torch.bfloat16)
+    kIn = torch.randint(-128, 128, (B, Tq, DI), generator=g, dtype=torch.int8)
+    dk, dv, dkI = k.cuda(), v.cuda(), kI.cuda()
+    m.esa_cache_append(kn.cuda(), vn.cuda(), kIn.cuda(), dk, dv, dkI, m.shape_from(sh))
+    ek, ev, ekI = k.clone(), v.clone(), kI.clone()
+    ek[:, q_offset:] = kn
+    ev[:, q_offset:] = vn
+    ekI[:, q_offset:] = kIn
+    assert torch.equal(dk.cpu().view(torch.int16), ek.view(torch.int16))
+    assert torch.equal(dv.cpu().view(torch.int16), ev.view(torch.int16))
+    assert torch.equal(dkI.cpu(), ekI)
+    dk2 = k.cuda()
+    m.esa_cache_append(None, None, kIn.cuda(), None, None, dkI, m.shape_from(sh))
+    assert torch.equal(dk2.cpu().view(torch.int16), k.view(torch.int16))
