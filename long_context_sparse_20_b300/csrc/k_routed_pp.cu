@@ -482,58 +482,133 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t id_s = idesc(kBN, 1u, 0u), id_i = idesc(kBN, 0u, 0u),
                                id_o = idesc(D, F16P ? 0u : 1u, 1u);
             constexpr int nparts = F16P ? 1 : 2;
-            for (int t = 0; t < nt && ok; t++) {
-                const int slot = t % kSlots;
-                const uint32_t sl = sbase + L::RING + slot * L::SLOT;
-                ok = wait_or_abort(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status) &&
-                     (!use_si || wait_or_abort(bar(bars.kh_ready[t % 2]), (uint32_t)(t / 2) & 1u, a.wait_ns, &abort_flag,
-                                         a.status));
-                if (!ok) break;
-                for (int x = 0; x < 2 && ok; x++) {
-                    if (t >= ntx[x]) continue;
-                    if (t > 0)
-                        ok = wait_or_abort(bar(bars.s_free[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag, a.status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t colS = x * kColsPerTile;
+            // S of key tile u for query tile x (its K in ring slot u % kSlots)
+            auto issue_s = [&](int x, int u) {
+                const uint32_t su = sbase + L::RING + (u % kSlots) * L::SLOT;
+                tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; kk++)
-                        mma_ss(tmem + colS,
-                               sdesc(sbase + L::Q + x * L::QT + (kk / 4) * (kRowsT * 128) + (kk % 4) * 32, 16, 1024, 2),
-                               sdesc(sl + L::SK + (kk / 4) * (kBN * 128) + (kk % 4) * 32, 16, 1024, 2), id_s, kk > 0);
-                    if (use_si) {
-                        // SI overwrites the columns that held P of tile t-1
+                for (int kk = 0; kk < D / 16; kk++)
+                    mma_ss(tmem + x * kColsPerTile,
+                           sdesc(sbase + L::Q + x * L::QT + (kk / 4) * (kRowsT * 128) + (kk % 4) * 32, 16, 1024, 2),
+                           sdesc(su + L::SK + (kk / 4) * (kBN * 128) + (kk % 4) * 32, 16, 1024, 2), id_s, kk > 0);
+            };
+            auto done = [&](unsigned long long &x, uint32_t parity) { return mbar_try_wait(bar(x), parity); };
+            // Full heads, event-driven issue: per query tile x, ns[x] is the
+            // next key tile whose scores go out, np[x] the next whose P V does.
+            // S(u) needs K(u) and the softmax to hold S(u-1) in registers (S's
+            // columns are free), so it is computed while that softmax works on
+            // tile u-1; P V(u) needs the softmax's P(u). Whichever query tile
+            // is ready goes first. Ring slot t is released once both tiles'
+            // P V(t) are issued. (Sparse heads keep a fixed order below: their
+            // indexer scores overwrite P's columns, and there the event-driven
+            // order measured slower.)
+            if (!use_si) {
+                int ns[2] = {0, 0}, np[2] = {0, 0}, fr = 0;
+                unsigned long long t_idle = 0;
+                bool idle = false;
+                while (ok && (np[0] < ntx[0] || np[1] < ntx[1])) {
+                    bool progress = false;
+                    for (int x = 0; x < 2; x++) {
+                        const int u = ns[x];
+                        if (u < ntx[x] && done(bars.full[u % kSlots], (uint32_t)(u / kSlots) & 1u) &&
+                            (u == 0 || done(bars.s_free[x], (uint32_t)(u - 1) & 1u))) {
+                            issue_s(x, u);
+                            mma_commit(bar(bars.s_ready[x]));
+                            ns[x] = u + 1;
+                            progress = true;
+                        }
+                        const int v = np[x];
+                        if (v < ns[x] && done(bars.p_ready[x], (uint32_t)v & 1u)) {
+                            tc_fence_after();
+                            const uint32_t colS = x * kColsPerTile;
+                            const uint32_t sl = sbase + L::RING + (v % kSlots) * L::SLOT;
+#pragma unroll
+                            for (int part = 0; part < nparts; part++)
+#pragma unroll
+                                for (int kk = 0; kk < kBN / 16; kk++)
+                                    mma_ts(tmem + colS + 128, tmem + colS + 64 + part * 32 + kk * 8,
+                                           sdesc(sl + L::SV + kk * 2048, kBN * 128, 1024, 2), id_o,
+                                           (v > 0 || part > 0 || kk > 0));
+                            mma_commit(bar(bars.pv_done[x]));
+                            np[x] = v + 1;
+                            progress = true;
+                            while (fr < nt && (np[0] > fr || fr >= ntx[0]) && (np[1] > fr || fr >= ntx[1])) {
+                                mma_commit(bar(bars.slot_free[fr % kSlots]));
+                                fr++;
+                            }
+                        }
+                    }
+                    // a bounded wait for the next event: on time-out the call
+                    // aborts with the status set (every waiter then gives up)
+                    if (progress) {
+                        idle = false;
+                    } else {
+                        unsigned long long now;
+                        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+                        if (!idle) {
+                            idle = true;
+                            t_idle = now;
+                        } else if ((long long)(now - t_idle) > a.wait_ns || abort_flag) {
+                            set_status(a.status, ESA_ERR_TIMEOUT);
+                            abort_flag = 1;
+                            ok = false;
+                        }
+                    }
+                }
+            } else {
+                for (int t = 0; t < nt && ok; t++) {
+                    const int slot = t % kSlots;
+                    const uint32_t sl = sbase + L::RING + slot * L::SLOT;
+                    ok = wait_or_abort(bar(bars.full[slot]), (uint32_t)(t / kSlots) & 1u, a.wait_ns, &abort_flag, a.status) &&
+                         (!use_si || wait_or_abort(bar(bars.kh_ready[t % 2]), (uint32_t)(t / 2) & 1u, a.wait_ns, &abort_flag,
+                                             a.status));
+                    if (!ok) break;
+                    for (int x = 0; x < 2 && ok; x++) {
+                        if (t >= ntx[x]) continue;
                         if (t > 0)
-                            ok = wait_or_abort(bar(bars.pv_done[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag,
-                                         a.status);
+                            ok = wait_or_abort(bar(bars.s_free[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag, a.status);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t kh = sbase + L::KH + (t % 2) * L::KHB;
+                        const uint32_t colS = x * kColsPerTile;
 #pragma unroll
-                        for (int kk = 0; kk < DI / 16; kk++)
-                            mma_ss(tmem + colS + 64, sdesc(sbase + L::QE + x * L::QET + kk * 256, 128, DI / 8 * 128),
-                                   sdesc(kh + kk * 256, 128, DI / 8 * 128), id_i, kk > 0);
+                        for (int kk = 0; kk < D / 16; kk++)
+                            mma_ss(tmem + colS,
+                                   sdesc(sbase + L::Q + x * L::QT + (kk / 4) * (kRowsT * 128) + (kk % 4) * 32, 16, 1024, 2),
+                                   sdesc(sl + L::SK + (kk / 4) * (kBN * 128) + (kk % 4) * 32, 16, 1024, 2), id_s, kk > 0);
+                        if (use_si) {
+                            // SI overwrites the columns that held P of tile t-1
+                            if (t > 0)
+                                ok = wait_or_abort(bar(bars.pv_done[x]), (uint32_t)(t - 1) & 1u, a.wait_ns, &abort_flag,
+                                             a.status);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint32_t kh = sbase + L::KH + (t % 2) * L::KHB;
+#pragma unroll
+                            for (int kk = 0; kk < DI / 16; kk++)
+                                mma_ss(tmem + colS + 64, sdesc(sbase + L::QE + x * L::QET + kk * 256, 128, DI / 8 * 128),
+                                       sdesc(kh + kk * 256, 128, DI / 8 * 128), id_i, kk > 0);
+                        }
+                        mma_commit(bar(bars.s_ready[x]));
                     }
-                    mma_commit(bar(bars.s_ready[x]));
-                }
-                if (!ok) break;
-                if (use_si) mma_commit(bar(bars.kh_free[t % 2]));
-                for (int x = 0; x < 2 && ok; x++) {
-                    if (t >= ntx[x]) continue;
-                    ok = wait_or_abort(bar(bars.p_ready[x]), (uint32_t)t & 1u, a.wait_ns, &abort_flag, a.status);
                     if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t colS = x * kColsPerTile;
+                    if (use_si) mma_commit(bar(bars.kh_free[t % 2]));
+                    for (int x = 0; x < 2 && ok; x++) {
+                        if (t >= ntx[x]) continue;
+                        ok = wait_or_abort(bar(bars.p_ready[x]), (uint32_t)t & 1u, a.wait_ns, &abort_flag, a.status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t colS = x * kColsPerTile;
 #pragma unroll
-                    for (int part = 0; part < nparts; part++)
+                        for (int part = 0; part < nparts; part++)
 #pragma unroll
-                        for (int kk = 0; kk < kBN / 16; kk++)
-                            mma_ts(tmem + colS + 128, tmem + colS + 64 + part * 32 + kk * 8,
-                                   sdesc(sl + L::SV + kk * 2048, kBN * 128, 1024, 2), id_o,
-                                   (t > 0 || part > 0 || kk > 0));
-                    mma_commit(bar(bars.pv_done[x]));
+                            for (int kk = 0; kk < kBN / 16; kk++)
+                                mma_ts(tmem + colS + 128, tmem + colS + 64 + part * 32 + kk * 8,
+                                       sdesc(sl + L::SV + kk * 2048, kBN * 128, 1024, 2), id_o,
+                                       (t > 0 || part > 0 || kk > 0));
+                        mma_commit(bar(bars.pv_done[x]));
+                    }
+                    if (ok) mma_commit(bar(bars.slot_free[slot]));
                 }
-                if (ok) mma_commit(bar(bars.slot_free[slot]));
             }
             // every MMA issued has completed before the CTA frees tensor memory
             mma_commit(bar(bars.mma_end));
