@@ -24,10 +24,17 @@ namespace esa {
 // workspace: [row selection: status word, tensor-core scratch][thr][routed_pp: flag, fp16 values].
 // With per-head index sets the selection runs on the per-head rows (one
 // (T, P) per row and indexer head, [B, Tq, H_I, 2]).
+// The selection's bitmask of every row's selected keys (the warp-specialised
+// kernel masks sparse heads with it instead of recomputing indexer scores).
+size_t routed_mask_bytes(const Shape &s) {
+    const Shape r = selection_rows(s);
+    return align256((size_t)(r.B * r.Tq) * (size_t)sel_mask_words(r) * 4);
+}
+
 size_t ws_routed(const Shape &s, int K) {
     const Shape r = selection_rows(s);
     return align256(ws_row_select(r, K)) + align256((size_t)r.B * r.Tq * 2 * 4) +
-           (routed_pp_supported(s) ? ws_routed_pp(s) : 0);
+           (routed_pp_supported(s) ? align256(ws_routed_pp(s)) + routed_mask_bytes(s) : 0);
 }
 
 esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
@@ -40,13 +47,15 @@ esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16
     int32_t *thr = reinterpret_cast<int32_t *>(base + sel_bytes);
     const int32_t *w = per_head_of(s) ? unit_weight() : wI;
     if (!w) return ESA_ERR_CUDA;
-    esa_status e = launch_row_select(qI, kI, w, r, K, nullptr, nullptr, thr, ws, sel_bytes, st);
+    const bool pp = routed_pp_supported(s);
+    char *pp_ws = base + sel_bytes + align256((size_t)r.B * r.Tq * 2 * 4);
+    uint32_t *mask = pp ? reinterpret_cast<uint32_t *>(pp_ws + align256(ws_routed_pp(s))) : nullptr;
+    esa_status e = launch_row_select(qI, kI, w, r, K, nullptr, nullptr, thr, ws, sel_bytes, st, mask);
     if (e != ESA_OK) return e;
     int32_t *status = reinterpret_cast<int32_t *>(ws);
-    if (routed_pp_supported(s)) {
-        void *pp_ws = base + sel_bytes + align256((size_t)r.B * r.Tq * 2 * 4);
-        return launch_routed_pp(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, pp_ws, status, st);
-    }
+    if (pp)
+        return launch_routed_pp(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, pp_ws, status, st,
+                                reinterpret_cast<const uint64_t *>(mask));
     if (per_head_of(s)) return ESA_ERR_UNSUPPORTED;  // the fallback kernel masks with one set per row
     return launch_routed_tc(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, status, st);
 }

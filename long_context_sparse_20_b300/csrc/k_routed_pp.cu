@@ -75,6 +75,11 @@ struct PpArgs {
     int Hq, Hkv, H_I;
     int relu;  // ReLU on each indexer head's dot product
     int pset;  // one index set per indexer head: query head h masks with set h / (Hq / H_I), weight 1
+    // the selection's bitmask of every row's selected keys ([rows][mask_w64]
+    // 64-bit words, bit c of word t = key 64 t + c), or null: then sparse
+    // heads rebuild the mask from indexer scores on the tensor cores
+    const uint64_t *mask;
+    long long mask_w64;
     float scale_log2;
 };
 
@@ -162,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // non-negative weight (max(0, w d) = w max(0, d)); several heads do
         // not collapse, so their mask scores come from dp4a
         exact_all = (a.relu && !(nih == 1 && (a.pset || a.wI[0] >= 0))) ? 0 : 1;
+        if (a.mask) exact_all = 0;  // the mask replaces the indexer scores
         abort_flag = 0;
     }
     tc_fence_before();
@@ -186,6 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 Pp = a.thr[2 * ((row0 + r) * nsets + iset) + 1];
             }
             Tf = (float)Tint;
+        }
+        if (sparse && !a.mask) {
             // collapsed indexer query q_eff = sum_h w_h qI_h (fp16, exact while
             // |q_eff| <= 2048 and every partial sum of q_eff . kI stays below 2^24)
             long long absum = 0;
@@ -224,6 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
+        // with the selection's bitmask: this row's word of the next key tile,
+        // loaded one tile ahead (whole-prefix rows, T = INT32_MIN, keep every key)
+        const bool use_mask = sparse && a.mask != nullptr && r < rows && Tint != INT32_MIN;
+        const uint64_t *mrow = use_mask ? a.mask + ((row0 + r) * nsets + iset) * a.mask_w64 : nullptr;
+        uint64_t mnext = use_mask && ntt > 0 ? __ldg(mrow) : ~0ull;
         for (int t = 0; t < ntt && ok; t++) {
             if (!wait_or_abort(bar(bars.s_ready[x]), (uint32_t)t & 1u, a.wait_ns, &abort_flag, a.status)) {
                 ok = false;
@@ -261,6 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+            } else if (sparse && a.mask) {
+                keep = mnext;
+                mnext = use_mask && t + 1 < ntt ? __ldg(mrow + t + 1) : ~0ull;
             } else if (sparse) {
                 // exact integer mask scores with dp4a from the raw keys of the slot
                 const int slot = t % kSlots;
@@ -408,13 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sl = sbase + L::RING + slot * L::SLOT;
                 const uint32_t fb = bar(bars.full[slot]);
                 const int krow = (int)(b * a.Tk + (long long)t * kBN);
-                mbar_expect_tx(fb, (unsigned)(2 * kBN * D * 2 + (sparse ? kBN * DI : 0)));
+                const bool raw_ki = sparse && !a.mask;  // the indexer keys, unless the mask replaces them
+                mbar_expect_tx(fb, (unsigned)(2 * kBN * D * 2 + (raw_ki ? kBN * DI : 0)));
 #pragma unroll
                 for (int p = 0; p < NP; p++) {
                     tma3(sl + L::SK + p * (kBN * 128), mk, p * 64, kvh, krow, fb);
                     tma3(sl + L::SV + p * (kBN * 128), mv, p * 64, kvh, krow, fb);
                 }
-                if (sparse) tma2(sl + L::SKI, mki, 0, krow, fb);
+                if (raw_ki) tma2(sl + L::SKI, mki, 0, krow, fb);
             }
             issued = t;
             return true;
@@ -681,8 +698,10 @@ bool routed_pp_supported(const Shape &s) {
 esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
                             const int8_t *kI, const int32_t *wI, const uint8_t *route, const int32_t *thr,
                             const Shape &s, float scale, const float *g, const uint16_t *lin, float *out,
-                            void *pp_ws, int32_t *status, cudaStream_t st) {
+                            void *pp_ws, int32_t *status, cudaStream_t st, const uint64_t *mask) {
     PpArgs a{};
+    a.mask = mask;
+    a.mask_w64 = sel_mask_words(s) / 2;
     a.lin = lin;
     a.qI = qI;
     a.wI = wI;

@@ -113,6 +113,8 @@ struct TcSelArgs {
     const uint16_t *kh;
     const int32_t *wI;
     int32_t *idx, *cnt, *thr, *flags, *status;
+    uint32_t *mask;  // optional: selected keys as bits, [rows][mask_w]
+    long long mask_w;
     long long B, Tq, Tk, Tkp, q_offset, wait_ns;
     int H_I, K;
     int pos_div;  // rows per query position (one per indexer head with per-head sets)
@@ -541,6 +543,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                             last = __ffs(lb) - 1;
                         }
                         if (my_take > 0 && my_tb + my_take == need) st.P[r] = j0 + last;
+                        if (a.mask && r < nrows) a.mask[(row0 + r) * a.mask_w + (j0 >> 5)] = sel;
                         if (orow) {
                             while (sel) {
                                 const int bit = __ffs(sel) - 1;
@@ -808,12 +811,13 @@ size_t ws_row_select(const Shape &s, int K) {
 }
 
 esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
-                             int32_t *idx, int32_t *cnt, int32_t *thr, void *ws, size_t ws_bytes, cudaStream_t st) {
+                             int32_t *idx, int32_t *cnt, int32_t *thr, void *ws, size_t ws_bytes, cudaStream_t st,
+                             uint32_t *mask) {
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     if (s.B * s.Tq == 0) return ESA_OK;
     TcPlan p = plan_tc(s, K);
     if (!p.ok || ws_bytes < p.bytes)
-        return launch_rows_dp4a(qI, kI, wI, s, K, idx, cnt, thr, nullptr, status, st);
+        return launch_rows_dp4a(qI, kI, wI, s, K, idx, cnt, thr, nullptr, status, st, mask);
     char *base = static_cast<char *>(ws);
     uint16_t *kh = reinterpret_cast<uint16_t *>(base + p.kh_off);
     int32_t *flags = reinterpret_cast<int32_t *>(base + p.flag_off);
@@ -834,6 +838,8 @@ esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *
     a.idx = idx;
     a.cnt = cnt;
     a.thr = thr;
+    a.mask = mask;
+    a.mask_w = sel_mask_words(s);
     a.flags = flags;
     a.status = status;
     a.B = s.B;
@@ -850,7 +856,7 @@ esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *
     if (cudaLaunchKernel(fn, dim3((unsigned)(s.B * p.ntile)), dim3(kThreadsTc), args, smem, st) != cudaSuccess)
         return ESA_ERR_CUDA;
     // query tiles whose collapsed indexer query is not exact in fp16
-    return launch_rows_dp4a(qI, kI, wI, s, K, idx, cnt, thr, flags, status, st);
+    return launch_rows_dp4a(qI, kI, wI, s, K, idx, cnt, thr, flags, status, st, mask);
 }
 
 }  // namespace esa
