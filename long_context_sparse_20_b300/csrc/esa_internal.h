@@ -121,9 +121,10 @@ esa_status launch_decode_step(const uint16_t *q, const uint16_t *k, const uint16
 // least kStatusBytes runs the dp4a kernel alone.
 size_t ws_row_select(const Shape &s, int K);
 // With mask != nullptr the final pass also writes each row's selected keys
-// as a bitmask: uint32 [rows][sel_mask_words(s)], bit j of word w = key
-// 32 w + j selected (keys past the row's prefix: 0). Rows hold whole
-// 128-key tiles: both selection kernels write a tile's words at once.
+// as a bitmask, word-major: uint32 [sel_mask_words(s)][rows], bit j of
+// word w of a row = key 32 w + j selected (keys past the row's prefix: 0;
+// words past its last key tile: not written). Rows hold whole 128-key
+// tiles: both selection kernels write a tile's words at once.
 inline long long sel_mask_words(const Shape &s) { return 4 * ((s.Tk + 127) / 128); }
 esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *wI, const Shape &s, int K,
                              int32_t *idx, int32_t *cnt, int32_t *thr, void *ws, size_t ws_bytes, cudaStream_t st,
@@ -179,17 +180,15 @@ esa_status launch_routed_tc(const uint16_t *q, const uint16_t *k, const uint16_t
 
 // Warp-specialised variant (two query tiles per CTA; TMA producer warp, MMA
 // warp, two softmax warpgroups); routed_pp_supported() tells whether its
-// buffers fit for this shape.
+// buffers fit for this shape. Sparse heads mask with `mask`, the
+// selection's bitmask of every row's selected keys (launch_row_select's
+// mask output, word-major: [sel_mask_words][selection rows]).
 // Its workspace (ws_routed_pp bytes): a flag word area and an fp16 copy of V.
 bool routed_pp_supported(const Shape &s);
 size_t ws_routed_pp(const Shape &s);
-// mask: the selection's bitmask of selected keys (sel_mask_words(s) / 2
-// 64-bit words per selection row), or null (sparse heads then compute
-// indexer scores on the tensor cores and mask against thr).
-esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
-                            const int8_t *kI, const int32_t *wI, const uint8_t *route, const int32_t *thr,
-                            const Shape &s, float scale, const float *g, const uint16_t *lin, float *out,
-                            void *pp_ws, int32_t *status, cudaStream_t st, const uint64_t *mask = nullptr);
+esa_status launch_routed_pp(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint8_t *route,
+                            const int32_t *thr, const uint32_t *mask, const Shape &s, float scale, const float *g,
+                            const uint16_t *lin, float *out, void *pp_ws, int32_t *status, cudaStream_t st);
 
 // ---- attention router (full or sparse per head) --------------------------
 size_t ws_route_heads(const Shape &s);

@@ -53,9 +53,7 @@ esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16
     esa_status e = launch_row_select(qI, kI, w, r, K, nullptr, nullptr, thr, ws, sel_bytes, st, mask);
     if (e != ESA_OK) return e;
     int32_t *status = reinterpret_cast<int32_t *>(ws);
-    if (pp)
-        return launch_routed_pp(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, pp_ws, status, st,
-                                reinterpret_cast<const uint64_t *>(mask));
+    if (pp) return launch_routed_pp(q, k, v, route, thr, mask, s, scale, g, lin, out, pp_ws, status, st);
     if (per_head_of(s)) return ESA_ERR_UNSUPPORTED;  // the fallback kernel masks with one set per row
     return launch_routed_tc(q, k, v, qI, kI, wI, route, thr, s, scale, g, lin, out, status, st);
 }

@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
                                                               long long q_offset, int H_I, int K, int pos_div,
                                                               int relu, const int32_t *__restrict__ only_flagged,
                                                               int32_t *__restrict__ status, uint32_t *__restrict__ mask,
-                                                              long long mask_w) {
+                                                              long long mask_rows) {
     constexpr int W = DI / 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     RowState &rs = *reinterpret_cast<RowState *>(smem_raw);
@@ -382,8 +382,9 @@ __global__ void __launch_bounds__(kThreads) row_select_kernel(const int8_t *__re
                 }
                 const long long tkey = (long long)ti * kTK + w * 16;
                 if (take_bits_hi != 0xffffffffu) rs.P[r] = (int)(tkey + take_bits_hi);
-                if (mask && r < nrows)  // the row's bitmask, 16 keys at a time
-                    reinterpret_cast<uint16_t *>(mask)[(row0 + r) * 2 * mask_w + (tkey >> 4)] = (uint16_t)sel;
+                if (mask && r < nrows)  // the row's bitmask (word-major), 16 keys at a time
+                    reinterpret_cast<uint16_t *>(mask)[((tkey >> 5) * mask_rows + row0 + r) * 2 + ((tkey >> 4) & 1)] =
+                        (uint16_t)sel;
                 if (write_idx && r < nrows) {
                     int32_t *orow = idx + (row0 + r) * (long long)K;
                     unsigned sb = sel;
@@ -454,11 +455,11 @@ esa_status launch_rows_dp4a(const int8_t *qI, const int8_t *kI, const int32_t *w
     if (!ensure_smem(fn, smem)) return ESA_ERR_CUDA;
     long long B = s.B, Tq = s.Tq, Tk = s.Tk, qo = s.q_offset;
     int H_I = s.H_I, pos_div = s.pos_div, relu = relu_of(s) ? 1 : 0;
-    long long mask_w = sel_mask_words(s);
+    long long mask_rows = s.B * s.Tq;
     void *args[] = {(void *)&qI,  (void *)&kI,      (void *)&wI,   (void *)&idx, (void *)&cnt,
                     (void *)&thr, (void *)&B,       (void *)&Tq,   (void *)&Tk,  (void *)&qo,
                     (void *)&H_I, (void *)&K,       (void *)&pos_div, (void *)&relu,
-                    (void *)&only_flagged, (void *)&status, (void *)&mask, (void *)&mask_w};
+                    (void *)&only_flagged, (void *)&status, (void *)&mask, (void *)&mask_rows};
     cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)tiles), dim3(kThreads), args, smem, st);
     return e == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }

@@ -113,8 +113,8 @@ struct TcSelArgs {
     const uint16_t *kh;
     const int32_t *wI;
     int32_t *idx, *cnt, *thr, *flags, *status;
-    uint32_t *mask;  // optional: selected keys as bits, [rows][mask_w]
-    long long mask_w;
+    uint32_t *mask;  // optional: selected keys as bits, word-major [words][mask_rows]
+    long long mask_rows;
     long long B, Tq, Tk, Tkp, q_offset, wait_ns;
     int H_I, K;
     int pos_div;  // rows per query position (one per indexer head with per-head sets)
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) rows_tc_kernel(const __grid_con
                             last = __ffs(lb) - 1;
                         }
                         if (my_take > 0 && my_tb + my_take == need) st.P[r] = j0 + last;
-                        if (a.mask && r < nrows) a.mask[(row0 + r) * a.mask_w + (j0 >> 5)] = sel;
+                        if (a.mask && r < nrows) a.mask[(long long)(j0 >> 5) * a.mask_rows + row0 + r] = sel;
                         if (orow) {
                             while (sel) {
                                 const int bit = __ffs(sel) - 1;
@@ -839,7 +839,7 @@ esa_status launch_row_select(const int8_t *qI, const int8_t *kI, const int32_t *
     a.cnt = cnt;
     a.thr = thr;
     a.mask = mask;
-    a.mask_w = sel_mask_words(s);
+    a.mask_rows = s.B * s.Tq;
     a.flags = flags;
     a.status = status;
     a.B = s.B;
