@@ -237,7 +237,10 @@ ESA_API esa_status esa_gated_mix(const float *attn, const uint16_t *lin, const f
  * heads; with ESA_PER_HEAD_SETS the set of indexer head h / (Hq/H_I)),
  * attention over it, then the gate mix with lin when g and lin are
  * given. Every head of the layer runs in one attention launch (on the
- * tensor cores, accumulators in tensor memory). scale is normally 1/sqrt(D). */
+ * tensor cores, accumulators in tensor memory); the selection before it
+ * leaves every row's selected keys as a bitmask in the workspace (about
+ * B*Tq*Tk/8 bytes, times H_I with per-head sets), which the sparse heads
+ * mask with. scale is normally 1/sqrt(D). */
 ESA_API esa_status esa_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
                            const int8_t *kI, const int32_t *wI, const uint8_t *route, const esa_shape *s, int top_k,
                            float scale, const float *g, const uint16_t *lin, float *out, void *ws, size_t ws_bytes,

@@ -47,7 +47,9 @@
 //          256 integers);
 //   final  selected = s > T, or s == T among the first K - #{s > T} ties in
 //          position order, written in ascending order; also the threshold
-//          form (T, P), P the position of the last tie taken.
+//          form (T, P), P the position of the last tie taken, and on request
+//          the selected keys as a bitmask (one word per 32 keys and row,
+//          word-major), which the routed kernel masks sparse heads with.
 #include <stdlib.h>
 #include <string.h>
 
