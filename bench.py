@@ -614,10 +614,15 @@ def decode_section(dev, esa, E, name: str, args, world: int, e2e: bool) -> dict:
     clocks = clk.summary()
     replays = max_over_ranks(replays, world, dev)
     ms_step = statistics.median(replays) / args.steps
-    run_breakdown()
-    torch.cuda.synchronize()
-    sel_avg = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    att_avg = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    # per-kernel times: the event-bracketed graph replayed five times, each
+    # kernel's mean over the steps of a replay, the median over the replays
+    sel_r, att_r = [], []
+    for _ in range(5):
+        run_breakdown()
+        torch.cuda.synchronize()
+        sel_r.append(statistics.mean(e[0].elapsed_time(e[1]) for e in evs))
+        att_r.append(statistics.mean(e[1].elapsed_time(e[2]) for e in evs))
+    sel_avg, att_avg = statistics.median(sel_r), statistics.median(att_r)
     check_status()
 
     peak_gbs, _, peak_kind = _load_peaks()
@@ -648,6 +653,7 @@ def decode_section(dev, esa, E, name: str, args, world: int, e2e: bool) -> dict:
                      "peak_kind": peak_kind, "traffic": traffic, "algorithmic_bytes": dom_bytes,
                      "avg_launch_us": dom_ms * 1e3},
         "kernels_us": kernels,
+        "kernel_replays_us": {"first": [round(x * 1e3, 2) for x in sel_r], "second": [round(x * 1e3, 2) for x in att_r]},
         "step_roofline": {"achieved": (sel_bytes + att_bytes) / (ms_step / 1e3) / 1e9, "peak": peak_gbs,
                           "frac": (sel_bytes + att_bytes) / (ms_step / 1e3) / 1e9 / peak_gbs,
                           "algorithmic_bytes": sel_bytes + att_bytes},
