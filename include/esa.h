@@ -69,8 +69,8 @@
  *                        which needs Hq % H_I == 0 and, for attention, one of
  *                        Hq/H_I and Hq/Hkv to divide the other. The routed
  *                        call masks each sparse head with its own set (on its
- *                        warp-specialised kernel, D = 128 with D_I <= 64;
- *                        other shapes return ESA_ERR_UNSUPPORTED).
+ *                        warp-specialised kernel; shapes it does not fit
+ *                        return ESA_ERR_UNSUPPORTED).
  *
  * Tensor layouts:
  *   qI  int8  [B, Tq, H_I, D_I]     indexer queries

@@ -120,9 +120,7 @@ def test_host_validation_rejects_before_launch():
 def test_host_validation_of_indexer_flags():
     """Unknown flag bits are invalid; per-head sets need Hq % H_I == 0 and, for
     attention, heads per set and heads per key/value head dividing one
-    another; the routed call takes per-head sets only on its warp-specialised
-    kernel, which does not fit D = 128 with D_I = 128. All of it is decided
-    before any launch."""
+    another. All of it is decided before any launch."""
     import long_context_sparse_20_b300 as esa
     L = esa._lib
     fake = ctypes.c_void_p(0x1000)
@@ -133,9 +131,9 @@ def test_host_validation_of_indexer_flags():
         sh = _shape(esa, flags=esa.PER_HEAD_SETS, **kw)
         assert L.esa_sparse_attn(fake, fake, fake, fake, fake, ctypes.byref(sh), 4, 0.125, None, None, fake, None,
                                  fake, 1 << 20, None) == code, kw
-    sh = _shape(esa, flags=esa.PER_HEAD_SETS, Hq=4, Hkv=4, H_I=2, D=128, D_I=128)
+    sh = _shape(esa, flags=esa.PER_HEAD_SETS, Hq=6, Hkv=6, H_I=4)
     assert L.esa_routed_attn(fake, fake, fake, fake, fake, fake, fake, ctypes.byref(sh), 4, 0.125, None, None, fake,
-                             fake, 1 << 20, None) == esa.ERR_UNSUPPORTED
+                             fake, 1 << 20, None) == esa.ERR_INVALID  # 6 % 4
 
 
 def test_workspace_size_rejects_bad_shapes():

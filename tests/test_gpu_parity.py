@@ -479,6 +479,22 @@ def test_routed_per_head_sets(over, routes):
     assert_thr_equal(thr.reshape(-1, 2), O.threshold(inp["qI"], inp["kI"], inp["wI"], sh, K).reshape(-1, 2))
 
 
+@pytest.mark.parametrize("over", [ROUTED_CASES[1], ROUTED_CASES[2], ROUTED_PER_HEAD_CASES[2]],
+                         ids=["gqa-D64", "chunk-in-cache", "per-head-sets"])
+def test_routed_with_dp4a_selection(monkeypatch, over):
+    """The dp4a row selection (ESA_ROW_SELECT=dp4a; the path of query tiles
+    outside the exact fp16 range) writes the same bitmask of selected keys
+    that the routed kernel masks sparse heads with: exact outputs, with one
+    set per row and with per-head sets."""
+    monkeypatch.setenv("ESA_ROW_SELECT", "dp4a")
+    cfg, sh, inp = _case(seed=516, routed=True, **over)
+    inp["route"] = torch.ones_like(inp["route"])
+    inp["route"][..., 0] = 0  # one full head, the rest sparse
+    K = cfg["top_k"]
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, K)
+    assert_close(gpu_routed(to_dev(inp), sh, K), ref)
+
+
 def test_threshold_per_head_ties():
     """Per-head threshold forms on tie-heavy scores (small int8 range), with
     and without the ReLU."""
