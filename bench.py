@@ -350,21 +350,21 @@ def prefill_section(dev, esa, E, reps: int = 2, seq: int = 0,
             ms = ms_sel + ms_att
             flops = 4.0 * D * B * Hq * sel_pairs
             entry["kernels_ms"] = {"topk_select": ms_sel, "sparse_attn": ms_att}
-            if sh["flags"] & esa.PER_HEAD_SETS:
-                # the same outputs through the fused routed launch with every
-                # head sparse (per-head thresholds, dense masked tiles on tcgen05)
-                del idx, cnt, wsel, watt
-                torch.cuda.empty_cache()
-                route = torch.ones(B, Hq, dtype=torch.uint8, device=dev)
-                wsr = esa.workspace_for(esa.OP_ROUTED_ATTN, shape, K, dev)
-                ms_r = timed(lambda: esa.esa_routed_attn(d["q"], d["k"], d["v"], d["qI"], d["kI"], d["wI"], route,
-                                                         shape, K, scale, d["g"], d["lin"], out, wsr, st))
-                assert esa.esa_read_status(wsr, st) == 0
-                entry["kernels_ms"]["routed_attn_all_sparse"] = ms_r
-                if ms_r < ms:
-                    entry["path"] = "esa_routed_attn, every head sparse"
-                    ms = ms_r
-                del wsr, route
+            # the same outputs through the one-call API (no lse, no index
+            # outputs): prefill shapes whose prefixes hold few times the
+            # selected keys take the routed kernel with every head sparse
+            del idx, cnt, wsel, watt
+            torch.cuda.empty_cache()
+            wsg = esa.workspace_for(esa.OP_GATED_SPARSE_ATTN, shape, K, dev)
+            ms_g = timed(lambda: esa.esa_gated_sparse_attn(d["q"], d["k"], d["v"], d["qI"], d["kI"], d["wI"], shape, K,
+                                                           scale, d["g"], d["lin"], out, None, None, None, wsg, st))
+            assert esa.esa_read_status(wsg, st) == 0
+            entry["kernels_ms"]["gated_one_call"] = ms_g
+            entry["path"] = "esa_topk_select + esa_sparse_attn"
+            if ms_g < ms:
+                entry["path"] = "esa_gated_sparse_attn (one call)"
+                ms = ms_g
+            del wsg
         entry.update({"ms": ms, "tok_per_s": B * S / (ms / 1e3), "algorithmic_tflops": flops / (ms / 1e3) / 1e12,
                       "tensor_peak_tflops": tf_peak, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / tf_peak,
                       "peak_kind": kind})
@@ -763,6 +763,8 @@ def summarise(dec: dict, mdec: dict | None, prefill: dict | None, kda: dict | No
             p = prefill[name]
             e = {"ms": _r(p["ms"]), "tok_s": _r(p["tok_per_s"]), "bf16_frac": _r(p["frac_of_bf16_peak"], 3)}
             e.update({k: _r(v) for k, v in p["kernels_ms"].items()})
+            if "path" in p:
+                e["path"] = "one call" if p["path"].startswith("esa_gated") else "two calls"
             e["cpu_tok_s"] = _r((p.get("cpu_baseline") or {}).get("tok_per_s"))
             out[key] = e
             if "router" in p:

@@ -205,7 +205,13 @@ ESA_API esa_status esa_sparse_attn(const uint16_t *q, const uint16_t *k, const u
  * esa_topk_select's).
  * It runs the selection kernel and the gathered-attention kernel back to
  * back on `stream` (the attention launched early on the programmatic
- * edge). With the environment variable ESA_DECODE_PATH=fused, decode-like
+ * edge). Prefill-like shapes whose causal prefixes hold at most 12 times
+ * the selected keys (summed over the rows) and whose buffers fit the routed
+ * kernel, called without lse, run esa_routed_attn's path instead with every
+ * head sparse: the selection also writes its bitmask of selected keys and
+ * the attention masks dense tiles on the tensor cores (same index sets,
+ * outputs within the same tolerance). With the environment variable
+ * ESA_DECODE_PATH=fused, decode-like
  * shapes (few rows, long prefixes: B*Tq up to half the SMs, one index set
  * per row, D in {64, 128}, (Hq/Hkv rounded up to 16) * Hkv up to 128
  * query-head rows) take ONE cooperative launch instead: each block scores

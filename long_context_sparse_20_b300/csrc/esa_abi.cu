@@ -197,10 +197,28 @@ size_t gated_xoff(const Shape &x, int K) {
     const size_t sets = (size_t)(r.B * r.Tq);
     return gated_scratch_off(x, K) + align256(sets * K * 4) + align256(sets * 4);
 }
+// Prefill-like shapes (not the split selection's) whose dense masked
+// attention visits at most kRoutedPairRatio times the selected pairs run
+// the selection with its bitmask output and the routed kernel with every
+// head sparse: on the tensor cores that beats gathering the selected keys
+// (long prefill, S = 32768, K = 2048: 8.1x the pairs, 7.96 against 9.76 ms;
+// a 16K chunk over a 131072-key cache: 60x, 27.1 against 8.35 ms).
+constexpr double kRoutedPairRatio = 12.0;
+bool gated_routed_path(const Shape &x, int K) {
+    if (plan_split_select(selection_rows(x), K).ok || !routed_pp_supported(x)) return false;
+    // per sequence: sum over rows of (p + 1) and of min(K, p + 1), p = q_offset + t
+    const double Tq = (double)x.Tq, qo = (double)x.q_offset;
+    const double dense = Tq * qo + Tq * (Tq + 1) / 2;
+    const double ts = std::min(Tq, std::max(0.0, (double)K - qo));  // rows whose whole prefix is kept
+    const double sel = ts * qo + ts * (ts + 1) / 2 + (Tq - ts) * K;
+    return sel > 0 && dense <= kRoutedPairRatio * sel;
+}
+
 size_t gated_ws(const Shape &x, int K) {
     DecodePlan dp = decode_single_launch() ? plan_decode_step(x, K) : DecodePlan{};
     if (dp.ok) return dp.ws_bytes;
-    return gated_xoff(x, K) + align256(plan_sparse_attn(x, K).x_bytes);
+    const size_t two = gated_xoff(x, K) + align256(plan_sparse_attn(x, K).x_bytes);
+    return gated_routed_path(x, K) ? std::max(two, ws_routed(x, K)) : two;
 }
 
 }  // namespace
@@ -325,9 +343,14 @@ esa_status esa_gated_sparse_attn(const uint16_t *q, const uint16_t *k, const uin
         if ((e = check_ws(ws, ws_bytes, dp.ws_bytes))) return e;
         return launch_decode_step(q, k, v, qI, kI, wI, x, top_k, scale, g, lin, out, lse, idx, cnt, ws, dp, st);
     }
+    if ((e = check_ws(ws, ws_bytes, gated_ws(x, top_k)))) return e;
+    // prefill where dense masked tiles on the tensor cores beat gathers: the
+    // selection (index sets, threshold forms, bitmask), then the routed
+    // kernel with every head sparse (it has no log-sum-exp output)
+    if (!lse && gated_routed_path(x, top_k))
+        return launch_routed_attn(q, k, v, qI, kI, wI, nullptr, x, top_k, scale, g, lin, out, ws, st, idx, cnt);
     // two launches: the selection into idx/cnt (or workspace room), then the
     // attention over the gathered keys
-    if ((e = check_ws(ws, ws_bytes, gated_ws(x, top_k)))) return e;
     const Shape r = selection_rows(x);
     const size_t sel_bytes = align256(topk_ws(x, top_k));
     const size_t scr = gated_scratch_off(x, top_k);

@@ -166,10 +166,12 @@ esa_status launch_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16
 
 // ---- routed (full | sparse per head) attention ---------------------------
 size_t ws_routed(const Shape &s, int K);
+// route == nullptr: every head sparse (the warp-specialised kernel only).
+// idx/cnt (optional) receive the selection's index sets as well.
 esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
                               const int8_t *kI, const int32_t *wI, const uint8_t *route, const Shape &s, int K,
                               float scale, const float *g, const uint16_t *lin, float *out, void *ws,
-                              cudaStream_t st);
+                              cudaStream_t st, int32_t *idx = nullptr, int32_t *cnt = nullptr);
 
 // tcgen05 routed attention (tensor-memory accumulators), given the threshold
 // form (T, P) of every row's Top-K set in thr (int32 pairs [rows][2]).

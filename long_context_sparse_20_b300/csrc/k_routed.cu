@@ -40,7 +40,7 @@ size_t ws_routed(const Shape &s, int K) {
 esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int8_t *qI,
                               const int8_t *kI, const int32_t *wI, const uint8_t *route, const Shape &s, int K,
                               float scale, const float *g, const uint16_t *lin, float *out, void *ws,
-                              cudaStream_t st) {
+                              cudaStream_t st, int32_t *idx, int32_t *cnt) {
     char *base = static_cast<char *>(ws);
     const Shape r = selection_rows(s);
     const size_t sel_bytes = align256(ws_row_select(r, K));
@@ -50,7 +50,8 @@ esa_status launch_routed_attn(const uint16_t *q, const uint16_t *k, const uint16
     const bool pp = routed_pp_supported(s);
     char *pp_ws = base + sel_bytes + align256((size_t)r.B * r.Tq * 2 * 4);
     uint32_t *mask = pp ? reinterpret_cast<uint32_t *>(pp_ws + align256(ws_routed_pp(s))) : nullptr;
-    esa_status e = launch_row_select(qI, kI, w, r, K, nullptr, nullptr, thr, ws, sel_bytes, st, mask);
+    if (!pp && !route) return ESA_ERR_UNSUPPORTED;
+    esa_status e = launch_row_select(qI, kI, w, r, K, idx, cnt, thr, ws, sel_bytes, st, mask);
     if (e != ESA_OK) return e;
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     if (pp) return launch_routed_pp(q, k, v, route, thr, mask, s, scale, g, lin, out, pp_ws, status, st);

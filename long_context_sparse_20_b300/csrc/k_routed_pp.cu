@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = (int)(bid % a.Hq);
     const long long b = bid / a.Hq;
     const int kvh = h / (a.Hq / a.Hkv);
-    const bool sparse = a.route[b * a.Hq + h] != 0;
+    const bool sparse = a.route ? a.route[b * a.Hq + h] != 0 : true;  // no routes: every head sparse
     // the index set this head masks with: its own indexer head's (per-head
     // sets) or the row's one set
     const int iset = a.pset ? h / (a.Hq / a.H_I) : 0;

@@ -152,6 +152,28 @@ def test_fused_call_on_shapes_that_take_two_launches(over):
     assert_close(res["out"], ref)
 
 
+@pytest.mark.parametrize("over", [
+    dict(B=1, Tq=300, Tk=300, Hq=4, Hkv=1, D=64, D_I=32, top_k=64),                  # prefill rows
+    dict(B=2, Tq=70, Tk=600, q_offset=530, Hq=8, Hkv=2, D=128, D_I=64, top_k=128),   # chunked prefill
+    dict(B=1, Tq=200, Tk=200, Hq=8, Hkv=2, D=128, H_I=4, D_I=64, top_k=40, flags=3),  # per-head sets, ReLU
+], ids=["prefill", "chunked", "per-head-sets"])
+def test_gated_call_on_the_routed_path(over):
+    """Prefill shapes whose causal prefixes hold few times the selected keys,
+    called without lse, take the routed kernel with every head sparse (the
+    selection's bitmask masks dense tiles): the same index sets and outputs
+    within tolerance, with and without the index outputs."""
+    cfg, sh, inp = _case(seed=308, **over)
+    K = cfg["top_k"]
+    res = gpu_gated(to_dev(inp), sh, K, want_lse=False)
+    check_against_oracle(inp, sh, K, res)
+    res = gpu_gated(to_dev(inp), sh, K, want_idx=False, want_lse=False)
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, K)
+    assert_close(res["out"], ref)
+    res = gpu_gated(to_dev(inp), sh, K, want_idx=False, want_lse=False, gate=False)
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, K, gate=False)
+    assert_close(res["out"], ref)
+
+
 def test_fused_workspace_reuse_across_shapes():
     """Back-to-back calls on one workspace, alternating shapes: the control
     state each call leaves behind is what the next one needs."""
