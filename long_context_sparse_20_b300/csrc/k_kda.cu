@@ -15,9 +15,10 @@
 // s += beta_t (v_t[c] - k_t . s) k_t. Two kernels:
 //   kda_kernel (many steps) holds the state in registers for the whole
 //   sequence: NS lanes share CC columns, each lane R = Dk/NS key channels of
-//   them (Dk = 128: 16 lanes x 8 channels x 2 columns; Dk = 64: 8 x 8 x 1);
-//   a block of 4 warps holds 16 columns of one (sequence, head), grid
-//   (Dv/16, H, B).
+//   them (Dk = 128: 16 lanes x 8 channels x 2 columns, or x 1 column when
+//   that grid fits on the SMs at one block each; Dk = 64: 8 x 8 x 1); a
+//   block of 4 warps holds 16 (or 8) columns of one (sequence, head), grid
+//   (Dv/16 or Dv/8, H, B).
 //   - The inputs of 32 steps (the head's q, k and alpha rows, the block's v
 //     values, beta) are staged in shared memory with cp.async, double
 //     buffered, laid out so that the NS lanes of a column group read
@@ -508,8 +509,17 @@ esa_status launch_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
         return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
     }
     // 8 key channels per lane: at Dk = 128, 16 lanes hold two columns each
-    // (the operands a lane loads serve both); at Dk = 64, 8 lanes one column
-    if (Dk == 128) return launch_kda_t<128, 16, 2>(a, B, st);
+    // (the operands a lane loads serve both), or one column each when that
+    // grid of twice the blocks still gives every block an SM of its own: a
+    // block's steps are one dependent chain per warp, so half the columns
+    // finish sooner (B1 x 32768 steps, 8 heads: 4.35 ms against 5.52 ms).
+    // Two such blocks on one SM issue more instructions for the same columns
+    // than one two-column block (16 heads: 6.46 ms against 5.52 ms). At
+    // Dk = 64, 8 lanes one column.
+    if (Dk == 128) {
+        if ((long long)(Dv / 8) * H * B <= device_info().sms) return launch_kda_t<128, 16, 1>(a, B, st);
+        return launch_kda_t<128, 16, 2>(a, B, st);
+    }
     if (Dk == 64) return launch_kda_t<64, 8, 1>(a, B, st);
     return ESA_ERR_UNSUPPORTED;
 }

@@ -61,6 +61,9 @@ KDA_CASES = [
     dict(B=1, T=100, H=2, Dk=128, Dv=64, state=True),  # several chunks, ragged tail
     dict(B=1, T=257, H=2, Dk=128, Dv=128, state=False),
     dict(B=3, T=70, H=1, Dk=64, Dv=16, state=True),    # one column block
+    # at Dk = 128 a grid that fits on the SMs at one block each holds one
+    # column per lane, larger ones two: this one launches 1024 blocks
+    dict(B=4, T=41, H=32, Dk=128, Dv=128, state=True),
 ]
 
 
