@@ -312,11 +312,29 @@ ESA_API esa_status esa_route_heads(const uint16_t *k, const float *W1, const flo
  * Dk in {64, 128}; Dv a multiple of 16 in 16..512 (else ESA_ERR_UNSUPPORTED);
  * B, H <= 65535. q, k, v, alpha, state_in, state_out and o 16-byte aligned,
  * lin 8-byte, beta 4-byte (else ESA_ERR_INVALID). o and lin must not overlap
- * any input. fp32 arithmetic in a fixed order (deterministic); no workspace,
- * and no device-side error is possible. */
+ * any input. fp32 arithmetic in a fixed order (deterministic).
+ * Workspace (optional): with ws == NULL the steps run one after another on
+ * the state, and no device-side error is possible. With ws != NULL and
+ * T > 4, the call takes the chunked form: the steps in chunks of 16, each
+ * chunk's couplings computed for all chunks at once, then the state carried
+ * from chunk to chunk by a few small matrix products (the same results up to
+ * fp32 rounding order). A chunk whose cumulative forgetting factor leaves
+ * [2^-60, 2^60] for some key channel runs its steps one by one. ws must then
+ * hold esa_kda_workspace_size() bytes and be 256-byte aligned (else
+ * ESA_ERR_WORKSPACE); it needs no initialisation. Its first word is a status
+ * word that the call clears first: a bounded device wait for a chunk's data
+ * that runs out sets ESA_ERR_TIMEOUT there (read it with esa_read_status)
+ * and leaves that block's outputs unwritten. T <= 4 never uses ws. */
 ESA_API esa_status esa_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                            const float *beta, const float *state_in, int64_t B, int64_t T, int32_t H, int32_t Dk,
-                           int32_t Dv, float scale, float *o, uint16_t *lin, float *state_out, void *stream);
+                           int32_t Dv, float scale, float *o, uint16_t *lin, float *state_out, void *ws,
+                           size_t ws_bytes, void *stream);
+
+/* Bytes of workspace esa_kda() needs for its chunked form at this shape: one
+ * record of fp32 matrices per (sequence, head, chunk of 16 steps), for at
+ * most 256 chunks at a time, plus a carried state when there are more; 0 when
+ * T <= 4 or the shape is not supported. */
+ESA_API size_t esa_kda_workspace_size(int64_t B, int64_t T, int32_t H, int32_t Dk, int32_t Dv);
 
 /* Top-K selection without a caller workspace. The pages have no counterpart
  * to this call: it is a convenience of this library.

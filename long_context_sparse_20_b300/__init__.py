@@ -58,7 +58,8 @@ _SIGS = {
     "esa_topk_select_noalloc": (_i32, [_vp, _vp, _vp, _sp, ctypes.c_int, _vp, _vp, _vp, _vp]),
     "esa_route_heads": (_i32, [_vp, _vp, _vp, _vp, _vp, _sp, ctypes.c_int, _vp, _vp, _vp, _sz, _vp]),
     "esa_kda": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int64, ctypes.c_int64, _i32, _i32, _i32, ctypes.c_float,
-                       _vp, _vp, _vp, _vp]),
+                       _vp, _vp, _vp, _vp, _sz, _vp]),
+    "esa_kda_workspace_size": (_sz, [ctypes.c_int64, ctypes.c_int64, _i32, _i32, _i32]),
     "esa_read_status": (_i32, [_vp, _vp, ctypes.POINTER(_i32)]),
     "esa_status_string": (ctypes.c_char_p, [_i32]),
     "esa_binary_version": (ctypes.c_int, []),
@@ -202,12 +203,19 @@ def esa_route_heads(k, W1, b1, W2, b2, shape: esa_shape, route, margin, ws: Work
                                 _p(margin), ws.ptr, ws.nbytes, _stream(stream, k)), "esa_route_heads")
 
 
+def esa_kda_workspace_size(B: int, T: int, H: int, Dk: int, Dv: int) -> int:
+    """Bytes of workspace the chunked form of esa_kda needs (0: none)."""
+    return int(_lib.esa_kda_workspace_size(B, T, H, Dk, Dv))
+
+
 def esa_kda(q, k, v, alpha, beta, state_in=None, o=None, lin=None, state_out=None, scale: float | None = None,
-            stream=None):
+            ws=None, chunked: bool = True, stream=None):
     """The KDA linear-attention branch: q, k bf16 [B, T, H, Dk]; v bf16
     [B, T, H, Dv]; alpha fp32 [B, T, H, Dk]; beta fp32 [B, T, H]; state_in /
     state_out fp32 [B, H, Dk, Dv] (may be the same tensor); o fp32 and lin
-    bf16 [B, T, H, Dv]. scale defaults to 1/sqrt(Dk)."""
+    bf16 [B, T, H, Dv]. scale defaults to 1/sqrt(Dk). chunked: the chunked
+    form, in ``ws`` (a uint8 device tensor of esa_kda_workspace_size bytes;
+    allocated here when None); otherwise the steps one by one."""
     B, T, H, Dk = (int(x) for x in q.shape)
     Dv = int(v.shape[-1])
     for t, want in ((k, q.shape), (alpha, q.shape), (v, (B, T, H, Dv)), (beta, (B, T, H))):
@@ -218,8 +226,16 @@ def esa_kda(q, k, v, alpha, beta, state_in=None, o=None, lin=None, state_out=Non
     for t in (alpha, beta, state_in, state_out, o):
         assert t is None or t.dtype == torch.float32, t.dtype
     sc = Dk ** -0.5 if scale is None else float(scale)
+    wp, wn = None, 0
+    if chunked:
+        need = esa_kda_workspace_size(B, T, H, Dk, Dv)
+        if need:
+            if ws is None:
+                ws = torch.empty(need + 256, dtype=torch.uint8, device=q.device)
+            off = (-ws.data_ptr()) % 256
+            wp, wn = ctypes.c_void_p(ws.data_ptr() + off), ws.numel() - off
     _check(_lib.esa_kda(_p(_bits(q)), _p(_bits(k)), _p(_bits(v)), _p(alpha), _p(beta), _p(state_in), B, T, H, Dk, Dv,
-                        sc, _p(o), _p(_bits(lin)), _p(state_out), _stream(stream, q)), "esa_kda")
+                        sc, _p(o), _p(_bits(lin)), _p(state_out), wp, wn, _stream(stream, q)), "esa_kda")
 
 
 def esa_read_status(ws: Workspace, stream=None) -> int:

@@ -415,20 +415,33 @@ esa_status esa_route_heads(const uint16_t *k, const float *W1, const float *b1, 
     return launch_route_heads(k, W1, b1, W2, b2, x, hidden, route, margin, ws, (cudaStream_t)stream);
 }
 
-esa_status esa_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
-                   const float *state_in, int64_t B, int64_t T, int32_t H, int32_t Dk, int32_t Dv, float scale, float *o,
-                   uint16_t *lin, float *state_out, void *stream) {
+static esa_status kda_shape_ok(int64_t B, int64_t T, int32_t H, int32_t Dk, int32_t Dv) {
     if (B < 0 || T < 0 || H < 1) return ESA_ERR_INVALID;
     if (Dk != 64 && Dk != 128) return ESA_ERR_UNSUPPORTED;
     if (Dv < 16 || Dv > 512 || Dv % 16 != 0) return ESA_ERR_UNSUPPORTED;
     if (B > 65535 || H > 65535) return ESA_ERR_UNSUPPORTED;
+    return ESA_OK;
+}
+
+size_t esa_kda_workspace_size(int64_t B, int64_t T, int32_t H, int32_t Dk, int32_t Dv) {
+    if (kda_shape_ok(B, T, H, Dk, Dv) != ESA_OK || !kda_uses_chunks(T)) return 0;
+    return kda_chunked_ws_bytes(B, T, H, Dk, Dv);
+}
+
+esa_status esa_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
+                   const float *state_in, int64_t B, int64_t T, int32_t H, int32_t Dk, int32_t Dv, float scale, float *o,
+                   uint16_t *lin, float *state_out, void *ws, size_t ws_bytes, void *stream) {
+    esa_status e = kda_shape_ok(B, T, H, Dk, Dv);
+    if (e) return e;
     if (T > 0 && (!q || !k || !v || !alpha || !beta)) return ESA_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(state_in) ||
         !aligned16(state_out) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lin) & 7u) ||
         (reinterpret_cast<uintptr_t>(beta) & 3u))
         return ESA_ERR_INVALID;
     if (B == 0 || (T == 0 && !state_out)) return ESA_OK;
-    return launch_kda(q, k, v, alpha, beta, state_in, B, T, H, Dk, Dv, scale, o, lin, state_out, (cudaStream_t)stream);
+    if (ws && kda_uses_chunks(T) && (e = check_ws(ws, ws_bytes, kda_chunked_ws_bytes(B, T, H, Dk, Dv)))) return e;
+    return launch_kda(q, k, v, alpha, beta, state_in, B, T, H, Dk, Dv, scale, o, lin, state_out, ws,
+                      (cudaStream_t)stream);
 }
 
 esa_status esa_read_status(void *ws, void *stream, int32_t *dev_status) {

@@ -198,9 +198,17 @@ esa_status launch_route_heads(const uint16_t *k, const float *W1, const float *b
                               const Shape &s, int hidden, uint8_t *route, float *margin, void *ws, cudaStream_t st);
 
 // ---- KDA linear-attention branch ----------------------------------------
+// ws == nullptr: the step-by-step kernels; otherwise (more than a few steps)
+// the chunked form, whose chunk records take kda_chunked_ws_bytes() of ws
 esa_status launch_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
                       const float *state_in, long long B, long long T, int H, int Dk, int Dv, float scale, float *o,
-                      uint16_t *lin, float *state_out, cudaStream_t st);
+                      uint16_t *lin, float *state_out, void *ws, cudaStream_t st);
+bool kda_uses_chunks(long long T);
+size_t kda_chunked_ws_bytes(long long B, long long T, int H, int Dk, int Dv);
+esa_status launch_kda_chunked(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                              const float *beta, const float *state_in, long long B, long long T, int H, int Dk,
+                              int Dv, float scale, float *o, uint16_t *lin, float *state_out, void *ws,
+                              cudaStream_t st);
 
 // Wait limit for inter-block waits, in ns (ESA_WAIT_LIMIT_NS overrides) and
 // the count of extra arrivals a barrier waits for (ESA_DEBUG_EXTRA_ARRIVALS;

@@ -494,10 +494,14 @@ esa_status launch_kda_t(const KdaArgs &a, long long B, cudaStream_t st) {
 
 }  // namespace
 
+bool kda_uses_chunks(long long T) { return T > kDecodeSteps; }
+
 esa_status launch_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
                       const float *state_in, long long B, long long T, int H, int Dk, int Dv, float scale, float *o,
-                      uint16_t *lin, float *state_out, cudaStream_t st) {
+                      uint16_t *lin, float *state_out, void *ws, cudaStream_t st) {
     const KdaArgs a{q, k, v, alpha, beta, state_in, o, state_out, lin, T, H, Dv, scale};
+    if (ws && kda_uses_chunks(T))
+        return launch_kda_chunked(q, k, v, alpha, beta, state_in, B, T, H, Dk, Dv, scale, o, lin, state_out, ws, st);
     if (T <= kDecodeSteps) {  // a few steps: one streaming pass over the state
         dim3 grid((unsigned)(Dv / kDecCols), (unsigned)H, (unsigned)B);
         if (Dk == 128)

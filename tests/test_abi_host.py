@@ -156,8 +156,9 @@ def test_host_validation_of_kda():
     f = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails (or returns) first
     mis = ctypes.c_void_p(0x1008)
 
-    def call(q=f, k=f, v=f, a=f, b=f, s_in=None, B=1, T=4, H=2, Dk=128, Dv=128, o=f, lin=None, s_out=None):
-        return L.esa_kda(q, k, v, a, b, s_in, B, T, H, Dk, Dv, 0.1, o, lin, s_out, None)
+    def call(q=f, k=f, v=f, a=f, b=f, s_in=None, B=1, T=4, H=2, Dk=128, Dv=128, o=f, lin=None, s_out=None, ws=None,
+             ws_bytes=0):
+        return L.esa_kda(q, k, v, a, b, s_in, B, T, H, Dk, Dv, 0.1, o, lin, s_out, ws, ws_bytes, None)
 
     assert call(Dk=96) == esa.ERR_UNSUPPORTED
     assert call(Dv=24) == esa.ERR_UNSUPPORTED and call(Dv=1024) == esa.ERR_UNSUPPORTED
@@ -169,3 +170,25 @@ def test_host_validation_of_kda():
     # nothing to do: no launch
     assert call(B=0) == esa.OK
     assert call(q=None, k=None, v=None, a=None, b=None, T=0) == esa.OK
+    # the chunked form's workspace: too small or misaligned
+    need = esa.esa_kda_workspace_size(1, 100, 2, 128, 128)
+    assert need > 0
+    assert call(T=100, ws=ctypes.c_void_p(0x100000), ws_bytes=need - 1) == esa.ERR_WORKSPACE
+    assert call(T=100, ws=ctypes.c_void_p(0x100010), ws_bytes=need) == esa.ERR_WORKSPACE
+
+
+def test_kda_workspace_size():
+    """A 256-byte status word, then one record per (sequence, head, chunk of
+    16 steps) of fp32 words: two 16 x Dk matrices with rows padded to Dk + 4,
+    one with rows padded to Dk + 8, g_last (Dk), a flag (padded to four) and
+    two 16 x Dv matrices; at most 256 chunks at a time, plus the carried
+    state (256-byte aligned) beyond that. None for T <= 4 or unsupported
+    shapes."""
+    import long_context_sparse_20_b300 as esa
+    rec = lambda Dk, Dv: 4 * (2 * 16 * (Dk + 4) + 16 * (Dk + 8) + Dk + 4 + 2 * 16 * Dv)
+    assert esa.esa_kda_workspace_size(2, 100, 3, 128, 64) == 256 + 2 * 3 * 7 * rec(128, 64)
+    assert esa.esa_kda_workspace_size(1, 4096, 2, 64, 128) == 256 + 2 * 256 * rec(64, 128)
+    carry = 1 * 16 * 128 * 128 * 4
+    assert esa.esa_kda_workspace_size(1, 32768, 16, 128, 128) == 256 + carry + 16 * 256 * rec(128, 128)
+    assert esa.esa_kda_workspace_size(1, 4, 2, 128, 128) == 0
+    assert esa.esa_kda_workspace_size(1, 100, 2, 96, 128) == 0

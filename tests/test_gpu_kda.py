@@ -25,7 +25,7 @@ def _inputs(B, T, H, Dk, Dv, seed, state):
     return E.kda_inputs(B, T, H, Dk, Dv, seed, state=state)
 
 
-def _gpu(x: dict, state_in=None, inplace=False, lin=True, o=True):
+def _gpu(x: dict, state_in=None, inplace=False, lin=True, o=True, chunked=True):
     m = esa()
     B, T, H, Dk = (int(s) for s in x["q"].shape)
     Dv = int(x["v"].shape[-1])
@@ -34,9 +34,15 @@ def _gpu(x: dict, state_in=None, inplace=False, lin=True, o=True):
     lo = torch.zeros((B, T, H, Dv), dtype=torch.bfloat16, device="cuda") if lin else None
     si = state_in.cuda() if state_in is not None else None
     so = si if inplace else torch.full((B, H, Dk, Dv), float("nan"), dtype=torch.float32, device="cuda")
-    m.esa_kda(d["q"], d["k"], d["v"], d["alpha"], d["beta"], state_in=si, o=out, lin=lo, state_out=so)
+    m.esa_kda(d["q"], d["k"], d["v"], d["alpha"], d["beta"], state_in=si, o=out, lin=lo, state_out=so,
+              chunked=chunked)
     torch.cuda.synchronize()
     return (out.cpu() if o else None), (lo.cpu() if lin else None), so.cpu()
+
+
+# both forms of the recurrence: chunks of 16 steps (a workspace given), and
+# the steps one by one
+FORMS = pytest.mark.parametrize("chunked", [True, False], ids=["chunked", "stepwise"])
 
 
 def _check(o, lin, so, ro, rs):
@@ -67,30 +73,44 @@ KDA_CASES = [
 ]
 
 
+@FORMS
 @pytest.mark.parametrize("c", KDA_CASES, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
-def test_kda_small(c):
+def test_kda_small(c, chunked):
     x = _inputs(c["B"], c["T"], c["H"], c["Dk"], c["Dv"], 300 + c["T"], c["state"])
     ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x.get("state"))
-    o, lin, so = _gpu(x, state_in=x.get("state"))
+    o, lin, so = _gpu(x, state_in=x.get("state"), chunked=chunked)
     _check(o, lin, so, ro, rs)
 
 
-def test_kda_state_carried_across_calls():
+@pytest.mark.parametrize("inplace", [False, True])
+def test_kda_chunked_over_segments(inplace):
+    """More than 256 chunks (4096 steps) in one call: the chunked form runs
+    in segments and carries the state between them; a ragged last chunk;
+    the final state written over the initial one when asked."""
+    x = _inputs(2, 4500, 2, 64, 48, 77, True)
+    ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
+    o, lin, so = _gpu(x, state_in=x["state"].clone(), inplace=inplace)
+    _check(o, lin, so, ro, rs)
+
+
+@FORMS
+def test_kda_state_carried_across_calls(chunked):
     """Chunked prefill: 100 steps in one call, or 64 then 36 with the state
     updated in place, give the same bits (the state is carried in fp32 and
-    the split falls on the kernel's 32-step staging, so every step is
-    computed alike); a split at 45 (steps paired differently) matches the
-    oracle; both match the oracle."""
+    the split falls on a boundary of both forms' step groups, 32 staged
+    steps and 16-step chunks, so every step is computed alike); a split at
+    45 (steps grouped differently) matches the oracle; both match the
+    oracle."""
     x = _inputs(2, 100, 2, 128, 128, 71, True)
     ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
-    o, lin, so = _gpu(x, state_in=x["state"])
+    o, lin, so = _gpu(x, state_in=x["state"], chunked=chunked)
     _check(o, lin, so, ro, rs)
     for cut, exact in ((64, True), (45, False)):
         st = x["state"].clone().cuda()
         parts = []
         for a, b in ((0, cut), (cut, 100)):
             xs = {k: (v[:, a:b].contiguous() if k != "state" else v) for k, v in x.items()}
-            po, _, _ = _gpu(xs, state_in=st, inplace=True, lin=False)
+            po, _, _ = _gpu(xs, state_in=st, inplace=True, lin=False, chunked=chunked)
             parts.append(po)
         oc = torch.cat(parts, dim=1)
         if exact:
@@ -100,7 +120,8 @@ def test_kda_state_carried_across_calls():
             _check(oc, None, st.cpu(), ro, rs)
 
 
-def test_kda_empty_and_state_only():
+@FORMS
+def test_kda_empty_and_state_only(chunked):
     """T = 0 hands the initial state back; no outputs requested still
     advances the state."""
     x = _inputs(1, 6, 2, 64, 64, 72, True)
@@ -112,20 +133,22 @@ def test_kda_empty_and_state_only():
     torch.cuda.synchronize()
     assert torch.equal(so, si)
     _, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
-    _, _, so2 = _gpu(x, state_in=x["state"], lin=False, o=False)
+    _, _, so2 = _gpu(x, state_in=x["state"], lin=False, o=False, chunked=chunked)
     assert np.abs(so2.double().numpy() - rs).max() <= REL * np.abs(rs).max()
     # zero initial state when none is given
     ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"])
-    o, lin, so = _gpu(x)
+    o, lin, so = _gpu(x, chunked=chunked)
     _check(o, lin, so, ro, rs)
 
 
+@FORMS
 @pytest.mark.parametrize("T", [3, 70])
-def test_kda_extreme_gates(T):
-    """Gates at their ends on both kernels (a few steps and many): alpha = 0
-    (the state is wiped), alpha = 1 (nothing forgotten), beta = 0 (no
-    write) and beta = 1 (full replacement) mixed over steps, heads and
-    channels."""
+def test_kda_extreme_gates(T, chunked):
+    """Gates at their ends on every kernel (a few steps and many, both
+    forms): alpha = 0 (the state is wiped), alpha = 1 (nothing forgotten),
+    beta = 0 (no write) and beta = 1 (full replacement) mixed over steps,
+    heads and channels. In the chunked form nearly every chunk then holds a
+    zero forgetting factor and runs step by step."""
     x = _inputs(2, T, 3, 128, 64, 90 + T, True)
     rng = np.random.default_rng(T)
     a = x["alpha"].numpy().copy()
@@ -138,6 +161,23 @@ def test_kda_extreme_gates(T):
     bt[pb < 0.2] = 0.0
     bt[pb > 0.8] = 1.0
     x["beta"] = torch.from_numpy(bt)
+    ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
+    o, lin, so = _gpu(x, state_in=x["state"], chunked=chunked)
+    _check(o, lin, so, ro, rs)
+
+
+def test_kda_chunked_few_flagged_chunks():
+    """Forgetting factors of 0 or near it in a few places: chunks whose
+    cumulative factor falls below 2^-60 run step by step, the others as
+    matrix products (one with factors down to 2^-35), and the state passes
+    between the two kinds of chunk."""
+    x = _inputs(1, 200, 2, 128, 32, 78, True)
+    a = x["alpha"].numpy().copy()
+    a[0, 37, 0, 5] = 0.0        # chunk 2, head 0: flagged
+    a[0, 38:56, 1, 70] = 0.09   # head 1: 0.09^10 ~ 2^-35 in chunk 2, 0.09^8 in chunk 3: products
+    a[0, 100:116, 0, 9] = 0.01  # head 0: 0.01^12 ~ 2^-80 in chunk 6 (flagged), 0.01^4 in chunk 7
+    a[0, 150, :, :] = 0.0       # chunk 9, every channel of both heads: flagged
+    x["alpha"] = torch.from_numpy(a)
     ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
     o, lin, so = _gpu(x, state_in=x["state"])
     _check(o, lin, so, ro, rs)
@@ -152,12 +192,13 @@ def test_kda_decode_full():
     _check(o, lin, so, ro, rs)
 
 
-def test_kda_long_prefill_sampled_heads():
+@FORMS
+def test_kda_long_prefill_sampled_heads(chunked):
     """The long-prefill shape (32768 steps, 16 heads, 128 x 128 state): the
     GPU runs every head; the oracle recomputes two heads in full (every step,
     every output and the final state)."""
     x = _inputs(1, 32768, 16, 128, 128, 2003, False)
-    o, lin, so = _gpu(x)
+    o, lin, so = _gpu(x, chunked=chunked)
     heads = [0, 11]
     xs = {k: v[:, :, heads].contiguous() for k, v in x.items()}
     ro, rs = O.kda(xs["q"], xs["k"], xs["v"], xs["alpha"], xs["beta"])
