@@ -81,8 +81,31 @@ struct ChunkArgs {
 
 __device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
 
-// Prep block shared memory, in floats: Kt, Qt, Ki (rows padded), A, Bm, M
-// (rows of kC + 4), beta, then the chunk's raw inputs staged by cp.async:
+// acc[i] = sum_{l <= i} L[i][l] x(l) for a lower-triangular kC x kC matrix
+// L held transposed in shared memory (LT[l][i] = L[i][l], rows of MS words,
+// 16-byte aligned): column l of L is read four entries at a time (the same
+// address in every lane: one broadcast), and every acc[i] adds its terms in
+// order of l.
+template <int MS, typename X>
+__device__ __forceinline__ void tri_cols(const float *LT, X x, float (&acc)[kC]) {
+#pragma unroll
+    for (int i = 0; i < kC; i++) acc[i] = 0.f;
+#pragma unroll
+    for (int l = 0; l < kC; l++) {
+        const float xl = x(l);
+#pragma unroll
+        for (int i4 = l / 4 * 4; i4 < kC; i4 += 4) {
+            const float4 m = *reinterpret_cast<const float4 *>(LT + l * MS + i4);
+            if (i4 >= l) acc[i4] = fmaf(m.x, xl, acc[i4]);
+            if (i4 + 1 >= l) acc[i4 + 1] = fmaf(m.y, xl, acc[i4 + 1]);
+            if (i4 + 2 >= l) acc[i4 + 2] = fmaf(m.z, xl, acc[i4 + 2]);
+            acc[i4 + 3] = fmaf(m.w, xl, acc[i4 + 3]);
+        }
+    }
+}
+
+// Prep block shared memory, in floats: Kt, Qt, Ki (rows padded), A, Bm^T,
+// M^T (rows of kC + 4), beta, then the chunk's raw inputs staged by cp.async:
 // k, q (bf16 [kC][Dk]), alpha (fp32 [kC][Dk]), v (bf16 [kC][Dv], last: its
 // size depends on Dv).
 template <int DK>
@@ -96,11 +119,11 @@ struct PrepLayout {
 };
 
 template <int DK>
-__global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(const ChunkArgs a) {
+__global__ void __launch_bounds__(kPrepThreads, 4) kda_prep_kernel(const ChunkArgs a) {
     using L = PrepLayout<DK>;
     constexpr int P = L::P, MS = L::MS;
     extern __shared__ __align__(128) float sm[];
-    float *Kt = sm + L::KT, *Qt = sm + L::QT, *Ki = sm + L::KI, *Am = sm + L::AM, *Bm = sm + L::BM, *M = sm + L::MM;
+    float *Kt = sm + L::KT, *Qt = sm + L::QT, *Ki = sm + L::KI, *Am = sm + L::AM, *BmT = sm + L::BM, *MT = sm + L::MM;
     float *sb = sm + L::SB;
     const uint16_t *RKs = reinterpret_cast<const uint16_t *>(sm + L::RK);
     const uint16_t *RQs = reinterpret_cast<const uint16_t *>(sm + L::RQ);
@@ -168,26 +191,33 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(const ChunkArgs 
     }
     const int flagged = __syncthreads_or(bad);
 
-    // A = strictly-lower(Kt Ki^T), Bm = lower(Qt Ki^T)
-    for (int o = tid; o < 2 * kC * kC; o += kPrepThreads) {
-        const int which = o / (kC * kC), i = (o / kC) % kC, j = o % kC;
-        const float *x = (which ? Qt : Kt) + i * P;
-        const float *y = Ki + j * P;
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
+    // A = strictly-lower(Kt Ki^T), Bm = lower(Qt Ki^T): only the 2 x 2 tiles
+    // on or below the diagonal (36 of each), one per thread; the entries
+    // above the diagonal are never read
+    if (tid < 72) {
+        const int which = tid / 36;
+        int tq = tid % 36, I = 0;
+        while (tq > I) tq -= ++I;  // tile (I, J = tq), J <= I
+        const int J = tq;
+        const float *x0 = (which ? Qt : Kt) + 2 * I * P, *x1 = x0 + P;
+        const float *y0 = Ki + 2 * J * P, *y1 = y0 + P;
+        float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
+#pragma unroll 4
         for (int d = 0; d < DK; d += 4) {
-            const float4 xv = *reinterpret_cast<const float4 *>(x + d);
-            const float4 yv = *reinterpret_cast<const float4 *>(y + d);
-            s0 = fmaf(xv.x, yv.x, s0);
-            s1 = fmaf(xv.y, yv.y, s1);
-            s0 = fmaf(xv.z, yv.z, s0);
-            s1 = fmaf(xv.w, yv.w, s1);
+            const float4 a0 = *reinterpret_cast<const float4 *>(x0 + d), a1 = *reinterpret_cast<const float4 *>(x1 + d);
+            const float4 b0 = *reinterpret_cast<const float4 *>(y0 + d), b1 = *reinterpret_cast<const float4 *>(y1 + d);
+            s00 = fmaf(a0.x, b0.x, s00); s00 = fmaf(a0.y, b0.y, s00); s00 = fmaf(a0.z, b0.z, s00); s00 = fmaf(a0.w, b0.w, s00);
+            s01 = fmaf(a0.x, b1.x, s01); s01 = fmaf(a0.y, b1.y, s01); s01 = fmaf(a0.z, b1.z, s01); s01 = fmaf(a0.w, b1.w, s01);
+            s10 = fmaf(a1.x, b0.x, s10); s10 = fmaf(a1.y, b0.y, s10); s10 = fmaf(a1.z, b0.z, s10); s10 = fmaf(a1.w, b0.w, s10);
+            s11 = fmaf(a1.x, b1.x, s11); s11 = fmaf(a1.y, b1.y, s11); s11 = fmaf(a1.z, b1.z, s11); s11 = fmaf(a1.w, b1.w, s11);
         }
-        const float s = s0 + s1;
-        if (which == 0)
-            Am[i * MS + j] = j < i ? s : 0.f;
-        else
-            Bm[i * MS + j] = j <= i ? s : 0.f;
+        // A as is, Bm transposed; A keeps j < i, Bm j <= i
+        const int lo = which ? 0 : 1, si = which ? 1 : MS, sj = which ? MS : 1;
+        float *R = (which ? BmT : Am) + 2 * I * si + 2 * J * sj;
+        R[0] = 2 * J <= 2 * I - lo ? s00 : 0.f;
+        R[sj] = 2 * J + 1 <= 2 * I - lo ? s01 : 0.f;
+        R[si] = 2 * J <= 2 * I + 1 - lo ? s10 : 0.f;
+        R[si + sj] = 2 * J + 1 <= 2 * I + 1 - lo ? s11 : 0.f;
     }
     __syncthreads();
 
@@ -202,7 +232,7 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(const ChunkArgs 
 #pragma unroll
         for (int i = 0; i < kC; i++) {
             const float m = sb[i] * ((i == j ? 1.f : 0.f) - acc[i]);
-            M[i * MS + j] = m;
+            MT[j * MS + i] = m;
 #pragma unroll
             for (int l = i + 1; l < kC; l++) acc[l] = fmaf(Am[l * MS + i], m, acc[l]);
         }
@@ -212,46 +242,27 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(const ChunkArgs 
     // Wk = M Kt, Qp = Qt - Bm Wk, per key channel
     if (tid < DK) {
         const int d = tid;
-        float kt[kC], wk[kC];
+        float wk[kC], bw[kC];
+        tri_cols<MS>(MT, [&](int l) { return Kt[l * P + d]; }, wk);
 #pragma unroll
-        for (int l = 0; l < kC; l++) kt[l] = Kt[l * P + d];
+        for (int i = 0; i < kC; i++) Wk[i * P + d] = wk[i];
+        tri_cols<MS>(BmT, [&](int l) { return wk[l]; }, bw);
 #pragma unroll
-        for (int i = 0; i < kC; i++) {
-            float s = 0.f;
-#pragma unroll
-            for (int l = 0; l <= i; l++) s = fmaf(M[i * MS + l], kt[l], s);
-            wk[i] = s;
-            Wk[i * P + d] = s;
-        }
-#pragma unroll
-        for (int i = 0; i < kC; i++) {
-            float s = 0.f;
-#pragma unroll
-            for (int l = 0; l <= i; l++) s = fmaf(Bm[i * MS + l], wk[l], s);
-            Qp[i * P + d] = Qt[i * P + d] - s;
-        }
+        for (int i = 0; i < kC; i++) Qp[i * P + d] = Qt[i * P + d] - bw[i];
     }
     // U = M V, Up = Bm U, per value column
     for (int c = tid; c < Dv; c += kPrepThreads) {
+        // keep the compiler from holding M^T and Bm^T in registers across
+        // columns (it would need several hundred)
+        asm volatile("" ::: "memory");
         float *U = Ucol + (c / kNC) * 2 * kC * kNC + c % kNC, *Up = U + kC * kNC;
-        float vv[kC], u[kC];
+        float u[kC], up[kC];
+        tri_cols<MS>(MT, [&](int l) { return bf(RVs[l * Dv + c]); }, u);
 #pragma unroll
-        for (int l = 0; l < kC; l++) vv[l] = bf(RVs[l * Dv + c]);
+        for (int i = 0; i < kC; i++) U[i * kNC] = u[i];
+        tri_cols<MS>(BmT, [&](int l) { return u[l]; }, up);
 #pragma unroll
-        for (int i = 0; i < kC; i++) {
-            float s = 0.f;
-#pragma unroll
-            for (int l = 0; l <= i; l++) s = fmaf(M[i * MS + l], vv[l], s);
-            u[i] = s;
-            U[i * kNC] = s;
-        }
-#pragma unroll
-        for (int i = 0; i < kC; i++) {
-            float s = 0.f;
-#pragma unroll
-            for (int l = 0; l <= i; l++) s = fmaf(Bm[i * MS + l], u[l], s);
-            Up[i * kNC] = s;
-        }
+        for (int i = 0; i < kC; i++) Up[i * kNC] = up[i];
     }
     if (tid == 0) reinterpret_cast<int *>(gl + DK)[0] = flagged;
 }
@@ -271,19 +282,6 @@ __device__ __forceinline__ void mma_tf32_1688(float *d, const uint32_t *a, const
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
-// A B with A and B given in fp32 fragments, as three tf32 products added
-// into three accumulators (lo*hi, hi*lo, hi*hi), which run in parallel
-__device__ __forceinline__ void mma_3xtf32(float (&d)[3][4], const float *a, const float *b) {
-    uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-    for (int i = 0; i < 4; i++) tf32_split(a[i], ah[i], al[i]);
-#pragma unroll
-    for (int i = 0; i < 2; i++) tf32_split(b[i], bh[i], bl[i]);
-    mma_tf32_1688(d[0], al, bh);
-    mma_tf32_1688(d[1], ah, bl);
-    mma_tf32_1688(d[2], ah, bh);
-}
-
 // Scan block shared memory, in floats: the state slice transposed (ST, 16
 // rows of Dk, padded), kStages chunk stages (a record's shared part, then
 // this block's U and Up), D, the split-sum partials, the stage barriers.
@@ -294,7 +292,7 @@ struct ScanLayout {
     static constexpr int WK = 0, QP = WK + kC * P, KL = QP + kC * P, GL = KL + kC * PK, FLAG = GL + DK;
     static constexpr int UU = RA, UP = UU + kC * kNC, STAGE = UP + kC * kNC;
     static constexpr int ST = 0, S0 = ST + kNC * P, DD = S0 + kStages * STAGE, RED = DD + kC * PD;
-    static constexpr int BARS = RED + 2 * 2 * kC * PR;  // two K halves of the 2C x 16 product
+    static constexpr int BARS = RED + 4 * 2 * kC * PR;  // four K quarters of the 2C x 16 product
     static constexpr size_t BYTES = (size_t)BARS * 4 + kStages * 8;
     static constexpr int TPD = kScanThreads / DK;  // threads per key channel in the step-by-step path
     static constexpr int CPT = kNC / TPD;          // columns per such thread
@@ -359,8 +357,8 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
             ST[c * P + r] = acc[i][e];
         }
 
-    // X = [Wk; Qp] S by warp (m-tile mt: Wk or Qp rows, n-tile nt, K half kh)
-    const int mt = warp & 1, nt = (warp >> 1) & 1, kh = warp >> 2;
+    // X = [Wk; Qp] S by warp (m-tile mt: Wk or Qp rows; K quarter kq; both n-tiles)
+    const int mt = warp & 1, kq = warp >> 1;
 
     int j = 0;
     for (; j < a.nch; j++) {
@@ -375,8 +373,6 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
         if (reinterpret_cast<const int *>(buf + L::FLAG)[0] == 0) {
             {
                 const float *X = buf + (mt ? L::QP : L::WK);
-                const float *Y = ST + (8 * nt + g) * P;
-                // even and odd k-steps into separate accumulators: short MMA chains
                 float xa[2][3][4];
 #pragma unroll
                 for (int u = 0; u < 2; u++)
@@ -385,27 +381,42 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
 #pragma unroll
                         for (int e = 0; e < 4; e++) xa[u][p3][e] = 0.f;
 #pragma unroll
-                for (int ks = 0; ks < DK / 16; ks++) {
-                    const int k0 = kh * (DK / 2) + 8 * ks;
+                for (int ks = 0; ks < DK / 32; ks++) {
+                    const int k0 = kq * (DK / 4) + 8 * ks;
                     const float af[4] = {X[g * P + k0 + t4], X[(g + 8) * P + k0 + t4], X[g * P + k0 + t4 + 4],
                                          X[(g + 8) * P + k0 + t4 + 4]};
-                    const float bf2[2] = {Y[k0 + t4], Y[k0 + t4 + 4]};
-                    mma_3xtf32(xa[ks & 1], af, bf2);
-                }
-                float x[4];
+                    uint32_t ah[4], al[4];
 #pragma unroll
-                for (int e = 0; e < 4; e++)
-                    x[e] = ((xa[0][0][e] + xa[1][0][e]) + (xa[0][1][e] + xa[1][1][e])) + (xa[0][2][e] + xa[1][2][e]);
-                float *R = RED + kh * 2 * kC * PR + (16 * mt + g) * PR + 8 * nt + 2 * t4;
-                *reinterpret_cast<float2 *>(R) = make_float2(x[0], x[1]);
-                *reinterpret_cast<float2 *>(R + 8 * PR) = make_float2(x[2], x[3]);
+                    for (int i = 0; i < 4; i++) tf32_split(af[i], ah[i], al[i]);
+#pragma unroll
+                    for (int u = 0; u < 2; u++) {
+                        const float *Y = ST + (8 * u + g) * P + k0 + t4;
+                        uint32_t bh[2], bl[2];
+                        tf32_split(Y[0], bh[0], bl[0]);
+                        tf32_split(Y[4], bh[1], bl[1]);
+                        mma_tf32_1688(xa[u][0], al, bh);
+                        mma_tf32_1688(xa[u][1], ah, bl);
+                        mma_tf32_1688(xa[u][2], ah, bh);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 2; u++) {
+                    float x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) x[e] = (xa[u][0][e] + xa[u][1][e]) + xa[u][2][e];
+                    float *R = RED + kq * 2 * kC * PR + (16 * mt + g) * PR + 8 * u + 2 * t4;
+                    *reinterpret_cast<float2 *>(R) = make_float2(x[0], x[1]);
+                    *reinterpret_cast<float2 *>(R + 8 * PR) = make_float2(x[2], x[3]);
+                }
             }
             __syncthreads();
             {
                 // thread tid: D at (row, col) = (tid / 16, tid % 16); O at the same place
                 const int row = tid >> 4, col = tid & 15;
-                const float w = RED[row * PR + col] + RED[2 * kC * PR + row * PR + col];
-                const float z = RED[(16 + row) * PR + col] + RED[2 * kC * PR + (16 + row) * PR + col];
+                constexpr int Q = 2 * kC * PR;  // one K quarter's partial sums
+                const float *Rw = RED + row * PR + col, *Rz = Rw + 16 * PR;
+                const float w = ((Rw[0] + Rw[Q]) + Rw[2 * Q]) + Rw[3 * Q];
+                const float z = ((Rz[0] + Rz[Q]) + Rz[2 * Q]) + Rz[3 * Q];
                 DD[row * PD + col] = buf[L::UU + row * kNC + col] - w;
                 if (row < n) {
                     const float o = a.scale * (z + buf[L::UP + row * kNC + col]);
@@ -429,11 +440,18 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
             for (int ks = 0; ks < kC / 8; ks++) {
                 const float *K0 = KL + (8 * ks + t4) * PK + 16 * mt2 + g, *K4 = K0 + 4 * PK;
                 const float af[4] = {K0[0], K0[8], K4[0], K4[8]};
+                uint32_t ah[4], al[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) tf32_split(af[i], ah[i], al[i]);
 #pragma unroll
                 for (int i = 0; i < TPW; i++) {
                     const float *D0 = DD + (8 * ks + t4) * PD + 8 * (nt2 + i) + g;
-                    const float bf2[2] = {D0[0], D0[4 * PD]};
-                    mma_3xtf32(pa[i], af, bf2);
+                    uint32_t bh[2], bl[2];
+                    tf32_split(D0[0], bh[0], bl[0]);
+                    tf32_split(D0[4 * PD], bh[1], bl[1]);
+                    mma_tf32_1688(pa[i][0], al, bh);
+                    mma_tf32_1688(pa[i][1], ah, bl);
+                    mma_tf32_1688(pa[i][2], ah, bh);
                 }
             }
 #pragma unroll
