@@ -490,6 +490,17 @@ def kda_section(dev, esa, E, reps: int = 3, T: int = 32768, oracle: bool = False
                            "alu_peak_tflops": alu_peak, "frac_of_alu": flops / (best / 1e3) / 1e12 / alu_peak,
                            "alu_peak_from": f"148 SMs x 128 fp32 lanes x 2 flops x {sm_mhz:.0f} MHz",
                            "stepwise_ms": step_ms, "workspace_bytes": int(ws.numel() - 256)}
+    # the chunked form's tensor-core work: per step and head, X = [Wk; Qp] S
+    # (2 Dk Dv MACs) and the state update (Dk Dv MACs), each fp32 product as
+    # three tf32 products; against the tf32 peak scaled from the measured bf16
+    # peak by the nominal ratio (1.1 / 2.25 PFLOP/s dense)
+    _, bf16_peak, bkind = _load_peaks()
+    tf32_peak = bf16_peak * 1.1 / 2.25
+    tflops = 3 * 2 * 3.0 * B * H * T * D * D
+    res["long_prefill"]["tensor_view"] = {
+        "executed_tf32_flops": tflops, "achieved_tflops": tflops / (best / 1e3) / 1e12,
+        "tf32_peak_tflops": tf32_peak, "peak_from": f"{bkind} bf16 {bf16_peak:.0f} TFLOP/s x 1.1/2.25",
+        "frac": tflops / (best / 1e3) / 1e12 / tf32_peak}
     if oracle:
         one = {k: v[:, :, :1].contiguous() for k, v in xh.items()}
         t0 = time.perf_counter()
@@ -786,6 +797,7 @@ def summarise(dec: dict, mdec: dict | None, prefill: dict | None, kda: dict | No
         if "long_prefill" in kda:
             k = kda["long_prefill"]
             out["kda_prefill"] = {"ms": _r(k["ms"]), "alu_frac": _r(k["frac_of_alu"], 3),
+                                  "tf32_frac": _r((k.get("tensor_view") or {}).get("frac"), 3),
                                   "stepwise_ms": _r(k.get("stepwise_ms")),
                                   "cpu_tok_s": _r((k.get("cpu_baseline") or {}).get("tok_per_s"))}
     return out
