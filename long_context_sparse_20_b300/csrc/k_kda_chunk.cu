@@ -47,7 +47,7 @@ namespace {
 constexpr int kC = 16;             // steps per chunk
 constexpr int kNC = 16;            // value columns per scan block
 constexpr int kPrepThreads = 128;
-constexpr int kScanThreads = 256;
+constexpr int kScanThreads = 256;  // the scan's compute threads (a copy warp besides)
 constexpr int kSegChunks = 256;    // chunks per prep + scan pair
 constexpr int kStages = 6;         // chunk records in flight per scan block
 constexpr float kGLo = 0x1p-60f, kGHi = 0x1p60f;
@@ -293,7 +293,7 @@ struct ScanLayout {
     static constexpr int UU = RA, UP = UU + kC * kNC, STAGE = UP + kC * kNC;
     static constexpr int ST = 0, S0 = ST + kNC * P, DD = S0 + kStages * STAGE, RED = DD + kC * PD;
     static constexpr int BARS = RED + 4 * 2 * kC * PR;  // four K quarters of the 2C x 16 product
-    static constexpr size_t BYTES = (size_t)BARS * 4 + kStages * 8;
+    static constexpr size_t BYTES = (size_t)BARS * 4 + 2 * kStages * 8;  // full, then free barriers
     static constexpr int TPD = kScanThreads / DK;  // threads per key channel in the step-by-step path
     static constexpr int CPT = kNC / TPD;          // columns per such thread
     static constexpr int MT = DK / 16;             // 16-row tiles of the state slice
@@ -315,12 +315,28 @@ __device__ __forceinline__ void scan_issue(float *stage, uint32_t bar, const Chu
     bulk_g2s(smem_u32(stage + L::UU), rec + L::RA + (long long)cb * 2 * kC * kNC, 2 * kC * kNC * 4, bar, pol);
 }
 
+// Barrier 1 over the scan's compute threads only (the copy warp never
+// joins): a plain one, and one that also ANDs a flag over them.
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kScanThreads) : "memory"); }
+__device__ __forceinline__ bool cbar_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kScanThreads)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Warp MMA fragment coordinates (m16n8k8, tf32): lane = 4 g + t.
 //   A (16 x 8): a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4)
 //   B (8 x 8):  b0 (k = t, n = g), b1 (k = t + 4, n = g)
 //   C (16 x 8): c0 (g, 2t), c1 (g, 2t + 1), c2 (g + 8, 2t), c3 (g + 8, 2t + 1)
 template <int DK>
-__global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs a) {
+__global__ void __launch_bounds__(kScanThreads + 32) kda_scan_kernel(const ChunkArgs a) {
     using L = ScanLayout<DK>;
     constexpr int P = L::P, PK = L::PK, PD = L::PD, PR = L::PR, CPT = L::CPT, WPC = DK / 32, TPW = L::TPW;
     extern __shared__ __align__(128) float sm[];
@@ -328,17 +344,38 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
     const int cb = blockIdx.x, c0 = cb * kNC, h = blockIdx.y;
     const long long b = blockIdx.z;
     float *ST = sm + L::ST, *DD = sm + L::DD, *RED = sm + L::RED;
-    const uint32_t bar0 = smem_u32(sm + L::BARS);
-    const uint64_t pol = l2_evict_last_policy();  // a record's shared part is read by every column block
+    // stage s: barrier full(s) completes when chunk data has landed in it,
+    // free(s) when every compute warp is done with it
+    const uint32_t bar0 = smem_u32(sm + L::BARS), fbar0 = bar0 + 8 * kStages;
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; i++) mbar_init(bar0 + 8 * i, 1);
+        for (int i = 0; i < kStages; i++) {
+            mbar_init(bar0 + 8 * i, 1);
+            mbar_init(fbar0 + 8 * i, kScanThreads / 32);
+        }
         mbar_fence_init();
     }
-    __syncthreads();
-    if (tid == 0)
-        for (int j = 0; j < kStages && j < a.nch; j++)
-            scan_issue<DK>(sm + L::S0 + j * L::STAGE, bar0 + 8 * j, a, b, h, cb, j, pol);
+    __syncthreads();  // the last barrier over all threads: the copy warp leaves below
+    if (warp == kScanThreads / 32) {
+        // the copy warp: chunk j into stage j % kStages once that stage is free
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_last_policy();  // a record's shared part is read by every column block
+            int issued = 0;
+            for (int j = 0; j < a.nch; j++) {
+                const int sj = j % kStages;
+                if (j >= kStages && !mbar_wait_bounded(fbar0 + 8 * sj, (uint32_t)(j / kStages - 1) & 1u, a.wait_ns)) {
+                    atomicCAS(reinterpret_cast<int *>(a.status), 0, (int)ESA_ERR_TIMEOUT);
+                    break;
+                }
+                scan_issue<DK>(sm + L::S0 + sj * L::STAGE, bar0 + 8 * sj, a, b, h, cb, j, pol);
+                issued = j + 1;
+            }
+            // no copy may still be landing when the block ends
+            for (int i = issued > kStages ? issued - kStages : 0; i < issued; i++)
+                mbar_wait_bounded(bar0 + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u, a.wait_ns);
+        }
+        return;
+    }
 
     // The state slice S (Dk x 16) in warp-MMA accumulator form: warp w holds
     // tiles (m-tile, n-tile) = (w % MT, w / MT + i) for i < TPW, i.e. rows
@@ -367,7 +404,7 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
         const int sj = j % kStages;
         const uint32_t bar = bar0 + 8 * sj;
         const bool got = mbar_wait_bounded(bar, (uint32_t)(j / kStages) & 1u, a.wait_ns);
-        if (!__syncthreads_and(got)) break;  // chunk j's record and the state slice are in place
+        if (!cbar_and(got)) break;  // chunk j's record and the state slice are in place
         const float *buf = sm + L::S0 + sj * L::STAGE;
 
         if (reinterpret_cast<const int *>(buf + L::FLAG)[0] == 0) {
@@ -409,7 +446,7 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
                     *reinterpret_cast<float2 *>(R + 8 * PR) = make_float2(x[2], x[3]);
                 }
             }
-            __syncthreads();
+            cbar();
             {
                 // thread tid: D at (row, col) = (tid / 16, tid % 16); O at the same place
                 const int row = tid >> 4, col = tid & 15;
@@ -425,7 +462,7 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
                     if (a.lin) a.lin[e] = (uint16_t)(pack_bf16(o, 0.f) & 0xffffu);
                 }
             }
-            __syncthreads();
+            cbar();
             // S' = g_last * S + Kl^T D: A = Kl^T (rows d, columns i), B = D
             const float *KL = buf + L::KL, *GL = buf + L::GL;
             const float g0 = GL[16 * mt2 + g], g8 = GL[16 * mt2 + g + 8];
@@ -487,7 +524,7 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
                 if (lane == 0)
 #pragma unroll
                     for (int c = 0; c < CPT; c++) RED[(ch * WPC + wd) * CPT + c] = p[c];
-                __syncthreads();
+                cbar();
                 const float bt = a.beta[row];
 #pragma unroll
                 for (int c = 0; c < CPT; c++) {
@@ -505,7 +542,7 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
                 if (lane == 0)
 #pragma unroll
                     for (int c = 0; c < CPT; c++) RED[256 + (ch * WPC + wd) * CPT + c] = p[c];
-                __syncthreads();
+                cbar();
                 if (d == 0) {
 #pragma unroll
                     for (int c = 0; c < CPT; c++) {
@@ -521,25 +558,21 @@ __global__ void __launch_bounds__(kScanThreads) kda_scan_kernel(const ChunkArgs 
             }
 #pragma unroll
             for (int c = 0; c < CPT; c++) ST[(ch * CPT + c) * P + d] = s[c];
-            __syncthreads();
+            cbar();
 #pragma unroll
             for (int i = 0; i < TPW; i++)
 #pragma unroll
                 for (int e = 0; e < 4; e++) acc[i][e] = ST[st_col(i, e) * P + st_row(i, e)];
         }
-        __syncthreads();  // the state slice is written; stage sj, D and RED are free
-        if (tid == 0 && j + kStages < a.nch)
-            scan_issue<DK>(sm + L::S0 + sj * L::STAGE, bar, a, b, h, cb, j + kStages, pol);
+        // this warp is done with stage sj (the next chunk's top barrier
+        // orders the state slice, D and the partial sums)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fbar0 + 8 * sj);
     }
     if (j < a.nch) {
-        // a record never arrived: report it, wait (bounded) for the copies
-        // still in flight into this block's stages, and leave the state as is
-        if (tid == 0) {
-            atomicCAS(reinterpret_cast<int *>(a.status), 0, (int)ESA_ERR_TIMEOUT);
-            for (int i = j; i < a.nch && i < j + kStages; i++)
-                mbar_wait_bounded(bar0 + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u, a.wait_ns);
-        }
-        __syncthreads();
+        // a record never arrived: report it and leave the state as is (the
+        // copy warp waits, bounded, for its copies in flight)
+        if (tid == 0) atomicCAS(reinterpret_cast<int *>(a.status), 0, (int)ESA_ERR_TIMEOUT);
         return;
     }
     if (a.dst) {
@@ -566,7 +599,7 @@ esa_status launch_chunked_t(ChunkArgs a, long long B, long long nchunks, const f
         a.src = first ? state_in : carry;
         a.dst = last ? state_out : carry;
         kda_prep_kernel<DK><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)B), kPrepThreads, psmem, st>>>(a);
-        kda_scan_kernel<DK><<<dim3((unsigned)(a.Dv / kNC), (unsigned)a.H, (unsigned)B), kScanThreads, smem, st>>>(a);
+        kda_scan_kernel<DK><<<dim3((unsigned)(a.Dv / kNC), (unsigned)a.H, (unsigned)B), kScanThreads + 32, smem, st>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }
