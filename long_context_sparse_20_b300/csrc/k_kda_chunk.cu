@@ -37,6 +37,8 @@
 //   bulk copies kStages chunks ahead.
 // Padded steps of a ragged last chunk have k = q = 0, alpha = 1, beta = 0:
 // they write nothing and forget nothing. Every sum is fp32 in a fixed order.
+#include <climits>
+
 #include "esa_device.cuh"
 #include "esa_internal.h"
 
@@ -71,6 +73,8 @@ struct ChunkArgs {
     float *rec;         // records of this segment: [B][H][seg_cap]
     int32_t *status;    // the workspace status word
     long long wait_ns;  // limit of a wait for a chunk record
+    int hold_from;      // the copy warp posts no chunk from this one on (a
+                        // test's way to make the wait run out; else never)
     long long T;        // steps per sequence
     long long c_begin;  // first chunk of the segment
     int nch;            // chunks in the segment
@@ -361,7 +365,7 @@ __global__ void __launch_bounds__(kScanThreads + 32) kda_scan_kernel(const Chunk
         if (lane == 0) {
             const uint64_t pol = l2_evict_last_policy();  // a record's shared part is read by every column block
             int issued = 0;
-            for (int j = 0; j < a.nch; j++) {
+            for (int j = 0; j < a.nch && j < a.hold_from; j++) {
                 const int sj = j % kStages;
                 if (j >= kStages && !mbar_wait_bounded(fbar0 + 8 * sj, (uint32_t)(j / kStages - 1) & 1u, a.wait_ns)) {
                     atomicCAS(reinterpret_cast<int *>(a.status), 0, (int)ESA_ERR_TIMEOUT);
@@ -628,7 +632,7 @@ esa_status launch_kda_chunked(const uint16_t *q, const uint16_t *k, const uint16
         p += align256((size_t)B * H * Dk * Dv * 4);
     }
     ChunkArgs a{q, k, v, alpha, beta, nullptr, nullptr, o, lin, reinterpret_cast<float *>(p),
-                static_cast<int32_t *>(ws), wait_limit_ns(), T, 0, 0,
+                static_cast<int32_t *>(ws), wait_limit_ns(), debug_extra_arrivals() > 0 ? 1 : INT_MAX, T, 0, 0,
                 (int)(nchunks < kSegChunks ? nchunks : kSegChunks), H, Dv, scale};
     if (Dk == 128) return launch_chunked_t<128>(a, B, nchunks, state_in, state_out, carry, st);
     if (Dk == 64) return launch_chunked_t<64>(a, B, nchunks, state_in, state_out, carry, st);

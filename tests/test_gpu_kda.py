@@ -25,7 +25,7 @@ def _inputs(B, T, H, Dk, Dv, seed, state):
     return E.kda_inputs(B, T, H, Dk, Dv, seed, state=state)
 
 
-def _gpu(x: dict, state_in=None, inplace=False, lin=True, o=True, chunked=True):
+def _gpu(x: dict, state_in=None, inplace=False, lin=True, o=True, chunked=True, ws=None):
     m = esa()
     B, T, H, Dk = (int(s) for s in x["q"].shape)
     Dv = int(x["v"].shape[-1])
@@ -35,7 +35,7 @@ def _gpu(x: dict, state_in=None, inplace=False, lin=True, o=True, chunked=True):
     si = state_in.cuda() if state_in is not None else None
     so = si if inplace else torch.full((B, H, Dk, Dv), float("nan"), dtype=torch.float32, device="cuda")
     m.esa_kda(d["q"], d["k"], d["v"], d["alpha"], d["beta"], state_in=si, o=out, lin=lo, state_out=so,
-              chunked=chunked)
+              chunked=chunked, ws=ws)
     torch.cuda.synchronize()
     return (out.cpu() if o else None), (lo.cpu() if lin else None), so.cpu()
 
@@ -180,6 +180,38 @@ def test_kda_chunked_few_flagged_chunks():
     x["alpha"] = torch.from_numpy(a)
     ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
     o, lin, so = _gpu(x, state_in=x["state"])
+    _check(o, lin, so, ro, rs)
+
+
+def test_kda_chunked_wait_timeout_reports_status(monkeypatch):
+    """The scan's compute warps wait, bounded, for each chunk's record. With
+    the copy warp held after the first chunk the wait runs out: the call
+    returns, the workspace's status word says TIMEOUT, the first chunk's
+    outputs are written and the later steps and the final state are not;
+    the next call clears the status and is exact."""
+    import ctypes
+    m = esa()
+    B, T, H, Dk, Dv = 1, 100, 2, 64, 32
+    x = _inputs(B, T, H, Dk, Dv, 79, True)
+    ws = torch.zeros(m.esa_kda_workspace_size(B, T, H, Dk, Dv) + 256, dtype=torch.uint8, device="cuda")
+    wptr = ctypes.c_void_p(ws.data_ptr() + (-ws.data_ptr()) % 256)
+
+    def status():
+        v = ctypes.c_int32(0)
+        assert m._lib.esa_read_status(wptr, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream),
+                                      ctypes.byref(v)) == m.OK
+        return v.value
+
+    monkeypatch.setenv("ESA_DEBUG_EXTRA_ARRIVALS", "1")
+    monkeypatch.setenv("ESA_WAIT_LIMIT_NS", "20000000")
+    o, _, so = _gpu(x, state_in=x["state"], ws=ws)
+    assert status() == m.ERR_TIMEOUT
+    assert torch.isfinite(o[:, :16]).all() and torch.isnan(o[:, 16:]).all() and torch.isnan(so).all()
+    monkeypatch.delenv("ESA_DEBUG_EXTRA_ARRIVALS")
+    monkeypatch.delenv("ESA_WAIT_LIMIT_NS")
+    ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
+    o, lin, so = _gpu(x, state_in=x["state"], ws=ws)
+    assert status() == m.OK
     _check(o, lin, so, ro, rs)
 
 
