@@ -34,7 +34,8 @@
 //   tf32 parts and three products are summed, which keeps near-fp32
 //   accuracy (about 2^-20 relative per product).
 //   A block's part of a chunk record is two contiguous pieces, brought in by
-//   bulk copies kStages chunks ahead.
+//   bulk copies up to kStages chunks ahead: a copy warp posts them, eight
+//   compute warps consume them.
 // Padded steps of a ragged last chunk have k = q = 0, alpha = 1, beta = 0:
 // they write nothing and forget nothing. Every sum is fp32 in a fixed order.
 #include <climits>
