@@ -372,6 +372,11 @@ __global__ void __launch_bounds__(kKdaThreads) kda_decode_kernel(const KdaArgs a
     const int c0 = blockIdx.x * kDecCols, h = blockIdx.y;
     const long long b = blockIdx.z;
     const long long sbase = (b * a.H + h) * (long long)DK * a.Dv + c0 + cg * 4;
+    // launched as a programmatic dependent: the next launch in the stream may
+    // be scheduled now, and this one reads nothing before the previous work
+    // in the stream has completed
+    pdl_launch_dependents();
+    pdl_wait();
     float4 S[RJ];
 #pragma unroll
     for (int j = 0; j < RJ; j++)
@@ -503,14 +508,25 @@ esa_status launch_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, c
     if (ws && kda_uses_chunks(T))
         return launch_kda_chunked(q, k, v, alpha, beta, state_in, B, T, H, Dk, Dv, scale, o, lin, state_out, ws, st);
     if (T <= kDecodeSteps) {  // a few steps: one streaming pass over the state
-        dim3 grid((unsigned)(Dv / kDecCols), (unsigned)H, (unsigned)B);
-        if (Dk == 128)
-            kda_decode_kernel<128><<<grid, kKdaThreads, 0, st>>>(a);
-        else if (Dk == 64)
-            kda_decode_kernel<64><<<grid, kKdaThreads, 0, st>>>(a);
-        else
-            return ESA_ERR_UNSUPPORTED;
-        return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
+        const void *fn = Dk == 128 ? reinterpret_cast<const void *>(&kda_decode_kernel<128>)
+                                   : reinterpret_cast<const void *>(&kda_decode_kernel<64>);
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)(Dv / kDecCols), (unsigned)H, (unsigned)B);
+        cfg.blockDim = dim3(kKdaThreads);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        void *args[] = {(void *)&a};
+        cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+        if (e != cudaSuccess) {  // a plain launch
+            cudaGetLastError();
+            cfg.numAttrs = 0;
+            e = cudaLaunchKernelExC(&cfg, fn, args);
+        }
+        return e == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
     }
     // 8 key channels per lane: at Dk = 128, 16 lanes hold two columns each
     // (the operands a lane loads serve both), or one column each when that
