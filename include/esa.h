@@ -324,16 +324,23 @@ ESA_API esa_status esa_route_heads(const uint16_t *k, const float *W1, const flo
  * ESA_ERR_WORKSPACE); it needs no initialisation. Its first word is a status
  * word that the call clears first: a bounded device wait for a chunk's data
  * that runs out sets ESA_ERR_TIMEOUT there (read it with esa_read_status)
- * and leaves that block's outputs unwritten. T <= 4 never uses ws. */
+ * and leaves that block's outputs unwritten. T <= 4 never uses ws.
+ * Streams: a call of more than 256 chunks (4096 steps) runs the couplings
+ * of the next 256 chunks on a second stream of this library's own (one per
+ * host thread and device, created on first use and kept) while `stream`
+ * carries the state through the current ones; event edges join it to
+ * `stream` before the call returns to it, so the call is ordered on `stream`
+ * as any other, and may be captured in a CUDA graph. */
 ESA_API esa_status esa_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                            const float *beta, const float *state_in, int64_t B, int64_t T, int32_t H, int32_t Dk,
                            int32_t Dv, float scale, float *o, uint16_t *lin, float *state_out, void *ws,
                            size_t ws_bytes, void *stream);
 
-/* Bytes of workspace esa_kda() needs for its chunked form at this shape: one
- * record of fp32 matrices per (sequence, head, chunk of 16 steps), for at
- * most 256 chunks at a time, plus a carried state when there are more; 0 when
- * T <= 4 or the shape is not supported. */
+/* Bytes of workspace esa_kda() needs for its chunked form at this shape: a
+ * status word, one record of fp32 matrices per (sequence, head, chunk of 16
+ * steps) for at most 256 chunks at a time, and when there are more chunks a
+ * carried state and a second set of records (one set filled while the other
+ * is read); 0 when T <= 4 or the shape is not supported. */
 ESA_API size_t esa_kda_workspace_size(int64_t B, int64_t T, int32_t H, int32_t Dk, int32_t Dv);
 
 /* Top-K selection without a caller workspace. The pages have no counterpart

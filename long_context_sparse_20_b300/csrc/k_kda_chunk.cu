@@ -52,7 +52,7 @@ constexpr int kNC = 16;            // value columns per scan block
 constexpr int kPrepThreads = 128;
 constexpr int kScanThreads = 256;  // the scan's compute threads (a copy warp besides)
 constexpr int kSegChunks = 256;    // chunks per prep + scan pair
-constexpr int kStages = 6;         // chunk records in flight per scan block
+constexpr int kStages = 3;         // chunk records in flight per scan block
 constexpr float kGLo = 0x1p-60f, kGHi = 0x1p60f;
 
 // Chunk record, fp32 words. The part every column block reads, rows padded
@@ -588,37 +588,89 @@ __global__ void __launch_bounds__(kScanThreads + 32) kda_scan_kernel(const Chunk
     }
 }
 
+// A side stream and five events per host thread and device, for running a
+// segment's prep beside the previous segment's scan (created once, kept).
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, prep[2] = {}, scan[2] = {};
+    bool ok = false, tried = false;
+};
+SideStream &side_stream() {
+    thread_local SideStream r[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    SideStream &x = r[dev & 63];
+    if (!x.tried) {
+        x.tried = true;
+        bool ok = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) == cudaSuccess;
+        for (cudaEvent_t *e : {&x.fork, &x.prep[0], &x.prep[1], &x.scan[0], &x.scan[1]})
+            ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) cudaGetLastError();
+        x.ok = ok;
+    }
+    return x;
+}
+
+// Segments of up to kSegChunks chunks. With more than one, segment s's
+// records go to buffer s & 1 and its prep runs on a side stream, beside the
+// scan of segment s - 1 (the scan block leaves room on its SM for two prep
+// blocks); event edges order prep(s) after scan(s - 2) (the buffer is free)
+// and scan(s) after prep(s). Nothing waits on a flag: only stream events.
 template <int DK>
 esa_status launch_chunked_t(ChunkArgs a, long long B, long long nchunks, const float *state_in, float *state_out,
-                            float *carry, cudaStream_t st) {
+                            float *carry, float *rec1, cudaStream_t st) {
     using L = ScanLayout<DK>;
     const void *fn = reinterpret_cast<const void *>(&kda_scan_kernel<DK>);
     const size_t smem = L::BYTES, psmem = PrepLayout<DK>::bytes(a.Dv);
     if (!ensure_smem(fn, smem) ||
         !ensure_smem(reinterpret_cast<const void *>(&kda_prep_kernel<DK>), PrepLayout<DK>::bytes(512)))
         return ESA_ERR_CUDA;
-    for (long long c = 0; c < nchunks; c += kSegChunks) {
-        const bool first = c == 0, last = c + kSegChunks >= nchunks;
-        a.c_begin = c;
-        a.nch = (int)(last ? nchunks - c : kSegChunks);
-        a.src = first ? state_in : carry;
-        a.dst = last ? state_out : carry;
-        kda_prep_kernel<DK><<<dim3((unsigned)a.nch, (unsigned)a.H, (unsigned)B), kPrepThreads, psmem, st>>>(a);
-        kda_scan_kernel<DK><<<dim3((unsigned)(a.Dv / kNC), (unsigned)a.H, (unsigned)B), kScanThreads + 32, smem, st>>>(a);
+    float *rec0 = a.rec;
+    const long long nseg = (nchunks + kSegChunks - 1) / kSegChunks;
+    SideStream *side = nseg > 1 ? &side_stream() : nullptr;
+    const bool overlap = side && side->ok && rec1;
+    if (overlap && (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork) != cudaSuccess))
+        return ESA_ERR_CUDA;
+    for (long long sg = 0; sg < nseg; sg++) {
+        const long long c = sg * kSegChunks;
+        const bool last = sg == nseg - 1;
+        ChunkArgs x = a;
+        x.c_begin = c;
+        x.nch = (int)(last ? nchunks - c : kSegChunks);
+        x.src = sg == 0 ? state_in : carry;
+        x.dst = last ? state_out : carry;
+        x.rec = overlap && (sg & 1) ? rec1 : rec0;
+        const dim3 pgrid((unsigned)x.nch, (unsigned)x.H, (unsigned)B), sgrid((unsigned)(x.Dv / kNC), (unsigned)x.H,
+                                                                           (unsigned)B);
+        if (!overlap) {
+            kda_prep_kernel<DK><<<pgrid, kPrepThreads, psmem, st>>>(x);
+            kda_scan_kernel<DK><<<sgrid, kScanThreads + 32, smem, st>>>(x);
+            continue;
+        }
+        const int ib = (int)(sg & 1);
+        if (sg >= 2 && cudaStreamWaitEvent(side->s, side->scan[ib]) != cudaSuccess) return ESA_ERR_CUDA;
+        kda_prep_kernel<DK><<<pgrid, kPrepThreads, psmem, side->s>>>(x);
+        if (cudaEventRecord(side->prep[ib], side->s) != cudaSuccess ||
+            cudaStreamWaitEvent(st, side->prep[ib]) != cudaSuccess)
+            return ESA_ERR_CUDA;
+        kda_scan_kernel<DK><<<sgrid, kScanThreads + 32, smem, st>>>(x);
+        if (cudaEventRecord(side->scan[ib], st) != cudaSuccess) return ESA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }
 
 }  // namespace
 
-// Workspace: the status word (kStatusBytes), the carried state when there
-// is more than one segment, then the records of one segment.
+// Workspace: the status word (kStatusBytes); with more than one segment the
+// carried state and two record buffers, else one.
 size_t kda_chunked_ws_bytes(long long B, long long T, int H, int Dk, int Dv) {
     if (T <= 0) return 0;
     const long long nchunks = (T + kC - 1) / kC;
-    const long long cap = nchunks < kSegChunks ? nchunks : kSegChunks;
-    const size_t carry = nchunks > kSegChunks ? align256((size_t)B * H * Dk * Dv * 4) : 0;
-    return kStatusBytes + carry + (size_t)B * H * cap * rec_floats(Dk, Dv) * 4;
+    const bool multi = nchunks > kSegChunks;
+    const long long cap = multi ? kSegChunks : nchunks;
+    const size_t carry = multi ? align256((size_t)B * H * Dk * Dv * 4) : 0;
+    const size_t recs = align256((size_t)B * H * cap * rec_floats(Dk, Dv) * 4);
+    return kStatusBytes + carry + (multi ? 2 : 1) * recs;
 }
 
 esa_status launch_kda_chunked(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
@@ -626,17 +678,20 @@ esa_status launch_kda_chunked(const uint16_t *q, const uint16_t *k, const uint16
                               int Dv, float scale, float *o, uint16_t *lin, float *state_out, void *ws,
                               cudaStream_t st) {
     const long long nchunks = (T + kC - 1) / kC;
+    const bool multi = nchunks > kSegChunks;
+    const long long cap = multi ? kSegChunks : nchunks;
     char *p = static_cast<char *>(ws) + kStatusBytes;
-    float *carry = nullptr;
-    if (nchunks > kSegChunks) {
+    float *carry = nullptr, *rec1 = nullptr;
+    if (multi) {
         carry = reinterpret_cast<float *>(p);
         p += align256((size_t)B * H * Dk * Dv * 4);
+        rec1 = reinterpret_cast<float *>(p + align256((size_t)B * H * cap * rec_floats(Dk, Dv) * 4));
     }
     ChunkArgs a{q, k, v, alpha, beta, nullptr, nullptr, o, lin, reinterpret_cast<float *>(p),
                 static_cast<int32_t *>(ws), wait_limit_ns(), debug_extra_arrivals() > 0 ? 1 : INT_MAX, T, 0, 0,
-                (int)(nchunks < kSegChunks ? nchunks : kSegChunks), H, Dv, scale};
-    if (Dk == 128) return launch_chunked_t<128>(a, B, nchunks, state_in, state_out, carry, st);
-    if (Dk == 64) return launch_chunked_t<64>(a, B, nchunks, state_in, state_out, carry, st);
+                (int)cap, H, Dv, scale};
+    if (Dk == 128) return launch_chunked_t<128>(a, B, nchunks, state_in, state_out, carry, rec1, st);
+    if (Dk == 64) return launch_chunked_t<64>(a, B, nchunks, state_in, state_out, carry, rec1, st);
     return ESA_ERR_UNSUPPORTED;
 }
 

@@ -181,14 +181,17 @@ def test_kda_workspace_size():
     """A 256-byte status word, then one record per (sequence, head, chunk of
     16 steps) of fp32 words: two 16 x Dk matrices with rows padded to Dk + 4,
     one with rows padded to Dk + 8, g_last (Dk), a flag (padded to four) and
-    two 16 x Dv matrices; at most 256 chunks at a time, plus the carried
-    state (256-byte aligned) beyond that. None for T <= 4 or unsupported
+    two 16 x Dv matrices (the records 256-byte aligned as a whole); at most
+    256 chunks at a time, plus the carried state (256-byte aligned) and a
+    second set of records beyond that. None for T <= 4 or unsupported
     shapes."""
     import long_context_sparse_20_b300 as esa
     rec = lambda Dk, Dv: 4 * (2 * 16 * (Dk + 4) + 16 * (Dk + 8) + Dk + 4 + 2 * 16 * Dv)
-    assert esa.esa_kda_workspace_size(2, 100, 3, 128, 64) == 256 + 2 * 3 * 7 * rec(128, 64)
-    assert esa.esa_kda_workspace_size(1, 4096, 2, 64, 128) == 256 + 2 * 256 * rec(64, 128)
+    a256 = lambda n: (n + 255) // 256 * 256
+    assert esa.esa_kda_workspace_size(2, 100, 3, 128, 64) == 256 + a256(2 * 3 * 7 * rec(128, 64))
+    assert esa.esa_kda_workspace_size(1, 4096, 2, 64, 128) == 256 + a256(2 * 256 * rec(64, 128))
     carry = 1 * 16 * 128 * 128 * 4
-    assert esa.esa_kda_workspace_size(1, 32768, 16, 128, 128) == 256 + carry + 16 * 256 * rec(128, 128)
+    # more than 256 chunks: two record buffers (one filled while the other is read)
+    assert esa.esa_kda_workspace_size(1, 32768, 16, 128, 128) == 256 + carry + 2 * a256(16 * 256 * rec(128, 128))
     assert esa.esa_kda_workspace_size(1, 4, 2, 128, 128) == 0
     assert esa.esa_kda_workspace_size(1, 100, 2, 96, 128) == 0

@@ -183,6 +183,41 @@ def test_kda_chunked_few_flagged_chunks():
     _check(o, lin, so, ro, rs)
 
 
+def test_kda_chunked_in_a_cuda_graph():
+    """A call of several segments (their preps on a side stream beside the
+    scans, joined by events) captured in a CUDA graph and replayed gives the
+    bits of the same call made directly."""
+    m = esa()
+    x = _inputs(1, 8300, 2, 128, 32, 80, True)
+    d = {k: v.cuda() for k, v in x.items()}
+    B, T, H, Dk, Dv = 1, 8300, 2, 128, 32
+    ws = torch.empty(m.esa_kda_workspace_size(B, T, H, Dk, Dv) + 256, dtype=torch.uint8, device="cuda")
+    outs = []
+    for graph in (False, True):
+        o = torch.full((B, T, H, Dv), float("nan"), device="cuda")
+        so = torch.full((B, H, Dk, Dv), float("nan"), device="cuda")
+
+        def call():
+            m.esa_kda(d["q"], d["k"], d["v"], d["alpha"], d["beta"], state_in=d["state"], o=o, state_out=so, ws=ws)
+
+        if graph:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    call()
+            torch.cuda.current_stream().wait_stream(s)
+            g.replay()
+        else:
+            call()
+        torch.cuda.synchronize()
+        outs.append((o.cpu(), so.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    ro, rs = O.kda(x["q"], x["k"], x["v"], x["alpha"], x["beta"], state_in=x["state"])
+    _check(outs[1][0], None, outs[1][1], ro, rs)
+
+
 def test_kda_chunked_wait_timeout_reports_status(monkeypatch):
     """The scan's compute warps wait, bounded, for each chunk's record. With
     the copy warp held after the first chunk the wait runs out: the call
