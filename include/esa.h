@@ -325,12 +325,13 @@ ESA_API esa_status esa_route_heads(const uint16_t *k, const float *W1, const flo
  * word that the call clears first: a bounded device wait for a chunk's data
  * that runs out sets ESA_ERR_TIMEOUT there (read it with esa_read_status)
  * and leaves that block's outputs unwritten. T <= 4 never uses ws.
- * Streams: a call of more than 256 chunks (4096 steps) runs the couplings
- * of the next 256 chunks on a second stream of this library's own (one per
- * host thread and device, created on first use and kept) while `stream`
- * carries the state through the current ones; event edges join it to
- * `stream` before the call returns to it, so the call is ordered on `stream`
- * as any other, and may be captured in a CUDA graph. */
+ * Streams: a call of more than 256 chunks (4096 steps) carries the state
+ * through each 256 chunks on a second stream of this library's own (one per
+ * host thread and device, at the device's greatest priority, created on
+ * first use and kept) while `stream` computes the next 256 chunks'
+ * couplings; event edges join the two, and `stream` waits for the last
+ * carry, so the call is ordered on `stream` as any other and may be captured
+ * in a CUDA graph. */
 ESA_API esa_status esa_kda(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                            const float *beta, const float *state_in, int64_t B, int64_t T, int32_t H, int32_t Dk,
                            int32_t Dv, float scale, float *o, uint16_t *lin, float *state_out, void *ws,

@@ -588,8 +588,9 @@ __global__ void __launch_bounds__(kScanThreads + 32) kda_scan_kernel(const Chunk
     }
 }
 
-// A side stream and five events per host thread and device, for running a
-// segment's prep beside the previous segment's scan (created once, kept).
+// A side stream (at the device's greatest priority) and five events per
+// host thread and device, for running the scans beside the next segments'
+// preps (created once, kept).
 struct SideStream {
     cudaStream_t s = nullptr;
     cudaEvent_t fork = nullptr, prep[2] = {}, scan[2] = {};
@@ -602,7 +603,9 @@ SideStream &side_stream() {
     SideStream &x = r[dev & 63];
     if (!x.tried) {
         x.tried = true;
-        bool ok = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) == cudaSuccess;
+        int least = 0, greatest = 0;
+        bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
+                  cudaStreamCreateWithPriority(&x.s, cudaStreamNonBlocking, greatest) == cudaSuccess;
         for (cudaEvent_t *e : {&x.fork, &x.prep[0], &x.prep[1], &x.scan[0], &x.scan[1]})
             ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
         if (!ok) cudaGetLastError();
@@ -612,10 +615,12 @@ SideStream &side_stream() {
 }
 
 // Segments of up to kSegChunks chunks. With more than one, segment s's
-// records go to buffer s & 1 and its prep runs on a side stream, beside the
-// scan of segment s - 1 (the scan block leaves room on its SM for two prep
-// blocks); event edges order prep(s) after scan(s - 2) (the buffer is free)
-// and scan(s) after prep(s). Nothing waits on a flag: only stream events.
+// records go to buffer s & 1; the preps run on `st` and the scans on the
+// side stream, so that prep(s + 1) runs beside scan(s) (the scan block
+// leaves room on its SM for two prep blocks, and the side stream's priority
+// places scan blocks first as SMs free up). Event edges order scan(s) after
+// prep(s), prep(s) after scan(s - 2) (its buffer is free), and `st` after
+// the last scan. Nothing waits on a flag: only stream events.
 template <int DK>
 esa_status launch_chunked_t(ChunkArgs a, long long B, long long nchunks, const float *state_in, float *state_out,
                             float *carry, float *rec1, cudaStream_t st) {
@@ -648,13 +653,14 @@ esa_status launch_chunked_t(ChunkArgs a, long long B, long long nchunks, const f
             continue;
         }
         const int ib = (int)(sg & 1);
-        if (sg >= 2 && cudaStreamWaitEvent(side->s, side->scan[ib]) != cudaSuccess) return ESA_ERR_CUDA;
-        kda_prep_kernel<DK><<<pgrid, kPrepThreads, psmem, side->s>>>(x);
-        if (cudaEventRecord(side->prep[ib], side->s) != cudaSuccess ||
-            cudaStreamWaitEvent(st, side->prep[ib]) != cudaSuccess)
+        if (sg >= 2 && cudaStreamWaitEvent(st, side->scan[ib]) != cudaSuccess) return ESA_ERR_CUDA;
+        kda_prep_kernel<DK><<<pgrid, kPrepThreads, psmem, st>>>(x);
+        if (cudaEventRecord(side->prep[ib], st) != cudaSuccess ||
+            cudaStreamWaitEvent(side->s, side->prep[ib]) != cudaSuccess)
             return ESA_ERR_CUDA;
-        kda_scan_kernel<DK><<<sgrid, kScanThreads + 32, smem, st>>>(x);
-        if (cudaEventRecord(side->scan[ib], st) != cudaSuccess) return ESA_ERR_CUDA;
+        kda_scan_kernel<DK><<<sgrid, kScanThreads + 32, smem, side->s>>>(x);
+        if (cudaEventRecord(side->scan[ib], side->s) != cudaSuccess) return ESA_ERR_CUDA;
+        if (last && cudaStreamWaitEvent(st, side->scan[ib]) != cudaSuccess) return ESA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? ESA_OK : ESA_ERR_CUDA;
 }
