@@ -26,8 +26,12 @@
  *     workspace too small) are returned before anything is launched.
  *   - Device-side errors never trap: kernels record the first error code in
  *     the workspace status word and return; read it with esa_read_status().
- *   - The library allocates no device memory and keeps no global state; it
- *     is thread-safe as long as concurrent calls use distinct workspaces.
+ *   - The library allocates no device memory at run time and keeps no
+ *     state between calls beyond what this header names: the fixed scratch
+ *     array of esa_topk_select_noalloc, and the side stream and events of
+ *     esa_kda's chunked form (one set per host thread and device, created
+ *     on first use and kept). It is thread-safe as long as concurrent calls
+ *     use distinct workspaces.
  *   - Workspace: a caller-allocated device buffer of at least
  *     esa_workspace_size() bytes, 256-byte aligned, zero-filled once before
  *     its first use (esa_workspace_init). Calls leave it ready for the next
