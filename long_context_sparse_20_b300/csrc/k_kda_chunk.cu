@@ -32,7 +32,7 @@
 //   Dk), then D and O, then S' = g_last * S + Kl^T D. Both products run on
 //   the tensor cores (mma.sync, tf32): each fp32 operand is split into two
 //   tf32 parts and three products are summed, which keeps near-fp32
-//   accuracy (about 2^-20 relative per product).
+//   accuracy (within 2^-19 relative per product).
 //   A block's part of a chunk record is two contiguous pieces, brought in by
 //   bulk copies up to kStages chunks ahead: a copy warp posts them, eight
 //   compute warps consume them.
@@ -274,8 +274,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4) kda_prep_kernel(const ChunkAr
 
 // fp32 x as the sum of two tf32 values, each its leading 11 significant
 // bits (the low 13 of the fp32 pattern cleared): hi, then lo from the exact
-// remainder x - hi. hi + lo carries 22 significant bits, so three tf32
-// products (hi*hi, hi*lo, lo*hi) give a product to about 3 * 2^-22 relative.
+// remainder x - hi (at most 13 significant bits). |x - hi - lo| < 2^-21 |x|,
+// and three tf32 products (hi*hi, hi*lo, lo*hi) give a product to within
+// 2^-19 relative, the dropped lo*lo the largest part.
 __device__ __forceinline__ void tf32_split(float x, uint32_t &hi, uint32_t &lo) {
     hi = __float_as_uint(x) & 0xffffe000u;
     lo = __float_as_uint(x - __uint_as_float(hi)) & 0xffffe000u;
