@@ -769,7 +769,7 @@ def summarise(dec: dict, mdec: dict | None, prefill: dict | None, kda: dict | No
     out = {}
     if prefill and "tiny_prefill" in prefill:
         p = prefill["tiny_prefill"]
-        out["1_tiny_prefill"] = {"ms": _r(p["ms"]), "tok_s": _r(p["tok_per_s"]), "bound": "launch",
+        out["1_tiny_prefill"] = {"ms": _r(p["ms"]), "tok_s": _r(p["tok_per_s"]), "bound": "latency",
                                  "cpu_tok_s": _r((p.get("cpu_baseline") or {}).get("tok_per_s"))}
     for key, d, c in (("2_decode", dec, cpu), ("5_million_decode", mdec, mcpu)):
         if d:

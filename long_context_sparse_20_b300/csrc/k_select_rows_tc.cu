@@ -783,11 +783,16 @@ struct TcPlan {
     size_t kh_off, flag_off, bytes;
 };
 
-// ESA_ROW_SELECT=dp4a keeps the row-tiled selection on the dp4a kernel
-// (a switch for comparing the two kernels; both give identical results)
+// ESA_ROW_SELECT=dp4a keeps the row-tiled selection on the dp4a kernel,
+// ESA_ROW_SELECT=tc on the tensor cores wherever they apply (switches for
+// comparing the two kernels; both give identical results)
 bool tc_disabled() {
     const char *e = getenv("ESA_ROW_SELECT");
     return e && strcmp(e, "dp4a") == 0;
+}
+bool tc_forced() {
+    const char *e = getenv("ESA_ROW_SELECT");
+    return e && strcmp(e, "tc") == 0;
 }
 
 TcPlan plan_tc(const Shape &s, int) {
@@ -798,6 +803,11 @@ TcPlan plan_tc(const Shape &s, int) {
     if (smem + sizeof(TcShared) + 1024 > device_info().smem_optin) return p;
     p.Tkp = (s.Tk + kKT - 1) / kKT * kKT;
     p.ntile = (s.Tq + kRowsT - 1) / kRowsT;
+    // a small problem on few 128-row query tiles (fewer than an eighth of the
+    // SMs, at most 4M query-key pairs): the dp4a kernel's 32-row tiles give
+    // four times the blocks and finish sooner (1024 queries over 1024 keys:
+    // 82 against 125 us). ESA_ROW_SELECT=tc keeps the tensor cores.
+    if (!tc_forced() && s.B * p.ntile * 8 < device_info().sms && s.B * s.Tq * s.Tk <= (1LL << 22)) return TcPlan{};
     p.kh_off = kStatusBytes;
     p.flag_off = p.kh_off + align256((size_t)s.B * p.Tkp * s.D_I * 2);
     p.bytes = p.flag_off + align256((size_t)s.B * p.ntile * 4);

@@ -174,6 +174,21 @@ def test_gated_call_on_the_routed_path(over):
     assert_close(res["out"], ref)
 
 
+def test_small_prefill_default_rule(monkeypatch):
+    """The library's own choice for a small prefill (no ESA_ROW_SELECT): the
+    dp4a row selection for 1024 queries over 1024 keys (8 row tiles of 128),
+    with its bitmask feeding the routed kernel in the one call: exact index
+    sets, and outputs within tolerance, with and without the index outputs."""
+    monkeypatch.delenv("ESA_ROW_SELECT", raising=False)
+    cfg, sh, inp = _case(seed=612, B=1, Tq=1024, Tk=1024, q_offset=0, Hq=4, Hkv=1, D=64, top_k=128, D_I=32)
+    K = cfg["top_k"]
+    res = gpu_gated(to_dev(inp), sh, K, want_lse=False)
+    check_against_oracle(inp, sh, K, res)
+    res = gpu_gated(to_dev(inp), sh, K, want_idx=False, want_lse=False)
+    _, _, ref, _ = O.gated_sparse_attention(inp, sh, K)
+    assert_close(res["out"], ref)
+
+
 def test_fused_workspace_reuse_across_shapes():
     """Back-to-back calls on one workspace, alternating shapes: the control
     state each call leaves behind is what the next one needs."""
